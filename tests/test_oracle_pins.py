@@ -1,0 +1,344 @@
+"""Pins of the CPU oracle to facts other than itself: library routines (bf16 rounding,
+sorting), closed forms, invariants and special cases of the decode step.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a wrong
+sign, index or grouping, a transposed operand, a sequential instead of parallel
+block) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+
+RNG = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------- bf16
+
+def test_bf16_widen_matches_torch_for_every_bit_pattern():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = O.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+    fin = np.isfinite(ref)
+    assert np.array_equal(ours[fin], ref[fin])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+
+
+def test_bf16_rounding_matches_torch_nearest_even():
+    x = RNG.standard_normal(200000).astype(np.float32) * np.float32(3.0)
+    # exact ties: bf16 value plus half an ulp, with even and odd low bit
+    base = RNG.standard_normal(5000).astype(np.float32)
+    b16 = base.view(np.uint32) & np.uint32(0xFFFF0000)
+    ties = (b16 | np.uint32(0x8000)).view(np.float32)
+    x = np.concatenate([x, ties, np.float32([0.0, -0.0, 1.0, -2.5, 1e30, -1e-30])])
+    ours = O.f64_to_bf16(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    big = np.abs(x) >= np.float32(2.0 ** -126)
+    assert np.array_equal(ours[big], ref[big])
+
+
+# ----------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_constant_vector_closed_form():
+    d, c, eps = 64, -0.37, 1e-6
+    g = RNG.standard_normal(d)
+    h = O.rms_norm(np.full(d, c), g, eps)
+    assert np.allclose(h, g * c / math.sqrt(c * c + eps), rtol=0, atol=1e-15)
+
+
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    x = RNG.standard_normal(128)
+    h = O.rms_norm(x, np.ones(128), 0.0)
+    assert abs(np.sqrt(np.mean(h * h)) - 1.0) < 1e-14
+    assert np.allclose(O.rms_norm(7.5 * x, np.ones(128), 0.0), h, atol=1e-14)
+
+
+# ----------------------------------------------------------------- RoPE
+
+def test_rope_position_zero_is_identity():
+    v = RNG.standard_normal((3, 16))
+    assert np.array_equal(O.rope(v, 0, 1e4), v)
+
+
+def test_rope_preserves_norm_and_depends_on_relative_position():
+    q, k = RNG.standard_normal(64), RNG.standard_normal(64)
+    for p in (1, 17, 4095):
+        assert abs(np.linalg.norm(O.rope(q, p, 1e6)) - np.linalg.norm(q)) < 1e-12
+    a = O.rope(q, 100, 1e4) @ O.rope(k, 37, 1e4)
+    b = O.rope(q, 163, 1e4) @ O.rope(k, 100, 1e4)
+    assert abs(a - b) < 1e-11
+
+
+def test_rope_basis_vector_closed_form_rotate_half():
+    hd, theta, p = 32, 1e4, 5
+    for i in (0, 3, 15):
+        e = np.zeros(hd); e[i] = 1.0
+        ang = p * theta ** (-2.0 * i / hd)
+        want = np.zeros(hd); want[i] = math.cos(ang); want[i + hd // 2] = math.sin(ang)
+        assert np.allclose(O.rope(e, p, theta), want, atol=1e-15)
+        e2 = np.zeros(hd); e2[i + hd // 2] = 1.0
+        want2 = np.zeros(hd); want2[i] = -math.sin(ang); want2[i + hd // 2] = math.cos(ang)
+        assert np.allclose(O.rope(e2, p, theta), want2, atol=1e-15)
+
+
+# ----------------------------------------------------------------- attention
+
+def test_attention_single_key_returns_its_value():
+    q = RNG.standard_normal((4, 8)); K = RNG.standard_normal((1, 2, 8))
+    V = RNG.standard_normal((1, 2, 8))
+    o = O.attention(q, K, V)
+    assert np.allclose(o[:2], V[0, 0]) and np.allclose(o[2:], V[0, 1])
+
+
+def test_attention_equal_keys_average_values():
+    q = RNG.standard_normal((2, 8)); k = RNG.standard_normal(8)
+    K = np.tile(k, (10, 1, 1)); V = RNG.standard_normal((10, 1, 8))
+    assert np.allclose(O.attention(q, K, V), V[:, 0].mean(0), atol=1e-14)
+
+
+def test_attention_two_keys_closed_form_with_sqrt_hd_scale():
+    hd = 16
+    q = np.zeros((1, hd)); q[0, 0] = 2.0
+    K = np.zeros((2, 1, hd)); K[0, 0, 0] = 3.0; K[1, 0, 0] = -1.0
+    V = RNG.standard_normal((2, 1, hd))
+    s0, s1 = 6.0 / math.sqrt(hd), -2.0 / math.sqrt(hd)
+    p0 = 1.0 / (1.0 + math.exp(s1 - s0))
+    assert np.allclose(O.attention(q, K, V)[0], p0 * V[0, 0] + (1 - p0) * V[1, 0],
+                       atol=1e-14)
+
+
+def test_attention_gqa_contiguous_groups():
+    Hq, Hkv, hd, n = 8, 2, 8, 5
+    q = RNG.standard_normal((Hq, hd)); K = RNG.standard_normal((n, Hkv, hd))
+    V = RNG.standard_normal((n, Hkv, hd)); V[:, 1] = 0.0
+    o = O.attention(q, K, V)
+    assert np.all(o[4:] == 0.0)                 # heads 4..7 -> kv head 1
+    assert np.all(np.abs(o[:4]).sum(1) > 0)     # heads 0..3 -> kv head 0
+
+
+def test_split_kv_merge_equals_full_softmax():
+    q = RNG.standard_normal((8, 32)); K = RNG.standard_normal((300, 2, 32)) * 2
+    V = RNG.standard_normal((300, 2, 32))
+    full = O.attention(q, K, V)
+    for cuts in ([100], [1, 2, 299], [37, 64, 200, 250]):
+        edges = [0] + cuts + [300]
+        parts = [O.attention_partial(q, K[a:b], V[a:b]) for a, b in zip(edges, edges[1:])]
+        assert np.allclose(O.merge_partials(parts), full, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------- router / experts
+
+def test_topk_matches_stable_full_sort_with_ties():
+    for _ in range(200):
+        r = np.round(RNG.standard_normal(32), 1)      # many exact ties
+        k = int(RNG.integers(1, 9))
+        idx, w, margin = O.router_topk(r, k)
+        ref = np.lexsort((np.arange(32), -r))[:k]   # by -r, then index
+        assert np.array_equal(idx, ref)
+        assert abs(w.sum() - 1.0) < 1e-12
+        srt = np.sort(r)[::-1]
+        assert margin == srt[k - 1] - srt[k]
+
+
+def test_topk_softmax_closed_forms():
+    r = np.array([0.3, 2.0, -1.0, 1.5])
+    idx, w, _ = O.router_topk(r, 1)
+    assert list(idx) == [1] and w[0] == 1.0
+    idx, w, _ = O.router_topk(r, 2)
+    assert list(idx) == [1, 3]
+    assert abs(w[0] - 1 / (1 + math.exp(1.5 - 2.0))) < 1e-15
+
+
+def test_swiglu_scalar_closed_form():
+    h = np.array([0.7]); wg = np.array([[1.3]]); wu = np.array([[-0.4]])
+    wd = np.array([[2.0]])
+    z = 1.3 * 0.7
+    want = 2.0 * (z / (1 + math.exp(-z))) * (-0.4 * 0.7)
+    assert abs(O.swiglu_expert(h, wg, wu, wd)[0] - want) < 1e-15
+
+
+# ----------------------------------------------------------------- whole layer
+
+TINY = dict(n_layers=2, d_model=32, n_q_heads=4, n_kv_heads=2, head_dim=8, n_experts=4,
+            top_k=2, d_ff=16, vocab=50, rope_theta=1e4, rms_eps=1e-6, sliding_window=0,
+            swa_layers=(), page_size=16)
+
+
+def _setup(cfg=TINY, lens=(37, 5), seed=0, gain_jitter=0.2, std=0.2):
+    W = synth.make_weights(cfg, seed=seed, gain_jitter=gain_jitter, std=std)
+    pt, npages = synth.make_page_table(list(lens), seed=seed)
+    k, v = synth.make_kv(cfg, npages, seed=seed)
+    return W, pt, k, v
+
+
+def _x(B, d, seed=3):
+    return np.random.default_rng(seed).standard_normal((B, d))
+
+
+def test_parallel_block_is_additive_in_its_two_branches():
+    W, pt, k, v = _setup()
+    x = _x(2, 32)
+    kv = synth.HostKV(k, v)
+    full, _ = O.layer_step(TINY, synth.HostWeights(W), kv, 0, x, [37, 5], pt)
+    Wa = dict(W); Wa["w_down"] = torch.zeros_like(W["w_down"])
+    attn_only, _ = O.layer_step(TINY, synth.HostWeights(Wa), kv, 0, x, [37, 5], pt)
+    Wm = dict(W); Wm["wo"] = torch.zeros_like(W["wo"])
+    moe_only, _ = O.layer_step(TINY, synth.HostWeights(Wm), kv, 0, x, [37, 5], pt)
+    assert np.allclose(full - x, (attn_only - x) + (moe_only - x), atol=1e-13)
+    assert np.abs(attn_only - x).max() > 1e-3 and np.abs(moe_only - x).max() > 1e-3
+
+
+def test_zero_branches_leave_residual_and_logits_reduce_to_head_matvec():
+    W, pt, k, v = _setup()
+    W["wo"] = torch.zeros_like(W["wo"]); W["w_down"] = torch.zeros_like(W["w_down"])
+    tok = [7, 41]
+    out = O.decode_step(TINY, synth.HostWeights(W), synth.HostKV(k, v), tok, [37, 5], pt)
+    x0 = O.bf16_to_f64(W["embed"][tok].view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(out["hidden"][-1], x0)
+    g = O.bf16_to_f64(W["final_norm"].view(torch.int16).numpy().view(np.uint16))
+    lm = O.bf16_to_f64(W["lm_head"].view(torch.int16).numpy().view(np.uint16))
+    for b in range(2):
+        h = x0[b] / math.sqrt(np.mean(x0[b] ** 2) + 1e-6) * g
+        assert np.allclose(out["logits"][b], lm @ h, atol=1e-12)
+        assert out["greedy"][b] == int(np.argmax(lm @ h))
+
+
+def test_all_experts_with_identical_weights_equal_dense_swiglu():
+    cfg = dict(TINY, top_k=4)
+    W, pt, k, v = _setup(cfg)
+    for name in ("w_gate", "w_up", "w_down"):
+        W[name][:, 1:] = W[name][:, :1]
+    W["wo"] = torch.zeros_like(W["wo"])
+    x = _x(2, 32)
+    HW = synth.HostWeights(W)
+    y, info = O.layer_step(cfg, HW, synth.HostKV(k, v), 0, x, [37, 5], pt)
+    g = O.bf16_to_f64(HW.attn_norm(0))
+    wg, wu, wd = (O.bf16_to_f64(a) for a in HW.expert(0, 0))
+    for b in range(2):
+        h = x[b] / math.sqrt(np.mean(x[b] ** 2) + 1e-6) * g
+        dense = wd @ ((wg @ h) / (1 + np.exp(-(wg @ h))) * (wu @ h))
+        assert np.allclose(y[b] - x[b], dense, atol=1e-13)
+        assert sorted(info["idx"][b]) == [0, 1, 2, 3]
+
+
+def test_first_token_attends_only_to_itself():
+    W, pt, k, v = _setup(lens=(0,))
+    W["w_down"] = torch.zeros_like(W["w_down"])
+    x = _x(1, 32)
+    HW = synth.HostWeights(W)
+    y, info = O.layer_step(TINY, HW, synth.HostKV(k, v), 0, x, [0], pt)
+    v16 = O.bf16_to_f64(info["kv"][0]["v"])             # [Hkv, hd]
+    o = np.concatenate([v16[(i * 2) // 4] for i in range(4)])
+    assert np.allclose(y[0] - x[0], O.bf16_to_f64(HW.wo(0)) @ o, atol=1e-13)
+
+
+def test_kv_write_goes_to_page_table_slot_with_rotated_bf16_k():
+    W, pt, k, v = _setup()
+    x = _x(2, 32)
+    HW = synth.HostWeights(W)
+    _, info = O.layer_step(TINY, HW, synth.HostKV(k, v), 1, x, [37, 5], pt)
+    for b, p in ((0, 37), (1, 5)):
+        rec = info["kv"][b]
+        assert rec["page"] == pt[b][p // 16] and rec["slot"] == p % 16
+        g = O.bf16_to_f64(HW.attn_norm(1))
+        h = x[b] / math.sqrt(np.mean(x[b] ** 2) + 1e-6) * g
+        kn = O.rope((O.bf16_to_f64(HW.wk(1)) @ h).reshape(2, 8), p, 1e4)
+        assert np.array_equal(rec["k"], O.f64_to_bf16(kn))
+
+
+def test_paged_gather_equals_contiguous_cache_bit_exact():
+    W, pt, k, v = _setup(lens=(45,))
+    x = _x(1, 32)
+    HW = synth.HostWeights(W)
+    y1, _ = O.layer_step(TINY, HW, synth.HostKV(k, v), 0, x, [45], pt)
+    # same logical cache stored contiguously: logical page i at physical page i
+    n = pt.shape[1]
+    idx = torch.as_tensor(pt[0].astype(np.int64))
+    k2, v2 = k[:, idx].clone(), v[:, idx].clone()
+    pt2 = np.arange(n, dtype=np.int32)[None]
+    y2, _ = O.layer_step(TINY, HW, synth.HostKV(k2, v2), 0, x, [45], pt2)
+    assert np.array_equal(y1, y2)
+
+
+def test_sliding_window_ignores_keys_outside_and_full_window_matches():
+    cfg = dict(TINY, sliding_window=8, swa_layers=(1,))
+    W, pt, k, v = _setup(cfg, lens=(40,))
+    x = _x(1, 32)
+    HW = synth.HostWeights(W)
+    base, _ = O.layer_step(cfg, HW, synth.HostKV(k, v), 1, x, [40], pt)
+    k2, v2 = k.clone(), v.clone()
+    for pos in range(0, 33):             # window of 8 at p=40 keeps 33..40
+        k2[1, pt[0][pos // 16], :, pos % 16] = float("nan")
+        v2[1, pt[0][pos // 16], :, pos % 16] = float("nan")
+    got, _ = O.layer_step(cfg, HW, synth.HostKV(k2, v2), 1, x, [40], pt)
+    assert np.array_equal(base, got)
+    full_cfg = dict(cfg, sliding_window=41)
+    a, _ = O.layer_step(full_cfg, HW, synth.HostKV(k, v), 1, x, [40], pt)
+    b, _ = O.layer_step(TINY, HW, synth.HostKV(k, v), 1, x, [40], pt)
+    assert np.array_equal(a, b)
+    # the window really cuts: a NaN at position 33 must reach the output
+    k2[1, pt[0][33 // 16], :, 33 % 16] = float("nan")
+    got, _ = O.layer_step(cfg, HW, synth.HostKV(k2, v2), 1, x, [40], pt)
+    assert np.isnan(got).any()
+
+
+def test_argmax_lowest_index_on_ties():
+    assert O.argmax_lowest([1.0, 3.0, 3.0, 2.0]) == 1
+
+
+# ----------------------------------------------------------------- SoL arithmetic
+
+def _golden(name):
+    import os
+    vals = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                kk, vv = line.split("=")
+                vals[kk.strip()] = float(vv)
+    return vals
+
+
+def test_sol_arithmetic_reproduces_the_pages_h100_numbers():
+    from persistent_moe_decode_cta_gb300 import sol
+    g = _golden("sol_h100.txt")
+    nbytes = g["weight_bytes"] + g["kv_bytes_8k"]
+    assert abs(nbytes - g["bytes_per_token"]) < 1e-9 * nbytes
+    tok = sol.sol_tok_s(nbytes, g["hbm_bytes_per_s"])
+    assert abs(tok - g["sol_tok_s"]) / g["sol_tok_s"] < 0.01
+    assert round(1e3 * sol.sol_seconds(nbytes, g["hbm_bytes_per_s"]), 1) == g["floor_ms"]
+    assert round(100 * g["megakernel_tok_s"] / g["sol_tok_s"]) == g["megakernel_pct_of_sol"]
+    assert round(100 * g["vllm_tok_s"] / g["sol_tok_s"]) == g["vllm_pct_of_sol"]
+    assert round(1e3 / g["vllm_tok_s"], 1) == g["vllm_ms_per_step"]
+    assert round(1e3 / g["megakernel_tok_s"], 1) == g["megakernel_ms_per_step"]
+    floor = g["floor_ms"]
+    assert round(g["vllm_ms_per_step"] - floor, 1) == g["vllm_ms_above_floor"]
+    assert round(g["megakernel_ms_per_step"] - floor, 1) == g["megakernel_ms_above_floor"]
+    closed = g["vllm_ms_per_step"] - g["megakernel_ms_per_step"]
+    assert round(closed, 1) == g["gap_closed_ms"]
+    assert abs(100 * closed / g["vllm_ms_above_floor"] - g["gap_closed_pct"]) < 2
+    assert round(g["megakernel_tok_s"] / g["vllm_tok_s"], 2) == g["speedup"]
+
+
+def test_param_counts_of_the_pages_scale_model():
+    from persistent_moe_decode_cta_gb300 import sol
+    g = _golden("sol_h100.txt")
+    pc = sol.param_counts(synth.MODELS["pages"])
+    assert pc["total"] == 30_532_012_032
+    # the pages round down: "30B" total, "3.3B" active (the full embedding table counted)
+    assert int(pc["total"] / 1e9) == int(g["total_params"] / 1e9)
+    assert int(pc["active_with_embedding"] / 1e8) == int(g["active_params"] / 1e8)
+    assert pc["active_step"] == 3_041_757_184
+
+
+def test_step_bytes_pages_b1_8k():
+    from persistent_moe_decode_cta_gb300 import sol
+    cfg = synth.model_config("pages_b1_8k")
+    sb = sol.step_bytes(cfg, [8192], [8] * 48)
+    assert sb["kv"] == 48 * 8192 * 2 * 4 * 128 * 2
+    assert abs(sb["weights"] - 6.0835e9) < 1e6
