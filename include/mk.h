@@ -1,0 +1,199 @@
+/*
+ * mk.h -- C ABI of the persistent MoE decode megakernel (libmk.so).
+ *
+ * One call to mk_decode_step() runs one batched decode step of a parallel-block
+ * mixture-of-experts transformer as ONE persistent kernel launch: one CTA per SM
+ * walks a host-built list of 32-int32 task descriptors, waits on and signals
+ * atomic counters in global memory, and claims attention and expert tiles whose
+ * number depends on live sequence lengths and routing from atomic work queues.
+ *   [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "One kernel for
+ *    the full decode step", "The calling convention that makes it hand-writable",
+ *    "Scheduling: mostly static, selectively dynamic";
+ *    Cohere open-sources fused LLM decode kernel with 1.58x vLLM claim: the 16 task
+ *    types and the 32-int32 descriptor.]
+ *
+ * Conventions for every call:
+ *   - Returns an mk_status code; nothing throws across the ABI.  mk_last_error()
+ *     gives a message for the last failing call on a handle.
+ *   - "device pointer" arguments are CUDA device addresses on the handle's device;
+ *     "host pointer" arguments are ordinary host memory.  `stream` is a
+ *     cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Errors raised inside the kernel (timeouts of a dependency wait, a page id or
+ *     token outside its range) are recorded in a device error word and surface at
+ *     the next mk_get_status().  Such a step's outputs are not valid.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mk_status {
+  MK_OK = 0,
+  MK_ERR_INVALID = 1,      /* bad argument (null pointer, size out of range)        */
+  MK_ERR_UNSUPPORTED = 2,  /* shape the kernels do not handle (see mk_create)       */
+  MK_ERR_CUDA = 3,         /* a CUDA runtime call failed                           */
+  MK_ERR_OOM = 4,          /* device allocation failed                             */
+  MK_ERR_TIMEOUT = 5,      /* a dependency wait inside the kernel gave up          */
+  MK_ERR_BAD_PAGE = 6,     /* a page-table entry was outside [0, n_pages)          */
+  MK_ERR_BAD_TOKEN = 7,    /* a token id was outside [0, vocab)                    */
+  MK_ERR_STATE = 8         /* call out of order (e.g. decode before mk_plan)       */
+} mk_status;
+
+/* Model shape.  The kernels need: head_dim in {32, 64, 128}; d_model, d_ff and
+ * (n_q_heads / n_kv_heads) * head_dim multiples of 128; n_q_heads divisible by
+ * n_kv_heads with a group of at most 8 query heads and group*head_dim <= 1024;
+ * n_experts <= 256; top_k <= 8; page_size == 16; max_batch <= 8; n_layers <= 64.
+ * swa_layer_mask bit l set = layer l uses a sliding window of sliding_window keys
+ * (the window holds the new token and the sliding_window - 1 keys before it).
+ * timeout_ms bounds every dependency wait inside the kernel (0 = 2000 ms). */
+typedef struct mk_config {
+  int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim;
+  int32_t n_experts, top_k, d_ff, vocab, page_size, max_batch;
+  int32_t sliding_window;
+  uint64_t swa_layer_mask;
+  float rope_theta, rms_eps;
+  int32_t timeout_ms;
+} mk_config;
+
+/* Model weights, all bf16 DEVICE pointers, row-major [out][in]:
+ *   embed, lm_head     [vocab][d_model]
+ *   final_norm         [d_model]
+ *   attn_norm[l]       [d_model]                      (host array of n_layers ptrs)
+ *   wq[l] [Hq*hd][d]   wk[l], wv[l] [Hkv*hd][d]       wo[l] [d][Hq*hd]
+ *   router[l]          [n_experts][d]
+ *   w_gate[l*E+e], w_up[l*E+e] [d_ff][d];  w_down[l*E+e] [d][d_ff]
+ * The arrays of pointers are HOST arrays.  mk_create copies everything into a
+ * handle-owned packed blob, so the caller may free its tensors afterwards. */
+typedef struct mk_weights {
+  const void* embed;
+  const void* lm_head;
+  const void* final_norm;
+  const void* const* attn_norm;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* router;
+  const void* const* w_gate;
+  const void* const* w_up;
+  const void* const* w_down;
+} mk_weights;
+
+typedef struct mk_handle mk_handle;
+
+/* Error details read back by mk_get_status(). */
+typedef struct mk_error_info {
+  int32_t code;      /* mk_status of the first device-side error, MK_OK if none  */
+  int32_t task;      /* descriptor index that raised it (-1 if not a task)       */
+  int32_t counter;   /* counter index waited on (timeouts)                       */
+  int32_t observed;  /* counter value seen at the timeout, or the bad id         */
+  int32_t target;    /* value waited for                                         */
+  int32_t sm;        /* CTA index                                                */
+} mk_error_info;
+
+/* Create a handle on the current CUDA device: validate `cfg`, allocate the packed
+ * weight blob and repack every matrix into per-tile, MMA-fragment-ordered tiles
+ * (see DESIGN.md "Weight packing").  `stream` orders the packing kernels; the call
+ * synchronises it before returning.  On error *out is NULL. */
+int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle** out);
+
+/* Build the task plan for a batch: per-SM descriptor lists, counter targets and
+ * the buffers of a step.  Called when the batch composition changes, not per step.
+ *   batch              1..max_batch
+ *   seq_lens_host      HOST int32[batch], cached tokens per sequence (the next
+ *                      step writes the new token at this position)
+ *   page_table_dev     DEVICE int32[batch][max_pages_per_seq]: physical page of
+ *                      logical page j of sequence b; entries past the sequence's
+ *                      length may be -1.  Must stay valid while the plan is used.
+ *   n_pages            pages in the caller's K/V pools
+ * The step reads seq_lens from a device copy that mk_decode_step advances by one
+ * after each step (unless mk_set_fixed(h, 1)). */
+int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host,
+            const int32_t* page_table_dev, int max_pages_per_seq, int n_pages);
+
+/* One decode step as ONE kernel launch on `stream` (asynchronous).
+ *   tokens_dev  DEVICE int32[batch]        input token per sequence
+ *   k_cache, v_cache  DEVICE bf16 [n_layers][n_pages][n_kv_heads][16][head_dim],
+ *               caller-owned; the step writes the new token's K/V into slot
+ *               seq_len % 16 of page page_table[b][seq_len / 16] of every layer
+ *               and attends over positions 0..seq_len (inclusive).
+ *   logits_dev  DEVICE float[batch][vocab] output. */
+int mk_decode_step(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void* v_cache,
+                   float* logits_dev, void* stream);
+
+/* The same step with HOST token and logit buffers: copies tokens host->device,
+ * runs mk_decode_step, copies logits device->host and synchronises `stream`.
+ * tokens_host int32[batch]; logits_host float[batch][vocab]. */
+int mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, void* k_cache,
+                        void* v_cache, float* logits_host, void* stream);
+
+/* The same step with the same device routines run as one kernel launch per
+ * opcode wave per layer (use_graph = 0), or that launch sequence captured once
+ * into a CUDA graph and replayed (use_graph = 1).  Measurement baselines. */
+int mk_decode_step_perop(mk_handle* h, const int32_t* tokens_dev, void* k_cache,
+                         void* v_cache, float* logits_dev, void* stream, int use_graph);
+
+/* Synchronise the handle's last stream and report the device error word; clears
+ * it.  Returns info->code. */
+int mk_get_status(mk_handle* h, mk_error_info* info);
+
+/* fixed = 1: steps do not advance seq_lens (repeated steps move identical bytes). */
+int mk_set_fixed(mk_handle* h, int fixed);
+
+/* Debug/inspection reads into HOST memory (synchronising).  `what`:
+ *   MK_READ_HIDDEN   float [n_layers+1][batch][d_model] residual entering each layer
+ *                    (index n_layers = input of the final norm)
+ *   MK_READ_ROUTES   int32 [n_layers][batch][top_k] selected experts
+ *   MK_READ_ROUTE_W  float [n_layers][batch][top_k] their softmax weights
+ *   MK_READ_ACTIVE   int32 [n_layers][1 + max_active*(2 + batch)]: per layer
+ *                    n_active, then per active slot: expert id, token count, and
+ *                    `batch` entries b*16 + j (token b, selection slot j)
+ *   MK_READ_SEQ_LENS int32 [batch]
+ *   MK_READ_COUNTERS uint32[n_counters] (all zero between steps)
+ *   MK_READ_ROUTER_LOGITS float [n_layers][batch][n_experts]
+ * `bytes` must equal the size of the requested array. */
+enum {
+  MK_READ_HIDDEN = 1, MK_READ_ROUTES = 2, MK_READ_ROUTE_W = 3, MK_READ_ACTIVE = 4,
+  MK_READ_SEQ_LENS = 5, MK_READ_COUNTERS = 6, MK_READ_ROUTER_LOGITS = 7
+};
+int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
+
+/* Integer facts about a handle/plan.  `what`: */
+enum {
+  MK_Q_NUM_SMS = 1, MK_Q_NUM_TASKS = 2, MK_Q_NUM_COUNTERS = 3, MK_Q_PACKED_BYTES = 4,
+  MK_Q_MAX_ACTIVE = 5, MK_Q_SPLIT_PAGES = 6, MK_Q_SMEM_BYTES = 7, MK_Q_PEROP_LAUNCHES = 8,
+  MK_Q_THREADS = 9, MK_Q_STAGE_BYTES = 10, MK_Q_NUM_STAGES = 11
+};
+int mk_query(mk_handle* h, int what, int64_t* out);
+
+/* Host-only planner run (no device needed): the descriptor table and the per-SM
+ * lists that mk_plan would build for `n_sms` SMs, for tests of the schedule.
+ *   tasks_out   int32[cap_tasks][32]      sm_off_out int32[n_sms + 1]
+ *   sm_list_out int32[cap_list]           info_out int32[16]: n_tasks, list
+ *   length, n_counters, max_active, split_pages, T_up, T_dn, rows per O-proj,
+ *   expert-down and up task, QKV tasks per group, router tasks, counter bases
+ *   (see DESIGN.md "Task descriptor").  Returns MK_ERR_INVALID if a cap is too
+ *   small (info_out[0..1] still hold the sizes needed). */
+int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out,
+                int cap_tasks, int32_t* sm_off_out, int32_t* sm_list_out, int cap_list,
+                int32_t* info_out);
+
+/* Message for the last failing call on h (or the last global failure if h is
+ * NULL).  The string is owned by the library. */
+const char* mk_last_error(mk_handle* h);
+
+/* Free everything the handle owns.  Safe on NULL. */
+void mk_destroy(mk_handle* h);
+
+/* ABI version (increments on any signature change). */
+int mk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

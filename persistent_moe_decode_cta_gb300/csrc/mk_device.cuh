@@ -1,0 +1,199 @@
+// Device primitives for the megakernel: shared-memory carving, mbarriers, bulk and
+// tensor-map copies, global acquire/release counters, MMA and ldmatrix wrappers.
+// Written for sm_103a; only documented PTX forms are used.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "mk.h"
+#include "mk_internal.h"
+
+namespace mk {
+
+// ---------------------------------------------------------------- smem layout
+struct Smem {
+  uint32_t ring;      // shared address of stage 0 (1024-aligned)
+  uint8_t* ring_g;    // generic pointer of stage 0
+  float* scratch;     // kScratchBytes
+  uint32_t scratch_s;
+  int* small;         // kSmallBytes
+  uint32_t bars;      // full[kStages], empty[kStages], mfull[kMbox], mempty[kMbox]
+  int4* mbox;
+
+  __device__ __forceinline__ uint32_t full(uint32_t s) const { return bars + 8u * s; }
+  __device__ __forceinline__ uint32_t empty(uint32_t s) const { return bars + 8u * (kStages + s); }
+  __device__ __forceinline__ uint32_t mfull(uint32_t m) const { return bars + 8u * (2 * kStages + m); }
+  __device__ __forceinline__ uint32_t mempty(uint32_t m) const {
+    return bars + 8u * (2 * kStages + kMbox + m);
+  }
+  __device__ __forceinline__ uint32_t stage(uint32_t seq) const {
+    return ring + (seq % kStages) * (uint32_t)kStageBytes;
+  }
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
+  Smem S;
+  uint32_t base = smem_u32(raw);
+  uint32_t aligned = (base + 1023u) & ~1023u;
+  uint8_t* g = raw + (aligned - base);
+  S.ring = aligned;
+  S.ring_g = g;
+  S.scratch = reinterpret_cast<float*>(g + kStages * kStageBytes);
+  S.scratch_s = aligned + kStages * kStageBytes;
+  S.small = reinterpret_cast<int*>(g + kStages * kStageBytes + kScratchBytes);
+  S.bars = aligned + kStages * kStageBytes + kScratchBytes + kSmallBytes;
+  S.mbox = reinterpret_cast<int4*>(g + kStages * kStageBytes + kScratchBytes + kSmallBytes +
+                                   kBarBytes);
+  return S;
+}
+
+// ---------------------------------------------------------------- timers
+__device__ __forceinline__ uint64_t gtime() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after `limit_ns` without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = gtime();
+  while (!mbar_try_wait(bar, parity)) {
+    if ((long long)(gtime() - t0) > limit_ns) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------- async copies
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- global sync
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_release(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_volatile(const int* p) {
+  return *reinterpret_cast<const volatile int*>(p);
+}
+
+__device__ __forceinline__ void bar_sync_consumers() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
+
+// ---------------------------------------------------------------- loads
+__device__ __forceinline__ float ldg_cg(const float* p) { return __ldcg(p); }
+__device__ __forceinline__ int ldg_cg(const int* p) { return __ldcg(p); }
+__device__ __forceinline__ uint32_t ldg_cg_u32(const void* p) {
+  return __ldcg(reinterpret_cast<const unsigned*>(p));
+}
+__device__ __forceinline__ float2 ldg_cg_f2(const float* p) {
+  return __ldcg(reinterpret_cast<const float2*>(p));
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// ---------------------------------------------------------------- bf16
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint16_t to_bf16(float x) {
+  __nv_bfloat16 v = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&v);
+}
+__device__ __forceinline__ float bf16_to_f(uint16_t u) {
+  return __uint_as_float(static_cast<uint32_t>(u) << 16);
+}
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// ---------------------------------------------------------------- tensor cores
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+}  // namespace mk

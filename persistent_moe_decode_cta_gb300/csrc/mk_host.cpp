@@ -1,0 +1,778 @@
+// Host side of libmk: the C ABI (include/mk.h), shape validation, the weight
+// packer driver, the task planner (static per-SM wave lists + claimer drains),
+// step launches (megakernel, per-op launches, CUDA graph of the per-op launches)
+// and status/debug reads.
+//
+// Planner: per layer the host emits named waves of tasks and deals the static
+// ones round-robin, task k of the step to SM k mod #SM; attention and expert
+// work is left to claimer ("drain") tasks that every SM runs, pulling items from
+// per-layer atomic queues [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on
+// H100, "Scheduling: mostly static, selectively dynamic"; Fuse decode into one
+// megakernel for 1.58x higher H100 throughput: the layer's wave order QKV, router,
+// attention, MoE projections, O-proj].
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "mk.h"
+#include "mk_internal.h"
+
+namespace mk {
+cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, int n_rows_packed,
+                        int n_src_rows, int K, long long ld, int col0, int mode, int hd, cudaStream_t st);
+cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_t st);
+cudaError_t prepare_megakernel();
+int megakernel_occupancy(int* blocks);
+cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                              bool cooperative, cudaStream_t st);
+}  // namespace mk
+
+using namespace mk;
+
+namespace {
+
+thread_local std::string g_err;
+
+// ------------------------------------------------------------------ shapes
+struct Shape {
+  int L, d, Hq, Hkv, hd, E, topk, f, V, gs, nrb_d, max_batch;
+  int r_qkv, qkv_rows_group, qkv_tpg;
+  int r_router, n_router_tasks, e_pad;
+  int r_o, t_o, k_o;
+  int r_up, t_up, r_dn, t_dn;
+  int r_lm, v_pad, n_lm_tasks;
+  size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, up_bytes_e, dn_bytes_e, lm_bytes, embed_bytes;
+  size_t off_qkv, off_o, off_router, off_up, off_dn, off_lm, off_embed, total;
+};
+
+int fail(std::string* dst, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  if (dst) *dst = buf;
+  return code;
+}
+
+int derive_shape(const mk_config* c, Shape& s, std::string* err) {
+  if (!c) return fail(err, MK_ERR_INVALID, "config is NULL");
+  s.L = c->n_layers; s.d = c->d_model; s.Hq = c->n_q_heads; s.Hkv = c->n_kv_heads; s.hd = c->head_dim;
+  s.E = c->n_experts; s.topk = c->top_k; s.f = c->d_ff; s.V = c->vocab; s.max_batch = c->max_batch;
+  if (s.L < 1 || s.L > 64) return fail(err, MK_ERR_UNSUPPORTED, "n_layers %d not in [1, 64]", s.L);
+  if (s.hd != 32 && s.hd != 64 && s.hd != 128) return fail(err, MK_ERR_UNSUPPORTED, "head_dim %d not in {32,64,128}", s.hd);
+  if (s.d < 128 || s.d % 128 || s.d > 2048) return fail(err, MK_ERR_UNSUPPORTED, "d_model %d must be a multiple of 128 <= 2048", s.d);
+  if (s.f < 128 || s.f % 128 || s.f > 2048) return fail(err, MK_ERR_UNSUPPORTED, "d_ff %d must be a multiple of 128 <= 2048", s.f);
+  if (s.Hkv < 1 || s.Hq < 1 || s.Hq % s.Hkv) return fail(err, MK_ERR_UNSUPPORTED, "n_q_heads %d not divisible by n_kv_heads %d", s.Hq, s.Hkv);
+  s.gs = s.Hq / s.Hkv;
+  if (s.gs > 8) return fail(err, MK_ERR_UNSUPPORTED, "query group %d > 8", s.gs);
+  if ((s.gs * s.hd) % 128 || s.gs * s.hd > 1024) return fail(err, MK_ERR_UNSUPPORTED, "group*head_dim %d must be a multiple of 128 <= 1024", s.gs * s.hd);
+  if (s.E < 1 || s.E > 256) return fail(err, MK_ERR_UNSUPPORTED, "n_experts %d not in [1, 256]", s.E);
+  if (s.topk < 1 || s.topk > 8 || s.topk > s.E) return fail(err, MK_ERR_UNSUPPORTED, "top_k %d not in [1, min(8, E)]", s.topk);
+  if (c->page_size != 16) return fail(err, MK_ERR_UNSUPPORTED, "page_size %d != 16", c->page_size);
+  if (s.max_batch < 1 || s.max_batch > kMaxBatch) return fail(err, MK_ERR_UNSUPPORTED, "max_batch %d not in [1, 8]", s.max_batch);
+  if (s.V < 1) return fail(err, MK_ERR_INVALID, "vocab %d", s.V);
+  if (c->sliding_window < 0) return fail(err, MK_ERR_INVALID, "sliding_window %d < 0", c->sliding_window);
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return fail(err, MK_ERR_INVALID, "bad rms_eps / rope_theta");
+  s.nrb_d = s.d / kRowBlock;
+  s.qkv_rows_group = (s.gs + 2) * s.hd;
+  s.r_qkv = (s.qkv_rows_group % 64 == 0) ? 64 : (s.qkv_rows_group % 32 == 0 ? 32 : 16);
+  s.qkv_tpg = s.qkv_rows_group / s.r_qkv;
+  s.r_router = 16;
+  s.e_pad = (s.E + 15) / 16 * 16;
+  s.n_router_tasks = s.e_pad / s.r_router;
+  s.r_o = 64; s.t_o = s.d / s.r_o; s.k_o = s.gs * s.hd;
+  s.r_up = 64; s.t_up = 2 * s.f / s.r_up;
+  s.r_dn = 64; s.t_dn = s.d / s.r_dn;
+  s.r_lm = 64; s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
+  s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
+  s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
+  s.router_layer_bytes = (size_t)s.e_pad * s.d * 2;
+  s.up_bytes_e = (size_t)2 * s.f * s.d * 2;
+  s.dn_bytes_e = (size_t)s.d * s.f * 2;
+  s.lm_bytes = (size_t)s.v_pad * s.d * 2;
+  s.embed_bytes = (size_t)s.V * s.d * 2;
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t r = o; o += (n + 255) / 256 * 256; return r; };
+  s.off_qkv = take(s.qkv_layer_bytes * s.L);
+  s.off_o = take(s.o_layer_bytes * s.L);
+  s.off_router = take(s.router_layer_bytes * s.L);
+  s.off_up = take(s.up_bytes_e * s.E * s.L);
+  s.off_dn = take(s.dn_bytes_e * s.E * s.L);
+  s.off_lm = take(s.lm_bytes);
+  s.off_embed = take(s.embed_bytes);
+  s.total = o;
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------ planner
+enum Wave { W_QKV = 0, W_ROUTER, W_ATT, W_UP, W_DN, W_OPROJ, W_COUNT };
+
+struct PlanOut {
+  int B = 0, maxa = 0, n_sm = 0;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_up, c_rb, c_done, n_ctr;
+  int rb_target;
+  std::vector<int32_t> tasks;     // n_tasks * 32
+  std::vector<int32_t> sm_off;    // n_segs * (n_sm + 1), absolute offsets into sm_list
+  std::vector<int32_t> sm_list;
+  int n_segs = 0;
+  int n_tasks() const { return (int)(tasks.size() / kDescInts); }
+};
+
+bool parse_wave_order(const char* s, std::vector<int>& order) {
+  // letters: q=QKV r=router a=attention u=expert up d=expert down o=O-proj
+  order.clear();
+  for (const char* c = s; *c; ++c) {
+    switch (*c) {
+      case 'q': order.push_back(W_QKV); break;
+      case 'r': order.push_back(W_ROUTER); break;
+      case 'a': order.push_back(W_ATT); break;
+      case 'u': order.push_back(W_UP); break;
+      case 'd': order.push_back(W_DN); break;
+      case 'o': order.push_back(W_OPROJ); break;
+      default: return false;
+    }
+  }
+  if (order.size() != W_COUNT) return false;
+  auto pos = [&](int w) { return (int)(std::find(order.begin(), order.end(), w) - order.begin()); };
+  for (int w = 0; w < W_COUNT; ++w) if (pos(w) >= W_COUNT) return false;
+  // every order that respects the dependencies is deadlock-free with in-order lists
+  return pos(W_QKV) < pos(W_ATT) && pos(W_ATT) < pos(W_OPROJ) && pos(W_ROUTER) < pos(W_UP) &&
+         pos(W_UP) < pos(W_DN);
+}
+
+int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, PlanOut& P, std::string* err) {
+  if (B < 1 || B > s.max_batch) return fail(err, MK_ERR_INVALID, "batch %d not in [1, %d]", B, s.max_batch);
+  if (n_sm < 1) return fail(err, MK_ERR_INVALID, "n_sms %d", n_sm);
+  P = PlanOut();
+  P.B = B; P.n_sm = n_sm;
+  P.maxa = std::min(s.E, B * s.topk);
+  const int L = s.L;
+  int c = 0;
+  P.c_lr = c; c += L + 1;
+  P.c_qkvg = c; c += L * s.Hkv;
+  P.c_rt = c; c += L;
+  P.c_rr = c; c += L;
+  P.c_att = c; c += L * B * s.Hkv;
+  P.c_og = c; c += L * s.Hkv;
+  P.c_up = c; c += L * P.maxa;
+  P.c_rb = c; c += L * s.nrb_d;
+  P.c_done = c; c += 1;
+  P.n_ctr = c;
+  P.rb_target = s.Hkv * (kRowBlock / s.r_o) + P.maxa * (kRowBlock / s.r_dn);
+
+  auto add = [&](int op, int layer, int aux, int row0, int nrows, int k0, int klen, int wc, int wt, int sc,
+                 int st, size_t woff, int wbytes, int wave) {
+    const int id = P.n_tasks();
+    P.tasks.resize(P.tasks.size() + kDescInts, 0);
+    int32_t* T = &P.tasks[(size_t)id * kDescInts];
+    T[D_OP] = op; T[D_LAYER] = layer; T[D_AUX] = aux; T[D_ROW0] = row0; T[D_NROWS] = nrows;
+    T[D_K0] = k0; T[D_KLEN] = klen; T[D_WAIT_CTR] = wc; T[D_WAIT_TARGET] = wt; T[D_SIG_CTR] = sc;
+    T[D_SIG_TARGET] = st; T[D_WOFF_LO] = (int32_t)(uint32_t)(woff & 0xffffffffull);
+    T[D_WOFF_HI] = (int32_t)(uint32_t)(woff >> 32); T[D_WBYTES] = wbytes; T[D_QUEUE] = -1;
+    T[D_TASK_ID] = id; T[D_WAVE] = wave;
+    return id;
+  };
+
+  // ---- descriptors
+  const int t_embed = add(OP_EMBED, 0, 0, 0, 0, 0, 0, -1, 0, P.c_lr + 0, s.nrb_d, 0, 0, -1);
+  std::vector<std::vector<int>> waves((size_t)L * W_COUNT);
+  std::vector<int> drains((size_t)L * W_COUNT, -1);
+  for (int l = 0; l < L; ++l) {
+    auto& wq = waves[(size_t)l * W_COUNT + W_QKV];
+    for (int g = 0; g < s.Hkv; ++g)
+      for (int t = 0; t < s.qkv_tpg; ++t)
+        wq.push_back(add(OP_QKV, l, g, t * s.r_qkv, s.r_qkv, 0, s.d, P.c_lr + l, s.nrb_d,
+                         P.c_qkvg + l * s.Hkv + g, s.qkv_tpg,
+                         s.off_qkv + l * s.qkv_layer_bytes + (size_t)g * s.qkv_rows_group * s.d * 2 +
+                             (size_t)t * s.r_qkv * s.d * 2,
+                         s.r_qkv * s.d * 2, W_QKV));
+    auto& wr = waves[(size_t)l * W_COUNT + W_ROUTER];
+    for (int t = 0; t < s.n_router_tasks; ++t)
+      wr.push_back(add(OP_ROUTER, l, 0, t * s.r_router, s.r_router, 0, s.d, P.c_lr + l, s.nrb_d, P.c_rt + l,
+                       s.n_router_tasks, s.off_router + l * s.router_layer_bytes + (size_t)t * s.r_router * s.d * 2,
+                       s.r_router * s.d * 2, W_ROUTER));
+    drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
+    drains[(size_t)l * W_COUNT + W_UP] = add(OP_UP_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, -1, 0, 0, 0, W_UP);
+    drains[(size_t)l * W_COUNT + W_DN] = add(OP_DN_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, -1, 0, 0, 0, W_DN);
+    auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
+    for (int g = 0; g < s.Hkv; ++g)
+      for (int t = 0; t < s.t_o; ++t)
+        wo.push_back(add(OP_OPROJ, l, g, t * s.r_o, s.r_o, g * s.k_o, s.k_o, P.c_og + l * s.Hkv + g, B,
+                         P.c_rb + l * s.nrb_d + (t * s.r_o) / kRowBlock, P.rb_target,
+                         s.off_o + l * s.o_layer_bytes + (size_t)g * s.d * s.k_o * 2 + (size_t)t * s.r_o * s.k_o * 2,
+                         s.r_o * s.k_o * 2, W_OPROJ));
+  }
+  std::vector<int> lm;
+  for (int t = 0; t < s.n_lm_tasks; ++t)
+    lm.push_back(add(OP_LMHEAD, L, 0, t * s.r_lm, s.r_lm, 0, s.d, P.c_lr + L, s.nrb_d, -1, 0,
+                     s.off_lm + (size_t)t * s.r_lm * s.d * 2, s.r_lm * s.d * 2, -1));
+
+  // ---- segments
+  auto emit_segment = [&](const std::vector<std::vector<int>>& lists) {
+    int o = (int)P.sm_list.size();
+    for (int sm = 0; sm < n_sm; ++sm) {
+      P.sm_off.push_back(o);
+      for (int t : lists[sm]) P.sm_list.push_back(t);
+      o += (int)lists[sm].size();
+    }
+    P.sm_off.push_back(o);
+    P.n_segs++;
+  };
+  auto is_drain = [](int w) { return w == W_ATT || w == W_UP || w == W_DN; };
+  // segment 0: the whole step for the megakernel
+  {
+    std::vector<std::vector<int>> lists(n_sm);
+    lists[0].push_back(t_embed);
+    long long cursor = 0;
+    for (int l = 0; l < L; ++l)
+      for (int w : order) {
+        if (is_drain(w)) {
+          for (int sm = 0; sm < n_sm; ++sm) lists[sm].push_back(drains[(size_t)l * W_COUNT + w]);
+        } else {
+          for (int t : waves[(size_t)l * W_COUNT + w]) lists[cursor++ % n_sm].push_back(t);
+        }
+      }
+    for (int t : lm) lists[cursor++ % n_sm].push_back(t);
+    emit_segment(lists);
+  }
+  // segments 1..: one launch per wave per layer (embed first, LM head last)
+  {
+    std::vector<std::vector<int>> lists(n_sm);
+    lists[0].push_back(t_embed);
+    emit_segment(lists);
+    for (int l = 0; l < L; ++l)
+      for (int w : order) {
+        std::vector<std::vector<int>> ls(n_sm);
+        if (is_drain(w)) {
+          for (int sm = 0; sm < n_sm; ++sm) ls[sm].push_back(drains[(size_t)l * W_COUNT + w]);
+        } else {
+          long long cur = 0;
+          for (int t : waves[(size_t)l * W_COUNT + w]) ls[cur++ % n_sm].push_back(t);
+        }
+        emit_segment(ls);
+      }
+    std::vector<std::vector<int>> ll(n_sm);
+    long long cur = 0;
+    for (int t : lm) ll[cur++ % n_sm].push_back(t);
+    emit_segment(ll);
+  }
+  return MK_OK;
+}
+
+int choose_split_pages(int max_pages) {
+  // about 32 splits per (sequence, group) at the longest context, in whole 8-page
+  // ring stages, at least one stage
+  int sp = (max_pages + 31) / 32;
+  sp = (sp + 7) / 8 * 8;
+  return std::max(8, sp);
+}
+
+const char* default_order() { return "qraudo"; }
+
+}  // namespace
+
+// ------------------------------------------------------------------ handle
+struct mk_handle {
+  mk_config cfg;
+  Shape s;
+  int dev = 0, n_sm = 0;
+  std::string err;
+  uint8_t* wblob = nullptr;
+  float* norms = nullptr;  // attn [L][d] then final [d]
+  // plan
+  bool planned = false;
+  PlanOut P;
+  int B = 0, max_pages = 0, n_pages = 0, split_pages = 0, max_items_bg = 0;
+  const int32_t* page_table = nullptr;
+  std::vector<void*> bufs;  // plan allocations
+  int32_t *d_tasks = nullptr, *d_sm_off = nullptr, *d_sm_list = nullptr;
+  Params prm{};
+  int32_t* d_tokens = nullptr;
+  float* d_logits = nullptr;
+  int fixed = 0;
+  cudaStream_t last_stream = nullptr;
+  // tensor maps
+  CUtensorMap tmK{}, tmV{};
+  void *tm_k = nullptr, *tm_v = nullptr;
+  // graph of the per-op launches
+  cudaGraphExec_t graph = nullptr;
+  const void* g_key[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  int g_fixed = -1;
+};
+
+namespace {
+
+int cuda_fail(mk_handle* h, cudaError_t e, const char* what) {
+  return fail(h ? &h->err : nullptr, MK_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CK(h, call)                                              \
+  do {                                                           \
+    cudaError_t _e = (call);                                     \
+    if (_e != cudaSuccess) return cuda_fail((h), _e, #call);     \
+  } while (0)
+
+void free_plan(mk_handle* h) {
+  for (void* p : h->bufs) cudaFree(p);
+  h->bufs.clear();
+  if (h->graph) { cudaGraphExecDestroy(h->graph); h->graph = nullptr; }
+  h->planned = false;
+  h->tm_k = h->tm_v = nullptr;
+}
+
+template <class T>
+int alloc(mk_handle* h, T** p, size_t count) {
+  void* q = nullptr;
+  const size_t bytes = std::max<size_t>(count * sizeof(T), 16);
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) return fail(&h->err, MK_ERR_OOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  e = cudaMemset(q, 0, bytes);
+  if (e != cudaSuccess) { cudaFree(q); return cuda_fail(h, e, "cudaMemset"); }
+  h->bufs.push_back(q);
+  *p = static_cast<T*>(q);
+  return MK_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D view of a K or V pool: rows = (layer, page, kv head, token), columns = head dim.
+int encode_kv_map(mk_handle* h, CUtensorMap* tm, void* base) {
+  auto fn = get_encode();
+  if (!fn) return fail(&h->err, MK_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const Shape& s = h->s;
+  const cuuint64_t rows = (cuuint64_t)s.L * h->n_pages * s.Hkv * 16;
+  const int inner = s.hd < 64 ? s.hd : 64;
+  cuuint64_t dims[2] = {(cuuint64_t)s.hd, rows};
+  cuuint64_t strides[1] = {(cuuint64_t)s.hd * 2};
+  cuuint32_t box[2] = {(cuuint32_t)inner, 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  inner == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(&h->err, MK_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return MK_OK;
+}
+
+int prepare_step(mk_handle* h, const int32_t* tokens, void* k, void* v, float* logits) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
+  if (!tokens || !k || !v || !logits) return fail(&h->err, MK_ERR_INVALID, "NULL step pointer");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return fail(&h->err, MK_ERR_INVALID, "K/V pools must be 16-byte aligned");
+  CK(h, cudaSetDevice(h->dev));
+  if (k != h->tm_k) { int r = encode_kv_map(h, &h->tmK, k); if (r) return r; h->tm_k = k; }
+  if (v != h->tm_v) { int r = encode_kv_map(h, &h->tmV, v); if (r) return r; h->tm_v = v; }
+  Params& p = h->prm;
+  p.tokens = tokens;
+  p.kc = static_cast<uint16_t*>(k);
+  p.vc = static_cast<uint16_t*>(v);
+  p.logits = logits;
+  p.fixed = h->fixed;
+  return MK_OK;
+}
+
+int launch_segment(mk_handle* h, int seg, bool cooperative, bool reset, cudaStream_t st) {
+  Params p = h->prm;
+  p.sm_off = h->d_sm_off + (size_t)seg * (h->n_sm + 1);
+  p.do_reset = reset ? 1 : 0;
+  cudaError_t e = launch_megakernel(p, h->tmK, h->tmV, h->n_sm, cooperative, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch");
+  return MK_OK;
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" {
+
+int mk_version(void) { return 1; }
+
+const char* mk_last_error(mk_handle* h) { return h ? h->err.c_str() : g_err.c_str(); }
+
+int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle** out) {
+  if (!out) return fail(nullptr, MK_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  Shape s;
+  int r = derive_shape(cfg, s, nullptr);
+  if (r) return r;
+  if (!w || !w->embed || !w->lm_head || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv ||
+      !w->wo || !w->router || !w->w_gate || !w->w_up || !w->w_down)
+    return fail(nullptr, MK_ERR_INVALID, "weights struct has a NULL member");
+  for (int l = 0; l < s.L; ++l)
+    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->router[l])
+      return fail(nullptr, MK_ERR_INVALID, "NULL weight pointer at layer %d", l);
+  for (int i = 0; i < s.L * s.E; ++i)
+    if (!w->w_gate[i] || !w->w_up[i] || !w->w_down[i])
+      return fail(nullptr, MK_ERR_INVALID, "NULL expert pointer at index %d", i);
+
+  mk_handle* h = new mk_handle();
+  h->cfg = *cfg;
+  if (h->cfg.timeout_ms <= 0) h->cfg.timeout_ms = 2000;
+  h->s = s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto bail = [&](int code) { *out = nullptr; mk_destroy(h); return code; };
+  cudaError_t e = cudaGetDevice(&h->dev);
+  if (e != cudaSuccess) { cuda_fail(h, e, "cudaGetDevice"); return bail(MK_ERR_CUDA); }
+  e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->dev);
+  if (e != cudaSuccess) { cuda_fail(h, e, "cudaDeviceGetAttribute"); return bail(MK_ERR_CUDA); }
+  int smem_optin = 0;
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->dev);
+  if (smem_optin < kSmemBytes) {
+    fail(&h->err, MK_ERR_UNSUPPORTED, "device allows %d B shared memory per block, kernel needs %d", smem_optin, kSmemBytes);
+    return bail(MK_ERR_UNSUPPORTED);
+  }
+  e = prepare_megakernel();
+  if (e != cudaSuccess) { cuda_fail(h, e, "cudaFuncSetAttribute"); return bail(MK_ERR_CUDA); }
+  e = cudaMalloc(&h->wblob, s.total);
+  if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "packed weights (%zu B): %s", s.total, cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
+  e = cudaMalloc(&h->norms, sizeof(float) * ((size_t)s.L * s.d + s.d));
+  if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "norms: %s", cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
+
+  // ---- pack
+  const int L = s.L, d = s.d, hd = s.hd, gs = s.gs, f = s.f, E = s.E;
+#define PK(...)                                                          \
+  do {                                                                   \
+    cudaError_t _e = launch_pack(__VA_ARGS__, st);                       \
+    if (_e != cudaSuccess) { cuda_fail(h, _e, "pack"); return bail(MK_ERR_CUDA); } \
+  } while (0)
+  for (int l = 0; l < L; ++l) {
+    uint8_t* q = h->wblob + s.off_qkv + l * s.qkv_layer_bytes;
+    for (int g = 0; g < s.Hkv; ++g) {
+      uint8_t* grp = q + (size_t)g * s.qkv_rows_group * d * 2;
+      const uint16_t* wq = static_cast<const uint16_t*>(w->wq[l]) + (size_t)g * gs * hd * d;
+      const uint16_t* wk = static_cast<const uint16_t*>(w->wk[l]) + (size_t)g * hd * d;
+      const uint16_t* wv = static_cast<const uint16_t*>(w->wv[l]) + (size_t)g * hd * d;
+      PK(grp, wq, nullptr, gs * hd, gs * hd, d, d, 0, PACK_ROPE, hd);
+      PK(grp + (size_t)gs * hd * d * 2, wk, nullptr, hd, hd, d, d, 0, PACK_ROPE, hd);
+      PK(grp + (size_t)(gs + 1) * hd * d * 2, wv, nullptr, hd, hd, d, d, 0, PACK_ROPE, hd);
+    }
+    uint8_t* o = h->wblob + s.off_o + l * s.o_layer_bytes;
+    for (int g = 0; g < s.Hkv; ++g)
+      PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o, PACK_IDENT, hd);
+    PK(h->wblob + s.off_router + l * s.router_layer_bytes, w->router[l], nullptr, s.e_pad, E, d, d, 0, PACK_IDENT, hd);
+    for (int e2 = 0; e2 < E; ++e2) {
+      const int i = l * E + e2;
+      PK(h->wblob + s.off_up + (size_t)i * s.up_bytes_e, w->w_gate[i], w->w_up[i], 2 * f, f, d, d, 0, PACK_GATE_UP, hd);
+      PK(h->wblob + s.off_dn + (size_t)i * s.dn_bytes_e, w->w_down[i], nullptr, d, d, f, f, 0, PACK_IDENT, hd);
+    }
+    e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
+    if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
+  }
+  PK(h->wblob + s.off_lm, w->lm_head, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, hd);
+#undef PK
+  e = launch_convert(h->norms + (size_t)L * d, w->final_norm, d, st);
+  if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
+  e = cudaMemcpyAsync(h->wblob + s.off_embed, w->embed, s.embed_bytes, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) { cuda_fail(h, e, "embed copy"); return bail(MK_ERR_CUDA); }
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) { cuda_fail(h, e, "pack sync"); return bail(MK_ERR_CUDA); }
+  *out = h;
+  return MK_OK;
+}
+
+int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, int cap_tasks,
+                int32_t* sm_off_out, int32_t* sm_list_out, int cap_list, int32_t* info_out) {
+  Shape s;
+  int r = derive_shape(cfg, s, nullptr);
+  if (r) return r;
+  std::vector<int> order;
+  parse_wave_order(default_order(), order);
+  PlanOut P;
+  r = build_plan(s, batch, n_sms, order, P, nullptr);
+  if (r) return r;
+  const int list_len = P.sm_off[n_sms];  // segment 0 only
+  if (info_out) {
+    int32_t* I = info_out;
+    I[0] = P.n_tasks(); I[1] = list_len; I[2] = P.n_ctr; I[3] = P.maxa; I[4] = 0;
+    I[5] = s.t_up; I[6] = s.t_dn; I[7] = s.r_o; I[8] = s.r_dn; I[9] = s.r_up; I[10] = s.qkv_tpg;
+    I[11] = s.n_router_tasks; I[12] = P.rb_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
+  }
+  if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
+    return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
+  std::memcpy(tasks_out, P.tasks.data(), P.tasks.size() * sizeof(int32_t));
+  std::memcpy(sm_off_out, P.sm_off.data(), (n_sms + 1) * sizeof(int32_t));
+  std::memcpy(sm_list_out, P.sm_list.data(), list_len * sizeof(int32_t));
+  return MK_OK;
+}
+
+int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t* page_table_dev,
+            int max_pages_per_seq, int n_pages) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (!seq_lens_host || !page_table_dev) return fail(&h->err, MK_ERR_INVALID, "NULL seq_lens or page table");
+  if (max_pages_per_seq < 1 || n_pages < 1) return fail(&h->err, MK_ERR_INVALID, "max_pages_per_seq/n_pages < 1");
+  const Shape& s = h->s;
+  if (batch < 1 || batch > s.max_batch) return fail(&h->err, MK_ERR_INVALID, "batch %d not in [1, %d]", batch, s.max_batch);
+  for (int b = 0; b < batch; ++b)
+    if (seq_lens_host[b] < 0 || seq_lens_host[b] >= max_pages_per_seq * 16)
+      return fail(&h->err, MK_ERR_INVALID, "seq_len[%d] = %d does not fit %d pages", b, seq_lens_host[b], max_pages_per_seq);
+  if ((long long)s.L * n_pages * s.Hkv * 16 >= (1ll << 31))
+    return fail(&h->err, MK_ERR_UNSUPPORTED, "K/V pool too large for 32-bit row coordinates");
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaDeviceSynchronize());
+  free_plan(h);
+  std::vector<int> order;
+  const char* env = getenv("MK_WAVE_ORDER");
+  if (!parse_wave_order(env && *env ? env : default_order(), order))
+    return fail(&h->err, MK_ERR_INVALID, "bad wave order '%s'", env ? env : "");
+  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err);
+  if (r) return r;
+  int occ = 0;
+  megakernel_occupancy(&occ);
+  if (occ < 1) return fail(&h->err, MK_ERR_UNSUPPORTED, "megakernel cannot be resident (occupancy %d)", occ);
+  PlanOut& P = h->P;
+  h->B = batch;
+  h->max_pages = max_pages_per_seq;
+  h->n_pages = n_pages;
+  h->page_table = page_table_dev;
+  h->split_pages = choose_split_pages(max_pages_per_seq);
+  if (const char* sp = getenv("MK_SPLIT_PAGES")) { int v = atoi(sp); if (v >= 8 && v % 8 == 0) h->split_pages = v; }
+  h->max_items_bg = (max_pages_per_seq + h->split_pages - 1) / h->split_pages + 1;
+
+  Params& p = h->prm;
+  p = Params{};
+  const int L = s.L, B = batch;
+  p.L = L; p.d = s.d; p.Hq = s.Hq; p.Hkv = s.Hkv; p.hd = s.hd; p.E = s.E; p.topk = s.topk; p.f = s.f;
+  p.V = s.V; p.gs = s.gs; p.nrb_d = s.nrb_d; p.B = B; p.maxa = P.maxa;
+  p.max_pages = max_pages_per_seq; p.n_pages = n_pages; p.window = h->cfg.sliding_window;
+  p.swa_mask = h->cfg.swa_layer_mask; p.theta = h->cfg.rope_theta; p.eps = h->cfg.rms_eps;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.hd));
+  p.split_pages = h->split_pages; p.max_items_bg = h->max_items_bg;
+  p.r_up = s.r_up; p.r_dn = s.r_dn; p.t_up = s.t_up; p.t_dn = s.t_dn; p.qkv_tpg = s.qkv_tpg;
+  p.n_router_tasks = s.n_router_tasks;
+  p.timeout_ns = (long long)h->cfg.timeout_ms * 1000000ll;
+  p.wblob = h->wblob; p.off_up = (long long)s.off_up; p.off_dn = (long long)s.off_dn;
+  p.up_bytes_e = (long long)s.up_bytes_e; p.dn_bytes_e = (long long)s.dn_bytes_e;
+  p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
+  p.embed = reinterpret_cast<const uint16_t*>(h->wblob + s.off_embed);
+  p.page_table = page_table_dev;
+  const size_t maxa = (size_t)P.maxa;
+#define AL(ptr, n) do { int _r = alloc(h, &(ptr), (n)); if (_r) { free_plan(h); return _r; } } while (0)
+  AL(p.seq_lens, B);
+  AL(p.X, (size_t)(L + 1) * B * s.d);
+  AL(p.SS, (size_t)(L + 1) * s.nrb_d * B);
+  AL(p.Q, (size_t)L * B * s.Hq * s.hd);
+  AL(p.attp, (size_t)L * s.Hkv * B * h->max_items_bg * s.gs * (s.hd + 2));
+  AL(p.atto, (size_t)L * B * s.Hq * s.hd);
+  AL(p.opart, (size_t)L * s.Hkv * B * s.d);
+  AL(p.rlog, (size_t)L * B * s.E);
+  AL(p.ridx, (size_t)L * B * s.topk);
+  AL(p.rw, (size_t)L * B * s.topk);
+  AL(p.active, (size_t)L * maxa);
+  AL(p.nact, (size_t)L);
+  AL(p.act_cnt, (size_t)L * maxa);
+  AL(p.act_tok, (size_t)L * maxa * B);
+  AL(p.aup, (size_t)L * maxa * B * s.f);
+  AL(p.Y, (size_t)L * B * s.topk * s.d);
+  AL(p.ctr, (size_t)P.n_ctr);
+  AL(p.qhead, (size_t)3 * L);
+  AL(p.qcount, (size_t)3 * L);
+  AL(p.err, 16);
+  AL(h->d_tasks, P.tasks.size());
+  AL(h->d_sm_off, P.sm_off.size());
+  AL(h->d_sm_list, P.sm_list.size());
+  AL(h->d_tokens, B);
+  AL(h->d_logits, (size_t)B * s.V);
+#undef AL
+  p.c_lr = P.c_lr; p.c_qkvg = P.c_qkvg; p.c_rt = P.c_rt; p.c_rr = P.c_rr; p.c_att = P.c_att; p.c_og = P.c_og;
+  p.c_up = P.c_up; p.c_rb = P.c_rb; p.c_done = P.c_done; p.n_ctr = P.n_ctr; p.n_queues = 3 * L;
+  p.rb_target = P.rb_target;
+  p.tasks = h->d_tasks; p.sm_off = h->d_sm_off; p.sm_list = h->d_sm_list;
+  CK(h, cudaMemcpy(h->d_tasks, P.tasks.data(), P.tasks.size() * 4, cudaMemcpyHostToDevice));
+  CK(h, cudaMemcpy(h->d_sm_off, P.sm_off.data(), P.sm_off.size() * 4, cudaMemcpyHostToDevice));
+  CK(h, cudaMemcpy(h->d_sm_list, P.sm_list.data(), P.sm_list.size() * 4, cudaMemcpyHostToDevice));
+  CK(h, cudaMemcpy(p.seq_lens, seq_lens_host, (size_t)B * 4, cudaMemcpyHostToDevice));
+  h->planned = true;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void* v_cache, float* logits_dev,
+                   void* stream) {
+  int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
+  if (r) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  return launch_segment(h, 0, true, true, st);
+}
+
+int mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, void* k_cache, void* v_cache,
+                        float* logits_host, void* stream) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
+  if (!tokens_host || !logits_host) return fail(&h->err, MK_ERR_INVALID, "NULL host buffer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  CK(h, cudaMemcpyAsync(h->d_tokens, tokens_host, (size_t)h->B * 4, cudaMemcpyHostToDevice, st));
+  int r = mk_decode_step(h, h->d_tokens, k_cache, v_cache, h->d_logits, stream);
+  if (r) return r;
+  CK(h, cudaMemcpyAsync(logits_host, h->d_logits, (size_t)h->B * h->s.V * 4, cudaMemcpyDeviceToHost, st));
+  CK(h, cudaStreamSynchronize(st));
+  return MK_OK;
+}
+
+int mk_decode_step_perop(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void* v_cache,
+                         float* logits_dev, void* stream, int use_graph) {
+  int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
+  if (r) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  const int first = 1, last = h->P.n_segs - 1;
+  if (!use_graph) {
+    for (int seg = first; seg <= last; ++seg) {
+      r = launch_segment(h, seg, false, seg == last, st);
+      if (r) return r;
+    }
+    return MK_OK;
+  }
+  const void* key[5] = {tokens_dev, k_cache, v_cache, logits_dev, stream};
+  if (!h->graph || std::memcmp(key, h->g_key, sizeof key) != 0 || h->g_fixed != h->fixed) {
+    if (h->graph) { cudaGraphExecDestroy(h->graph); h->graph = nullptr; }
+    cudaStream_t cap = nullptr;
+    CK(h, cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) { cudaStreamDestroy(cap); return cuda_fail(h, e, "begin capture"); }
+    for (int seg = first; seg <= last && r == MK_OK; ++seg) r = launch_segment(h, seg, false, seg == last, cap);
+    e = cudaStreamEndCapture(cap, &g);
+    cudaStreamDestroy(cap);
+    if (r) { if (g) cudaGraphDestroy(g); return r; }
+    if (e != cudaSuccess) return cuda_fail(h, e, "end capture");
+    e = cudaGraphInstantiate(&h->graph, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) { h->graph = nullptr; return cuda_fail(h, e, "graph instantiate"); }
+    std::memcpy(h->g_key, key, sizeof key);
+    h->g_fixed = h->fixed;
+  }
+  CK(h, cudaGraphLaunch(h->graph, st));
+  return MK_OK;
+}
+
+int mk_get_status(mk_handle* h, mk_error_info* info) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  mk_error_info tmp;
+  mk_error_info* o = info ? info : &tmp;
+  std::memset(o, 0, sizeof *o);
+  if (!h->planned) return MK_OK;
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaStreamSynchronize(h->last_stream));
+  int32_t e[16];
+  CK(h, cudaMemcpy(e, h->prm.err, sizeof e, cudaMemcpyDeviceToHost));
+  o->code = e[E_CODE]; o->task = e[E_TASK]; o->counter = e[E_CTR]; o->observed = e[E_OBS];
+  o->target = e[E_TARGET]; o->sm = e[E_SM];
+  if (o->code) {
+    CK(h, cudaMemset(h->prm.err, 0, sizeof e));
+    fail(&h->err, o->code, "device error %d (task %d, counter %d, observed %d, target %d, sm %d)", o->code,
+         o->task, o->counter, o->observed, o->target, o->sm);
+  }
+  return o->code;
+}
+
+int mk_set_fixed(mk_handle* h, int fixed) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  h->fixed = fixed ? 1 : 0;
+  return MK_OK;
+}
+
+int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
+  if (!h || !host_out) return fail(h ? &h->err : nullptr, MK_ERR_INVALID, "NULL argument");
+  if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
+  const Shape& s = h->s;
+  const Params& p = h->prm;
+  const size_t L = s.L, B = h->B;
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaDeviceSynchronize());
+  auto copy = [&](const void* src, size_t n) -> int {
+    if (n != bytes) return fail(&h->err, MK_ERR_INVALID, "mk_read(%d): need %zu bytes, got %zu", what, n, bytes);
+    CK(h, cudaMemcpy(host_out, src, n, cudaMemcpyDeviceToHost));
+    return MK_OK;
+  };
+  switch (what) {
+    case MK_READ_HIDDEN: return copy(p.X, (L + 1) * B * s.d * 4);
+    case MK_READ_ROUTES: return copy(p.ridx, L * B * s.topk * 4);
+    case MK_READ_ROUTE_W: return copy(p.rw, L * B * s.topk * 4);
+    case MK_READ_SEQ_LENS: return copy(p.seq_lens, B * 4);
+    case MK_READ_COUNTERS: return copy(p.ctr, (size_t)p.n_ctr * 4);
+    case MK_READ_ROUTER_LOGITS: return copy(p.rlog, L * B * s.E * 4);
+    case MK_READ_ACTIVE: {
+      const size_t maxa = p.maxa, per = 1 + maxa * (2 + B);
+      if (bytes != L * per * 4) return fail(&h->err, MK_ERR_INVALID, "mk_read(ACTIVE): need %zu bytes", L * per * 4);
+      std::vector<int32_t> nact(L), act(L * maxa), cnt(L * maxa), tok(L * maxa * B);
+      CK(h, cudaMemcpy(nact.data(), p.nact, L * 4, cudaMemcpyDeviceToHost));
+      CK(h, cudaMemcpy(act.data(), p.active, L * maxa * 4, cudaMemcpyDeviceToHost));
+      CK(h, cudaMemcpy(cnt.data(), p.act_cnt, L * maxa * 4, cudaMemcpyDeviceToHost));
+      CK(h, cudaMemcpy(tok.data(), p.act_tok, L * maxa * B * 4, cudaMemcpyDeviceToHost));
+      int32_t* o = static_cast<int32_t*>(host_out);
+      for (size_t l = 0; l < L; ++l) {
+        int32_t* r = o + l * per;
+        r[0] = nact[l];
+        for (size_t a = 0; a < maxa; ++a) {
+          int32_t* q = r + 1 + a * (2 + B);
+          q[0] = act[l * maxa + a];
+          q[1] = cnt[l * maxa + a];
+          for (size_t b = 0; b < B; ++b) q[2 + b] = tok[(l * maxa + a) * B + b];
+        }
+      }
+      return MK_OK;
+    }
+    default:
+      return fail(&h->err, MK_ERR_INVALID, "mk_read: unknown item %d", what);
+  }
+}
+
+int mk_query(mk_handle* h, int what, int64_t* out) {
+  if (!out) return fail(h ? &h->err : nullptr, MK_ERR_INVALID, "out is NULL");
+  switch (what) {
+    case MK_Q_SMEM_BYTES: *out = kSmemBytes; return MK_OK;
+    case MK_Q_THREADS: *out = kThreads; return MK_OK;
+    case MK_Q_STAGE_BYTES: *out = kStageBytes; return MK_OK;
+    case MK_Q_NUM_STAGES: *out = kStages; return MK_OK;
+    default: break;
+  }
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  switch (what) {
+    case MK_Q_NUM_SMS: *out = h->n_sm; return MK_OK;
+    case MK_Q_PACKED_BYTES: *out = (int64_t)h->s.total; return MK_OK;
+    default: break;
+  }
+  if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
+  switch (what) {
+    case MK_Q_NUM_TASKS: *out = h->P.n_tasks(); return MK_OK;
+    case MK_Q_NUM_COUNTERS: *out = h->P.n_ctr; return MK_OK;
+    case MK_Q_MAX_ACTIVE: *out = h->P.maxa; return MK_OK;
+    case MK_Q_SPLIT_PAGES: *out = h->split_pages; return MK_OK;
+    case MK_Q_PEROP_LAUNCHES: *out = h->P.n_segs - 1; return MK_OK;
+    default: return fail(&h->err, MK_ERR_INVALID, "mk_query: unknown item %d", what);
+  }
+}
+
+void mk_destroy(mk_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->dev);
+  cudaDeviceSynchronize();
+  free_plan(h);
+  if (h->wblob) cudaFree(h->wblob);
+  if (h->norms) cudaFree(h->norms);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// Internal definitions shared by the host planner and the device code of libmk.
+//
+// Task descriptor: 32 int32 fields per task.  The pages specify the width (32
+// int32) and list opcode, layer, output tile, split-K coordinates, and the
+// counters a task waits on and signals [Cohere open-sources fused LLM decode
+// kernel with 1.58x vLLM claim, descriptor paragraph]; the concrete field order
+// below is this library's.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace mk {
+
+// ---- CTA shape -------------------------------------------------------------
+// 8 consumer warps (MMA + epilogues) and 1 producer warp (descriptor walk, queue
+// claims, bulk/TMA copies into the shared-memory ring).  One CTA per SM.
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;
+
+// ---- shared memory ---------------------------------------------------------
+constexpr int kStageBytes = 32768;            // one ring slot
+constexpr int kStages = 6;                    // 192 KB of copies in flight per SM
+constexpr int kScratchBytes = 32768;          // cross-warp reductions / merges
+constexpr int kSmallBytes = 1024;             // per-warp scalars, flags
+constexpr int kMbox = 8;                      // producer -> consumer task mailbox
+constexpr int kFragBytes = 512;               // one 16x16 bf16 MMA A-fragment
+constexpr int kFragsPerStage = kStageBytes / kFragBytes;
+constexpr int kMaxNrb = 8;                    // GEMV task rows <= 128
+constexpr int kMaxKsw = 16;                   // GEMV task K <= 2048 (16 k16-steps/warp)
+constexpr int kBarBytes = (2 * kStages + 2 * kMbox) * 8;
+constexpr int kMboxBytes = kMbox * 16;
+constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kScratchBytes +
+                           kSmallBytes + kBarBytes + kMboxBytes;
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
+
+constexpr int kDescInts = 32;
+constexpr int kMaxBatch = 8;
+constexpr int kRowBlock = 128;                // residual row block (rows of d_model)
+
+enum Op : int32_t {
+  OP_END = 0,
+  OP_EMBED = 1,      // x0 = embed[token], row-block sums of squares
+  OP_QKV = 2,        // QKV_PROJ tile + RoPE + K/V append
+  OP_ROUTER = 3,     // ROUTER_GEMM tile; last tile runs ROUTER_TOPK + ROUTE_FINALIZE
+  OP_ATT_DRAIN = 4,  // ATTN_DRAIN: claim (group, seq, split) items; last split of a
+                     // (seq, group) runs ATTN_COMBINE
+  OP_UP_DRAIN = 5,   // MOE_UPGATE_ACT_DRAIN (gather fused into the operand load)
+  OP_DN_DRAIN = 6,   // MOE_DOWN_DRAIN (weights the output by the routing weight)
+  OP_OPROJ = 7,      // O_PROJ split-K by KV group
+  OP_LMHEAD = 8,     // final RMSNorm + LM_HEAD tile
+};
+
+enum DescField : int {
+  D_OP = 0, D_LAYER = 1, D_AUX = 2, D_ROW0 = 3, D_NROWS = 4, D_K0 = 5, D_KLEN = 6,
+  D_WAIT_CTR = 7, D_WAIT_TARGET = 8, D_SIG_CTR = 9, D_SIG_TARGET = 10,
+  D_WOFF_LO = 11, D_WOFF_HI = 12, D_WBYTES = 13, D_QUEUE = 14, D_TASK_ID = 15,
+  D_WAVE = 16
+};
+
+// Row-map modes of the weight packer.
+enum PackMode : int { PACK_IDENT = 0, PACK_ROPE = 1, PACK_GATE_UP = 2 };
+
+// Device error word layout (int32[16]).
+enum ErrField : int { E_CODE = 0, E_TASK = 1, E_CTR = 2, E_OBS = 3, E_TARGET = 4,
+                      E_SM = 5, E_ABORT = 8 };
+
+struct Params {
+  // shape
+  int L, d, Hq, Hkv, hd, E, topk, f, V, gs, nrb_d, B, maxa;
+  int max_pages, n_pages, window;
+  unsigned long long swa_mask;
+  float theta, eps, scale_log2;
+  int split_pages, max_items_bg;
+  int r_up, r_dn, t_up, t_dn, qkv_tpg, n_router_tasks;
+  long long timeout_ns;
+  int fixed, do_reset;
+  // weights
+  const uint8_t* wblob;
+  long long off_up, off_dn, up_bytes_e, dn_bytes_e;
+  const float* attn_norm;   // [L][d]
+  const float* final_norm;  // [d]
+  const uint16_t* embed;    // [V][d] bf16
+  // step inputs / outputs
+  const int* tokens;
+  const int* page_table;    // [B][max_pages]
+  int* seq_lens;            // [B]
+  uint16_t* kc;             // [L][n_pages][Hkv][16][hd] bf16
+  uint16_t* vc;
+  float* logits;            // [B][V]
+  // activations (per layer)
+  float* X;                 // [L+1][B][d]
+  float* SS;                // [L+1][nrb_d][B]
+  uint16_t* Q;              // [L][B][Hq*hd]
+  float* attp;              // [L][Hkv][B][max_items_bg][gs*(hd+2)]
+  uint16_t* atto;           // [L][B][Hq*hd]
+  float* opart;             // [L][Hkv][B][d]
+  float* rlog;              // [L][B][E]
+  int* ridx;                // [L][B][topk]
+  float* rw;                // [L][B][topk]
+  int* active;              // [L][maxa]
+  int* nact;                // [L]
+  int* act_cnt;             // [L][maxa]
+  int* act_tok;             // [L][maxa][B]  (b*16 + j)
+  uint16_t* aup;            // [L][maxa][B][f]
+  float* Y;                 // [L][B][topk][d]
+  // synchronisation
+  unsigned* ctr;
+  int* qhead;               // [3L]
+  int* qcount;              // [3L]
+  int* err;                 // [16]
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_up, c_rb, c_done, n_ctr, n_queues;
+  int rb_target;
+  // plan (one segment)
+  const int* tasks;
+  const int* sm_off;
+  const int* sm_list;
+};
+
+}  // namespace mk
