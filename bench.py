@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the persistent MoE decode megakernel.
+
+Prints ONE JSON line on rank 0.  Default workload: the pages-scale synthetic MoE
+(48 parallel attention+MoE layers, d 2048, 32/4 heads x 128, 128 experts top-8,
+ffn 768, vocab 151936) at batch 1 with 8192 cached tokens, one decode step per
+megakernel launch, inputs resident in HBM.  The per-step working set (~6.9 GB of
+weights + KV) is far larger than the 129 MB L2, so no L2 flush is needed between
+steps.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+N > 1 runs under torchrun as independent replicas (the step has no data-parallel
+split; each rank decodes its own batch): value = all ranks' tokens / max-over-ranks
+time.  `--impl reference` times the CPU oracle (a bounded slice of the same step,
+scaled to a full step) on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s at bs1 & bs8; achieved HBM GB/s as % of weight+KV SoL"
+UNIT = "tok/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--workload", default="pages_b1_8k")
+    ap.add_argument("--mode", default="mega", choices=["mega", "perop", "graph"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-baselines", action="store_true", help="skip per-op / graph arms")
+    ap.add_argument("--no-bs8", action="store_true", help="skip the batch-8 ragged measurement")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return rank, ws, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int, device="cuda") -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [ln.strip().split(",") for ln in self.f.read().splitlines() if ln.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "persistent_moe_decode_cta_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    e = t.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def build_state(workload, seed, device):
+    import torch
+
+    import synth
+    from persistent_moe_decode_cta_gb300 import binding as B
+    cfg = synth.model_config(workload)
+    seq = synth.seq_lens_for(workload, seed)
+    W = synth.make_weights(cfg, seed=seed, device=device)
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    st = plan_workload(mk, cfg, workload, seq, seed, device)
+    return cfg, mk, st, W
+
+
+def plan_workload(mk, cfg, workload, seq, seed, device):
+    import torch
+
+    import synth
+    pt, npages = synth.make_page_table(seq, steps=1, seed=seed)
+    k, v = synth.make_kv(cfg, npages, seed=seed, device=device)
+    tokens = synth.make_tokens(len(seq), cfg["vocab"], seed=seed, device=device)
+    pt_dev = torch.as_tensor(pt, device=device)
+    mk.plan(seq, pt_dev, npages)
+    mk.set_fixed(True)
+    logits = torch.empty(len(seq), cfg["vocab"], device=device)
+    return dict(seq=seq, pt=pt_dev, npages=npages, k=k, v=v, tokens=tokens, logits=logits,
+                workload=workload)
+
+
+def time_device(run_step, K, W, ws, stream):
+    """W untimed steps; then K steps bracketed by barrier + synchronize, with CUDA
+    events on the launching stream around every launch.  Returns (total_s,
+    per-launch seconds)."""
+    import torch
+    for _ in range(W):
+        run_step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        evs[i][0].record(stream)
+        run_step()
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    total = t0.elapsed_time(t1) / 1e3
+    per = [a.elapsed_time(b) / 1e3 for a, b in evs]
+    return total, per
+
+
+def union_sizes(mk, L):
+    return [len(a) for a in mk.active()][:L]
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+class OracleSampler:
+    """The CPU oracle timed on a slice of one decode step of a workload: layer steps
+    (layer-0 weights drawn on the host, the workload's batch and context length) and
+    1/lm_frac of the LM head, scaled to a full step.  Weights are drawn once, before
+    any timing."""
+
+    def __init__(self, workload, seed, lm_frac=16):
+        import numpy as np
+
+        import oracle
+        import synth
+        self.O = oracle
+        self.cfg = synth.model_config(workload)
+        self.seq = synth.seq_lens_for(workload, seed)
+        self.B = len(self.seq)
+        self.W = synth.LazyHostWeights(self.cfg, seed)
+        self.kv = synth.LazyHostKV(self.cfg, seed)
+        self.pt, _ = synth.make_page_table(self.seq, steps=1, seed=seed)
+        self.x0 = np.random.default_rng(seed).standard_normal((self.B, self.cfg["d_model"])) * 0.02
+        self.lm_frac = lm_frac
+        self.n_lm = self.cfg["vocab"] // lm_frac
+        self.workload = workload
+        self.O.layer_step(self.cfg, self.W, self.kv, 0, self.x0, self.seq, self.pt)
+        self.W.lm_head(self.n_lm)
+        W = self.W
+        n_lm = self.n_lm
+
+        class LM:
+            def final_norm(self): return W.final_norm()
+            def lm_head(self): return W.lm_head(n_lm)
+        self.lm = LM()
+
+    def step_seconds(self, budget_s=0.0, max_layers=1):
+        """Seconds of a full step, estimated from >= 1 timed layer steps."""
+        x = self.x0
+        t0 = time.perf_counter()
+        n = 0
+        while n < 1 or (n < max_layers and (time.perf_counter() - t0) < budget_s):
+            x, _ = self.O.layer_step(self.cfg, self.W, self.kv, 0, x, self.seq, self.pt)
+            n += 1
+        t_layers = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        self.O.lm_head(self.cfg, self.lm, x)
+        t_lm = time.perf_counter() - t1
+        self.last = (n, t_layers + t_lm)
+        return t_layers / n * self.cfg["n_layers"] + t_lm * self.lm_frac
+
+    def describe(self):
+        n, t = self.last
+        return (f"{self.workload}: {n} layer step(s) at B={self.B} + 1/{self.lm_frac} of the LM "
+                f"head, float64 numpy oracle, scaled to {self.cfg['n_layers']} layers + the full "
+                f"LM head; {t:.1f} s timed")
+
+
+def cpu_cores():
+    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(threads) if threads else os.cpu_count()
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return 0
+    smp = OracleSampler(args.workload, args.seed, lm_frac=64)
+    per = []
+    for i in range(args.warmup + args.steps):
+        s = smp.step_seconds()
+        if i >= args.warmup:
+            per.append(s)
+    step_s = statistics.mean(per)
+    value = smp.B / step_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "batch": smp.B},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": "each step: " + smp.describe()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    args = parse_args()
+    rank, ws, local = dist_init()
+    if args.impl == "reference":
+        return run_reference(args, rank, ws)
+
+    import torch
+
+    from persistent_moe_decode_cta_gb300 import binding as Bd
+    from persistent_moe_decode_cta_gb300 import sol
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    stream = torch.cuda.current_stream()
+    cfg, mk, st, W = build_state(args.workload, args.seed, device)
+    B = len(st["seq"])
+
+    def step_mega():
+        mk.step(st["tokens"], st["k"], st["v"], st["logits"])
+
+    def step_perop():
+        mk.step_perop(st["tokens"], st["k"], st["v"], st["logits"], use_graph=False)
+
+    def step_graph():
+        mk.step_perop(st["tokens"], st["k"], st["v"], st["logits"], use_graph=True)
+
+    run = {"mega": step_mega, "perop": step_perop, "graph": step_graph}[args.mode]
+    launches_per_step = 1 if args.mode == "mega" else mk.query(Bd.MK_Q_PEROP_LAUNCHES)
+    clocks = ClockSampler(local)
+    # warm-up outside the sampler, then the timed region with the sampler running
+    run()
+    torch.cuda.synchronize()
+    status = mk.status()
+    if status["code"] != 0:
+        raise RuntimeError(f"device error: {status}")
+    clocks.start()
+    total_s, per = time_device(run, args.steps, args.warmup, ws, stream)
+    ck = clocks.stop()
+    status = mk.status()
+    if status["code"] != 0:
+        raise RuntimeError(f"device error: {status}")
+    total_s = max_over_ranks(total_s, ws, device)
+    ms_per_step = total_s / args.steps * 1e3
+    value = ws * B * args.steps / total_s
+
+    # algorithmic bytes of one step (union of routed experts read back from the GPU)
+    us = union_sizes(mk, cfg["n_layers"])
+    sb = sol.step_bytes(cfg, st["seq"], us)
+    peaks, peak_kind = measured_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    launch_s = statistics.mean(per) / launches_per_step if args.mode != "mega" else statistics.mean(per)
+    achieved = sb["total"] / statistics.mean(per) / 1e9
+    traffic = profiled_traffic(args.workload) if args.mode == "mega" else None
+    sol_tok = sol.sol_tok_s(sb["total"], hbm * 1e9, B)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random bf16 weights ~N(0,0.02), K/V ~N(0,1))",
+            "config": {"workload": args.workload, "batch": B, "seq_lens": st["seq"]
+                       if B <= 8 else None, "mode": args.mode,
+                       "l2": "per-step working set %.2f GB >> 129 MB L2; no flush" % (sb["total"] / 1e9),
+                       "parallelism": f"replicas x{ws}"},
+            "gpu_launches": launches_per_step * args.steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": traffic,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "algorithmic_bytes_per_launch": sb["total"],
+                         "launch_ms": launch_s * 1e3},
+            "sol": {"bytes_per_step": sb["total"], "weights": sb["weights"], "kv": sb["kv"],
+                    "writes": sb["writes"], "sol_tok_s": sol_tok,
+                    "frac_of_sol": value / ws / sol_tok,
+                    "union_experts_mean": statistics.mean(us)},
+            "clocks": ck}
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    if not args.no_e2e and args.mode == "mega":
+        tok_h = st["tokens"].cpu().pin_memory()
+        log_h = torch.empty(B, cfg["vocab"], dtype=torch.float32).pin_memory()
+        for _ in range(args.warmup):
+            mk.step_host(tok_h, st["k"], st["v"], log_h)
+        barrier(ws)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            mk.step_host(tok_h, st["k"], st["v"], log_h)
+        el = max_over_ranks(time.perf_counter() - t0, ws, device)
+        barrier(ws)
+        line["e2e"] = {"value": ws * B * args.steps / el, "unit": UNIT,
+                       "h2d_bytes_per_step": B * 4, "d2h_bytes_per_step": B * cfg["vocab"] * 4}
+
+    # ---- the same opcodes as separate launches, and as one CUDA graph
+    if not args.no_baselines and args.mode == "mega":
+        bl = {}
+        for name, fn in (("perop", step_perop), ("graph", step_graph)):
+            k2 = max(5, args.steps // 4)
+            t, _ = time_device(fn, k2, 2, ws, stream)
+            t = max_over_ranks(t, ws, device)
+            bl[name] = {"value": ws * B * k2 / t, "ms_per_step": t / k2 * 1e3,
+                        "launches_per_step": mk.query(Bd.MK_Q_PEROP_LAUNCHES)}
+        if mk.status()["code"] != 0:
+            raise RuntimeError("device error in per-op arms")
+        line["baselines"] = bl
+
+    # ---- batch 8, ragged lengths, sliding window on odd layers (same weights)
+    if not args.no_bs8 and args.workload == "pages_b1_8k":
+        import synth
+        wl8 = "pages_b8_ragged_swa"
+        cfg8 = synth.model_config(wl8)
+        seq8 = synth.seq_lens_for(wl8, args.seed)
+        # the sliding window is a plan-time property of the layers: re-create with it
+        del st
+        mk.close()
+        torch.cuda.empty_cache()
+        mk = Bd.Megakernel(cfg8, W, max_batch=8)
+        st8 = plan_workload(mk, cfg8, wl8, seq8, args.seed, device)
+
+        def step8():
+            mk.step(st8["tokens"], st8["k"], st8["v"], st8["logits"])
+        step8()
+        t8, per8 = time_device(step8, max(10, args.steps // 2), args.warmup, ws, stream)
+        if mk.status()["code"] != 0:
+            raise RuntimeError("device error in bs8 arm")
+        k8 = max(10, args.steps // 2)
+        t8 = max_over_ranks(t8, ws, device)
+        us8 = union_sizes(mk, cfg8["n_layers"])
+        sb8 = sol.step_bytes(cfg8, seq8, us8)
+        v8 = ws * 8 * k8 / t8
+        ach8 = sb8["total"] / statistics.mean(per8) / 1e9
+        line["bs8"] = {"workload": wl8, "value": v8, "unit": UNIT, "ms_per_step": t8 / k8 * 1e3,
+                       "bytes_per_step": sb8["total"], "achieved_gbs": ach8, "frac": ach8 / hbm,
+                       "sol_tok_s": sol.sol_tok_s(sb8["total"], hbm * 1e9, 8),
+                       "union_experts_mean": statistics.mean(us8), "seq_lens": seq8}
+        st = st8
+
+    # ---- CPU oracle baseline (rank 0, N = 1)
+    if not args.no_cpu and rank == 0 and ws == 1:
+        smp = OracleSampler(args.workload, args.seed)
+        step_s = smp.step_seconds(budget_s=12.0, max_layers=48)
+        line["cpu_baseline"] = {"value": smp.B / step_s, "unit": UNIT, "cores": cpu_cores(),
+                                "kind": "oracle", "sample": smp.describe()}
+    mk.close()
+    del W
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

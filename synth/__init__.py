@@ -78,6 +78,9 @@ def seq_lens_for(workload: str, seed: int = 0) -> list[int]:
     return [int(v) for v in rng.integers(lo, hi + 1, size=w["batch"])]
 
 
+EXPERT_TENSORS = ("w_gate", "w_up", "w_down")
+
+
 def make_weights(cfg: dict, seed: int = 0, device="cpu", gain_jitter: float = 0.0,
                  std: float = 0.02) -> dict:
     """All model tensors, bf16, row-major [out, in] for every projection.
@@ -86,7 +89,8 @@ def make_weights(cfg: dict, seed: int = 0, device="cpu", gain_jitter: float = 0.
     wk/wv [L, Hkv*hd, d]; wo [L, d, Hq*hd]; router [L, E, d];
     w_gate/w_up [L, E, f, d]; w_down [L, E, d, f].
     Gains are 1.0, or 1 + gain_jitter * N(0, 1) when gain_jitter > 0 (so that tests
-    see the gain multiply).  Each layer slice has its own generator.
+    see the gain multiply).  Each layer slice (and each expert of a layer) has its own
+    generator.
     """
     L, d, Hq, Hkv, hd = (cfg[k] for k in ("n_layers", "d_model", "n_q_heads",
                                           "n_kv_heads", "head_dim"))
@@ -101,7 +105,11 @@ def make_weights(cfg: dict, seed: int = 0, device="cpu", gain_jitter: float = 0.
     for name, shp in shapes.items():
         t = torch.empty((L,) + shp, dtype=bf, device=device)
         for l in range(L):
-            t[l].normal_(0.0, std, generator=_gen(device, seed, name, l))
+            if name in EXPERT_TENSORS:
+                for e in range(E):
+                    t[l, e].normal_(0.0, std, generator=_gen(device, seed, name, l, e))
+            else:
+                t[l].normal_(0.0, std, generator=_gen(device, seed, name, l))
         W[name] = t
     for name in ("embed", "lm_head"):
         W[name] = torch.empty((V, d), dtype=bf, device=device).normal_(
@@ -213,6 +221,94 @@ class HostKV:
         return _u16(self.k[l].index_select(0, idx)), _u16(self.v[l].index_select(0, idx))
 
 
+class LazyHostWeights:
+    """Oracle weight accessors that draw each tensor on the host when first asked
+    for, from the same per-layer / per-expert seeds as make_weights (host and device
+    generators differ, so the values differ from a device draw; shapes and
+    distribution are the same).  Used to time the oracle on a slice of the
+    pages-scale model without materialising all 61 GB."""
+
+    def __init__(self, cfg: dict, seed: int = 0, std: float = 0.02):
+        self.cfg, self.seed, self.std = cfg, seed, std
+        self._cache = {}
+
+    def _draw(self, key, shape, *parts):
+        if key not in self._cache:
+            t = torch.empty(shape, dtype=torch.bfloat16).normal_(
+                0.0, self.std, generator=_gen("cpu", self.seed, *parts))
+            self._cache[key] = _u16(t)
+        return self._cache[key]
+
+    def _dims(self):
+        c = self.cfg
+        return (c["d_model"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"], c["n_experts"],
+                c["d_ff"], c["vocab"])
+
+    def embed_rows(self, tokens):
+        d = self.cfg["d_model"]
+        out = np.empty((len(tokens), d), dtype=np.uint16)
+        for i, t in enumerate(tokens):
+            out[i] = self._draw(("emb", int(t)), (d,), self.seed, "embed_row", int(t))
+        return out
+
+    def attn_norm(self, l):
+        return _u16(torch.ones(self.cfg["d_model"], dtype=torch.bfloat16))
+
+    def final_norm(self):
+        return _u16(torch.ones(self.cfg["d_model"], dtype=torch.bfloat16))
+
+    def wq(self, l):
+        d, Hq, _, hd, _, _, _ = self._dims()
+        return self._draw(("wq", l), (Hq * hd, d), "wq", l)
+
+    def wk(self, l):
+        d, _, Hkv, hd, _, _, _ = self._dims()
+        return self._draw(("wk", l), (Hkv * hd, d), "wk", l)
+
+    def wv(self, l):
+        d, _, Hkv, hd, _, _, _ = self._dims()
+        return self._draw(("wv", l), (Hkv * hd, d), "wv", l)
+
+    def wo(self, l):
+        d, Hq, _, hd, _, _, _ = self._dims()
+        return self._draw(("wo", l), (d, Hq * hd), "wo", l)
+
+    def router(self, l):
+        d, _, _, _, E, _, _ = self._dims()
+        return self._draw(("wr", l), (E, d), "router", l)
+
+    def expert(self, l, e):
+        d, _, _, _, _, f, _ = self._dims()
+        return (self._draw(("g", l, e), (f, d), "w_gate", l, e),
+                self._draw(("u", l, e), (f, d), "w_up", l, e),
+                self._draw(("dn", l, e), (d, f), "w_down", l, e))
+
+    def lm_head(self, rows=None):
+        d, V = self.cfg["d_model"], self.cfg["vocab"]
+        n = V if rows is None else rows
+        return self._draw(("lm", n), (n, d), "lm_head", n)
+
+
+class LazyHostKV:
+    """K/V page accessor that draws pages on the host on demand (same role as
+    HostKV, for timing the oracle on a slice of a long context)."""
+
+    def __init__(self, cfg: dict, seed: int = 0):
+        self.cfg, self.seed = cfg, seed
+        self._cache = {}
+
+    def pages(self, l, page_ids):
+        Hkv, hd = self.cfg["n_kv_heads"], self.cfg["head_dim"]
+        key = (l, tuple(int(p) for p in page_ids))
+        if key not in self._cache:
+            n = len(page_ids)
+            g = _gen("cpu", self.seed, "kvpages", l)
+            k = torch.empty((n, Hkv, PAGE, hd), dtype=torch.bfloat16).normal_(0, 1, generator=g)
+            v = torch.empty((n, Hkv, PAGE, hd), dtype=torch.bfloat16).normal_(0, 1, generator=g)
+            self._cache = {key: (_u16(k), _u16(v))}
+        return self._cache[key]
+
+
 def max_active_experts(cfg: dict, batch: int) -> int:
     return min(cfg["n_experts"], batch * cfg["top_k"])
 
@@ -227,4 +323,5 @@ def describe(workload: str) -> str:
 
 __all__ = ["MODELS", "WORKLOADS", "PAGE", "model_config", "seq_lens_for", "make_weights",
            "make_page_table", "make_kv", "make_tokens", "HostWeights", "HostKV",
+           "LazyHostWeights", "LazyHostKV",
            "pages_needed", "max_active_experts", "describe"]
