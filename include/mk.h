@@ -97,9 +97,10 @@ typedef struct mk_error_info {
 } mk_error_info;
 
 /* Create a handle on the current CUDA device: validate `cfg`, allocate the packed
- * weight blob and repack every matrix into per-tile, MMA-fragment-ordered tiles
- * (see DESIGN.md "Weight packing").  `stream` orders the packing kernels; the call
- * synchronises it before returning.  On error *out is NULL. */
+ * weight blob and repack every matrix into contiguous per-task tiles whose 16-byte
+ * units are the mma.sync A-fragments in the order the consumer warps read them.
+ * `stream` orders the packing kernels; the call synchronises it before returning.
+ * On error *out is NULL. */
 int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle** out);
 
 /* Build the task plan for a batch: per-SM descriptor lists, counter targets and
@@ -142,6 +143,16 @@ int mk_decode_step_perop(mk_handle* h, const int32_t* tokens_dev, void* k_cache,
  * it.  Returns info->code. */
 int mk_get_status(mk_handle* h, mk_error_info* info);
 
+/* Task timeline for profiling.  records_dev: DEVICE uint64 [capacity][8], owned by
+ * the caller; every task executed by a later step appends one record
+ *   [0] sm | opcode << 8 | layer << 16 | (ran a fan-in follow-up) << 24
+ *   [1] claimed item (attention split / expert tile) or 0
+ *   [2..7] %globaltimer ns: received, dependency met, first weight/KV chunk landed,
+ *          MMA loop done, fan-in follow-up started (0 if none), done.
+ * capacity 0 (or records_dev NULL with capacity 0) turns tracing off.  Resets the
+ * record count.  Synchronising. */
+int mk_set_trace(mk_handle* h, void* records_dev, int capacity);
+
 /* fixed = 1: steps do not advance seq_lens (repeated steps move identical bytes). */
 int mk_set_fixed(mk_handle* h, int fixed);
 
@@ -156,10 +167,13 @@ int mk_set_fixed(mk_handle* h, int fixed);
  *   MK_READ_SEQ_LENS int32 [batch]
  *   MK_READ_COUNTERS uint32[n_counters] (all zero between steps)
  *   MK_READ_ROUTER_LOGITS float [n_layers][batch][n_experts]
+ *   MK_READ_TRACE_COUNT uint32 [1] records appended since mk_set_trace (may exceed
+ *                    the capacity; records past it were dropped)
  * `bytes` must equal the size of the requested array. */
 enum {
   MK_READ_HIDDEN = 1, MK_READ_ROUTES = 2, MK_READ_ROUTE_W = 3, MK_READ_ACTIVE = 4,
-  MK_READ_SEQ_LENS = 5, MK_READ_COUNTERS = 6, MK_READ_ROUTER_LOGITS = 7
+  MK_READ_SEQ_LENS = 5, MK_READ_COUNTERS = 6, MK_READ_ROUTER_LOGITS = 7,
+  MK_READ_TRACE_COUNT = 8
 };
 int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
 
@@ -175,9 +189,10 @@ int mk_query(mk_handle* h, int what, int64_t* out);
  * lists that mk_plan would build for `n_sms` SMs, for tests of the schedule.
  *   tasks_out   int32[cap_tasks][32]      sm_off_out int32[n_sms + 1]
  *   sm_list_out int32[cap_list]           info_out int32[16]: n_tasks, list
- *   length, n_counters, max_active, split_pages, T_up, T_dn, rows per O-proj,
- *   expert-down and up task, QKV tasks per group, router tasks, counter bases
- *   (see DESIGN.md "Task descriptor").  Returns MK_ERR_INVALID if a cap is too
+ *   length, n_counters, max_active, 0, expert-up tiles per expert, expert-down
+ *   tiles per expert, rows per O-proj / expert-down / expert-up task, QKV tasks
+ *   per KV group, router tasks, residual row-block target, index of the done
+ *   counter, number of plan segments, LM-head tasks.  Returns MK_ERR_INVALID if a cap is too
  *   small (info_out[0..1] still hold the sizes needed). */
 int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out,
                 int cap_tasks, int32_t* sm_off_out, int32_t* sm_list_out, int cap_list,

@@ -22,14 +22,14 @@ STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID", 2: "MK_ERR_UNSUPPORTED", 3: "MK
                 7: "MK_ERR_BAD_TOKEN", 8: "MK_ERR_STATE"}
 
 MK_READ_HIDDEN, MK_READ_ROUTES, MK_READ_ROUTE_W, MK_READ_ACTIVE = 1, 2, 3, 4
-MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS = 5, 6, 7
+MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT = 5, 6, 7, 8
 (MK_Q_NUM_SMS, MK_Q_NUM_TASKS, MK_Q_NUM_COUNTERS, MK_Q_PACKED_BYTES, MK_Q_MAX_ACTIVE,
  MK_Q_SPLIT_PAGES, MK_Q_SMEM_BYTES, MK_Q_PEROP_LAUNCHES, MK_Q_THREADS, MK_Q_STAGE_BYTES,
  MK_Q_NUM_STAGES) = range(1, 12)
 
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_step_host",
-           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_read", "mk_query",
+           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace", "mk_read", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
 
 
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_decode_step_perop.argtypes = [H, vp, vp, vp, vp, vp, i32]
     lib.mk_get_status.argtypes = [H, ctypes.POINTER(mk_error_info)]
     lib.mk_set_fixed.argtypes = [H, i32]
+    lib.mk_set_trace.argtypes = [H, vp, i32]
     lib.mk_read.argtypes = [H, i32, vp, sz]
     lib.mk_query.argtypes = [H, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.mk_plan_dry.argtypes = [ctypes.POINTER(mk_config), i32, i32, vp, i32, vp, vp, i32, vp]
@@ -200,6 +201,12 @@ def mk_set_fixed(h, fixed: bool):
     _check(load_library().mk_set_fixed(h, int(bool(fixed))), h)
 
 
+def mk_set_trace(h, records, capacity: int):
+    """records: uint64/int64 CUDA tensor [capacity, 8] (or None with capacity 0)."""
+    _check(load_library().mk_set_trace(h, records.data_ptr() if records is not None else None,
+                                       int(capacity)), h)
+
+
 def mk_read(h, what: int, shape, dtype) -> np.ndarray:
     out = np.empty(shape, dtype=dtype)
     _check(load_library().mk_read(h, what, out.ctypes.data, out.nbytes), h)
@@ -264,6 +271,21 @@ class Megakernel:
 
     def set_fixed(self, fixed=True):
         mk_set_fixed(self.h, fixed)
+
+    def trace_on(self, capacity=1 << 20):
+        import torch
+        self._trace = torch.zeros((capacity, 8), dtype=torch.int64, device="cuda")
+        mk_set_trace(self.h, self._trace, capacity)
+
+    def trace_off(self):
+        mk_set_trace(self.h, None, 0)
+        self._trace = None
+
+    def trace_records(self):
+        """int64 array [n, 8] of the records appended since trace_on()."""
+        n = int(mk_read(self.h, MK_READ_TRACE_COUNT, (1,), np.uint32)[0])
+        n = min(n, self._trace.shape[0])
+        return self._trace[:n].cpu().numpy()
 
     def query(self, what):
         return mk_query(self.h, what)

@@ -27,8 +27,9 @@
 #include "mk_internal.h"
 
 namespace mk {
-cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, int n_rows_packed,
-                        int n_src_rows, int K, long long ld, int col0, int mode, int hd, cudaStream_t st);
+cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, const void* src_c,
+                        int n_rows_packed, int n_src_rows, int K, long long ld, int col0, int mode, int hd,
+                        int gs, int grp, int tile_rows, cudaStream_t st);
 cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_t st);
 cudaError_t prepare_megakernel();
 int megakernel_occupancy(int* blocks);
@@ -300,6 +301,7 @@ struct mk_handle {
   Params prm{};
   int32_t* d_tokens = nullptr;
   float* d_logits = nullptr;
+  unsigned* d_trace_n = nullptr;
   int fixed = 0;
   cudaStream_t last_stream = nullptr;
   // tensor maps
@@ -459,28 +461,26 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
   } while (0)
   for (int l = 0; l < L; ++l) {
     uint8_t* q = h->wblob + s.off_qkv + l * s.qkv_layer_bytes;
-    for (int g = 0; g < s.Hkv; ++g) {
-      uint8_t* grp = q + (size_t)g * s.qkv_rows_group * d * 2;
-      const uint16_t* wq = static_cast<const uint16_t*>(w->wq[l]) + (size_t)g * gs * hd * d;
-      const uint16_t* wk = static_cast<const uint16_t*>(w->wk[l]) + (size_t)g * hd * d;
-      const uint16_t* wv = static_cast<const uint16_t*>(w->wv[l]) + (size_t)g * hd * d;
-      PK(grp, wq, nullptr, gs * hd, gs * hd, d, d, 0, PACK_ROPE, hd);
-      PK(grp + (size_t)gs * hd * d * 2, wk, nullptr, hd, hd, d, d, 0, PACK_ROPE, hd);
-      PK(grp + (size_t)(gs + 1) * hd * d * 2, wv, nullptr, hd, hd, d, d, 0, PACK_ROPE, hd);
-    }
+    for (int g = 0; g < s.Hkv; ++g)
+      PK(q + (size_t)g * s.qkv_rows_group * d * 2, w->wq[l], w->wk[l], w->wv[l], s.qkv_rows_group, 0, d, d, 0,
+         PACK_QKV, hd, gs, g, s.r_qkv);
     uint8_t* o = h->wblob + s.off_o + l * s.o_layer_bytes;
     for (int g = 0; g < s.Hkv; ++g)
-      PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o, PACK_IDENT, hd);
-    PK(h->wblob + s.off_router + l * s.router_layer_bytes, w->router[l], nullptr, s.e_pad, E, d, d, 0, PACK_IDENT, hd);
+      PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o,
+         PACK_IDENT, hd, gs, 0, s.r_o);
+    PK(h->wblob + s.off_router + l * s.router_layer_bytes, w->router[l], nullptr, nullptr, s.e_pad, E, d, d, 0,
+       PACK_IDENT, hd, gs, 0, s.r_router);
     for (int e2 = 0; e2 < E; ++e2) {
       const int i = l * E + e2;
-      PK(h->wblob + s.off_up + (size_t)i * s.up_bytes_e, w->w_gate[i], w->w_up[i], 2 * f, f, d, d, 0, PACK_GATE_UP, hd);
-      PK(h->wblob + s.off_dn + (size_t)i * s.dn_bytes_e, w->w_down[i], nullptr, d, d, f, f, 0, PACK_IDENT, hd);
+      PK(h->wblob + s.off_up + (size_t)i * s.up_bytes_e, w->w_gate[i], w->w_up[i], nullptr, 2 * f, f, d, d, 0,
+         PACK_GATE_UP, hd, gs, 0, s.r_up);
+      PK(h->wblob + s.off_dn + (size_t)i * s.dn_bytes_e, w->w_down[i], nullptr, nullptr, d, d, f, f, 0, PACK_IDENT,
+         hd, gs, 0, s.r_dn);
     }
     e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
     if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
   }
-  PK(h->wblob + s.off_lm, w->lm_head, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, hd);
+  PK(h->wblob + s.off_lm, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, hd, gs, 0, s.r_lm);
 #undef PK
   e = launch_convert(h->norms + (size_t)L * d, w->final_norm, d, st);
   if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
@@ -594,11 +594,13 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(h->d_sm_list, P.sm_list.size());
   AL(h->d_tokens, B);
   AL(h->d_logits, (size_t)B * s.V);
+  AL(h->d_trace_n, 1);
 #undef AL
   p.c_lr = P.c_lr; p.c_qkvg = P.c_qkvg; p.c_rt = P.c_rt; p.c_rr = P.c_rr; p.c_att = P.c_att; p.c_og = P.c_og;
   p.c_up = P.c_up; p.c_rb = P.c_rb; p.c_done = P.c_done; p.n_ctr = P.n_ctr; p.n_queues = 3 * L;
   p.rb_target = P.rb_target;
   p.tasks = h->d_tasks; p.sm_off = h->d_sm_off; p.sm_list = h->d_sm_list;
+  p.trace = nullptr; p.trace_n = h->d_trace_n; p.trace_cap = 0;
   CK(h, cudaMemcpy(h->d_tasks, P.tasks.data(), P.tasks.size() * 4, cudaMemcpyHostToDevice));
   CK(h, cudaMemcpy(h->d_sm_off, P.sm_off.data(), P.sm_off.size() * 4, cudaMemcpyHostToDevice));
   CK(h, cudaMemcpy(h->d_sm_list, P.sm_list.data(), P.sm_list.size() * 4, cudaMemcpyHostToDevice));
@@ -687,6 +689,19 @@ int mk_get_status(mk_handle* h, mk_error_info* info) {
   return o->code;
 }
 
+int mk_set_trace(mk_handle* h, void* records_dev, int capacity) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
+  if (capacity < 0 || (capacity > 0 && !records_dev)) return fail(&h->err, MK_ERR_INVALID, "bad trace buffer");
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaDeviceSynchronize());
+  CK(h, cudaMemset(h->d_trace_n, 0, sizeof(unsigned)));
+  h->prm.trace = capacity > 0 ? static_cast<unsigned long long*>(records_dev) : nullptr;
+  h->prm.trace_cap = capacity;
+  if (h->graph) { cudaGraphExecDestroy(h->graph); h->graph = nullptr; }
+  return MK_OK;
+}
+
 int mk_set_fixed(mk_handle* h, int fixed) {
   if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
   h->fixed = fixed ? 1 : 0;
@@ -713,6 +728,7 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
     case MK_READ_SEQ_LENS: return copy(p.seq_lens, B * 4);
     case MK_READ_COUNTERS: return copy(p.ctr, (size_t)p.n_ctr * 4);
     case MK_READ_ROUTER_LOGITS: return copy(p.rlog, L * B * s.E * 4);
+    case MK_READ_TRACE_COUNT: return copy(h->d_trace_n, 4);
     case MK_READ_ACTIVE: {
       const size_t maxa = p.maxa, per = 1 + maxa * (2 + B);
       if (bytes != L * per * 4) return fail(&h->err, MK_ERR_INVALID, "mk_read(ACTIVE): need %zu bytes", L * per * 4);

@@ -60,7 +60,7 @@ enum DescField : int {
 };
 
 // Row-map modes of the weight packer.
-enum PackMode : int { PACK_IDENT = 0, PACK_ROPE = 1, PACK_GATE_UP = 2 };
+enum PackMode : int { PACK_IDENT = 0, PACK_QKV = 1, PACK_GATE_UP = 2 };
 
 // Device error word layout (int32[16]).
 enum ErrField : int { E_CODE = 0, E_TASK = 1, E_CTR = 2, E_OBS = 3, E_TARGET = 4,
@@ -112,6 +112,10 @@ struct Params {
   int* err;                 // [16]
   int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_up, c_rb, c_done, n_ctr, n_queues;
   int rb_target;
+  // optional task timeline (see trace_emit)
+  unsigned long long* trace;
+  unsigned* trace_n;
+  int trace_cap;
   // plan (one segment)
   const int* tasks;
   const int* sm_off;

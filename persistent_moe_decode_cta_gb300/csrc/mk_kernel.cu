@@ -35,6 +35,29 @@ __device__ void raise_err(const Params& p, int code, int task, int ctr, int obs,
 
 __device__ __forceinline__ bool aborted(const Params& p) { return ld_volatile(&p.err[E_ABORT]) != 0; }
 
+// Optional per-task timeline (Params::trace != nullptr): thread 0 stamps the
+// moments of a task into shared memory and appends one record when it ends.
+//   record (8 x u64): [0] sm | op << 8 | layer << 16 | fan-in << 24, [1] item,
+//   [2] received, [3] dependency met, [4] first weight/KV chunk landed,
+//   [5] MMA loop done, [6] fan-in follow-up started (0 if none), [7] task done.
+__device__ __forceinline__ unsigned long long* trace_slots(const Smem& S) {
+  return reinterpret_cast<unsigned long long*>(S.small + 192);
+}
+__device__ __forceinline__ void trace_mark(const Params& p, const Smem& S, int slot) {
+  if (p.trace && threadIdx.x == 0) trace_slots(S)[slot] = gtime();
+}
+__device__ void trace_emit(const Params& p, const Smem& S, int op, int layer, int item) {
+  if (!p.trace || threadIdx.x != 0) return;
+  const unsigned idx = atomicAdd(p.trace_n, 1u);
+  if (idx >= (unsigned)p.trace_cap) return;
+  unsigned long long* r = p.trace + (size_t)idx * 8;
+  unsigned long long* t = trace_slots(S);
+  r[0] = (unsigned long long)blockIdx.x | ((unsigned long long)op << 8) |
+         ((unsigned long long)(layer & 0xff) << 16) | ((unsigned long long)(t[6] != 0) << 24);
+  r[1] = (unsigned long long)(unsigned)item;
+  r[2] = t[0]; r[3] = t[1]; r[4] = t[2]; r[5] = t[3]; r[6] = t[6]; r[7] = gtime();
+}
+
 // Spin until ctr >= target (acquire), bounded by the timeout and the abort flag.
 __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
   const unsigned* c = p.ctr + ci;
@@ -56,8 +79,14 @@ __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
 
 // Consumer-side wait: thread 0 polls, the others learn the result at a barrier.
 __device__ bool consumer_wait(const Params& p, const Smem& S, int ci, unsigned target, int task) {
-  if (ci < 0) return true;
-  if (threadIdx.x == 0) S.small[0] = wait_ge(p, ci, target, task) ? 1 : 0;
+  if (ci < 0) {
+    trace_mark(p, S, 1);
+    return true;
+  }
+  if (threadIdx.x == 0) {
+    S.small[0] = wait_ge(p, ci, target, task) ? 1 : 0;
+    if (p.trace) trace_slots(S)[1] = gtime();
+  }
   bar_sync_consumers();
   const int ok = S.small[0];
   bar_sync_consumers();
@@ -341,40 +370,36 @@ __device__ __forceinline__ void build_bfrag(BFrag& fr, int ksw, F&& pair) {
   }
 }
 
-// acc[rb] += W_tile[rb] * act over this warp's k-steps; consumes the task's chunks.
+// acc[rb] += W_tile[rb] * act over this warp's k16-steps ks = warp + 8 j, consuming the
+// task's ring chunks.  Tiles are packed so that fragment (rb, ks) sits at index
+// (j * NRB + rb) * 8 + warp: every 32 KB chunk holds 8 / NRB consecutive j for all
+// row blocks, so chunk, register and smem indices are compile-time constants.
+template <int NRB>
 __device__ __forceinline__ bool gemv_mainloop(const Params& p, const Smem& S, uint32_t& cseq, int nch,
-                                              int nrb, int ks_total, int ksw, const BFrag& fr,
-                                              float (&acc)[kMaxNrb][4]) {
+                                              int ksw, const BFrag& fr, float (&acc)[NRB][4]) {
+  constexpr int JPC = 8 / NRB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int r = 0; r < kMaxNrb; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+  for (int r = 0; r < NRB; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
   if (nch <= 0) return true;
-  int chunk = 0;
-  if (!wait_full(p, S, cseq)) return false;
 #pragma unroll
-  for (int rb = 0; rb < kMaxNrb; ++rb) {
-    if (rb < nrb) {
+  for (int j = 0; j < kMaxKsw; ++j) {
+    if (j < ksw) {
+      const int c = j / JPC;
+      if (j % JPC == 0) {
+        if (c > 0) release_stage(S, cseq + c - 1);
+        if (!wait_full(p, S, cseq + c)) return false;
+        if (c == 0) trace_mark(p, S, 2);
+      }
+      const uint32_t base = S.stage(cseq + c) + ((j % JPC) * NRB * 8 + warp) * kFragBytes + lane * 16;
 #pragma unroll
-      for (int j = 0; j < kMaxKsw; ++j) {
-        if (j < ksw) {
-          const int fi = rb * ks_total + warp + 8 * j;
-          const int c = fi / kFragsPerStage;
-          while (chunk < c) {
-            release_stage(S, cseq + chunk);
-            ++chunk;
-            if (!wait_full(p, S, cseq + chunk)) return false;
-          }
-          const uint4 a = lds128(S.stage(cseq + chunk) + (fi % kFragsPerStage) * kFragBytes + lane * 16);
-          mma_bf16(acc[rb], a.x, a.y, a.z, a.w, fr.b0[j], fr.b1[j]);
-        }
+      for (int rb = 0; rb < NRB; ++rb) {
+        const uint4 a = lds128(base + rb * 8 * kFragBytes);
+        mma_bf16(acc[rb], a.x, a.y, a.z, a.w, fr.b0[j], fr.b1[j]);
       }
     }
   }
-  while (chunk < nch) {
-    release_stage(S, cseq + chunk);
-    ++chunk;
-    if (chunk < nch && !wait_full(p, S, cseq + chunk)) return false;
-  }
+  release_stage(S, cseq + (ksw - 1) / JPC);
   cseq += nch;
   return true;
 }
@@ -382,22 +407,32 @@ __device__ __forceinline__ bool gemv_mainloop(const Params& p, const Smem& S, ui
 // Cross-warp sum.  Afterwards thread (warp w, lane) holds out[] for row block w:
 // out[0] = (row 16w+g, token 2c), out[1] = (16w+g, 2c+1), out[2] = (16w+g+8, 2c),
 // out[3] = (16w+g+8, 2c+1), g = lane/4, c = lane%4.
-__device__ __forceinline__ void gemv_reduce(const Smem& S, int nrb, const float (&acc)[kMaxNrb][4],
-                                            float (&out)[4]) {
+template <int NRB>
+__device__ __forceinline__ void gemv_reduce(const Smem& S, const float (&acc)[NRB][4], float (&out)[4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float4* scr = reinterpret_cast<float4*>(S.scratch);
 #pragma unroll
-  for (int rb = 0; rb < kMaxNrb; ++rb)
-    if (rb < nrb) scr[(warp * kMaxNrb + rb) * 32 + lane] = make_float4(acc[rb][0], acc[rb][1], acc[rb][2], acc[rb][3]);
+  for (int rb = 0; rb < NRB; ++rb)
+    scr[(warp * NRB + rb) * 32 + lane] = make_float4(acc[rb][0], acc[rb][1], acc[rb][2], acc[rb][3]);
   bar_sync_consumers();
   out[0] = out[1] = out[2] = out[3] = 0.f;
-  if (warp < nrb) {
+  if (warp < NRB) {
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float4 v = scr[(w * kMaxNrb + warp) * 32 + lane];
+      const float4 v = scr[(w * NRB + warp) * 32 + lane];
       out[0] += v.x; out[1] += v.y; out[2] += v.z; out[3] += v.w;
     }
   }
+}
+
+template <int NRB>
+__device__ __forceinline__ bool gemv_run(const Params& p, const Smem& S, uint32_t& cseq, int nch, int ksw,
+                                         const BFrag& fr, float (&v)[4]) {
+  float acc[NRB][4];
+  if (!gemv_mainloop<NRB>(p, S, cseq, nch, ksw, fr, acc)) return false;
+  trace_mark(p, S, 3);
+  gemv_reduce<NRB>(S, acc, v);
+  return true;
 }
 
 // 1 / rms of x_b (layer input) from the per-row-block sums of squares.
@@ -560,6 +595,7 @@ __device__ bool signal_fanin(const Params& p, const Smem& S, int ci, unsigned ta
     __threadfence();
     const unsigned old = atom_add_acq_rel(p.ctr + ci, 1u);
     S.small[1] = (old + 1 == target) ? 1 : 0;
+    if (p.trace && old + 1 == target) trace_slots(S)[6] = gtime();
   }
   bar_sync_consumers();
   const bool last = S.small[1] != 0;
@@ -609,8 +645,7 @@ __device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const 
     tok_list = p.act_tok + ((size_t)l * p.maxa + a_slot) * p.B;
   }
   const int nrb = nrows / 16;
-  const int ks_total = klen / 16;
-  const int ksw = ks_total / kConsumerWarps;
+  const int ksw = klen / 16 / kConsumerWarps;
 
   BFrag fr;
   if (op == OP_OPROJ) {
@@ -639,10 +674,15 @@ __device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const 
     build_norm_bfrag(p, fr, ksw, last ? p.L : l, last ? p.final_norm : p.attn_norm + (size_t)l * p.d, b);
   }
 
-  float acc[kMaxNrb][4];
-  if (!gemv_mainloop(p, S, cseq, nch, nrb, ks_total, ksw, fr, acc)) return false;
   float v[4];
-  gemv_reduce(S, nrb, acc, v);
+  bool ran;
+  switch (nrb) {
+    case 1: ran = gemv_run<1>(p, S, cseq, nch, ksw, fr, v); break;
+    case 2: ran = gemv_run<2>(p, S, cseq, nch, ksw, fr, v); break;
+    case 4: ran = gemv_run<4>(p, S, cseq, nch, ksw, fr, v); break;
+    default: ran = gemv_run<8>(p, S, cseq, nch, ksw, fr, v); break;
+  }
+  if (!ran) return false;
 
   // ---- epilogue: thread (warp = row block, lane) owns rows 16w+g8, 16w+g8+8, tokens 2c, 2c+1
   if (warp < nrb) {
@@ -819,6 +859,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
     const int n = min(8, it.np - c0);
     const bool have = warp < n;
     if (!wait_full(p, S, cseq)) return false;
+    if (c0 == 0) trace_mark(p, S, 2);
     float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     if (have) {
       const uint32_t pbase = S.stage(cseq) + warp * kPageB;
@@ -881,6 +922,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
   }
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  trace_mark(p, S, 3);
 
   // ---- merge the 8 warps' (m, l, o)
   float* sm_m = reinterpret_cast<float*>(S.small + 16);  // [8][8]
@@ -1048,6 +1090,10 @@ __device__ void consumer(const Params& p, const Smem& S) {
     if (ent.x < 0) break;
     const int* T = p.tasks + ent.x * kDescInts;
     const int nch = ent.z;
+    if (p.trace && threadIdx.x == 0) {
+      unsigned long long* t = trace_slots(S);
+      t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = 0ull;
+    }
     if (abort_now) skip = true;
     if (skip) {
       if (!drain_chunks(p, S, cseq, nch)) break;
@@ -1068,6 +1114,7 @@ __device__ void consumer(const Params& p, const Smem& S) {
         break;
     }
     if (!ok) skip = true;
+    trace_emit(p, S, T[D_OP], T[D_LAYER], ent.y);
   }
 }
 
@@ -1122,40 +1169,53 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================== weight packer
-// Packs a [rows][K] slice of a row-major bf16 matrix into 16x16 MMA A-fragments:
-// packed 16-row block rb, k16-step ks, lane -> 16 bytes
-//   (g, 2c..2c+1) (g+8, 2c..2c+1) (g, 2c+8..2c+9) (g+8, 2c+8..2c+9),  g = lane/4, c = lane%4,
-// with fragments ordered [rb][ks][lane], so a tile of consecutive row blocks is
-// one contiguous byte range.  Packed row r maps to a source row by `mode`.
+// Packs a row-major bf16 matrix into 16x16 MMA A-fragments (16 bytes per lane):
+//   lane -> (g, 2c..2c+1) (g+8, 2c..2c+1) (g, 2c+8..2c+9) (g+8, 2c+8..2c+9), g = lane/4, c = lane%4.
+// Packed rows are cut into tiles of `tile_rows`; inside a tile of NRB row blocks,
+// fragment (row block rb, k16-step ks = w + 8 j) is stored at index (j*NRB + rb)*8 + w,
+// the order in which consumer warp w walks the tile.  Packed row r maps to a source
+// row by `mode`: identity; QKV (a KV group's query heads, then its K head and V head,
+// each head's rows permuted so rows g and g+8 of a 16-row block are the RoPE pair
+// (i, i + hd/2)); or GATE_UP (8 gate rows then the 8 matching up rows per block).
 __global__ void mk_pack_kernel(uint8_t* __restrict__ dst, const uint16_t* __restrict__ src_a,
-                               const uint16_t* __restrict__ src_b, int n_rows_packed, int n_src_rows,
-                               int K, long long ld, int col0, int mode, int hd) {
+                               const uint16_t* __restrict__ src_b, const uint16_t* __restrict__ src_c,
+                               int n_rows_packed, int n_src_rows, int K, long long ld, int col0, int mode,
+                               int hd, int gs, int grp, int tile_rows) {
   const long long total = (long long)(n_rows_packed / 16) * (K / 16) * 32;
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= total) return;
   const int lane = (int)(u & 31);
-  const long long t = u >> 5;
-  const int ks = (int)(t % (K / 16));
-  const int rb = (int)(t / (K / 16));
-  const int g = lane >> 2, c = lane & 3;
+  const long long fr = u >> 5;
+  const int nrb_t = tile_rows / 16;
+  const int ks_n = K / 16;
+  const long long per_tile = (long long)nrb_t * ks_n;
+  const int t = (int)(fr / per_tile);
+  const int fi = (int)(fr % per_tile);
+  const int j = fi / (nrb_t * 8), rem = fi % (nrb_t * 8);
+  const int rb = t * nrb_t + rem / 8;
+  const int ks = rem % 8 + 8 * j;
+  const int g8 = lane >> 2, c = lane & 3;
   uint16_t out[8];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const int r = rb * 16 + g + ((q & 1) ? 8 : 0);
+    const int r = rb * 16 + g8 + ((q & 1) ? 8 : 0);
     const int k = 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
     const uint16_t* src = src_a;
     long long srow = r;
-    if (mode == PACK_ROPE) {
-      const int head = r / hd, j = r % hd, m = j / 16, i = j % 16;
+    long long nsrc = n_src_rows;
+    if (mode == PACK_QKV) {
+      const int head = r / hd, jj = r % hd, m = jj / 16, i = jj % 16;
       const int dim = (i < 8) ? 8 * m + i : hd / 2 + 8 * m + (i - 8);
-      srow = (long long)head * hd + dim;
+      if (head < gs) { src = src_a; srow = (long long)(grp * gs + head) * hd + dim; }
+      else { src = (head == gs) ? src_b : src_c; srow = (long long)grp * hd + dim; }
+      nsrc = 1ll << 40;
     } else if (mode == PACK_GATE_UP) {
       const int blk = r / 16, i = r % 16;
       src = (i < 8) ? src_a : src_b;
       srow = 8LL * blk + (i & 7);
     }
     for (int e = 0; e < 2; ++e)
-      out[2 * q + e] = (srow < n_src_rows) ? src[srow * ld + col0 + k + e] : (uint16_t)0;
+      out[2 * q + e] = (srow < nsrc) ? src[srow * ld + col0 + k + e] : (uint16_t)0;
   }
   uint4 v;
   v.x = out[0] | ((uint32_t)out[1] << 16);
@@ -1175,15 +1235,16 @@ __global__ void mk_convert_kernel(float* __restrict__ dst, const uint16_t* __res
 // ============================================================== host-side launchers
 namespace mk {
 
-cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, int n_rows_packed,
-                        int n_src_rows, int K, long long ld, int col0, int mode, int hd,
-                        cudaStream_t st) {
+cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, const void* src_c,
+                        int n_rows_packed, int n_src_rows, int K, long long ld, int col0, int mode, int hd,
+                        int gs, int grp, int tile_rows, cudaStream_t st) {
   const long long total = (long long)(n_rows_packed / 16) * (K / 16) * 32;
   if (total == 0) return cudaSuccess;
   const int threads = 256;
   const long long blocks = (total + threads - 1) / threads;
   mk_pack_kernel<<<(unsigned)blocks, threads, 0, st>>>(dst, (const uint16_t*)src_a, (const uint16_t*)src_b,
-                                                     n_rows_packed, n_src_rows, K, ld, col0, mode, hd);
+                                                     (const uint16_t*)src_c, n_rows_packed, n_src_rows, K, ld,
+                                                     col0, mode, hd, gs, grp, tile_rows);
   return cudaGetLastError();
 }
 

@@ -33,6 +33,9 @@ MODELS = {
                   n_experts=128, top_k=8, d_ff=768, vocab=151936, rope_theta=1e6,
                   rms_eps=1e-6, sliding_window=0, swa_layers=()),
 }
+# Two layers of the pages-scale shape: small enough (3.7 GB) for profiler captures
+# and for the oracle to run in seconds, with every tile size of the full model.
+MODELS["pages_l2"] = dict(MODELS["pages"], n_layers=2)
 
 # Workloads: a model plus a batch of cached sequence lengths.
 WORKLOADS = {
@@ -42,6 +45,9 @@ WORKLOADS = {
     "pages_b8_ragged_swa": dict(model="pages", batch=8, lens=("uniform", 1024, 32768),
                                 sliding_window=4096, swa="odd"),
     "pages_b1_128k": dict(model="pages", batch=1, lens=("fixed", 131072)),
+    "pages_l2_b1_8k": dict(model="pages_l2", batch=1, lens=("fixed", 8192)),
+    "pages_l2_b8_ragged_swa": dict(model="pages_l2", batch=8, lens=("uniform", 1024, 32768),
+                                   sliding_window=4096, swa="odd"),
 }
 
 
