@@ -46,7 +46,8 @@ typedef enum mk_status {
 
 /* Model shape.  The kernels need: head_dim in {32, 64, 128}; d_model, d_ff and
  * (n_q_heads / n_kv_heads) * head_dim multiples of 128; n_q_heads divisible by
- * n_kv_heads with a group of at most 8 query heads and group*head_dim <= 1024;
+ * n_kv_heads (at most 8) with a group of at most 8 query heads and
+ * group*head_dim <= 1024;
  * n_experts <= 256; top_k <= 8; page_size == 16; max_batch <= 8; n_layers <= 64.
  * swa_layer_mask bit l set = layer l uses a sliding window of sliding_window keys
  * (the window holds the new token and the sliding_window - 1 keys before it).
@@ -143,12 +144,15 @@ int mk_decode_step_perop(mk_handle* h, const int32_t* tokens_dev, void* k_cache,
  * it.  Returns info->code. */
 int mk_get_status(mk_handle* h, mk_error_info* info);
 
-/* Task timeline for profiling.  records_dev: DEVICE uint64 [capacity][8], owned by
+/* Task timeline for profiling.  records_dev: DEVICE uint64 [capacity][16], owned by
  * the caller; every task executed by a later step appends one record
  *   [0] sm | opcode << 8 | layer << 16 | (ran a fan-in follow-up) << 24
  *   [1] claimed item (attention split / expert tile) or 0
- *   [2..7] %globaltimer ns: received, dependency met, first weight/KV chunk landed,
- *          MMA loop done, fan-in follow-up started (0 if none), done.
+ *   [2..7] %globaltimer ns: received, dependency met, operands built / first
+ *          weight or KV chunk landed, MMA loop done, fan-in follow-up started (0
+ *          if none), done
+ *   [8..11] sub-steps of a fan-in follow-up (route step: top-k done, lists
+ *          started, lists done, released), 0 where unused; [12..15] zero.
  * capacity 0 (or records_dev NULL with capacity 0) turns tracing off.  Resets the
  * record count.  Synchronising. */
 int mk_set_trace(mk_handle* h, void* records_dev, int capacity);

@@ -202,7 +202,7 @@ def mk_set_fixed(h, fixed: bool):
 
 
 def mk_set_trace(h, records, capacity: int):
-    """records: uint64/int64 CUDA tensor [capacity, 8] (or None with capacity 0)."""
+    """records: uint64/int64 CUDA tensor [capacity, 16] (or None with capacity 0)."""
     _check(load_library().mk_set_trace(h, records.data_ptr() if records is not None else None,
                                        int(capacity)), h)
 
@@ -274,7 +274,7 @@ class Megakernel:
 
     def trace_on(self, capacity=1 << 20):
         import torch
-        self._trace = torch.zeros((capacity, 8), dtype=torch.int64, device="cuda")
+        self._trace = torch.zeros((capacity, 16), dtype=torch.int64, device="cuda")
         mk_set_trace(self.h, self._trace, capacity)
 
     def trace_off(self):
@@ -282,7 +282,7 @@ class Megakernel:
         self._trace = None
 
     def trace_records(self):
-        """int64 array [n, 8] of the records appended since trace_on()."""
+        """int64 array [n, 16] of the records appended since trace_on()."""
         n = int(mk_read(self.h, MK_READ_TRACE_COUNT, (1,), np.uint32)[0])
         n = min(n, self._trace.shape[0])
         return self._trace[:n].cpu().numpy()

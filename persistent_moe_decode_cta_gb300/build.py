@@ -30,6 +30,7 @@ def nvcc_path() -> str:
 
 def _flags(extra_ptxas=False):
     f = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+         "-maxrregcount=224",
          "-I" + os.path.join(ROOT, "include"), "-I" + CSRC] + ARCH
     if extra_ptxas:
         f += ["-Xptxas", "-v"]

@@ -19,14 +19,19 @@ struct Smem {
   float* scratch;     // kScratchBytes
   uint32_t scratch_s;
   int* small;         // kSmallBytes
-  uint32_t bars;      // full[kStages], empty[kStages], mfull[kMbox], mempty[kMbox]
+  uint32_t bars;      // full[kStages], empty[kStages], mfull[kMbox], mempty[kMbox], sfull[kSq], sempty[kSq]
   int4* mbox;
+  int2* sq;           // signal requests [kSq]
 
   __device__ __forceinline__ uint32_t full(uint32_t s) const { return bars + 8u * s; }
   __device__ __forceinline__ uint32_t empty(uint32_t s) const { return bars + 8u * (kStages + s); }
   __device__ __forceinline__ uint32_t mfull(uint32_t m) const { return bars + 8u * (2 * kStages + m); }
   __device__ __forceinline__ uint32_t mempty(uint32_t m) const {
     return bars + 8u * (2 * kStages + kMbox + m);
+  }
+  __device__ __forceinline__ uint32_t sfull(uint32_t q) const { return bars + 8u * (2 * kStages + 2 * kMbox + q); }
+  __device__ __forceinline__ uint32_t sempty(uint32_t q) const {
+    return bars + 8u * (2 * kStages + 2 * kMbox + kSq + q);
   }
   __device__ __forceinline__ uint32_t stage(uint32_t seq) const {
     return ring + (seq % kStages) * (uint32_t)kStageBytes;
@@ -50,6 +55,7 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
   S.bars = aligned + kStages * kStageBytes + kScratchBytes + kSmallBytes;
   S.mbox = reinterpret_cast<int4*>(g + kStages * kStageBytes + kScratchBytes + kSmallBytes +
                                    kBarBytes);
+  S.sq = reinterpret_cast<int2*>(S.mbox + kMbox);
   return S;
 }
 
@@ -122,6 +128,12 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
   unsigned old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
@@ -149,6 +161,20 @@ __device__ __forceinline__ uint32_t ldg_cg_u32(const void* p) {
 }
 __device__ __forceinline__ float2 ldg_cg_f2(const float* p) {
   return __ldcg(reinterpret_cast<const float2*>(p));
+}
+// Predicated L2 loads: `v` keeps its value when `pred` is false.  Written as one
+// straight run of asm loads so that a whole operand's loads are in flight together.
+__device__ __forceinline__ void ldg_cg_pred(uint32_t& v, const void* ptr, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.cg.u32 %0, [%1];\n\t}"
+      : "+r"(v)
+      : "l"(ptr), "r"((int)pred));
+}
+__device__ __forceinline__ void ldg_cg_pred(float& v, const float* ptr, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.cg.f32 %0, [%1];\n\t}"
+      : "+f"(v)
+      : "l"(ptr), "r"((int)pred));
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;

@@ -31,6 +31,8 @@ cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, cons
                         int n_rows_packed, int n_src_rows, int K, long long ld, int col0, int mode, int hd,
                         int gs, int grp, int tile_rows, cudaStream_t st);
 cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_t st);
+cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+                            cudaStream_t st);
 cudaError_t prepare_megakernel();
 int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
@@ -49,10 +51,10 @@ struct Shape {
   int r_qkv, qkv_rows_group, qkv_tpg;
   int r_router, n_router_tasks, e_pad;
   int r_o, t_o, k_o;
-  int r_up, t_up, r_dn, t_dn;
+  int t_moe;
   int r_lm, v_pad, n_lm_tasks;
-  size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, up_bytes_e, dn_bytes_e, lm_bytes, embed_bytes;
-  size_t off_qkv, off_o, off_router, off_up, off_dn, off_lm, off_embed, total;
+  size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
+  size_t off_qkv, off_o, off_router, off_moe, off_lm, off_embed, total;
 };
 
 int fail(std::string* dst, int code, const char* fmt, ...) {
@@ -72,11 +74,12 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.E = c->n_experts; s.topk = c->top_k; s.f = c->d_ff; s.V = c->vocab; s.max_batch = c->max_batch;
   if (s.L < 1 || s.L > 64) return fail(err, MK_ERR_UNSUPPORTED, "n_layers %d not in [1, 64]", s.L);
   if (s.hd != 32 && s.hd != 64 && s.hd != 128) return fail(err, MK_ERR_UNSUPPORTED, "head_dim %d not in {32,64,128}", s.hd);
-  if (s.d < 128 || s.d % 128 || s.d > 2048) return fail(err, MK_ERR_UNSUPPORTED, "d_model %d must be a multiple of 128 <= 2048", s.d);
+  if (s.d < 256 || s.d % 256 || s.d > 2048) return fail(err, MK_ERR_UNSUPPORTED, "d_model %d must be a multiple of 256 <= 2048", s.d);
   if (s.f < 128 || s.f % 128 || s.f > 2048) return fail(err, MK_ERR_UNSUPPORTED, "d_ff %d must be a multiple of 128 <= 2048", s.f);
   if (s.Hkv < 1 || s.Hq < 1 || s.Hq % s.Hkv) return fail(err, MK_ERR_UNSUPPORTED, "n_q_heads %d not divisible by n_kv_heads %d", s.Hq, s.Hkv);
   s.gs = s.Hq / s.Hkv;
   if (s.gs > 8) return fail(err, MK_ERR_UNSUPPORTED, "query group %d > 8", s.gs);
+  if (s.Hkv > 8) return fail(err, MK_ERR_UNSUPPORTED, "n_kv_heads %d > 8", s.Hkv);
   if ((s.gs * s.hd) % 128 || s.gs * s.hd > 1024) return fail(err, MK_ERR_UNSUPPORTED, "group*head_dim %d must be a multiple of 128 <= 1024", s.gs * s.hd);
   if (s.E < 1 || s.E > 256) return fail(err, MK_ERR_UNSUPPORTED, "n_experts %d not in [1, 256]", s.E);
   if (s.topk < 1 || s.topk > 8 || s.topk > s.E) return fail(err, MK_ERR_UNSUPPORTED, "top_k %d not in [1, min(8, E)]", s.topk);
@@ -87,20 +90,19 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return fail(err, MK_ERR_INVALID, "bad rms_eps / rope_theta");
   s.nrb_d = s.d / kRowBlock;
   s.qkv_rows_group = (s.gs + 2) * s.hd;
-  s.r_qkv = (s.qkv_rows_group % 64 == 0) ? 64 : (s.qkv_rows_group % 32 == 0 ? 32 : 16);
+  s.r_qkv = (s.qkv_rows_group % 32 == 0) ? 32 : 16;  // 128 KB tiles at d 2048: one fits the ring
   s.qkv_tpg = s.qkv_rows_group / s.r_qkv;
   s.r_router = 16;
   s.e_pad = (s.E + 15) / 16 * 16;
   s.n_router_tasks = s.e_pad / s.r_router;
   s.r_o = 64; s.t_o = s.d / s.r_o; s.k_o = s.gs * s.hd;
-  s.r_up = 64; s.t_up = 2 * s.f / s.r_up;
-  s.r_dn = 64; s.t_dn = s.d / s.r_dn;
+  s.t_moe = s.f / kMoeFs;
   s.r_lm = 64; s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
   s.router_layer_bytes = (size_t)s.e_pad * s.d * 2;
-  s.up_bytes_e = (size_t)2 * s.f * s.d * 2;
-  s.dn_bytes_e = (size_t)s.d * s.f * 2;
+  s.moe_item_bytes = (size_t)3 * kMoeFs * s.d * 2;
+  s.moe_bytes_e = s.moe_item_bytes * s.t_moe;
   s.lm_bytes = (size_t)s.v_pad * s.d * 2;
   s.embed_bytes = (size_t)s.V * s.d * 2;
   size_t o = 0;
@@ -108,8 +110,7 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.off_qkv = take(s.qkv_layer_bytes * s.L);
   s.off_o = take(s.o_layer_bytes * s.L);
   s.off_router = take(s.router_layer_bytes * s.L);
-  s.off_up = take(s.up_bytes_e * s.E * s.L);
-  s.off_dn = take(s.dn_bytes_e * s.E * s.L);
+  s.off_moe = take(s.moe_bytes_e * s.E * s.L);
   s.off_lm = take(s.lm_bytes);
   s.off_embed = take(s.embed_bytes);
   s.total = o;
@@ -117,11 +118,11 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
 }
 
 // ------------------------------------------------------------------ planner
-enum Wave { W_QKV = 0, W_ROUTER, W_ATT, W_UP, W_DN, W_OPROJ, W_COUNT };
+enum Wave { W_QKV = 0, W_ROUTER, W_ATT, W_MOE, W_OPROJ, W_RESID, W_COUNT };
 
 struct PlanOut {
   int B = 0, maxa = 0, n_sm = 0;
-  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_up, c_rb, c_done, n_ctr;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_done, n_ctr;
   int rb_target;
   std::vector<int32_t> tasks;     // n_tasks * 32
   std::vector<int32_t> sm_off;    // n_segs * (n_sm + 1), absolute offsets into sm_list
@@ -131,15 +132,15 @@ struct PlanOut {
 };
 
 bool parse_wave_order(const char* s, std::vector<int>& order) {
-  // letters: q=QKV r=router a=attention u=expert up d=expert down o=O-proj
+  // letters: q=QKV r=router a=attention m=MoE items o=O-proj x=ADD_RMSNORM
   order.clear();
   for (const char* c = s; *c; ++c) {
     switch (*c) {
       case 'q': order.push_back(W_QKV); break;
       case 'r': order.push_back(W_ROUTER); break;
       case 'a': order.push_back(W_ATT); break;
-      case 'u': order.push_back(W_UP); break;
-      case 'd': order.push_back(W_DN); break;
+      case 'm': order.push_back(W_MOE); break;
+      case 'x': order.push_back(W_RESID); break;
       case 'o': order.push_back(W_OPROJ); break;
       default: return false;
     }
@@ -148,8 +149,8 @@ bool parse_wave_order(const char* s, std::vector<int>& order) {
   auto pos = [&](int w) { return (int)(std::find(order.begin(), order.end(), w) - order.begin()); };
   for (int w = 0; w < W_COUNT; ++w) if (pos(w) >= W_COUNT) return false;
   // every order that respects the dependencies is deadlock-free with in-order lists
-  return pos(W_QKV) < pos(W_ATT) && pos(W_ATT) < pos(W_OPROJ) && pos(W_ROUTER) < pos(W_UP) &&
-         pos(W_UP) < pos(W_DN);
+  return pos(W_QKV) < pos(W_ATT) && pos(W_ATT) < pos(W_OPROJ) && pos(W_ROUTER) < pos(W_MOE) &&
+         pos(W_MOE) < pos(W_RESID) && pos(W_OPROJ) < pos(W_RESID);
 }
 
 int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, PlanOut& P, std::string* err) {
@@ -166,11 +167,11 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   P.c_rr = c; c += L;
   P.c_att = c; c += L * B * s.Hkv;
   P.c_og = c; c += L * s.Hkv;
-  P.c_up = c; c += L * P.maxa;
+  P.c_md = c; c += L;
   P.c_rb = c; c += L * s.nrb_d;
   P.c_done = c; c += 1;
   P.n_ctr = c;
-  P.rb_target = s.Hkv * (kRowBlock / s.r_o) + P.maxa * (kRowBlock / s.r_dn);
+  P.rb_target = s.Hkv * (kRowBlock / s.r_o);  // O-proj tiles of a residual row block
 
   auto add = [&](int op, int layer, int aux, int row0, int nrows, int k0, int klen, int wc, int wt, int sc,
                  int st, size_t woff, int wbytes, int wave) {
@@ -204,8 +205,8 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
                        s.n_router_tasks, s.off_router + l * s.router_layer_bytes + (size_t)t * s.r_router * s.d * 2,
                        s.r_router * s.d * 2, W_ROUTER));
     drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
-    drains[(size_t)l * W_COUNT + W_UP] = add(OP_UP_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, -1, 0, 0, 0, W_UP);
-    drains[(size_t)l * W_COUNT + W_DN] = add(OP_DN_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, -1, 0, 0, 0, W_DN);
+    drains[(size_t)l * W_COUNT + W_MOE] =
+        add(OP_MOE_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
     auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
     for (int g = 0; g < s.Hkv; ++g)
       for (int t = 0; t < s.t_o; ++t)
@@ -213,6 +214,16 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
                          P.c_rb + l * s.nrb_d + (t * s.r_o) / kRowBlock, P.rb_target,
                          s.off_o + l * s.o_layer_bytes + (size_t)g * s.d * s.k_o * 2 + (size_t)t * s.r_o * s.k_o * 2,
                          s.r_o * s.k_o * 2, W_OPROJ));
+  }
+  for (int l = 0; l < L; ++l) {
+    auto& wx = waves[(size_t)l * W_COUNT + W_RESID];
+    for (int r = 0; r < s.nrb_d; ++r) {
+      const int t = add(OP_RESID, l, r, r * kRowBlock, kRowBlock, 0, 0, P.c_rb + l * s.nrb_d + r, P.rb_target,
+                        P.c_lr + l + 1, s.nrb_d, 0, 0, W_RESID);
+      P.tasks[(size_t)t * kDescInts + D_WAIT2_CTR] = P.c_md + l;
+      P.tasks[(size_t)t * kDescInts + D_WAIT2_TARGET] = P.maxa * s.t_moe;
+      wx.push_back(t);
+    }
   }
   std::vector<int> lm;
   for (int t = 0; t < s.n_lm_tasks; ++t)
@@ -230,7 +241,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     P.sm_off.push_back(o);
     P.n_segs++;
   };
-  auto is_drain = [](int w) { return w == W_ATT || w == W_UP || w == W_DN; };
+  auto is_drain = [](int w) { return w == W_ATT || w == W_MOE; };
   // segment 0: the whole step for the megakernel
   {
     std::vector<std::vector<int>> lists(n_sm);
@@ -279,7 +290,9 @@ int choose_split_pages(int max_pages) {
   return std::max(8, sp);
 }
 
-const char* default_order() { return "qraudo"; }
+// Router first: its weights are then prefetched behind the previous layer's tasks
+// rather than behind this layer's QKV tiles.
+const char* default_order() { return "rqamox"; }
 
 }  // namespace
 
@@ -291,6 +304,7 @@ struct mk_handle {
   std::string err;
   uint8_t* wblob = nullptr;
   float* norms = nullptr;  // attn [L][d] then final [d]
+  unsigned long long* rope_turns = nullptr;  // [hd/2]
   // plan
   bool planned = false;
   PlanOut P;
@@ -451,6 +465,19 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
   if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "packed weights (%zu B): %s", s.total, cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
   e = cudaMalloc(&h->norms, sizeof(float) * ((size_t)s.L * s.d + s.d));
   if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "norms: %s", cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
+  {
+    // RoPE inverse frequencies theta^(-2i/hd) as exact 0.64 fixed-point turns per position
+    std::vector<unsigned long long> turns(s.hd / 2);
+    for (int i = 0; i < s.hd / 2; ++i) {
+      const long double inv = powl((long double)cfg->rope_theta, -2.0L * i / s.hd);
+      const long double t = inv / (2.0L * 3.14159265358979323846264338327950288L);
+      turns[i] = (unsigned long long)(t * 18446744073709551616.0L);
+    }
+    e = cudaMalloc(&h->rope_turns, turns.size() * sizeof(unsigned long long));
+    if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "rope table: %s", cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
+    e = cudaMemcpy(h->rope_turns, turns.data(), turns.size() * sizeof(unsigned long long), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) { cuda_fail(h, e, "rope table copy"); return bail(MK_ERR_CUDA); }
+  }
 
   // ---- pack
   const int L = s.L, d = s.d, hd = s.hd, gs = s.gs, f = s.f, E = s.E;
@@ -472,10 +499,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
        PACK_IDENT, hd, gs, 0, s.r_router);
     for (int e2 = 0; e2 < E; ++e2) {
       const int i = l * E + e2;
-      PK(h->wblob + s.off_up + (size_t)i * s.up_bytes_e, w->w_gate[i], w->w_up[i], nullptr, 2 * f, f, d, d, 0,
-         PACK_GATE_UP, hd, gs, 0, s.r_up);
-      PK(h->wblob + s.off_dn + (size_t)i * s.dn_bytes_e, w->w_down[i], nullptr, nullptr, d, d, f, f, 0, PACK_IDENT,
-         hd, gs, 0, s.r_dn);
+      e = launch_pack_moe(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i], w->w_down[i], d,
+                          f, st);
+      if (e != cudaSuccess) { cuda_fail(h, e, "pack moe"); return bail(MK_ERR_CUDA); }
     }
     e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
     if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
@@ -506,7 +532,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
   if (info_out) {
     int32_t* I = info_out;
     I[0] = P.n_tasks(); I[1] = list_len; I[2] = P.n_ctr; I[3] = P.maxa; I[4] = 0;
-    I[5] = s.t_up; I[6] = s.t_dn; I[7] = s.r_o; I[8] = s.r_dn; I[9] = s.r_up; I[10] = s.qkv_tpg;
+    I[5] = s.t_moe; I[6] = (int)(s.moe_item_bytes / 1024); I[7] = s.r_o; I[8] = kMoeFs; I[9] = s.r_qkv; I[10] = s.qkv_tpg;
     I[11] = s.n_router_tasks; I[12] = P.rb_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
@@ -559,19 +585,23 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.swa_mask = h->cfg.swa_layer_mask; p.theta = h->cfg.rope_theta; p.eps = h->cfg.rms_eps;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.hd));
   p.split_pages = h->split_pages; p.max_items_bg = h->max_items_bg;
-  p.r_up = s.r_up; p.r_dn = s.r_dn; p.t_up = s.t_up; p.t_dn = s.t_dn; p.qkv_tpg = s.qkv_tpg;
+  p.t_moe = s.t_moe; p.qkv_tpg = s.qkv_tpg;
   p.n_router_tasks = s.n_router_tasks;
   p.timeout_ns = (long long)h->cfg.timeout_ms * 1000000ll;
-  p.wblob = h->wblob; p.off_up = (long long)s.off_up; p.off_dn = (long long)s.off_dn;
-  p.up_bytes_e = (long long)s.up_bytes_e; p.dn_bytes_e = (long long)s.dn_bytes_e;
+  p.inflight = 2;
+  if (const char* fl = getenv("MK_INFLIGHT")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight = v; }
+  p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
   p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
+  p.rope_turns = h->rope_turns;
   p.embed = reinterpret_cast<const uint16_t*>(h->wblob + s.off_embed);
   p.page_table = page_table_dev;
   const size_t maxa = (size_t)P.maxa;
 #define AL(ptr, n) do { int _r = alloc(h, &(ptr), (n)); if (_r) { free_plan(h); return _r; } } while (0)
   AL(p.seq_lens, B);
   AL(p.X, (size_t)(L + 1) * B * s.d);
-  AL(p.SS, (size_t)(L + 1) * s.nrb_d * B);
+  AL(p.SS, (size_t)(L + 1) * s.nrb_d * kSsStride);
+  AL(p.XG, (size_t)(L + 1) * B * s.d);
+  AL(p.XGL, (size_t)(L + 1) * B * s.d);
   AL(p.Q, (size_t)L * B * s.Hq * s.hd);
   AL(p.attp, (size_t)L * s.Hkv * B * h->max_items_bg * s.gs * (s.hd + 2));
   AL(p.atto, (size_t)L * B * s.Hq * s.hd);
@@ -583,9 +613,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(p.nact, (size_t)L);
   AL(p.act_cnt, (size_t)L * maxa);
   AL(p.act_tok, (size_t)L * maxa * B);
-  AL(p.aup, (size_t)L * maxa * B * s.f);
-  AL(p.Y, (size_t)L * B * s.topk * s.d);
-  AL(p.ctr, (size_t)P.n_ctr);
+  AL(p.moe, (size_t)L * B * s.d);
+  AL(p.ctr, (size_t)P.n_ctr * kCtrStride);
   AL(p.qhead, (size_t)3 * L);
   AL(p.qcount, (size_t)3 * L);
   AL(p.err, 16);
@@ -597,7 +626,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(h->d_trace_n, 1);
 #undef AL
   p.c_lr = P.c_lr; p.c_qkvg = P.c_qkvg; p.c_rt = P.c_rt; p.c_rr = P.c_rr; p.c_att = P.c_att; p.c_og = P.c_og;
-  p.c_up = P.c_up; p.c_rb = P.c_rb; p.c_done = P.c_done; p.n_ctr = P.n_ctr; p.n_queues = 3 * L;
+  p.c_md = P.c_md; p.c_rb = P.c_rb; p.c_done = P.c_done; p.n_ctr = P.n_ctr; p.n_queues = 3 * L;
   p.rb_target = P.rb_target;
   p.tasks = h->d_tasks; p.sm_off = h->d_sm_off; p.sm_list = h->d_sm_list;
   p.trace = nullptr; p.trace_n = h->d_trace_n; p.trace_cap = 0;
@@ -726,7 +755,14 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
     case MK_READ_ROUTES: return copy(p.ridx, L * B * s.topk * 4);
     case MK_READ_ROUTE_W: return copy(p.rw, L * B * s.topk * 4);
     case MK_READ_SEQ_LENS: return copy(p.seq_lens, B * 4);
-    case MK_READ_COUNTERS: return copy(p.ctr, (size_t)p.n_ctr * 4);
+    case MK_READ_COUNTERS: {
+      if (bytes != (size_t)p.n_ctr * 4) return fail(&h->err, MK_ERR_INVALID, "mk_read(COUNTERS): need %zu bytes", (size_t)p.n_ctr * 4);
+      std::vector<unsigned> raw((size_t)p.n_ctr * kCtrStride);
+      CK(h, cudaMemcpy(raw.data(), p.ctr, raw.size() * 4, cudaMemcpyDeviceToHost));
+      unsigned* o = static_cast<unsigned*>(host_out);
+      for (int i = 0; i < p.n_ctr; ++i) o[i] = raw[(size_t)i * kCtrStride];
+      return MK_OK;
+    }
     case MK_READ_ROUTER_LOGITS: return copy(p.rlog, L * B * s.E * 4);
     case MK_READ_TRACE_COUNT: return copy(h->d_trace_n, 4);
     case MK_READ_ACTIVE: {
@@ -788,6 +824,7 @@ void mk_destroy(mk_handle* h) {
   free_plan(h);
   if (h->wblob) cudaFree(h->wblob);
   if (h->norms) cudaFree(h->norms);
+  if (h->rope_turns) cudaFree(h->rope_turns);
   delete h;
 }
 

@@ -13,11 +13,15 @@
 namespace mk {
 
 // ---- CTA shape -------------------------------------------------------------
-// 8 consumer warps (MMA + epilogues) and 1 producer warp (descriptor walk, queue
-// claims, bulk/TMA copies into the shared-memory ring).  One CTA per SM.
+// 8 consumer warps (MMA + epilogues), 1 producer warp (descriptor walk, queue
+// claims, bulk/TMA copies into the shared-memory ring) and 1 storer warp (publishes
+// the consumers' completed outputs to the global counters, so consumers do not wait
+// on the release).  One CTA per SM.
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kStorerWarp = kConsumerWarps + 1;
+constexpr int kThreads = kConsumerThreads + 64;
 
 // ---- shared memory ---------------------------------------------------------
 constexpr int kStageBytes = 32768;            // one ring slot
@@ -25,19 +29,27 @@ constexpr int kStages = 6;                    // 192 KB of copies in flight per 
 constexpr int kScratchBytes = 32768;          // cross-warp reductions / merges
 constexpr int kSmallBytes = 1024;             // per-warp scalars, flags
 constexpr int kMbox = 8;                      // producer -> consumer task mailbox
+constexpr int kSq = 8;                        // consumer -> storer signal queue
 constexpr int kFragBytes = 512;               // one 16x16 bf16 MMA A-fragment
 constexpr int kFragsPerStage = kStageBytes / kFragBytes;
 constexpr int kMaxNrb = 8;                    // GEMV task rows <= 128
 constexpr int kMaxKsw = 16;                   // GEMV task K <= 2048 (16 k16-steps/warp)
-constexpr int kBarBytes = (2 * kStages + 2 * kMbox) * 8;
-constexpr int kMboxBytes = kMbox * 16;
+constexpr int kBarBytes = (2 * kStages + 2 * kMbox + 2 * kSq) * 8;
+constexpr int kMboxBytes = kMbox * 16 + kSq * 8;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kScratchBytes +
                            kSmallBytes + kBarBytes + kMboxBytes;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
 constexpr int kDescInts = 32;
+// Counters are padded to one 128-byte line each so that waiters on different
+// counters do not poll the same L2 line.
+constexpr int kCtrStride = 32;
+// Each residual row block's per-token sums of squares sit in their own 128-byte line
+// (every consumer of the normed input reads all of them).
+constexpr int kSsStride = 32;
 constexpr int kMaxBatch = 8;
 constexpr int kRowBlock = 128;                // residual row block (rows of d_model)
+constexpr int kMoeFs = 32;                    // d_ff rows of one MoE item (f-slice)
 
 enum Op : int32_t {
   OP_END = 0,
@@ -46,21 +58,29 @@ enum Op : int32_t {
   OP_ROUTER = 3,     // ROUTER_GEMM tile; last tile runs ROUTER_TOPK + ROUTE_FINALIZE
   OP_ATT_DRAIN = 4,  // ATTN_DRAIN: claim (group, seq, split) items; last split of a
                      // (seq, group) runs ATTN_COMBINE
-  OP_UP_DRAIN = 5,   // MOE_UPGATE_ACT_DRAIN (gather fused into the operand load)
-  OP_DN_DRAIN = 6,   // MOE_DOWN_DRAIN (weights the output by the routing weight)
+  OP_MOE_DRAIN = 5,  // MOE_UPGATE_ACT + MOE_DOWN + MOE_COMBINE for one (expert, f-slice)
+                     // item: gather fused into the operand load, SiLU-mul epilogue kept
+                     // in smem, the down slice's routing-weighted partial added into the
+                     // layer's MoE accumulator
   OP_OPROJ = 7,      // O_PROJ split-K by KV group
   OP_LMHEAD = 8,     // final RMSNorm + LM_HEAD tile
+  OP_RESID = 9,      // ADD_RMSNORM of one residual row block once the layer's O-proj
+                     // tiles for it and all MoE items are done
 };
 
 enum DescField : int {
   D_OP = 0, D_LAYER = 1, D_AUX = 2, D_ROW0 = 3, D_NROWS = 4, D_K0 = 5, D_KLEN = 6,
   D_WAIT_CTR = 7, D_WAIT_TARGET = 8, D_SIG_CTR = 9, D_SIG_TARGET = 10,
   D_WOFF_LO = 11, D_WOFF_HI = 12, D_WBYTES = 13, D_QUEUE = 14, D_TASK_ID = 15,
-  D_WAVE = 16
+  D_WAVE = 16, D_WAIT2_CTR = 17, D_WAIT2_TARGET = 18
 };
 
 // Row-map modes of the weight packer.
 enum PackMode : int { PACK_IDENT = 0, PACK_QKV = 1, PACK_GATE_UP = 2 };
+// MoE item (expert e, f-slice s = rows [32 s, 32 s + 32) of d_ff) packed as one
+// contiguous tile: the 64 interleaved gate/up rows x d_model (GEMV fragment order,
+// 4 row blocks), then the down slice W_down[:, 32 s : 32 s + 32] with consumer warp w
+// owning output rows [w d/8, (w+1) d/8) (fragment order [w][row block][k16-step]).
 
 // Device error word layout (int32[16]).
 enum ErrField : int { E_CODE = 0, E_TASK = 1, E_CTR = 2, E_OBS = 3, E_TARGET = 4,
@@ -73,12 +93,14 @@ struct Params {
   unsigned long long swa_mask;
   float theta, eps, scale_log2;
   int split_pages, max_items_bg;
-  int r_up, r_dn, t_up, t_dn, qkv_tpg, n_router_tasks;
+  int t_moe, qkv_tpg, n_router_tasks;  // t_moe = MoE items per expert = d_ff / kMoeFs
   long long timeout_ns;
   int fixed, do_reset;
+  int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   // weights
   const uint8_t* wblob;
-  long long off_up, off_dn, up_bytes_e, dn_bytes_e;
+  long long off_moe, moe_item_bytes;  // item (l, e, s) at off_moe + ((l*E + e)*t_moe + s) * item_bytes
+  const unsigned long long* rope_turns;  // [hd/2] inv_freq_i / (2 pi) as 0.64 fixed point
   const float* attn_norm;   // [L][d]
   const float* final_norm;  // [d]
   const uint16_t* embed;    // [V][d] bf16
@@ -91,7 +113,9 @@ struct Params {
   float* logits;            // [B][V]
   // activations (per layer)
   float* X;                 // [L+1][B][d]
-  float* SS;                // [L+1][nrb_d][B]
+  float* SS;                // [L+1][nrb_d][kSsStride]: token b's sum of squares at [.][.][b]
+  uint16_t* XG;             // [L+1][B][d] bf16(x_l * gain_l), gain_L = final norm
+  uint16_t* XGL;            // [L+1][B][d] bf16 of the rounding residue x_l*gain_l - XG
   uint16_t* Q;              // [L][B][Hq*hd]
   float* attp;              // [L][Hkv][B][max_items_bg][gs*(hd+2)]
   uint16_t* atto;           // [L][B][Hq*hd]
@@ -103,14 +127,13 @@ struct Params {
   int* nact;                // [L]
   int* act_cnt;             // [L][maxa]
   int* act_tok;             // [L][maxa][B]  (b*16 + j)
-  uint16_t* aup;            // [L][maxa][B][f]
-  float* Y;                 // [L][B][topk][d]
+  float* moe;               // [L][B][d] routing-weighted sum of the layer's expert outputs
   // synchronisation
   unsigned* ctr;
   int* qhead;               // [3L]
   int* qcount;              // [3L]
   int* err;                 // [16]
-  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_up, c_rb, c_done, n_ctr, n_queues;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_done, n_ctr, n_queues;
   int rb_target;
   // optional task timeline (see trace_emit)
   unsigned long long* trace;

@@ -37,9 +37,10 @@ __device__ __forceinline__ bool aborted(const Params& p) { return ld_volatile(&p
 
 // Optional per-task timeline (Params::trace != nullptr): thread 0 stamps the
 // moments of a task into shared memory and appends one record when it ends.
-//   record (8 x u64): [0] sm | op << 8 | layer << 16 | fan-in << 24, [1] item,
-//   [2] received, [3] dependency met, [4] first weight/KV chunk landed,
-//   [5] MMA loop done, [6] fan-in follow-up started (0 if none), [7] task done.
+//   record (16 x u64): [0] sm | op << 8 | layer << 16 | fan-in << 24, [1] item,
+//   [2] received, [3] dependency met (activation loads start), [4] first weight/KV
+//   chunk landed (activations built), [5] MMA loop done, [6] fan-in follow-up
+//   started (0 if none), [7] task done, [8..11] sub-steps of a fan-in follow-up.
 __device__ __forceinline__ unsigned long long* trace_slots(const Smem& S) {
   return reinterpret_cast<unsigned long long*>(S.small + 192);
 }
@@ -50,24 +51,34 @@ __device__ void trace_emit(const Params& p, const Smem& S, int op, int layer, in
   if (!p.trace || threadIdx.x != 0) return;
   const unsigned idx = atomicAdd(p.trace_n, 1u);
   if (idx >= (unsigned)p.trace_cap) return;
-  unsigned long long* r = p.trace + (size_t)idx * 8;
+  unsigned long long* r = p.trace + (size_t)idx * 16;
   unsigned long long* t = trace_slots(S);
   r[0] = (unsigned long long)blockIdx.x | ((unsigned long long)op << 8) |
          ((unsigned long long)(layer & 0xff) << 16) | ((unsigned long long)(t[6] != 0) << 24);
   r[1] = (unsigned long long)(unsigned)item;
   r[2] = t[0]; r[3] = t[1]; r[4] = t[2]; r[5] = t[3]; r[6] = t[6]; r[7] = gtime();
+  r[8] = t[8]; r[9] = t[9]; r[10] = t[10]; r[11] = t[11];
+  r[12] = r[13] = r[14] = r[15] = 0ull;
 }
 
-// Spin until ctr >= target (acquire), bounded by the timeout and the abort flag.
+// Spin until ctr >= target, bounded by the timeout and the abort flag.  Polls are
+// relaxed loads with a growing back-off (32 ns .. 256 ns) so that the many waiters
+// of a layer boundary do not saturate the counter's L2 line; the final observation
+// is followed by an acquire fence.
 __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
-  const unsigned* c = p.ctr + ci;
+  const unsigned* c = p.ctr + (size_t)ci * kCtrStride;
   if (ld_acquire(c) >= target) return true;
   const uint64_t t0 = gtime();
+  unsigned ns = 32;
   for (int it = 0;; ++it) {
-    __nanosleep(32);
-    const unsigned v = ld_acquire(c);
-    if (v >= target) return true;
-    if ((it & 15) == 15) {
+    __nanosleep(ns);
+    ns = ns < 256 ? ns * 2 : 256;
+    const unsigned v = ld_relaxed(c);
+    if (v >= target) {
+      fence_acq_rel_gpu();
+      return true;
+    }
+    if ((it & 7) == 7) {
       if (aborted(p)) return false;
       if ((long long)(gtime() - t0) > p.timeout_ns) {
         raise_err(p, MK_ERR_TIMEOUT, task, ci, (int)v, (int)target);
@@ -76,6 +87,8 @@ __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
     }
   }
 }
+
+__device__ __forceinline__ unsigned* ctr_ptr(const Params& p, int ci) { return p.ctr + (size_t)ci * kCtrStride; }
 
 // Consumer-side wait: thread 0 polls, the others learn the result at a barrier.
 __device__ bool consumer_wait(const Params& p, const Smem& S, int ci, unsigned target, int task) {
@@ -91,6 +104,35 @@ __device__ bool consumer_wait(const Params& p, const Smem& S, int ci, unsigned t
   const int ok = S.small[0];
   bar_sync_consumers();
   return ok != 0;
+}
+
+// Hand a counter release to the storer warp and carry on: each consumer warp orders
+// its own output stores before its lane 0 arrives on the request's mbarrier (CTA-scope
+// release); the storer waits for all eight warps (acquire) and then performs the
+// GPU-scope release-add, which covers the stores it has synchronised with.
+__device__ __forceinline__ void signal_async(const Params& p, const Smem& S, uint32_t& sseq, int ci, unsigned v) {
+  const uint32_t slot = sseq % kSq, use = sseq / kSq;
+  const int lane = threadIdx.x & 31;
+  if (use > 0 && lane == 0) mbar_wait(S.sempty(slot), (use - 1) & 1u, 8 * p.timeout_ns);
+  __syncwarp();
+  if (threadIdx.x == 0) S.sq[slot] = make_int2(ci, (int)v);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(S.sfull(slot));
+  ++sseq;
+}
+
+__device__ void storer(const Params& p, const Smem& S) {
+  for (uint32_t q = 0;; ++q) {
+    const uint32_t slot = q % kSq;
+    if (!mbar_wait(S.sfull(slot), (q / kSq) & 1u, 8 * p.timeout_ns)) {
+      raise_err(p, MK_ERR_TIMEOUT, -8, -1, (int)q, 0);
+      break;
+    }
+    const int2 r = S.sq[slot];
+    mbar_arrive(S.sempty(slot));
+    if (r.x < 0) break;
+    red_release(ctr_ptr(p, r.x), (unsigned)r.y);
+  }
 }
 
 __device__ __forceinline__ bool wait_full(const Params& p, const Smem& S, uint32_t seq) {
@@ -121,7 +163,7 @@ __device__ __forceinline__ int C_ATT(const Params& p, int l, int b, int g) {
   return p.c_att + (l * p.B + b) * p.Hkv + g;
 }
 __device__ __forceinline__ int C_OG(const Params& p, int l, int g) { return p.c_og + l * p.Hkv + g; }
-__device__ __forceinline__ int C_UP(const Params& p, int l, int a) { return p.c_up + l * p.maxa + a; }
+__device__ __forceinline__ int C_MD(const Params& p, int l) { return p.c_md + l; }
 __device__ __forceinline__ int C_RB(const Params& p, int l, int r) { return p.c_rb + l * p.nrb_d + r; }
 
 struct AttItem {
@@ -132,14 +174,17 @@ struct AttItem {
   int part;             // partial slot: ((g*B + b) * max_items_bg + s)
 };
 
+// seq_lens are constant during a step: the kernel prologue copies them to smem.
+__device__ __forceinline__ const int* seq_lens_s(const Smem& S) { return S.small + 224; }
+
 __device__ __forceinline__ int layer_window(const Params& p, int l) {
   return ((p.swa_mask >> l) & 1ull) ? p.window : 0;
 }
 
 // Splits of the cached keys in the window of sequence b at layer l.
-__device__ __forceinline__ void att_range(const Params& p, int l, int b, int& pos, int& lo,
+__device__ __forceinline__ void att_range(const Params& p, const Smem& S, int l, int b, int& pos, int& lo,
                                           int& first_pg, int& npg, int& ns) {
-  pos = p.seq_lens[b];
+  pos = seq_lens_s(S)[b];
   const int w = layer_window(p, l);
   lo = (w > 0) ? max(0, pos - w + 1) : 0;
   if (pos > lo) {
@@ -153,11 +198,11 @@ __device__ __forceinline__ void att_range(const Params& p, int l, int b, int& po
   }
 }
 
-__device__ int att_item_count(const Params& p, int l) {
+__device__ int att_item_count(const Params& p, const Smem& S, int l) {
   int per_g = 0;
   for (int b = 0; b < p.B; ++b) {
     int pos, lo, fp, npg, ns;
-    att_range(p, l, b, pos, lo, fp, npg, ns);
+    att_range(p, S, l, b, pos, lo, fp, npg, ns);
     per_g += ns + 1;
   }
   return per_g * p.Hkv;
@@ -165,19 +210,14 @@ __device__ int att_item_count(const Params& p, int l) {
 
 // Items are ordered by (group, sequence, split): group 0's items come first, in
 // step with the QKV tiles, which are dealt group by group.
-__device__ AttItem att_decode(const Params& p, int l, int item) {
-  int per_g = 0;
-  for (int b = 0; b < p.B; ++b) {
-    int pos, lo, fp, npg, ns;
-    att_range(p, l, b, pos, lo, fp, npg, ns);
-    per_g += ns + 1;
-  }
+__device__ AttItem att_decode(const Params& p, const Smem& S, int l, int item) {
+  const int per_g = att_item_count(p, S, l) / p.Hkv;
   AttItem it;
   it.g = item / per_g;
   int rem = item % per_g;
   for (int b = 0; b < p.B; ++b) {
     int pos, lo, fp, npg, ns;
-    att_range(p, l, b, pos, lo, fp, npg, ns);
+    att_range(p, S, l, b, pos, lo, fp, npg, ns);
     if (rem <= ns) {
       it.b = b;
       it.s = rem;
@@ -226,11 +266,37 @@ __device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int ta
   return true;
 }
 
+// Before chunk `seq` is issued: its stage must be free (consumed), and at most
+// p.inflight older chunks may still be in flight.  The ring can hold up to kStages
+// landed chunks ahead of the consumers, but only a few are requested at a time:
+// that is enough to keep HBM busy, and keeps the memory queues -- which every
+// other load of the step also waits in -- short.
 __device__ __forceinline__ bool acquire_stage(const Params& p, const Smem& S, uint32_t seq, int task) {
   const uint32_t use = seq / kStages;
-  if (use == 0) return true;
-  if (mbar_wait(S.empty(seq % kStages), (use - 1) & 1u, 8 * p.timeout_ns)) return true;
-  raise_err(p, MK_ERR_TIMEOUT, task, -4, (int)seq, 0);
+  if (use > 0 && !mbar_wait(S.empty(seq % kStages), (use - 1) & 1u, 8 * p.timeout_ns)) {
+    raise_err(p, MK_ERR_TIMEOUT, task, -4, (int)seq, 0);
+    return false;
+  }
+  if (seq >= (uint32_t)p.inflight) {
+    const uint32_t q = seq - p.inflight;
+    if (!mbar_wait(S.full(q % kStages), (q / kStages) & 1u, 8 * p.timeout_ns)) {
+      raise_err(p, MK_ERR_TIMEOUT, task, -6, (int)q, 0);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Claim just in time: a queue item is taken only when this CTA's consumers have
+// picked up every earlier mailbox entry but the last one, so an SM busy with a long
+// task does not hold items that idle SMs could start at once.  (No deadlock: a
+// consumer only waits on work that is already claimed -- expert-down items are
+// claimed after the expert-up queue is empty -- or on static tasks.)
+__device__ __forceinline__ bool claim_gate(const Params& p, const Smem& S, uint32_t mseq, int task) {
+  if (mseq < 2) return true;
+  const uint32_t q = mseq - 2;
+  if (mbar_wait(S.mempty(q % kMbox), (q / kMbox) & 1u, 8 * p.timeout_ns)) return true;
+  raise_err(p, MK_ERR_TIMEOUT, task, -7, (int)q, 0);
   return false;
 }
 
@@ -290,6 +356,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
     const int l = T[D_LAYER];
     switch (op) {
       case OP_EMBED:
+      case OP_RESID:
         ok = mbox_push(p, S, mseq, ti, 0, 0);
         break;
       case OP_QKV:
@@ -304,35 +371,32 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         break;
       }
       case OP_ATT_DRAIN: {
-        const int count = att_item_count(p, l);
+        const int count = att_item_count(p, S, l);
         int* head = p.qhead + l;
         while (ok) {
+          if (!(ok = claim_gate(p, S, mseq, ti))) break;
           const int item = atomicAdd(head, 1);
           if (item >= count) break;
-          const AttItem it = att_decode(p, l, item);
+          const AttItem it = att_decode(p, S, l, item);
           const int nch = 2 * ((it.np + 7) / 8);
           ok = mbox_push(p, S, mseq, ti, item, nch) && issue_kv(p, S, cseq, tmK, tmV, l, it, pol, ti);
         }
         break;
       }
-      case OP_UP_DRAIN:
-      case OP_DN_DRAIN: {
+      case OP_MOE_DRAIN: {
         if (!wait_ge(p, C_RR(p, l), 1u, ti)) { ok = false; break; }
-        const bool up = op == OP_UP_DRAIN;
-        const int q = (up ? p.L : 2 * p.L) + l;
+        const int q = p.L + l;
         const int count = ldg_cg(p.qcount + q);
-        const int per = up ? p.t_up : p.t_dn;
-        const long long tile_bytes = up ? (long long)p.r_up * p.d * 2 : (long long)p.r_dn * p.f * 2;
-        const int nch = (int)((tile_bytes + kStageBytes - 1) / kStageBytes);
+        const int nch = (int)((p.moe_item_bytes + kStageBytes - 1) / kStageBytes);
         while (ok) {
+          if (!(ok = claim_gate(p, S, mseq, ti))) break;
           const int item = atomicAdd(p.qhead + q, 1);
           if (item >= count) break;
-          const int a = item / per, t = item % per;
+          const int a = item / p.t_moe, t = item % p.t_moe;
           const int e = ldg_cg(p.active + l * p.maxa + a);
-          const long long base = up ? p.off_up + (long long)(l * p.E + e) * p.up_bytes_e
-                                    : p.off_dn + (long long)(l * p.E + e) * p.dn_bytes_e;
+          const long long off = p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
           ok = mbox_push(p, S, mseq, ti, item, nch) &&
-               issue_linear(p, S, cseq, p.wblob + base + t * tile_bytes, (int)tile_bytes, pol, ti);
+               issue_linear(p, S, cseq, p.wblob + off, (int)p.moe_item_bytes, pol, ti);
         }
         break;
       }
@@ -351,22 +415,22 @@ struct BFrag {
   uint32_t b0[kMaxKsw], b1[kMaxKsw];
 };
 
-// B operand (activations) for this warp's k16-steps ks = warp + 8 j: rows n = lane/4 are
-// tokens, k pairs at 2*(lane%4) and +8.  `pair(n, k)` returns bf16x2 of act[n][k..k+1].
-template <class F>
-__device__ __forceinline__ void build_bfrag(BFrag& fr, int ksw, F&& pair) {
+// B operand (activations) for this warp's k16-steps ks = warp + 8 j: row n = lane/4
+// of the operand is one token's activation row `row` (bf16, nullptr for a zero row);
+// the lane holds the pairs at k = 16 ks + 2 (lane%4) and k + 8.  All loads are
+// issued before any is used.
+__device__ __forceinline__ void load_bfrag(BFrag& fr, int ksw, const uint16_t* row) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n = lane >> 2, c = lane & 3;
+  const int c = lane & 3;
+  const bool on = row != nullptr;
+  const uint16_t* base = on ? row + 16 * warp + 2 * c : nullptr;
 #pragma unroll
   for (int j = 0; j < kMaxKsw; ++j) {
-    if (j < ksw) {
-      const int k = 16 * (warp + 8 * j) + 2 * c;
-      fr.b0[j] = pair(n, k);
-      fr.b1[j] = pair(n, k + 8);
-    } else {
-      fr.b0[j] = 0u;
-      fr.b1[j] = 0u;
-    }
+    fr.b0[j] = 0u;
+    fr.b1[j] = 0u;
+    const bool pj = on && j < ksw;
+    ldg_cg_pred(fr.b0[j], base + 128 * j, pj);
+    ldg_cg_pred(fr.b1[j], base + 128 * j + 8, pj);
   }
 }
 
@@ -374,9 +438,13 @@ __device__ __forceinline__ void build_bfrag(BFrag& fr, int ksw, F&& pair) {
 // task's ring chunks.  Tiles are packed so that fragment (rb, ks) sits at index
 // (j * NRB + rb) * 8 + warp: every 32 KB chunk holds 8 / NRB consecutive j for all
 // row blocks, so chunk, register and smem indices are compile-time constants.
+// With `lo` non-null the operand is the exact-ish sum hi + lo of two bf16 parts and
+// every fragment is multiplied twice (router logits: top-k decisions need them to
+// ~1e-5; the tensor-core work is negligible against the weight bytes).
 template <int NRB>
 __device__ __forceinline__ bool gemv_mainloop(const Params& p, const Smem& S, uint32_t& cseq, int nch,
-                                              int ksw, const BFrag& fr, float (&acc)[NRB][4]) {
+                                              int ksw, const BFrag& fr, float (&acc)[NRB][4],
+                                              const BFrag* lo = nullptr) {
   constexpr int JPC = 8 / NRB;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -396,6 +464,7 @@ __device__ __forceinline__ bool gemv_mainloop(const Params& p, const Smem& S, ui
       for (int rb = 0; rb < NRB; ++rb) {
         const uint4 a = lds128(base + rb * 8 * kFragBytes);
         mma_bf16(acc[rb], a.x, a.y, a.z, a.w, fr.b0[j], fr.b1[j]);
+        if (lo) mma_bf16(acc[rb], a.x, a.y, a.z, a.w, lo->b0[j], lo->b1[j]);
       }
     }
   }
@@ -427,256 +496,295 @@ __device__ __forceinline__ void gemv_reduce(const Smem& S, const float (&acc)[NR
 
 template <int NRB>
 __device__ __forceinline__ bool gemv_run(const Params& p, const Smem& S, uint32_t& cseq, int nch, int ksw,
-                                         const BFrag& fr, float (&v)[4]) {
+                                         const BFrag& fr, float (&v)[4], const BFrag* lo = nullptr) {
   float acc[NRB][4];
-  if (!gemv_mainloop<NRB>(p, S, cseq, nch, ksw, fr, acc)) return false;
+  if (!gemv_mainloop<NRB>(p, S, cseq, nch, ksw, fr, acc, lo)) return false;
   trace_mark(p, S, 3);
   gemv_reduce<NRB>(S, acc, v);
   return true;
 }
 
 // 1 / rms of x_b (layer input) from the per-row-block sums of squares.
+// 1/rms of token b entering `layer`, from the per-row-block sums of squares; all
+// partials are loaded before any is summed (one L2 round trip).
 __device__ __forceinline__ float rstd_of(const Params& p, int layer, int b) {
-  const float* ss = p.SS + (size_t)layer * p.nrb_d * p.B;
+  const float* ss = p.SS + (size_t)layer * p.nrb_d * kSsStride + b;
+  constexpr int kMaxRb = 2048 / kRowBlock;
+  float v[kMaxRb];
+#pragma unroll
+  for (int r = 0; r < kMaxRb; ++r) {
+    v[r] = 0.f;
+    ldg_cg_pred(v[r], ss + r * kSsStride, r < p.nrb_d);
+  }
   float s = 0.f;
-  for (int r = 0; r < p.nrb_d; ++r) s += ldg_cg(ss + r * p.B + b);
+#pragma unroll
+  for (int r = 0; r < kMaxRb; ++r) s += v[r];
   return rsqrtf(s / (float)p.d + p.eps);
 }
 
-// B operand from h = RMSNorm(x_layer) * gain; `b` is the token of this lane's
-// operand row (lane/4), or -1 for a zero row.
-__device__ __forceinline__ void build_norm_bfrag(const Params& p, BFrag& fr, int ksw, int layer,
-                                                 const float* gain, int b) {
-  float rs = 0.f;
-  const float* x = nullptr;
-  if (b >= 0) {
-    rs = rstd_of(p, layer, b);
-    x = p.X + ((size_t)layer * p.B + b) * p.d;
-  }
-  build_bfrag(fr, ksw, [&](int, int k) -> uint32_t {
-    if (b < 0) return 0u;
-    const float2 xv = ldg_cg_f2(x + k);
-    const float2 gv = *reinterpret_cast<const float2*>(gain + k);
-    return pack_bf16(xv.x * rs * gv.x, xv.y * rs * gv.y);
-  });
+// 1/rms of every token, computed once per CTA (threads 0..B-1) into shared memory.
+__device__ __forceinline__ float* rstd_smem(const Smem& S) { return reinterpret_cast<float*>(S.small + 240); }
+__device__ __forceinline__ void rstd_all(const Params& p, const Smem& S, int layer) {
+  if (threadIdx.x < p.B) rstd_smem(S)[threadIdx.x] = rstd_of(p, layer, threadIdx.x);
+  bar_sync_consumers();
+}
+
+// B operand of the normed input: bf16(x_layer * gain) pairs written by the residual
+// step (or the embedding), loaded as-is; the per-token 1/rms is applied to the GEMV
+// output in the epilogue.  `b` is the token of this lane's operand row (lane/4), or
+// -1 for a zero row.  Returns this lane's token's 1/rms (0 for a zero row).
+__device__ __forceinline__ float build_norm_bfrag(const Params& p, const Smem& S, BFrag& fr, int ksw, int layer,
+                                                 int b) {
+  load_bfrag(fr, ksw, b < 0 ? nullptr : p.XG + ((size_t)layer * p.B + b) * p.d);
+  rstd_all(p, S, layer);
+  return b < 0 ? 0.f : rstd_smem(S)[b];
 }
 
 // ============================================================== epilogues / fan-in steps
 
-// Route step: top-k of the router logits per token, softmax over the selected,
-// active-expert list (ascending expert id), per-expert token lists, MoE queue sizes.
+// Route step: top-k of the router logits per token (ties to the lower expert id),
+// softmax over the selected logits, the active-expert list in ascending expert id,
+// per-expert token lists in (token, slot) order, and the layer's MoE queue sizes.
+// Top-k by counting: thread (b, e) finds the rank of logit e = how many logits of
+// token b beat it; ranks below top_k are the selection, in descending order.
 __device__ void route_step(const Params& p, const Smem& S, int l) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int* sel = S.small + 16;  // [B][topk] <= 64 ints
-  if (warp < p.B) {
-    const int b = warp;
-    const float* r = p.rlog + ((size_t)l * p.B + b) * p.E;
-    float v[8];
-    int used = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < p.E) ? ldg_cg(r + e) : -INFINITY;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int* sel = S.small + 16;                               // [B][topk] expert ids (<= 64)
+  float* lg = S.scratch;                                 // [B][E] logits
+  int* slot_of = reinterpret_cast<int*>(S.scratch) + kMaxBatch * 256;  // [E]
+  int* act_s = slot_of + 256;                            // [maxa] active expert ids
+  const int BE = p.B * p.E;
+  for (int i = tid; i < BE; i += kConsumerThreads) lg[i] = ldg_cg(p.rlog + (size_t)l * BE + i);
+  for (int e = tid; e < p.E; e += kConsumerThreads) slot_of[e] = 0;
+  bar_sync_consumers();
+  for (int i = tid; i < BE; i += kConsumerThreads) {
+    const int b = i / p.E, e = i % p.E;
+    const float* r = lg + b * p.E;
+    const float ve = r[e];
+    int rank = 0;
+#pragma unroll 8
+    for (int f = 0; f < p.E; ++f) {
+      const float vf = r[f];
+      rank += (vf > ve || (vf == ve && f < e)) ? 1 : 0;
     }
-    float selv[8];
-    int sele[8];
-    for (int j = 0; j < p.topk; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < p.E && !((used >> i) & 1) && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
-      if ((be & 31) == lane) used |= 1 << (be >> 5);
-      selv[j] = bv;
-      sele[j] = be;
-    }
-    float sum = 0.f, w[8];
-    for (int j = 0; j < p.topk; ++j) { w[j] = __expf(selv[j] - selv[0]); sum += w[j]; }
-    if (lane < p.topk) {
-      float wj = 0.f; int ej = 0;
-      for (int j = 0; j < p.topk; ++j) if (j == lane) { wj = w[j] / sum; ej = sele[j]; }
-      p.ridx[((size_t)l * p.B + b) * p.topk + lane] = ej;
-      p.rw[((size_t)l * p.B + b) * p.topk + lane] = wj;
-      sel[b * p.topk + lane] = ej;
-    }
+    if (rank < p.topk) sel[b * p.topk + rank] = e;
   }
   bar_sync_consumers();
+  if (warp < p.B) {
+    const int b = warp;
+    const float* r = lg + b * p.E;
+    const int ej = (lane < p.topk) ? sel[b * p.topk + lane] : 0;
+    const float mx = r[sel[b * p.topk]];
+    const float w = (lane < p.topk) ? __expf(r[ej] - mx) : 0.f;
+    float sum = w;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < p.topk) {
+      p.ridx[((size_t)l * p.B + b) * p.topk + lane] = ej;
+      p.rw[((size_t)l * p.B + b) * p.topk + lane] = w / sum;
+    }
+  }
+  trace_mark(p, S, 8);
+  trace_mark(p, S, 9);
   if (warp == 0) {
-    int* used = reinterpret_cast<int*>(S.scratch);  // [E]
-    for (int e = lane; e < p.E; e += 32) used[e] = 0;
+    const int nsel = p.B * p.topk;  // <= 64
+    for (int i = lane; i < nsel; i += 32) slot_of[sel[i]] = 1;  // mark used
     __syncwarp();
-    for (int i = lane; i < p.B * p.topk; i += 32) used[sel[i]] = 1;
-    __syncwarp();
+    // ascending-id slots: exclusive prefix count of used experts
     const int per = (p.E + 31) / 32;
     int cnt = 0;
-    for (int i = 0; i < per; ++i) { const int e = lane * per + i; if (e < p.E && used[e]) ++cnt; }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) { const int t = __shfl_up_sync(0xffffffffu, incl, o); if (lane >= o) incl += t; }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int slot = incl - cnt;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
-      if (e < p.E && used[e]) { p.active[l * p.maxa + slot] = e; ++slot; }
+      if (e < p.E && slot_of[e]) ++cnt;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    int slot = incl - cnt;
+    __syncwarp();
+    for (int i = 0; i < per; ++i) {
+      const int e = lane * per + i;
+      if (e < p.E && slot_of[e]) {
+        p.active[l * p.maxa + slot] = e;
+        act_s[slot] = e;
+        slot_of[e] = slot + 1;  // 1-based; only this lane touches expert e here
+        ++slot;
+      }
     }
     __syncwarp();
-    __threadfence_block();
+    // token lists: selection i = b*topk + j goes to slot slot_of[sel[i]] - 1 at
+    // position = earlier selections of the same expert (at most one per token)
+    for (int i0 = 0; i0 < nsel; i0 += 32) {
+      const int i = i0 + lane;
+      const bool on = i < nsel;
+      const int e = on ? sel[i] : -1 - lane;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      int pos = __popc(same & ((1u << lane) - 1u));
+      for (int q = 0; q < i0; ++q) pos += (on && sel[q] == e) ? 1 : 0;
+      if (on)
+        p.act_tok[((size_t)l * p.maxa + slot_of[e] - 1) * p.B + pos] = (i / p.topk) * 16 + (i % p.topk);
+    }
     for (int a = lane; a < total; a += 32) {
-      const int e = p.active[l * p.maxa + a];
-      int c = 0;
-      for (int b = 0; b < p.B; ++b)
-        for (int j = 0; j < p.topk; ++j)
-          if (sel[b * p.topk + j] == e) { p.act_tok[((size_t)l * p.maxa + a) * p.B + c] = b * 16 + j; ++c; }
-      p.act_cnt[l * p.maxa + a] = c;
+      const int e = act_s[a];
+      int c2 = 0;
+      for (int i = 0; i < nsel; ++i) c2 += (sel[i] == e) ? 1 : 0;
+      p.act_cnt[l * p.maxa + a] = c2;
     }
     if (lane == 0) {
       p.nact[l] = total;
-      p.qcount[p.L + l] = total * p.t_up;
-      p.qcount[2 * p.L + l] = total * p.t_dn;
+      p.qcount[p.L + l] = total * p.t_moe;
+      // the MoE-done fan-in counts maxa * t_moe arrivals: the inactive slots' share
+      // arrives here (before any item can, since items need this route)
+      const unsigned pad = (unsigned)((p.maxa - total) * p.t_moe);
+      if (pad > 0) atomicAdd(ctr_ptr(p, C_MD(p, l)), pad);
     }
-    const unsigned pad = (unsigned)((p.maxa - total) * (kRowBlock / p.r_dn));
-    if (pad > 0)
-      for (int r = lane; r < p.nrb_d; r += 32) atomicAdd(p.ctr + C_RB(p, l, r), pad);
     __syncwarp();
     if (lane == 0) {
-      __threadfence();
-      red_release(p.ctr + C_RR(p, l), 1u);
+      if (p.trace) trace_slots(S)[10] = gtime();
+      red_release(ctr_ptr(p, C_RR(p, l)), 1u);
+      if (p.trace) trace_slots(S)[11] = gtime();
     }
   }
 }
 
-// Residual row block r of layer l: x_{l+1} = x_l + sum_g O-proj partial + sum_j w_j y_j,
-// and the block's sums of squares for the next RMSNorm.
-__device__ void residual_step(const Params& p, const Smem& S, int l, int r) {
+// ADD_RMSNORM for the residual row blocks in `mask` (bit r = rows [128 r, 128 r + 128))
+// of layer l, in one pass over the CTA: x_{l+1} = x_l + sum_g O-proj partial_g + MoE
+// accumulator; the next layer's operand bf16(x_{l+1} * gain_{l+1}) as hi/lo parts; the
+// blocks' per-token sums of squares; the next layer's MoE accumulator rows zeroed.
+// Then LR(l+1) += number of blocks.
+__device__ void residual_blocks(const Params& p, const Smem& S, uint32_t& sseq, int l, unsigned mask) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = r * kRowBlock + (tid & 127);
-  const int half = tid >> 7;
-  float* red = reinterpret_cast<float*>(S.small + 16);  // [8 warps][4]
-  for (int i = 0; i < 4; ++i) {
-    const int b = half + 2 * i;
-    float sq = 0.f;
-    if (b < p.B) {
-      float x = ldg_cg(p.X + ((size_t)l * p.B + b) * p.d + row);
-      for (int g = 0; g < p.Hkv; ++g) x += ldg_cg(p.opart + (((size_t)l * p.Hkv + g) * p.B + b) * p.d + row);
-      for (int j = 0; j < p.topk; ++j) x += ldg_cg(p.Y + (((size_t)l * p.B + b) * p.topk + j) * p.d + row);
-      p.X[((size_t)(l + 1) * p.B + b) * p.d + row] = x;
-      sq = x * x;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) red[warp * 4 + i] = sq;
-  }
-  bar_sync_consumers();
-  if (tid < p.B) {
-    const int b = tid, hf = b & 1, i = b >> 1;
-    float s = 0.f;
-    for (int w = 0; w < 4; ++w) s += red[(hf * 4 + w) * 4 + i];
-    p.SS[((size_t)(l + 1) * p.nrb_d + r) * p.B + b] = s;
-  }
-  bar_sync_consumers();
+  int* rbl = S.small + 16;  // list of the blocks (<= 16)
   if (tid == 0) {
-    __threadfence();
-    red_release(p.ctr + C_LR(p, l + 1), 1u);
+    int n = 0;
+    for (int r = 0; r < p.nrb_d; ++r)
+      if ((mask >> r) & 1u) rbl[n++] = r;
+    rbl[16] = n;
   }
+  bar_sync_consumers();
+  const int nblk = rbl[16];
+  const int nchunks = nblk * p.B * (kRowBlock / 32);  // warp-sized chunks of 32 rows
+  float* ssp = S.scratch;                             // [nblk * B][4] partial sums
+  const float* gain_next = (l + 1 < p.L) ? p.attn_norm + (size_t)(l + 1) * p.d : p.final_norm;
+#pragma unroll 4
+  for (int q = warp; q < nchunks; q += kConsumerWarps) {
+    const int blk = q >> 2;                      // (block index, token)
+    const int r = rbl[blk / p.B], b = blk % p.B;
+    const int row = r * kRowBlock + (q & 3) * 32 + lane;
+    constexpr int kMaxG = 8;
+    float part[2 + kMaxG];
+    part[0] = ldg_cg(p.X + ((size_t)l * p.B + b) * p.d + row);
+    part[1] = ldg_cg(p.moe + ((size_t)l * p.B + b) * p.d + row);
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g) {
+      part[2 + g] = 0.f;
+      ldg_cg_pred(part[2 + g], p.opart + (((size_t)l * p.Hkv + g) * p.B + b) * p.d + row, g < p.Hkv);
+    }
+    float x = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2 + kMaxG; ++k) x += part[k];
+    const size_t o = ((size_t)(l + 1) * p.B + b) * p.d + row;
+    p.X[o] = x;
+    const float xg = x * gain_next[row];
+    const uint16_t hi = to_bf16(xg);
+    p.XG[o] = hi;
+    p.XGL[o] = to_bf16(xg - bf16_to_f(hi));
+    if (l + 1 < p.L) p.moe[o] = 0.f;
+    float sq = x * x;
+#pragma unroll
+    for (int s2 = 16; s2 > 0; s2 >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s2);
+    if (lane == 0) ssp[q] = sq;
+  }
+  bar_sync_consumers();
+  for (int blk = tid; blk < nblk * p.B; blk += kConsumerThreads) {
+    const int r = rbl[blk / p.B], b = blk % p.B;
+    const float s4 = ssp[4 * blk] + ssp[4 * blk + 1] + ssp[4 * blk + 2] + ssp[4 * blk + 3];
+    p.SS[((size_t)(l + 1) * p.nrb_d + r) * kSsStride + b] = s4;
+  }
+  signal_async(p, S, sseq, C_LR(p, l + 1), (unsigned)nblk);
 }
 
 // Signal a fan-in counter; returns true (to all consumer threads) if this CTA was last.
 __device__ bool signal_fanin(const Params& p, const Smem& S, int ci, unsigned target) {
   bar_sync_consumers();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atom_add_acq_rel(p.ctr + ci, 1u);
+    const unsigned old = atom_add_acq_rel(ctr_ptr(p, ci), 1u);
     S.small[1] = (old + 1 == target) ? 1 : 0;
     if (p.trace && old + 1 == target) trace_slots(S)[6] = gtime();
   }
   bar_sync_consumers();
-  const bool last = S.small[1] != 0;
-  if (last) __threadfence();
-  return last;
+  return S.small[1] != 0;
 }
+// Publish this task's output: the barrier orders every consumer thread's stores
+// before thread 0's release-add at GPU scope; waiters acquire the counter.
 __device__ void signal_plain(const Params& p, int ci, unsigned v) {
   bar_sync_consumers();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    red_release(p.ctr + ci, v);
-  }
+  if (threadIdx.x == 0) red_release(ctr_ptr(p, ci), v);
 }
 
+
 // ============================================================== GEMV tasks
-__device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const int* T, int ti, int item, int nch) {
+// The B operand of consecutive tasks that read the same activation (same layer and
+// source: the layer's normed input, one expert's gathered rows or gated block, one
+// KV group's attention output) is built once: the later tasks skip both the
+// dependency wait (already met) and the loads.
+struct OperandKey {
+  int kind, layer, sub;
+  __device__ __forceinline__ bool operator==(const OperandKey& o) const {
+    return kind == o.kind && layer == o.layer && sub == o.sub;
+  }
+};
+
+__device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq,
+                                          const int* T, int ti, int nch, BFrag& fr, OperandKey& have,
+                                          float& rs_have) {
   const int op = T[D_OP];
   const int l = T[D_LAYER];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g8 = lane >> 2, c = lane & 3;
 
-  int nrows, klen, wait_ci;
-  unsigned wait_t;
-  int a_slot = 0, t_idx = 0, ntok = p.B;
-  const int* tok_list = nullptr;  // expert path: act_tok row of this active slot (b*16 + j)
-  if (op == OP_UP_DRAIN || op == OP_DN_DRAIN) {
-    const bool up = op == OP_UP_DRAIN;
-    const int per = up ? p.t_up : p.t_dn;
-    a_slot = item / per;
-    t_idx = item % per;
-    nrows = up ? p.r_up : p.r_dn;
-    klen = up ? p.d : p.f;
-    wait_ci = up ? C_RR(p, l) : C_UP(p, l, a_slot);
-    wait_t = up ? 1u : (unsigned)p.t_up;
-  } else {
-    nrows = T[D_NROWS];
-    klen = T[D_KLEN];
-    wait_ci = T[D_WAIT_CTR];
-    wait_t = (unsigned)T[D_WAIT_TARGET];
+  const int nrows = T[D_NROWS];
+  const int klen = T[D_KLEN];
+  OperandKey key;
+  switch (op) {
+    case OP_OPROJ: key = {5, l, T[D_AUX]}; break;
+    case OP_LMHEAD: key = {2, p.L, 0}; break;
+    default: key = {1, l, 0}; break;  // QKV and ROUTER share the layer's normed input
   }
-  if (!consumer_wait(p, S, wait_ci, wait_t, ti)) {
+  const bool reuse = key == have;
+  if (reuse) {
+    trace_mark(p, S, 1);
+  } else if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti)) {
     drain_chunks(p, S, cseq, nch);
     return false;
-  }
-  if (op == OP_UP_DRAIN || op == OP_DN_DRAIN) {
-    ntok = ldg_cg(p.act_cnt + l * p.maxa + a_slot);
-    tok_list = p.act_tok + ((size_t)l * p.maxa + a_slot) * p.B;
   }
   const int nrb = nrows / 16;
   const int ksw = klen / 16 / kConsumerWarps;
 
-  BFrag fr;
-  if (op == OP_OPROJ) {
-    const int k0 = T[D_K0];
-    const uint16_t* o = p.atto + (size_t)l * p.B * p.Hq * p.hd;
-    const int HQD = p.Hq * p.hd;
-    build_bfrag(fr, ksw, [&](int n, int k) -> uint32_t {
-      return n < p.B ? ldg_cg_u32(o + (size_t)n * HQD + k0 + k) : 0u;
-    });
-  } else if (op == OP_DN_DRAIN) {
-    const uint16_t* a = p.aup + ((size_t)l * p.maxa + a_slot) * p.B * p.f;
-    build_bfrag(fr, ksw, [&](int n, int k) -> uint32_t {
-      return n < ntok ? ldg_cg_u32(a + (size_t)n * p.f + k) : 0u;
-    });
-  } else {
-    // RMSNorm operand: QKV / ROUTER over the batch, UP over the expert's gathered
-    // tokens (MOE_GATHER folded into the operand load), LM_HEAD with the final norm
+  if (reuse) {
+  } else if (op == OP_OPROJ) {
     const int n = lane >> 2;
-    int b = -1;
-    if (op == OP_UP_DRAIN) {
-      if (n < ntok) b = ldg_cg(tok_list + n) >> 4;
-    } else if (n < p.B) {
-      b = n;
-    }
-    const bool last = op == OP_LMHEAD;
-    build_norm_bfrag(p, fr, ksw, last ? p.L : l, last ? p.final_norm : p.attn_norm + (size_t)l * p.d, b);
+    load_bfrag(fr, ksw, n < p.B ? p.atto + ((size_t)l * p.B + n) * p.Hq * p.hd + T[D_K0] : nullptr);
+  } else {
+    // RMSNorm operand of QKV / ROUTER (layer input) and LM_HEAD (final norm)
+    const int n = lane >> 2;
+    rs_have = build_norm_bfrag(p, S, fr, ksw, op == OP_LMHEAD ? p.L : l, n < p.B ? n : -1);
   }
+  have = key;
 
   float v[4];
   bool ran;
-  switch (nrb) {
+  if (op == OP_ROUTER) {
+    // residue part of the router operand (the hi part is the shared cached operand)
+    BFrag lo;
+    const int n = lane >> 2;
+    load_bfrag(lo, ksw, n < p.B ? p.XGL + ((size_t)l * p.B + n) * p.d : nullptr);
+    ran = (nrb == 1) ? gemv_run<1>(p, S, cseq, nch, ksw, fr, v, &lo) : gemv_run<2>(p, S, cseq, nch, ksw, fr, v, &lo);
+  } else switch (nrb) {
     case 1: ran = gemv_run<1>(p, S, cseq, nch, ksw, fr, v); break;
     case 2: ran = gemv_run<2>(p, S, cseq, nch, ksw, fr, v); break;
     case 4: ran = gemv_run<4>(p, S, cseq, nch, ksw, fr, v); break;
@@ -685,6 +793,13 @@ __device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const 
   if (!ran) return false;
 
   // ---- epilogue: thread (warp = row block, lane) owns rows 16w+g8, 16w+g8+8, tokens 2c, 2c+1
+  if (op == OP_QKV || op == OP_ROUTER || op == OP_LMHEAD) {
+    // 1/rms of tokens 2c and 2c+1 lives in lanes 8c and 8c+4 (operand row n = lane/4)
+    const float rs0 = __shfl_sync(0xffffffffu, rs_have, 8 * c);
+    const float rs1 = __shfl_sync(0xffffffffu, rs_have, 8 * c + 4);
+    v[0] *= rs0; v[2] *= rs0;
+    v[1] *= rs1; v[3] *= rs1;
+  }
   if (warp < nrb) {
     const int rlo = warp * 16 + g8;  // row within the task tile (row 'rlo + 8' is the pair)
     switch (op) {
@@ -695,17 +810,21 @@ __device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const 
         const int j = pr % p.hd;
         const int d1 = 8 * (j / 16) + g8, d2 = d1 + p.hd / 2;
         const bool rot = seg <= p.gs;
-        const double inv = rot ? exp(-2.0 * (double)d1 / (double)p.hd * log((double)p.theta)) : 0.0;
+        // angle = pos * inv_freq[d1]; turns = frac(pos * inv_freq / 2pi) computed exactly
+        // in 64-bit fixed point (rope_turns[i] = inv_freq_i / 2pi * 2^64), then sin/cos
+        // of 2*pi*turns in fp32.
+        const unsigned long long fturn = rot ? p.rope_turns[d1] : 0ull;
         for (int e = 0; e < 2; ++e) {
           const int n = 2 * c + e;
           if (n >= p.B) continue;
           const float x1 = v[e], x2 = v[2 + e];
-          const int pos = p.seq_lens[n];
+          const int pos = seq_lens_s(S)[n];
           float y1 = x1, y2 = x2;
           if (rot) {
-            double sn, cs;
-            sincos((double)pos * inv, &sn, &cs);
-            const float fc = (float)cs, fs = (float)sn;
+            const unsigned long long u = (unsigned long long)(unsigned)pos * fturn;
+            const float t = (float)(u >> 40) * 5.9604644775390625e-08f;  // 2^-24
+            float fs, fc;
+            sincospif(2.f * t, &fs, &fc);
             y1 = x1 * fc - x2 * fs;
             y2 = x2 * fc + x1 * fs;
           }
@@ -759,31 +878,6 @@ __device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const 
         }
         break;
       }
-      case OP_UP_DRAIN: {
-        const int frow = t_idx * (p.r_up / 2) + warp * 8 + g8;
-        for (int e = 0; e < 2; ++e) {
-          const int n = 2 * c + e;
-          if (n >= ntok) continue;
-          const float gt = v[e], u = v[2 + e];
-          const float a = gt / (1.f + __expf(-gt)) * u;
-          p.aup[(((size_t)l * p.maxa + a_slot) * p.B + n) * p.f + frow] = to_bf16(a);
-        }
-        break;
-      }
-      case OP_DN_DRAIN: {
-        const int r0 = t_idx * p.r_dn + rlo;
-        for (int e = 0; e < 2; ++e) {
-          const int n = 2 * c + e;
-          if (n >= ntok) continue;
-          const int pk = ldg_cg(tok_list + n);
-          const int b = pk >> 4, jj = pk & 15;
-          const float w = ldg_cg(p.rw + ((size_t)l * p.B + b) * p.topk + jj);
-          float* out = p.Y + (((size_t)l * p.B + b) * p.topk + jj) * p.d;
-          out[r0] = w * v[e];
-          out[r0 + 8] = w * v[2 + e];
-        }
-        break;
-      }
       default:
         break;
     }
@@ -792,27 +886,131 @@ __device__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, const 
   // ---- signal
   switch (op) {
     case OP_QKV:
-      signal_plain(p, T[D_SIG_CTR], 1u);
+    case OP_OPROJ:
+      signal_async(p, S, sseq, T[D_SIG_CTR], 1u);
       break;
     case OP_ROUTER:
       if (signal_fanin(p, S, T[D_SIG_CTR], (unsigned)T[D_SIG_TARGET])) route_step(p, S, l);
       break;
-    case OP_UP_DRAIN:
-      signal_plain(p, C_UP(p, l, a_slot), 1u);
-      break;
-    case OP_OPROJ: {
-      const int r = T[D_ROW0] / kRowBlock;
-      if (signal_fanin(p, S, C_RB(p, l, r), (unsigned)p.rb_target)) residual_step(p, S, l, r);
-      break;
-    }
-    case OP_DN_DRAIN: {
-      const int r = (t_idx * p.r_dn) / kRowBlock;
-      if (signal_fanin(p, S, C_RB(p, l, r), (unsigned)p.rb_target)) residual_step(p, S, l, r);
-      break;
-    }
     default:
       break;
   }
+  bar_sync_consumers();
+  return true;
+}
+
+// ADD_RMSNORM task of residual row block r: waits for all MoE items of the layer and
+// the block's O-proj tiles.
+__device__ bool task_resid(const Params& p, const Smem& S, uint32_t& sseq, const int* T, int ti) {
+  const int l = T[D_LAYER], r = T[D_AUX];
+  if (!consumer_wait(p, S, T[D_WAIT2_CTR], (unsigned)T[D_WAIT2_TARGET], ti)) return false;
+  if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti)) return false;
+  residual_blocks(p, S, sseq, l, 1u << r);
+  bar_sync_consumers();
+  return true;
+}
+
+// One MoE item: expert slot a = item / t_moe, f-slice s = item % t_moe.
+//   phase 1: [gate; up] rows of the slice times the expert's gathered normed tokens
+//            -> a = silu(gate) * up for 32 f-rows x n_tok, bf16 in shared memory;
+//   phase 2: W_down[:, slice] * a -> per-token partial of the expert output, times the
+//            token's routing weight, added into the layer's MoE accumulator.
+// Completion is counted on the layer's MoE-done counter (padded to max_active * t_moe
+// by the route step).
+__device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, const int* T,
+                                         int ti, int item, int nch, BFrag& fr, OperandKey& have, float& rs_have) {
+  const int l = T[D_LAYER];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g8 = lane >> 2, c = lane & 3;
+  const int a_slot = item / p.t_moe;
+  const OperandKey key = {3, l, a_slot};
+  const bool reuse = key == have;
+  if (reuse) {
+    trace_mark(p, S, 1);
+  } else if (!consumer_wait(p, S, C_RR(p, l), 1u, ti)) {
+    drain_chunks(p, S, cseq, nch);
+    return false;
+  }
+  const int ntok = ldg_cg(p.act_cnt + l * p.maxa + a_slot);
+  const int* tok_list = p.act_tok + ((size_t)l * p.maxa + a_slot) * p.B;
+  const int ksw1 = p.d / 128;
+  if (!reuse) {
+    const int n = lane >> 2;
+    const int b = (n < ntok) ? (ldg_cg(tok_list + n) >> 4) : -1;
+    rs_have = build_norm_bfrag(p, S, fr, ksw1, l, b);
+    have = key;
+  }
+  // this lane's two epilogue tokens (2c, 2c+1): batch index and routing weight
+  int bt[2];
+  float wt[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int n = 2 * c + e;
+    bt[e] = -1;
+    wt[e] = 0.f;
+    if (n < ntok) {
+      const int pk = ldg_cg(tok_list + n);
+      bt[e] = pk >> 4;
+      wt[e] = ldg_cg(p.rw + ((size_t)l * p.B + bt[e]) * p.topk + (pk & 15));
+    }
+  }
+  // ---- phase 1
+  const int nch1 = p.d / 256;  // 64 rows x d bf16 = d/256 ring chunks
+  float v[4];
+  if (!gemv_run<4>(p, S, cseq, nch1, ksw1, fr, v)) return false;
+  uint16_t* a_s = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(S.scratch) + 16384);  // [8][32]
+  {
+    const float rs0 = __shfl_sync(0xffffffffu, rs_have, 8 * c);
+    const float rs1 = __shfl_sync(0xffffffffu, rs_have, 8 * c + 4);
+    if (warp < 4) {  // row block w = gate rows 8w..8w+7 (row g8) paired with up rows (g8 + 8)
+      const int frow = warp * 8 + g8;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int n = 2 * c + e;
+        const float rs = e ? rs1 : rs0;
+        const float gt = v[e] * rs, up = v[2 + e] * rs;
+        const float a = (n < ntok) ? gt / (1.f + __expf(-gt)) * up : 0.f;
+        a_s[n * kMoeFs + frow] = to_bf16(a);
+      }
+    }
+  }
+  bar_sync_consumers();
+  // ---- phase 2: warp w owns output rows [w * rpw * 16, (w + 1) * rpw * 16)
+  uint32_t b2[2][2];
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    b2[ks][0] = *reinterpret_cast<const uint32_t*>(a_s + g8 * kMoeFs + 16 * ks + 2 * c);
+    b2[ks][1] = *reinterpret_cast<const uint32_t*>(a_s + g8 * kMoeFs + 16 * ks + 8 + 2 * c);
+  }
+  const int rpw = p.d / 128;
+  const int region = rpw * 2 * kFragBytes;
+  const int my_chunk = (warp * region) / kStageBytes;
+  const int my_off = (warp * region) % kStageBytes;
+  const int nch2 = nch - nch1;
+  float* out0 = bt[0] >= 0 ? p.moe + ((size_t)l * p.B + bt[0]) * p.d : nullptr;
+  float* out1 = bt[1] >= 0 ? p.moe + ((size_t)l * p.B + bt[1]) * p.d : nullptr;
+  for (int ch = 0; ch < nch2; ++ch) {
+    if (!wait_full(p, S, cseq)) return false;
+    if (ch == my_chunk) {
+      const uint32_t base = S.stage(cseq) + my_off + lane * 16;
+      for (int rb = 0; rb < rpw; ++rb) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const uint4 a = lds128(base + (rb * 2 + ks) * kFragBytes);
+          mma_bf16(acc, a.x, a.y, a.z, a.w, b2[ks][0], b2[ks][1]);
+        }
+        const int row = (warp * rpw + rb) * 16 + g8;
+        if (out0) { atomicAdd(out0 + row, wt[0] * acc[0]); atomicAdd(out0 + row + 8, wt[0] * acc[2]); }
+        if (out1) { atomicAdd(out1 + row, wt[1] * acc[1]); atomicAdd(out1 + row + 8, wt[1] * acc[3]); }
+      }
+    }
+    release_stage(S, cseq);
+    ++cseq;
+  }
+  trace_mark(p, S, 3);
+  // ---- signal the layer's MoE-done counter (waited on by the ADD_RMSNORM tasks)
+  signal_async(p, S, sseq, C_MD(p, l), 1u);
   bar_sync_consumers();
   return true;
 }
@@ -846,8 +1044,9 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
     const uint16_t* q = p.Q + ((size_t)l * p.B + it.b) * p.Hq * HD + (size_t)gs * it.g * HD;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = (g8 < gs) ? ldg_cg_u32(q + g8 * HD + 16 * ks + 2 * c) : 0u;
-      qa[ks][1] = (g8 < gs) ? ldg_cg_u32(q + g8 * HD + 16 * ks + 8 + 2 * c) : 0u;
+      qa[ks][0] = qa[ks][1] = 0u;
+      ldg_cg_pred(qa[ks][0], q + g8 * HD + 16 * ks + 2 * c, g8 < gs);
+      ldg_cg_pred(qa[ks][1], q + g8 * HD + 16 * ks + 8 + 2 * c, g8 < gs);
     }
   }
   float m_run = -INFINITY, l_run = 0.f;
@@ -988,43 +1187,62 @@ __device__ void attention_self(const Params& p, int l, const AttItem& it, int ta
 }
 
 // ATTN_COMBINE: log-sum-exp merge of the (ns + 1) partials of (b, g) -> o (bf16).
+// Warp h merges head h: lanes hold the items' (m, l) to form the weights, then every
+// lane accumulates HD/32 contiguous dims of each item's o with vector loads.
 template <int HD>
 __device__ void attention_combine(const Params& p, int l, int b, int g, int ns) {
+  constexpr int V = HD / 32;  // dims per lane: 4 (128), 2 (64), 1 (32)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gs = p.gs;
   const size_t stride = (size_t)gs * (HD + 2);
   const float* base = p.attp + ((size_t)l * p.Hkv * p.B * p.max_items_bg + (size_t)(g * p.B + b) * p.max_items_bg) * stride;
+  const int n = ns + 1;
   for (int h = warp; h < gs; h += kConsumerWarps) {
     float M = -INFINITY;
-    for (int s = lane; s <= ns; s += 32) M = fmaxf(M, ldg_cg(base + s * stride + gs * HD + h));
+    for (int s = lane; s < n; s += 32) M = fmaxf(M, ldg_cg(base + s * stride + gs * HD + h));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float Ls = 0.f;
-    for (int s = lane; s <= ns; s += 32) {
-      const float m = ldg_cg(base + s * stride + gs * HD + h);
-      Ls += ldg_cg(base + s * stride + gs * HD + gs + h) * exp2f(m - M);
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      const int s = s0 + lane;
+      float wgt = 0.f;
+      if (s < n) {
+        wgt = exp2f(ldg_cg(base + s * stride + gs * HD + h) - M);
+        Ls += wgt * ldg_cg(base + s * stride + gs * HD + gs + h);
+      }
+      const int cnt = min(32, n - s0);
+#pragma unroll 8
+      for (int t = 0; t < cnt; ++t) {
+        const float wt = __shfl_sync(0xffffffffu, wgt, t);
+        const float* o = base + (s0 + t) * stride + h * HD + lane * V;
+        if (V == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
+          acc[0] += wt * x.x; acc[V > 1 ? 1 : 0] += wt * x.y;
+          acc[V > 2 ? 2 : 0] += wt * x.z; acc[V > 3 ? 3 : 0] += wt * x.w;
+        } else if (V == 2) {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
+          acc[0] += wt * x.x; acc[V > 1 ? 1 : 0] += wt * x.y;
+        } else {
+          acc[0] += wt * __ldcg(o);
+        }
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    float acc[HD / 32];
-#pragma unroll
-    for (int i = 0; i < HD / 32; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s <= ns; ++s) {
-      const float wgt = exp2f(ldg_cg(base + s * stride + gs * HD + h) - M);
-#pragma unroll
-      for (int i = 0; i < HD / 32; ++i) acc[i] += wgt * ldg_cg(base + s * stride + h * HD + lane + 32 * i);
-    }
     const float inv = 1.f / Ls;
-    uint16_t* o = p.atto + ((size_t)l * p.B + b) * p.Hq * HD + (size_t)(gs * g + h) * HD;
+    uint16_t* out = p.atto + ((size_t)l * p.B + b) * p.Hq * HD + (size_t)(gs * g + h) * HD + lane * V;
 #pragma unroll
-    for (int i = 0; i < HD / 32; ++i) o[lane + 32 * i] = to_bf16(acc[i] * inv);
+    for (int i = 0; i < V; ++i) out[i] = to_bf16(acc[i] * inv);
   }
 }
 
 template <int HD>
-__device__ bool task_attention(const Params& p, const Smem& S, uint32_t& cseq, int l, int item, int nch, int ti) {
-  const AttItem it = att_decode(p, l, item);
+__device__ bool task_attention(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, int l, int item, int nch,
+                               int ti) {
+  const AttItem it = att_decode(p, S, l, item);
   if (!consumer_wait(p, S, C_QKVG(p, l, it.g), (unsigned)p.qkv_tpg, ti)) {
     drain_chunks(p, S, cseq, nch);
     return false;
@@ -1036,14 +1254,14 @@ __device__ bool task_attention(const Params& p, const Smem& S, uint32_t& cseq, i
   }
   if (signal_fanin(p, S, C_ATT(p, l, it.b, it.g), (unsigned)(it.ns + 1))) {
     attention_combine<HD>(p, l, it.b, it.g, it.ns);
-    signal_plain(p, C_OG(p, l, it.g), 1u);
+    signal_async(p, S, sseq, C_OG(p, l, it.g), 1u);
   }
   bar_sync_consumers();
   return true;
 }
 
 // ============================================================== embed
-__device__ void task_embed(const Params& p, const Smem& S, int ti) {
+__device__ void task_embed(const Params& p, const Smem& S, uint32_t& sseq, int ti) {
   const int tid = threadIdx.x;
   for (int i = tid; i < p.B * p.d; i += kConsumerThreads) {
     const int b = i / p.d, k = i % p.d;
@@ -1052,7 +1270,13 @@ __device__ void task_embed(const Params& p, const Smem& S, int ti) {
       if (k == 0) raise_err(p, MK_ERR_BAD_TOKEN, ti, -1, t, b);
       t = 0;
     }
-    p.X[(size_t)b * p.d + k] = bf16_to_f(p.embed[(size_t)t * p.d + k]);
+    const float x = bf16_to_f(p.embed[(size_t)t * p.d + k]);
+    p.X[(size_t)b * p.d + k] = x;
+    p.moe[(size_t)b * p.d + k] = 0.f;
+    const float xg = x * p.attn_norm[k];
+    const uint16_t hi = to_bf16(xg);
+    p.XG[(size_t)b * p.d + k] = hi;
+    p.XGL[(size_t)b * p.d + k] = to_bf16(xg - bf16_to_f(hi));
   }
   bar_sync_consumers();
   for (int i = tid; i < p.B * p.nrb_d; i += kConsumerThreads) {
@@ -1060,16 +1284,19 @@ __device__ void task_embed(const Params& p, const Smem& S, int ti) {
     const float* x = p.X + (size_t)b * p.d + r * kRowBlock;
     float s = 0.f;
     for (int k = 0; k < kRowBlock; ++k) s += x[k] * x[k];
-    p.SS[(size_t)r * p.B + b] = s;
+    p.SS[(size_t)r * kSsStride + b] = s;
   }
-  signal_plain(p, C_LR(p, 0), (unsigned)p.nrb_d);
+  signal_async(p, S, sseq, C_LR(p, 0), (unsigned)p.nrb_d);
   bar_sync_consumers();
 }
 
 // ============================================================== consumer loop
 __device__ void consumer(const Params& p, const Smem& S) {
-  uint32_t cseq = 0, mseq = 0;
+  uint32_t cseq = 0, mseq = 0, sseq = 0;
   bool skip = false;
+  BFrag fr;
+  OperandKey have = {-1, -1, -1};
+  float rs_have = 0.f;
   while (true) {
     // Thread 0 takes the mailbox entry and the abort flag; every consumer thread
     // then follows the same path, so the named barriers stay matched.
@@ -1092,7 +1319,7 @@ __device__ void consumer(const Params& p, const Smem& S) {
     const int nch = ent.z;
     if (p.trace && threadIdx.x == 0) {
       unsigned long long* t = trace_slots(S);
-      t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = 0ull;
+      t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = t[8] = t[9] = t[10] = t[11] = 0ull;
     }
     if (abort_now) skip = true;
     if (skip) {
@@ -1102,20 +1329,32 @@ __device__ void consumer(const Params& p, const Smem& S) {
     bool ok = true;
     switch (T[D_OP]) {
       case OP_EMBED:
-        task_embed(p, S, ent.x);
+        task_embed(p, S, sseq, ent.x);
+        break;
+      case OP_RESID:
+        ok = task_resid(p, S, sseq, T, ent.x);
         break;
       case OP_ATT_DRAIN:
-        if (p.hd == 128) ok = task_attention<128>(p, S, cseq, T[D_LAYER], ent.y, nch, ent.x);
-        else if (p.hd == 64) ok = task_attention<64>(p, S, cseq, T[D_LAYER], ent.y, nch, ent.x);
-        else ok = task_attention<32>(p, S, cseq, T[D_LAYER], ent.y, nch, ent.x);
+        // the cached GEMV operand is dropped here (re-defined below), so its
+        // registers are free while the attention routine runs
+        if (p.hd == 128) ok = task_attention<128>(p, S, cseq, sseq, T[D_LAYER], ent.y, nch, ent.x);
+        else if (p.hd == 64) ok = task_attention<64>(p, S, cseq, sseq, T[D_LAYER], ent.y, nch, ent.x);
+        else ok = task_attention<32>(p, S, cseq, sseq, T[D_LAYER], ent.y, nch, ent.x);
+        have = {-1, -1, -1};
+#pragma unroll
+        for (int j = 0; j < kMaxKsw; ++j) fr.b0[j] = fr.b1[j] = 0u;
+        break;
+      case OP_MOE_DRAIN:
+        ok = task_moe(p, S, cseq, sseq, T, ent.x, ent.y, nch, fr, have, rs_have);
         break;
       default:
-        ok = task_gemv(p, S, cseq, T, ent.x, ent.y, nch);
+        ok = task_gemv(p, S, cseq, sseq, T, ent.x, nch, fr, have, rs_have);
         break;
     }
     if (!ok) skip = true;
     trace_emit(p, S, T[D_OP], T[D_LAYER], ent.y);
   }
+  signal_async(p, S, sseq, -1, 0u);  // tells the storer to finish
 }
 
 // ============================================================== the kernel
@@ -1133,13 +1372,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(S.mfull(m), 1);
       mbar_init(S.mempty(m), 1);
     }
+    for (int q = 0; q < kSq; ++q) {
+      mbar_init(S.sfull(q), kConsumerWarps);
+      mbar_init(S.sempty(q), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
+  if (threadIdx.x < p.B) S.small[224 + threadIdx.x] = p.seq_lens[threadIdx.x];
   __syncthreads();
   const int warp = threadIdx.x >> 5;
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     if ((threadIdx.x & 31) == 0) producer(p, S, &tmK, &tmV);
+  } else if (warp == kStorerWarp) {
+    if ((threadIdx.x & 31) == 0) storer(p, S);
   } else {
     consumer(p, S);
   }
@@ -1147,7 +1393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // last CTA out resets the counters and queues for the next launch
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned old = atom_add_acq_rel(p.ctr + p.c_done, 1u);
+    const unsigned old = atom_add_acq_rel(ctr_ptr(p, p.c_done), 1u);
     S.small[2] = (old == gridDim.x - 1) ? 1 : 0;
   }
   __syncthreads();
@@ -1155,14 +1401,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __threadfence();
     if (p.do_reset) {
       for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x)
-        if (i != p.c_done) p.ctr[i] = 0u;
+        if (i != p.c_done) *ctr_ptr(p, i) = 0u;
       for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
       if (!p.fixed)
         for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.seq_lens[b] += 1;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      p.ctr[p.c_done] = 0u;
+      *ctr_ptr(p, p.c_done) = 0u;
       __threadfence();
     }
   }
@@ -1225,6 +1471,57 @@ __global__ void mk_pack_kernel(uint8_t* __restrict__ dst, const uint16_t* __rest
   reinterpret_cast<uint4*>(dst)[u] = v;
 }
 
+// All t = d_ff / 32 items of one expert (see the MoE item layout in mk_internal.h).
+__global__ void mk_pack_moe_kernel(uint8_t* __restrict__ dst, const uint16_t* __restrict__ gate,
+                                   const uint16_t* __restrict__ up, const uint16_t* __restrict__ down, int d,
+                                   int f) {
+  const int t_n = f / kMoeFs;
+  const long long gu_units = (long long)(2 * kMoeFs / 16) * (d / 16) * 32;
+  const long long dn_units = (long long)(d / 16) * (kMoeFs / 16) * 32;
+  const long long item_units = gu_units + dn_units;
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= item_units * t_n) return;
+  const int s = (int)(u / item_units);
+  long long r = u % item_units;
+  const int lane = (int)(r & 31);
+  const int g8 = lane >> 2, c = lane & 3;
+  uint16_t out[8];
+  if (r < gu_units) {
+    // gate/up tile: 4 row blocks (8 gate + 8 up rows each), GEMV order (j*4 + rb)*8 + w
+    const long long fi = r >> 5;
+    const int j = (int)(fi / 32), rem = (int)(fi % 32);
+    const int rb = rem / 8, ks = rem % 8 + 8 * j;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = g8 + ((q & 1) ? 8 : 0);                 // row within the block
+      const int k = 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
+      const uint16_t* src = (i < 8) ? gate : up;
+      const long long srow = (long long)s * kMoeFs + 8 * rb + (i & 7);
+      out[2 * q] = src[srow * d + k];
+      out[2 * q + 1] = src[srow * d + k + 1];
+    }
+  } else {
+    // down slice: warp w owns rows [w d/8, (w+1) d/8); order [w][row block][ks]
+    const long long fi = (r - gu_units) >> 5;
+    const int rpw = d / 128;
+    const int w = (int)(fi / (rpw * 2)), rem = (int)(fi % (rpw * 2));
+    const int rb = w * rpw + rem / 2, ks = rem % 2;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long row = (long long)rb * 16 + g8 + ((q & 1) ? 8 : 0);
+      const int col = s * kMoeFs + 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
+      out[2 * q] = down[row * f + col];
+      out[2 * q + 1] = down[row * f + col + 1];
+    }
+  }
+  uint4 v;
+  v.x = out[0] | ((uint32_t)out[1] << 16);
+  v.y = out[2] | ((uint32_t)out[3] << 16);
+  v.z = out[4] | ((uint32_t)out[5] << 16);
+  v.w = out[6] | ((uint32_t)out[7] << 16);
+  reinterpret_cast<uint4*>(dst)[u] = v;
+}
+
 __global__ void mk_convert_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, long long n) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = __uint_as_float((uint32_t)src[i] << 16);
@@ -1245,6 +1542,15 @@ cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, cons
   mk_pack_kernel<<<(unsigned)blocks, threads, 0, st>>>(dst, (const uint16_t*)src_a, (const uint16_t*)src_b,
                                                      (const uint16_t*)src_c, n_rows_packed, n_src_rows, K, ld,
                                                      col0, mode, hd, gs, grp, tile_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+                            cudaStream_t st) {
+  const long long units = ((long long)(2 * kMoeFs / 16) * (d / 16) * 32 + (long long)(d / 16) * (kMoeFs / 16) * 32) *
+                          (f / kMoeFs);
+  mk_pack_moe_kernel<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(dst, (const uint16_t*)gate,
+                                                                     (const uint16_t*)up, (const uint16_t*)down, d, f);
   return cudaGetLastError();
 }
 

@@ -3,8 +3,9 @@
 Acceptance (from the decode-step contract):
   * bookkeeping bit-exact: written K/V page/slot, untouched cache bytes unchanged,
     active-expert sets and per-expert token lists, counters back at zero;
-  * expert selection identical wherever the oracle's top-k margin >= 1e-3 (below
-    that either set is correct: the oracle is re-run with the GPU's choice forced);
+  * expert selection identical wherever the oracle's top-k margin >= 1e-3, the
+    oracle's router being evaluated on the GPU's own layer input (below that margin
+    either set is correct); the free-running oracle then takes the GPU's selections;
   * per-layer hidden-state relative L2 error <= 1e-2;
   * logits max |diff| <= 0.05 and the same greedy argmax (unless the oracle's
     top-2 gap is below 2 * max|diff|, a reported tie).
@@ -40,53 +41,50 @@ def setup(workload, seed=0, steps=1, gain_jitter=0.1, device="cuda", seq_lens=No
     return cfg, W, seq, pt, npages, k, v, tokens
 
 
-def gpu_forced_routes(cfg, ref, gpu_idx):
-    """(l, b) -> GPU selection wherever the sets differ; asserts each such place is
-    a near-tie of the oracle (margin < MARGIN)."""
-    forced = {}
-    for l, info in enumerate(ref["layers"]):
-        for b in range(gpu_idx.shape[1]):
-            o_set = set(int(e) for e in info["idx"][b])
-            g_set = set(int(e) for e in gpu_idx[l, b])
-            if o_set != g_set:
-                assert info["margin"][b] < MARGIN, (
-                    f"layer {l} seq {b}: expert sets differ with margin {info['margin'][b]}")
-                forced[(l, b)] = [int(e) for e in gpu_idx[l, b]]
-    return forced
+def check_routing_teacher_forced(cfg, HW, hid, gidx, gw, B):
+    """Routing decisions, layer by layer, against the oracle's router evaluated on the
+    GPU's own residual x_l: identical expert sets wherever the oracle's top-k margin
+    is >= MARGIN; weights within 1e-3 of the oracle's softmax over the GPU's
+    selection.  Returns the number of (layer, token) near-ties seen."""
+    ties = 0
+    for l in range(cfg["n_layers"]):
+        h = oracle.rms_norm(hid[l].astype(np.float64), oracle.bf16_to_f64(HW.attn_norm(l)),
+                            cfg["rms_eps"])
+        r = h @ oracle.bf16_to_f64(HW.router(l)).T
+        for b in range(B):
+            idx, _, margin = oracle.router_topk(r[b], cfg["top_k"])
+            g_sel = [int(e) for e in gidx[l, b]]
+            if margin >= MARGIN:
+                assert sorted(g_sel) == sorted(int(e) for e in idx), (l, b, margin, g_sel, idx)
+            else:
+                ties += 1
+            _, w_forced, _ = oracle.router_topk(r[b], cfg["top_k"], forced=g_sel)
+            assert np.abs(w_forced - gw[l, b]).max() < 1e-3, (l, b, w_forced, gw[l, b])
+    return ties
 
 
 def check_step(cfg, mk, W, seq, pt, kv_before, tokens_np, logits_gpu, k_after=None, v_after=None):
-    """Compare one GPU step with the oracle.  Returns a dict of measured errors."""
+    """Compare one GPU step with the oracle.  Returns a dict of measured errors.
+
+    Routing is validated teacher-forced (above); the numerics are then compared with
+    the oracle run free on its own residual stream but taking the GPU's (validated)
+    expert selections, so that a near-tie decided the other way does not turn into a
+    different model."""
     HW = synth.HostWeights(W)
     HK = synth.HostKV(*kv_before)
-    ref = oracle.decode_step(cfg, HW, HK, tokens_np, seq, pt)
+    B = len(seq)
+    hid = mk.hidden()
     gidx, gw = mk.routes()
-    forced = gpu_forced_routes(cfg, ref, gidx)
-    if forced:
-        ref = oracle.decode_step(cfg, HW, HK, tokens_np, seq, pt, forced=forced)
-    out = dict(forced=len(forced))
-    # routing: identical sets everywhere now (forced where near-tied); weights close
-    for l, info in enumerate(ref["layers"]):
-        for b in range(len(seq)):
-            assert sorted(int(e) for e in info["idx"][b]) == sorted(int(e) for e in gidx[l, b])
-            og = dict(zip((int(e) for e in info["idx"][b]), info["w"][b]))
-            for e, wv in zip(gidx[l, b], gw[l, b]):
-                assert abs(og[int(e)] - wv) < 2e-2, (l, b, e, og[int(e)], wv)
+    out = dict(near_ties=check_routing_teacher_forced(cfg, HW, hid, gidx, gw, B))
+    forced = {(l, b): [int(e) for e in gidx[l, b]]
+              for l in range(cfg["n_layers"]) for b in range(B)}
+    ref = oracle.decode_step(cfg, HW, HK, tokens_np, seq, pt, forced=forced)
     # active-expert bookkeeping: slot order = ascending expert id, token lists by (b, j)
     act = mk.active()
     for l, info in enumerate(ref["layers"]):
-        want = []
-        for e in sorted(info["experts"]):
-            want.append((e, sorted(info["experts"][e])))
-        got = [(e, lst) for e, lst in act[l]]
-        # the GPU's slot j for token b is its own selection order; compare (b) and expert
-        assert [e for e, _ in got] == [e for e, _ in want], (l, got, want)
-        for (e, gl), (_, wl) in zip(got, want):
-            assert [b for b, _ in gl] == [b for b, _ in wl]
-            for b, j in gl:
-                assert int(gidx[l, b, j]) == e
+        want = [(e, sorted(info["experts"][e])) for e in sorted(info["experts"])]
+        assert act[l] == want, (l, act[l], want)
     # hidden states
-    hid = mk.hidden()
     errs = [rel_l2(hid[i], ref["hidden"][i]) for i in range(cfg["n_layers"] + 1)]
     out["hidden_rel_l2_max"] = max(errs)
     assert max(errs) <= REL_L2, errs
@@ -119,7 +117,6 @@ def check_step(cfg, mk, W, seq, pt, kv_before, tokens_np, logits_gpu, k_after=No
         kb_m = kb.permute(0, 1, 3, 2, 4)[mask]
         ka_m = k_after.permute(0, 1, 3, 2, 4)[mask]
         assert torch.equal(kb_m.view(torch.int16), ka_m.view(torch.int16))
-        vb_m = kb_m = None
         assert torch.equal(kv_before[1].permute(0, 1, 3, 2, 4)[mask].view(torch.int16),
                            v_after.permute(0, 1, 3, 2, 4)[mask].view(torch.int16))
     return out
