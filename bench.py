@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--no-bs8", action="store_true", help="skip the batch-8 ragged measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--trace", default="",
+                    help="after timing, record one step's task timeline and write a per-opcode "
+                         "summary (JSON) to this path")
     return ap.parse_args()
 
 
@@ -68,6 +71,7 @@ def barrier(ws):
 
 
 def max_over_ranks(v: float, ws: int, device="cuda") -> float:
+    """Max of a per-rank value over all ranks (the slowest replica sets the time)."""
     if ws == 1:
         return v
     import torch
@@ -217,6 +221,38 @@ def time_device(run_step, K, W, ws, stream):
     return total, per
 
 
+OPNAMES = {1: "EMBED", 2: "QKV_PROJ", 3: "ROUTER", 4: "ATTN_DRAIN", 5: "MOE_DRAIN", 7: "O_PROJ",
+           8: "LM_HEAD", 9: "ADD_RMSNORM"}
+
+
+def task_trace_summary(mk, st, path):
+    """One traced megakernel step: per opcode, the mean time a task spends waiting for
+    its dependency, for its operands / first chunk, in its MMA loop and after it (us)."""
+    import numpy as np
+    import torch
+    mk.trace_on(1 << 18)
+    mk.step(st["tokens"], st["k"], st["v"], st["logits"])
+    torch.cuda.synchronize()
+    r = mk.trace_records().astype(np.int64)
+    mk.trace_off()
+    op = (r[:, 0] >> 8) & 0xFF
+    t0 = r[:, 2].min()
+    out = {"span_us": float((r[:, 7].max() - t0) / 1e3), "tasks": int(len(r)), "per_opcode": {}}
+    for o in sorted(set(op.tolist())):
+        m = op == o
+        def mean(a, b):
+            x = r[m, b] - r[m, a]
+            x = x[(r[m, a] > 0) & (r[m, b] > 0)]
+            return float(x.mean() / 1e3) if len(x) else None
+        out["per_opcode"][OPNAMES.get(o, str(o))] = dict(
+            n=int(m.sum()), dep_wait=mean(2, 3), operand_wait=mean(3, 4), loop=mean(4, 5),
+            after_loop=mean(5, 7), total=mean(2, 7))
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+    np.save(os.path.splitext(path)[0] + ".npy", r)
+    return {"path": path, "span_us": out["span_us"]}
+
+
 def union_sizes(mk, L):
     return [len(a) for a in mk.active()][:L]
 
@@ -320,6 +356,10 @@ def main():
     stream = torch.cuda.current_stream()
     cfg, mk, st, W = build_state(args.workload, args.seed, device)
     B = len(st["seq"])
+    if args.no_bs8 or args.workload != "pages_b1_8k":
+        # the unpacked weights are only needed again to build the batch-8 handle
+        W = None
+        torch.cuda.empty_cache()
 
     def step_mega():
         mk.step(st["tokens"], st["k"], st["v"], st["logits"])
@@ -394,6 +434,9 @@ def main():
         barrier(ws)
         line["e2e"] = {"value": ws * B * args.steps / el, "unit": UNIT,
                        "h2d_bytes_per_step": B * 4, "d2h_bytes_per_step": B * cfg["vocab"] * 4}
+
+    if args.trace:
+        line["trace"] = task_trace_summary(mk, st, args.trace)
 
     # ---- the same opcodes as separate launches, and as one CUDA graph
     if not args.no_baselines and args.mode == "mega":

@@ -190,14 +190,20 @@ enum {
 int mk_query(mk_handle* h, int what, int64_t* out);
 
 /* Host-only planner run (no device needed): the descriptor table and the per-SM
- * lists that mk_plan would build for `n_sms` SMs, for tests of the schedule.
+ * lists that mk_plan would build for `n_sms` SMs (the megakernel segment), for tests
+ * of the schedule.
  *   tasks_out   int32[cap_tasks][32]      sm_off_out int32[n_sms + 1]
- *   sm_list_out int32[cap_list]           info_out int32[16]: n_tasks, list
- *   length, n_counters, max_active, 0, expert-up tiles per expert, expert-down
- *   tiles per expert, rows per O-proj / expert-down / expert-up task, QKV tasks
- *   per KV group, router tasks, residual row-block target, index of the done
- *   counter, number of plan segments, LM-head tasks.  Returns MK_ERR_INVALID if a cap is too
- *   small (info_out[0..1] still hold the sizes needed). */
+ *   sm_list_out int32[cap_list]           info_out int32[32]:
+ *     [0] tasks  [1] list length  [2] counters  [3] max active experts  [4] 0
+ *     [5] MoE items per expert  [6] MoE item KiB  [7] O-proj tile rows
+ *     [8] MoE f-slice rows  [9] QKV tile rows  [10] QKV tiles per KV group
+ *     [11] router tiles  [12] residual row-block target  [13] done-counter index
+ *     [14] plan segments (1 + per-op launches)  [15] LM-head tiles
+ *     [16..23] counter bases: layer-ready, QKV-group, router-tiles, route-ready,
+ *              attention (layer, seq, group), O-group, MoE-done, row-block
+ *     [24] residual row blocks  [25] query heads per KV group
+ * Returns MK_ERR_INVALID if a cap is too small (info_out[0..1] still hold the sizes
+ * needed). */
 int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out,
                 int cap_tasks, int32_t* sm_off_out, int32_t* sm_list_out, int cap_list,
                 int32_t* info_out);

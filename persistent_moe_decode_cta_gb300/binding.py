@@ -220,10 +220,10 @@ def mk_query(h, what: int) -> int:
 
 
 def mk_plan_dry(cfg: dict, batch: int, n_sms: int, max_batch: int = 8):
-    """Host-only plan: (tasks [n,32], sm_off [n_sms+1], sm_list, info[16])."""
+    """Host-only plan: (tasks [n,32], sm_off [n_sms+1], sm_list, info[32])."""
     lib = load_library()
     c = make_config(cfg, max_batch)
-    info = np.zeros(16, dtype=np.int32)
+    info = np.zeros(32, dtype=np.int32)
     rc = lib.mk_plan_dry(ctypes.byref(c), batch, n_sms, None, 0, None, None, 0,
                          info.ctypes.data)
     n_tasks, n_list = int(info[0]), int(info[1])

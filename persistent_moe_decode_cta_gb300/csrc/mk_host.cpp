@@ -31,7 +31,7 @@ cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, cons
                         int n_rows_packed, int n_src_rows, int K, long long ld, int col0, int mode, int hd,
                         int gs, int grp, int tile_rows, cudaStream_t st);
 cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_t st);
-cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f, int fs,
                             cudaStream_t st);
 cudaError_t prepare_megakernel();
 int megakernel_occupancy(int* blocks);
@@ -51,7 +51,7 @@ struct Shape {
   int r_qkv, qkv_rows_group, qkv_tpg;
   int r_router, n_router_tasks, e_pad;
   int r_o, t_o, k_o;
-  int t_moe;
+  int moe_fs, t_moe;
   int r_lm, v_pad, n_lm_tasks;
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
   size_t off_qkv, off_o, off_router, off_moe, off_lm, off_embed, total;
@@ -96,12 +96,19 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.e_pad = (s.E + 15) / 16 * 16;
   s.n_router_tasks = s.e_pad / s.r_router;
   s.r_o = 64; s.t_o = s.d / s.r_o; s.k_o = s.gs * s.hd;
-  s.t_moe = s.f / kMoeFs;
+  // MoE f-slice width: 32 rows of d_ff (measured best at the pages-scale shape against
+  // 16/48/64: wider items start late on SMs still busy with attention items)
+  s.moe_fs = (s.f % 32 == 0) ? 32 : 16;
+  if (const char* e = getenv("MK_MOE_FS")) {
+    const int v = atoi(e);
+    if ((v == 16 || v == 32) && s.f % v == 0) s.moe_fs = v;
+  }
+  s.t_moe = s.f / s.moe_fs;
   s.r_lm = 64; s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
   s.router_layer_bytes = (size_t)s.e_pad * s.d * 2;
-  s.moe_item_bytes = (size_t)3 * kMoeFs * s.d * 2;
+  s.moe_item_bytes = (size_t)3 * s.moe_fs * s.d * 2;
   s.moe_bytes_e = s.moe_item_bytes * s.t_moe;
   s.lm_bytes = (size_t)s.v_pad * s.d * 2;
   s.embed_bytes = (size_t)s.V * s.d * 2;
@@ -500,7 +507,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
     for (int e2 = 0; e2 < E; ++e2) {
       const int i = l * E + e2;
       e = launch_pack_moe(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i], w->w_down[i], d,
-                          f, st);
+                          f, s.moe_fs, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "pack moe"); return bail(MK_ERR_CUDA); }
     }
     e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
@@ -532,8 +539,10 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
   if (info_out) {
     int32_t* I = info_out;
     I[0] = P.n_tasks(); I[1] = list_len; I[2] = P.n_ctr; I[3] = P.maxa; I[4] = 0;
-    I[5] = s.t_moe; I[6] = (int)(s.moe_item_bytes / 1024); I[7] = s.r_o; I[8] = kMoeFs; I[9] = s.r_qkv; I[10] = s.qkv_tpg;
+    I[5] = s.t_moe; I[6] = (int)(s.moe_item_bytes / 1024); I[7] = s.r_o; I[8] = s.moe_fs; I[9] = s.r_qkv; I[10] = s.qkv_tpg;
     I[11] = s.n_router_tasks; I[12] = P.rb_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
+    I[16] = P.c_lr; I[17] = P.c_qkvg; I[18] = P.c_rt; I[19] = P.c_rr; I[20] = P.c_att; I[21] = P.c_og;
+    I[22] = P.c_md; I[23] = P.c_rb; I[24] = s.nrb_d; I[25] = s.gs;
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
     return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
@@ -585,7 +594,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.swa_mask = h->cfg.swa_layer_mask; p.theta = h->cfg.rope_theta; p.eps = h->cfg.rms_eps;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)s.hd));
   p.split_pages = h->split_pages; p.max_items_bg = h->max_items_bg;
-  p.t_moe = s.t_moe; p.qkv_tpg = s.qkv_tpg;
+  p.moe_fs = s.moe_fs; p.t_moe = s.t_moe; p.qkv_tpg = s.qkv_tpg;
   p.n_router_tasks = s.n_router_tasks;
   p.timeout_ns = (long long)h->cfg.timeout_ms * 1000000ll;
   p.inflight = 2;

@@ -49,7 +49,12 @@ constexpr int kCtrStride = 32;
 constexpr int kSsStride = 32;
 constexpr int kMaxBatch = 8;
 constexpr int kRowBlock = 128;                // residual row block (rows of d_model)
-constexpr int kMoeFs = 32;                    // d_ff rows of one MoE item (f-slice)
+// j-groups per ring chunk of a GEMV tile with `nrb` 16-row blocks (chunk = jpc*nrb*4 KB)
+constexpr __host__ __device__ int gemv_jpc(int nrb) { return 8 / nrb > 0 ? 8 / nrb : 1; }
+// consumer warps whose down-slice regions share one ring chunk (a power of two)
+constexpr __host__ __device__ int moe_warps_per_chunk(int region_bytes) {
+  return region_bytes * 8 <= 32768 ? 8 : region_bytes * 4 <= 32768 ? 4 : region_bytes * 2 <= 32768 ? 2 : 1;
+}
 
 enum Op : int32_t {
   OP_END = 0,
@@ -77,10 +82,11 @@ enum DescField : int {
 
 // Row-map modes of the weight packer.
 enum PackMode : int { PACK_IDENT = 0, PACK_QKV = 1, PACK_GATE_UP = 2 };
-// MoE item (expert e, f-slice s = rows [32 s, 32 s + 32) of d_ff) packed as one
-// contiguous tile: the 64 interleaved gate/up rows x d_model (GEMV fragment order,
-// 4 row blocks), then the down slice W_down[:, 32 s : 32 s + 32] with consumer warp w
-// owning output rows [w d/8, (w+1) d/8) (fragment order [w][row block][k16-step]).
+// MoE item (expert e, f-slice s = rows [FS s, FS s + FS) of d_ff, FS in {16, 32})
+// packed as one contiguous tile: the 2 FS interleaved gate/up rows x d_model (GEMV
+// fragment order, FS/8 row blocks), then the down slice W_down[:, FS s : FS s + FS]
+// with consumer warp w owning output rows [w d/8, (w+1) d/8) (fragment order
+// [w][row block][k16-step]).
 
 // Device error word layout (int32[16]).
 enum ErrField : int { E_CODE = 0, E_TASK = 1, E_CTR = 2, E_OBS = 3, E_TARGET = 4,
@@ -93,7 +99,7 @@ struct Params {
   unsigned long long swa_mask;
   float theta, eps, scale_log2;
   int split_pages, max_items_bg;
-  int t_moe, qkv_tpg, n_router_tasks;  // t_moe = MoE items per expert = d_ff / kMoeFs
+  int moe_fs, t_moe, qkv_tpg, n_router_tasks;  // MoE item = moe_fs rows of d_ff; t_moe = d_ff / moe_fs
   long long timeout_ns;
   int fixed, do_reset;
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)

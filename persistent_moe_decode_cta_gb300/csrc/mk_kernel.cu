@@ -301,9 +301,9 @@ __device__ __forceinline__ bool claim_gate(const Params& p, const Smem& S, uint3
 }
 
 __device__ bool issue_linear(const Params& p, const Smem& S, uint32_t& cseq, const uint8_t* src,
-                             int bytes, uint64_t pol, int task) {
-  for (int off = 0; off < bytes; off += kStageBytes) {
-    const int n = min(kStageBytes, bytes - off);
+                             int bytes, uint64_t pol, int task, int chunk = kStageBytes) {
+  for (int off = 0; off < bytes; off += chunk) {
+    const int n = min(chunk, bytes - off);
     if (!acquire_stage(p, S, cseq, task)) return false;
     const uint32_t s = cseq % kStages;
     mbar_expect_tx(S.full(s), (uint32_t)n);
@@ -366,8 +366,10 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         const long long off = (long long)(((unsigned long long)(unsigned)T[D_WOFF_HI] << 32) |
                                           (unsigned)T[D_WOFF_LO]);
         const int bytes = T[D_WBYTES];
-        const int nch = (bytes + kStageBytes - 1) / kStageBytes;
-        ok = mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti);
+        const int nrb = T[D_NROWS] / 16;
+        const int cs = gemv_jpc(nrb) * nrb * 8 * kFragBytes;
+        const int nch = (bytes + cs - 1) / cs;
+        ok = mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs);
         break;
       }
       case OP_ATT_DRAIN: {
@@ -387,16 +389,23 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         if (!wait_ge(p, C_RR(p, l), 1u, ti)) { ok = false; break; }
         const int q = p.L + l;
         const int count = ldg_cg(p.qcount + q);
-        const int nch = (int)((p.moe_item_bytes + kStageBytes - 1) / kStageBytes);
+        // part 1 (gate/up tile) in whole k16-groups, part 2 (down slice) in warp regions
+        const int nrb1 = p.moe_fs / 8;
+        const int cs1 = gemv_jpc(nrb1) * nrb1 * 8 * kFragBytes;
+        const int gu_bytes = 2 * p.moe_fs * p.d * 2;
+        const int region = (p.d / 128) * (p.moe_fs / 16) * kFragBytes;
+        const int cs2 = moe_warps_per_chunk(region) * region;
+        const int dn_bytes = (int)p.moe_item_bytes - gu_bytes;
+        const int nch = (gu_bytes + cs1 - 1) / cs1 + (dn_bytes + cs2 - 1) / cs2;
         while (ok) {
           if (!(ok = claim_gate(p, S, mseq, ti))) break;
           const int item = atomicAdd(p.qhead + q, 1);
           if (item >= count) break;
           const int a = item / p.t_moe, t = item % p.t_moe;
           const int e = ldg_cg(p.active + l * p.maxa + a);
-          const long long off = p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
-          ok = mbox_push(p, S, mseq, ti, item, nch) &&
-               issue_linear(p, S, cseq, p.wblob + off, (int)p.moe_item_bytes, pol, ti);
+          const uint8_t* src = p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
+          ok = mbox_push(p, S, mseq, ti, item, nch) && issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1) &&
+               issue_linear(p, S, cseq, src + gu_bytes, dn_bytes, pol, ti, cs2);
         }
         break;
       }
@@ -436,8 +445,9 @@ __device__ __forceinline__ void load_bfrag(BFrag& fr, int ksw, const uint16_t* r
 
 // acc[rb] += W_tile[rb] * act over this warp's k16-steps ks = warp + 8 j, consuming the
 // task's ring chunks.  Tiles are packed so that fragment (rb, ks) sits at index
-// (j * NRB + rb) * 8 + warp: every 32 KB chunk holds 8 / NRB consecutive j for all
-// row blocks, so chunk, register and smem indices are compile-time constants.
+// (j * NRB + rb) * 8 + warp: every ring chunk holds JPC = floor(8 / NRB) consecutive j
+// for all row blocks (JPC * NRB * 4 KB <= 32 KB), so chunk, register and smem indices
+// are compile-time constants.
 // With `lo` non-null the operand is the exact-ish sum hi + lo of two bf16 parts and
 // every fragment is multiplied twice (router logits: top-k decisions need them to
 // ~1e-5; the tensor-core work is negligible against the weight bytes).
@@ -445,7 +455,7 @@ template <int NRB>
 __device__ __forceinline__ bool gemv_mainloop(const Params& p, const Smem& S, uint32_t& cseq, int nch,
                                               int ksw, const BFrag& fr, float (&acc)[NRB][4],
                                               const BFrag* lo = nullptr) {
-  constexpr int JPC = 8 / NRB;
+  constexpr int JPC = gemv_jpc(NRB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int r = 0; r < NRB; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
@@ -765,30 +775,34 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
   const int nrb = nrows / 16;
   const int ksw = klen / 16 / kConsumerWarps;
 
-  if (reuse) {
-  } else if (op == OP_OPROJ) {
-    const int n = lane >> 2;
-    load_bfrag(fr, ksw, n < p.B ? p.atto + ((size_t)l * p.B + n) * p.Hq * p.hd + T[D_K0] : nullptr);
-  } else {
-    // RMSNorm operand of QKV / ROUTER (layer input) and LM_HEAD (final norm)
-    const int n = lane >> 2;
-    rs_have = build_norm_bfrag(p, S, fr, ksw, op == OP_LMHEAD ? p.L : l, n < p.B ? n : -1);
-  }
-  have = key;
-
   float v[4];
   bool ran;
   if (op == OP_ROUTER) {
-    // residue part of the router operand (the hi part is the shared cached operand)
-    BFrag lo;
+    // the router's operand is hi + lo bf16 parts (hi is shared with the layer's QKV
+    // tiles; the residue lo is loaded for the router only)
     const int n = lane >> 2;
+    if (!reuse) rs_have = build_norm_bfrag(p, S, fr, ksw, l, n < p.B ? n : -1);
+    have = key;
+    BFrag lo;
     load_bfrag(lo, ksw, n < p.B ? p.XGL + ((size_t)l * p.B + n) * p.d : nullptr);
     ran = (nrb == 1) ? gemv_run<1>(p, S, cseq, nch, ksw, fr, v, &lo) : gemv_run<2>(p, S, cseq, nch, ksw, fr, v, &lo);
-  } else switch (nrb) {
-    case 1: ran = gemv_run<1>(p, S, cseq, nch, ksw, fr, v); break;
-    case 2: ran = gemv_run<2>(p, S, cseq, nch, ksw, fr, v); break;
-    case 4: ran = gemv_run<4>(p, S, cseq, nch, ksw, fr, v); break;
-    default: ran = gemv_run<8>(p, S, cseq, nch, ksw, fr, v); break;
+  } else {
+    if (!reuse) {
+      const int n = lane >> 2;
+      if (op == OP_OPROJ) {
+        load_bfrag(fr, ksw, n < p.B ? p.atto + ((size_t)l * p.B + n) * p.Hq * p.hd + T[D_K0] : nullptr);
+      } else {
+        // RMSNorm operand of QKV (layer input) and LM_HEAD (final norm)
+        rs_have = build_norm_bfrag(p, S, fr, ksw, op == OP_LMHEAD ? p.L : l, n < p.B ? n : -1);
+      }
+    }
+    have = key;
+    switch (nrb) {
+      case 1: ran = gemv_run<1>(p, S, cseq, nch, ksw, fr, v); break;
+      case 2: ran = gemv_run<2>(p, S, cseq, nch, ksw, fr, v); break;
+      case 4: ran = gemv_run<4>(p, S, cseq, nch, ksw, fr, v); break;
+      default: ran = gemv_run<8>(p, S, cseq, nch, ksw, fr, v); break;
+    }
   }
   if (!ran) return false;
 
@@ -917,6 +931,7 @@ __device__ bool task_resid(const Params& p, const Smem& S, uint32_t& sseq, const
 //            token's routing weight, added into the layer's MoE accumulator.
 // Completion is counted on the layer's MoE-done counter (padded to max_active * t_moe
 // by the route step).
+template <int FS>
 __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, const int* T,
                                          int ti, int item, int nch, BFrag& fr, OperandKey& have, float& rs_have) {
   const int l = T[D_LAYER];
@@ -954,15 +969,16 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
       wt[e] = ldg_cg(p.rw + ((size_t)l * p.B + bt[e]) * p.topk + (pk & 15));
     }
   }
-  // ---- phase 1
-  const int nch1 = p.d / 256;  // 64 rows x d bf16 = d/256 ring chunks
+  // ---- phase 1: 2*FS interleaved gate/up rows = FS/8 row blocks
+  constexpr int fs = FS, nrb1 = FS / 8;
+  const int nch1 = (ksw1 + gemv_jpc(nrb1) - 1) / gemv_jpc(nrb1);
   float v[4];
-  if (!gemv_run<4>(p, S, cseq, nch1, ksw1, fr, v)) return false;
-  uint16_t* a_s = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(S.scratch) + 16384);  // [8][32]
+  if (!gemv_run<nrb1>(p, S, cseq, nch1, ksw1, fr, v)) return false;
+  uint16_t* a_s = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(S.scratch) + 16384);  // [8][fs]
   {
     const float rs0 = __shfl_sync(0xffffffffu, rs_have, 8 * c);
     const float rs1 = __shfl_sync(0xffffffffu, rs_have, 8 * c + 4);
-    if (warp < 4) {  // row block w = gate rows 8w..8w+7 (row g8) paired with up rows (g8 + 8)
+    if (warp < nrb1) {  // row block w = gate rows 8w..8w+7 (row g8) paired with up rows (g8 + 8)
       const int frow = warp * 8 + g8;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
@@ -970,22 +986,24 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
         const float rs = e ? rs1 : rs0;
         const float gt = v[e] * rs, up = v[2 + e] * rs;
         const float a = (n < ntok) ? gt / (1.f + __expf(-gt)) * up : 0.f;
-        a_s[n * kMoeFs + frow] = to_bf16(a);
+        a_s[n * fs + frow] = to_bf16(a);
       }
     }
   }
   bar_sync_consumers();
-  // ---- phase 2: warp w owns output rows [w * rpw * 16, (w + 1) * rpw * 16)
-  uint32_t b2[2][2];
+  // ---- phase 2: warp w owns output rows [w * rpw * 16, (w + 1) * rpw * 16), K = fs
+  constexpr int k2 = FS / 16;
+  uint32_t b2[k2][2];
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    b2[ks][0] = *reinterpret_cast<const uint32_t*>(a_s + g8 * kMoeFs + 16 * ks + 2 * c);
-    b2[ks][1] = *reinterpret_cast<const uint32_t*>(a_s + g8 * kMoeFs + 16 * ks + 8 + 2 * c);
+  for (int ks = 0; ks < k2; ++ks) {
+    b2[ks][0] = *reinterpret_cast<const uint32_t*>(a_s + g8 * fs + 16 * ks + 2 * c);
+    b2[ks][1] = *reinterpret_cast<const uint32_t*>(a_s + g8 * fs + 16 * ks + 8 + 2 * c);
   }
   const int rpw = p.d / 128;
-  const int region = rpw * 2 * kFragBytes;
-  const int my_chunk = (warp * region) / kStageBytes;
-  const int my_off = (warp * region) % kStageBytes;
+  const int region = rpw * k2 * kFragBytes;
+  const int wpc = moe_warps_per_chunk(region);
+  const int my_chunk = warp / wpc;
+  const int my_off = (warp % wpc) * region;
   const int nch2 = nch - nch1;
   float* out0 = bt[0] >= 0 ? p.moe + ((size_t)l * p.B + bt[0]) * p.d : nullptr;
   float* out1 = bt[1] >= 0 ? p.moe + ((size_t)l * p.B + bt[1]) * p.d : nullptr;
@@ -996,8 +1014,8 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
       for (int rb = 0; rb < rpw; ++rb) {
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          const uint4 a = lds128(base + (rb * 2 + ks) * kFragBytes);
+        for (int ks = 0; ks < k2; ++ks) {
+          const uint4 a = lds128(base + (rb * k2 + ks) * kFragBytes);
           mma_bf16(acc, a.x, a.y, a.z, a.w, b2[ks][0], b2[ks][1]);
         }
         const int row = (warp * rpw + rb) * 16 + g8;
@@ -1345,7 +1363,8 @@ __device__ void consumer(const Params& p, const Smem& S) {
         for (int j = 0; j < kMaxKsw; ++j) fr.b0[j] = fr.b1[j] = 0u;
         break;
       case OP_MOE_DRAIN:
-        ok = task_moe(p, S, cseq, sseq, T, ent.x, ent.y, nch, fr, have, rs_have);
+        ok = (p.moe_fs == 32) ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, fr, have, rs_have)
+                              : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, fr, have, rs_have);
         break;
       default:
         ok = task_gemv(p, S, cseq, sseq, T, ent.x, nch, fr, have, rs_have);
@@ -1474,10 +1493,11 @@ __global__ void mk_pack_kernel(uint8_t* __restrict__ dst, const uint16_t* __rest
 // All t = d_ff / 32 items of one expert (see the MoE item layout in mk_internal.h).
 __global__ void mk_pack_moe_kernel(uint8_t* __restrict__ dst, const uint16_t* __restrict__ gate,
                                    const uint16_t* __restrict__ up, const uint16_t* __restrict__ down, int d,
-                                   int f) {
-  const int t_n = f / kMoeFs;
-  const long long gu_units = (long long)(2 * kMoeFs / 16) * (d / 16) * 32;
-  const long long dn_units = (long long)(d / 16) * (kMoeFs / 16) * 32;
+                                   int f, int fs) {
+  const int t_n = f / fs;
+  const int nrb1 = fs / 8, k2 = fs / 16;
+  const long long gu_units = (long long)nrb1 * (d / 16) * 32;
+  const long long dn_units = (long long)(d / 16) * k2 * 32;
   const long long item_units = gu_units + dn_units;
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= item_units * t_n) return;
@@ -1487,16 +1507,16 @@ __global__ void mk_pack_moe_kernel(uint8_t* __restrict__ dst, const uint16_t* __
   const int g8 = lane >> 2, c = lane & 3;
   uint16_t out[8];
   if (r < gu_units) {
-    // gate/up tile: 4 row blocks (8 gate + 8 up rows each), GEMV order (j*4 + rb)*8 + w
+    // gate/up tile: fs/8 row blocks (8 gate + 8 up rows each), GEMV order (j*nrb1 + rb)*8 + w
     const long long fi = r >> 5;
-    const int j = (int)(fi / 32), rem = (int)(fi % 32);
+    const int j = (int)(fi / (nrb1 * 8)), rem = (int)(fi % (nrb1 * 8));
     const int rb = rem / 8, ks = rem % 8 + 8 * j;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int i = g8 + ((q & 1) ? 8 : 0);                 // row within the block
       const int k = 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
       const uint16_t* src = (i < 8) ? gate : up;
-      const long long srow = (long long)s * kMoeFs + 8 * rb + (i & 7);
+      const long long srow = (long long)s * fs + 8 * rb + (i & 7);
       out[2 * q] = src[srow * d + k];
       out[2 * q + 1] = src[srow * d + k + 1];
     }
@@ -1504,12 +1524,12 @@ __global__ void mk_pack_moe_kernel(uint8_t* __restrict__ dst, const uint16_t* __
     // down slice: warp w owns rows [w d/8, (w+1) d/8); order [w][row block][ks]
     const long long fi = (r - gu_units) >> 5;
     const int rpw = d / 128;
-    const int w = (int)(fi / (rpw * 2)), rem = (int)(fi % (rpw * 2));
-    const int rb = w * rpw + rem / 2, ks = rem % 2;
+    const int w = (int)(fi / (rpw * k2)), rem = (int)(fi % (rpw * k2));
+    const int rb = w * rpw + rem / k2, ks = rem % k2;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const long long row = (long long)rb * 16 + g8 + ((q & 1) ? 8 : 0);
-      const int col = s * kMoeFs + 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
+      const int col = s * fs + 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
       out[2 * q] = down[row * f + col];
       out[2 * q + 1] = down[row * f + col + 1];
     }
@@ -1545,12 +1565,12 @@ cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f, int fs,
                             cudaStream_t st) {
-  const long long units = ((long long)(2 * kMoeFs / 16) * (d / 16) * 32 + (long long)(d / 16) * (kMoeFs / 16) * 32) *
-                          (f / kMoeFs);
+  const long long units = ((long long)(fs / 8) * (d / 16) * 32 + (long long)(d / 16) * (fs / 16) * 32) * (f / fs);
   mk_pack_moe_kernel<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(dst, (const uint16_t*)gate,
-                                                                     (const uint16_t*)up, (const uint16_t*)down, d, f);
+                                                                     (const uint16_t*)up, (const uint16_t*)down, d, f,
+                                                                     fs);
   return cudaGetLastError();
 }
 

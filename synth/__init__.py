@@ -36,6 +36,7 @@ MODELS = {
 # Two layers of the pages-scale shape: small enough (3.7 GB) for profiler captures
 # and for the oracle to run in seconds, with every tile size of the full model.
 MODELS["pages_l2"] = dict(MODELS["pages"], n_layers=2)
+MODELS["pages_l1"] = dict(MODELS["pages"], n_layers=1)
 
 # Workloads: a model plus a batch of cached sequence lengths.
 WORKLOADS = {
@@ -46,6 +47,7 @@ WORKLOADS = {
                                 sliding_window=4096, swa="odd"),
     "pages_b1_128k": dict(model="pages", batch=1, lens=("fixed", 131072)),
     "pages_l2_b1_8k": dict(model="pages_l2", batch=1, lens=("fixed", 8192)),
+    "pages_l1_b1_8k": dict(model="pages_l1", batch=1, lens=("fixed", 8192)),
     "pages_l2_b8_ragged_swa": dict(model="pages_l2", batch=8, lens=("uniform", 1024, 32768),
                                    sliding_window=4096, swa="odd"),
 }
