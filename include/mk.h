@@ -157,6 +157,14 @@ int mk_get_status(mk_handle* h, mk_error_info* info);
  * record count.  Synchronising. */
 int mk_set_trace(mk_handle* h, void* records_dev, int capacity);
 
+/* Testing hook (host-side fault injection): redirect the completion signal of
+ * descriptor `task` (an index into the plan's table, see mk_plan_dry) away from the
+ * counter its waiters poll.  The next step's waiters then give up after timeout_ms
+ * and the step reports MK_ERR_TIMEOUT (task, counter, observed, target) through
+ * mk_get_status; every CTA drains and exits, and the context stays usable.  Undo by
+ * calling mk_plan again.  Synchronising. */
+int mk_plan_drop_signal(mk_handle* h, int task);
+
 /* fixed = 1: steps do not advance seq_lens (repeated steps move identical bytes). */
 int mk_set_fixed(mk_handle* h, int fixed);
 

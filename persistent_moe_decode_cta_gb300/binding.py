@@ -29,7 +29,8 @@ MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT =
 
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_step_host",
-           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace", "mk_read", "mk_query",
+           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace",
+           "mk_plan_drop_signal", "mk_read", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
 
 
@@ -88,6 +89,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_get_status.argtypes = [H, ctypes.POINTER(mk_error_info)]
     lib.mk_set_fixed.argtypes = [H, i32]
     lib.mk_set_trace.argtypes = [H, vp, i32]
+    lib.mk_plan_drop_signal.argtypes = [H, i32]
     lib.mk_read.argtypes = [H, i32, vp, sz]
     lib.mk_query.argtypes = [H, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.mk_plan_dry.argtypes = [ctypes.POINTER(mk_config), i32, i32, vp, i32, vp, vp, i32, vp]
@@ -199,6 +201,10 @@ def mk_get_status(h) -> dict:
 
 def mk_set_fixed(h, fixed: bool):
     _check(load_library().mk_set_fixed(h, int(bool(fixed))), h)
+
+
+def mk_plan_drop_signal(h, task: int):
+    _check(load_library().mk_plan_drop_signal(h, int(task)), h)
 
 
 def mk_set_trace(h, records, capacity: int):

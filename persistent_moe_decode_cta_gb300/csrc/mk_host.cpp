@@ -740,6 +740,20 @@ int mk_set_trace(mk_handle* h, void* records_dev, int capacity) {
   return MK_OK;
 }
 
+int mk_plan_drop_signal(mk_handle* h, int task) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
+  if (task < 0 || task >= h->P.n_tasks()) return fail(&h->err, MK_ERR_INVALID, "task %d out of range", task);
+  int32_t* T = &h->P.tasks[(size_t)task * kDescInts];
+  if (T[D_SIG_CTR] < 0) return fail(&h->err, MK_ERR_INVALID, "task %d signals no counter", task);
+  T[D_SIG_CTR] = h->P.c_done;  // the launch-completion counter: never waited on by a task
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaDeviceSynchronize());
+  CK(h, cudaMemcpy(h->d_tasks + (size_t)task * kDescInts, T, kDescInts * 4, cudaMemcpyHostToDevice));
+  if (h->graph) { cudaGraphExecDestroy(h->graph); h->graph = nullptr; }
+  return MK_OK;
+}
+
 int mk_set_fixed(mk_handle* h, int fixed) {
   if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
   h->fixed = fixed ? 1 : 0;
