@@ -262,6 +262,9 @@ class Megakernel:
     def plan(self, seq_lens, page_table, n_pages):
         mk_plan(self.h, seq_lens, page_table, n_pages)
         self.B = len(seq_lens)
+        # every step reads the page table through the pointer given here: hold the
+        # tensor so that its memory is not recycled while the plan is in use
+        self._page_table = page_table
 
     def step(self, tokens, k_cache, v_cache, logits, stream=None):
         mk_decode_step(self.h, tokens, k_cache, v_cache, logits, stream)

@@ -70,19 +70,32 @@ def test_small_model_batch8_ragged_matches_oracle():
 
 
 def test_perop_graph_and_megakernel_agree():
+    """Each mode is checked against the oracle.  The modes are not bit-identical: the
+    MoE combine adds fp32 partials atomically, and a last-bit difference in the sum
+    can move the next layer's bf16 operand across a rounding boundary (one bf16 ulp,
+    which shifts every GEMV output of that layer by ~1e-4), or decide a router near-tie
+    the other way.  Rows whose expert selections match in every layer must therefore
+    agree within the logit tolerance of the oracle comparison; a row whose selection
+    differs has already been accepted as a near-tie by the oracle check."""
     cfg, W, seq, pt, pt_dev, npages, k, v, tokens, mk = _engine("small_b1_2k", [900, 31])
     mk.set_fixed(True)
-    outs = []
+    outs, routes = [], []
     for mode in ("mega", "perop", "graph", "mega"):
+        kb, vb = k.clone(), v.clone()
         lg = torch.empty(len(seq), cfg["vocab"], device="cuda")
         if mode == "mega":
             mk.step(tokens, k, v, lg)
         else:
             mk.step_perop(tokens, k, v, lg, use_graph=(mode == "graph"))
         assert mk.status()["code"] == 0
+        PU.check_step(cfg, mk, W, seq, pt, (kb, vb), tokens.cpu().numpy(), lg, k, v)
         outs.append(lg.cpu().numpy())
+        routes.append(np.sort(mk.routes()[0], axis=-1))
+    same = [b for b in range(len(seq)) if all(np.array_equal(r[:, b], routes[0][:, b])
+                                              for r in routes[1:])]
     for o in outs[1:]:
-        assert np.abs(o - outs[0]).max() < 1e-3   # fp32 atomic order of the MoE combine
+        if same:
+            assert np.abs(o[same] - outs[0][same]).max() <= PU.LOGIT_ABS
     assert list(mk.seq_lens()) == seq
     mk.close()
 
