@@ -134,6 +134,29 @@ int mk_decode_step(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void*
 int mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, void* k_cache,
                         void* v_cache, float* logits_host, void* stream);
 
+/* The same step as mk_decode_step for callers that cannot allocate device memory
+ * while they decode -- e.g. an embedding runtime that owns the whole device heap, or a
+ * code path that must not call cudaMalloc (which synchronises the device and may
+ * fail under memory pressure).  This call allocates nothing: the step's scratch (the
+ * per-layer activations, attention partials, routing tables, MoE accumulators,
+ * counters and queues that mk_plan otherwise provides) lives in one file-scope static
+ * device array of 64 MiB (kept on every GPU that loads the library until the process
+ * exits).  The pages have no counterpart to this entry point.
+ *   Arguments, layouts and results are those of mk_decode_step; the handle's packed
+ *   weights, plan and seq_lens are used as usual.  The per-step state that mk_read
+ *   returns (hidden states, routes, active lists, counters) is that of the last
+ *   mk_decode_step, not of this call, whose scratch is not the handle's.
+ *   Plans whose step scratch exceeds 64 MiB are rejected with MK_ERR_UNSUPPORTED and a
+ *   message giving the size needed (the pages-scale model needs ~21 MiB at batch 1 with
+ *   8K context, ~29 MiB at 128K, ~53 MiB at batch 2 with 32K, ~168 MiB at batch 8).
+ *   The first call on a device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture.  Every call clears the
+ *   counters and queues it needs (an asynchronous memset on `stream`) and overwrites
+ *   the rest, but all calls share the one array: calls that overlap on the GPU (other
+ *   streams, other handles) race and must be serialised by the caller. */
+int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void* v_cache,
+                           float* logits_dev, void* stream);
+
 /* The same step with the same device routines run as one kernel launch per
  * opcode wave per layer (use_graph = 0), or that launch sequence captured once
  * into a CUDA graph and replayed (use_graph = 1).  Measurement baselines. */

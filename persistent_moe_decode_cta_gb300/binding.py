@@ -28,7 +28,7 @@ MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT =
  MK_Q_NUM_STAGES) = range(1, 12)
 
 # exported symbols (kept equal to the declarations of include/mk.h)
-EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_step_host",
+EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_step_host", "mk_decode_step_noalloc",
            "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace",
            "mk_plan_drop_signal", "mk_read", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
@@ -85,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_plan.argtypes = [H, i32, ctypes.POINTER(ctypes.c_int32), vp, i32, i32]
     lib.mk_decode_step.argtypes = [H, vp, vp, vp, vp, vp]
     lib.mk_decode_step_host.argtypes = [H, vp, vp, vp, vp, vp]
+    lib.mk_decode_step_noalloc.argtypes = [H, vp, vp, vp, vp, vp]
     lib.mk_decode_step_perop.argtypes = [H, vp, vp, vp, vp, vp, i32]
     lib.mk_get_status.argtypes = [H, ctypes.POINTER(mk_error_info)]
     lib.mk_set_fixed.argtypes = [H, i32]
@@ -178,6 +179,13 @@ def mk_decode_step(h, tokens, k_cache, v_cache, logits, stream=None):
     _check(load_library().mk_decode_step(h, tokens.data_ptr(), k_cache.data_ptr(),
                                          v_cache.data_ptr(), logits.data_ptr(),
                                          _stream_ptr(stream)), h)
+
+
+def mk_decode_step_noalloc(h, tokens, k_cache, v_cache, logits, stream=None):
+    """mk_decode_step with the step scratch in the library's static device buffer."""
+    _check(load_library().mk_decode_step_noalloc(h, tokens.data_ptr(), k_cache.data_ptr(),
+                                                 v_cache.data_ptr(), logits.data_ptr(),
+                                                 _stream_ptr(stream)), h)
 
 
 def mk_decode_step_host(h, tokens_host, k_cache, v_cache, logits_host, stream=None):

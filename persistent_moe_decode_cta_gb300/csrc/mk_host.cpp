@@ -37,6 +37,7 @@ cudaError_t prepare_megakernel();
 int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                               bool cooperative, cudaStream_t st);
+cudaError_t static_scratch_address(void** ptr);
 }  // namespace mk
 
 using namespace mk;
@@ -654,6 +655,67 @@ int mk_decode_step(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   return launch_segment(h, 0, true, true, st);
+}
+
+// The step's scratch buffers (everything mk_plan allocates per step except the plan
+// state: seq_lens, error word, task lists, trace count, host-step staging) laid out in
+// one byte range, 256-byte aligned pieces.  Returns the bytes needed; with `base`
+// non-null also points the Params fields at it and reports the counter/queue span.
+static size_t step_scratch_layout(const mk_handle* h, uint8_t* base, Params* p, size_t* zero_off,
+                                  size_t* zero_bytes) {
+  const Shape& s = h->s;
+  const size_t L = s.L, B = h->B, maxa = h->P.maxa;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += (bytes + 255) / 256 * 256; return base ? base + r : nullptr; };
+  uint8_t* q;
+  q = take((L + 1) * B * s.d * 4);                              if (p) p->X = (float*)q;
+  q = take((L + 1) * s.nrb_d * kSsStride * 4);                  if (p) p->SS = (float*)q;
+  q = take((L + 1) * B * s.d * 2);                              if (p) p->XG = (uint16_t*)q;
+  q = take((L + 1) * B * s.d * 2);                              if (p) p->XGL = (uint16_t*)q;
+  q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->Q = (uint16_t*)q;
+  q = take(L * s.Hkv * B * (size_t)h->max_items_bg * s.gs * (s.hd + 2) * 4); if (p) p->attp = (float*)q;
+  q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->atto = (uint16_t*)q;
+  q = take(L * s.Hkv * B * s.d * 4);                            if (p) p->opart = (float*)q;
+  q = take(L * B * s.E * 4);                                    if (p) p->rlog = (float*)q;
+  q = take(L * B * s.topk * 4);                                 if (p) p->ridx = (int*)q;
+  q = take(L * B * s.topk * 4);                                 if (p) p->rw = (float*)q;
+  q = take(L * maxa * 4);                                       if (p) p->active = (int*)q;
+  q = take(L * 4);                                              if (p) p->nact = (int*)q;
+  q = take(L * maxa * 4);                                       if (p) p->act_cnt = (int*)q;
+  q = take(L * maxa * B * 4);                                   if (p) p->act_tok = (int*)q;
+  q = take(L * B * s.d * 4);                                    if (p) p->moe = (float*)q;
+  const size_t z0 = o;
+  q = take((size_t)h->P.n_ctr * kCtrStride * 4);                if (p) p->ctr = (unsigned*)q;
+  q = take(3 * L * 4);                                          if (p) p->qhead = (int*)q;
+  q = take(3 * L * 4);                                          if (p) p->qcount = (int*)q;
+  if (zero_off) *zero_off = z0;
+  if (zero_bytes) *zero_bytes = o - z0;
+  return o;
+}
+
+int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void* v_cache,
+                           float* logits_dev, void* stream) {
+  int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
+  if (r) return r;
+  const size_t need = step_scratch_layout(h, nullptr, nullptr, nullptr, nullptr);
+  if (need > kStaticScratchBytes)
+    return fail(&h->err, MK_ERR_UNSUPPORTED,
+                "mk_decode_step_noalloc: this plan needs %zu bytes of step scratch, the static buffer holds %zu "
+                "(reduce batch or context, or use mk_decode_step)", need, kStaticScratchBytes);
+  void* base = nullptr;
+  CK(h, static_scratch_address(&base));
+  Params p = h->prm;
+  size_t z_off = 0, z_bytes = 0;
+  step_scratch_layout(h, static_cast<uint8_t*>(base), &p, &z_off, &z_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // counters and queues must start at zero; everything else is written before it is read
+  CK(h, cudaMemsetAsync(static_cast<uint8_t*>(base) + z_off, 0, z_bytes, st));
+  h->last_stream = st;
+  p.sm_off = h->d_sm_off;
+  p.do_reset = 1;
+  cudaError_t e = launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch (static scratch)");
+  return MK_OK;
 }
 
 int mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, void* k_cache, void* v_cache,

@@ -41,6 +41,8 @@ constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kScrat
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
 
 constexpr int kDescInts = 32;
+// Size of the static step scratch of mk_decode_step_noalloc (64 MiB).
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 // Counters are padded to one 128-byte line each so that waiters on different
 // counters do not poll the same L2 line.
 constexpr int kCtrStride = 32;

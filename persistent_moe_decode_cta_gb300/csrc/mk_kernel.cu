@@ -1549,8 +1549,33 @@ __global__ void mk_convert_kernel(float* __restrict__ dst, const uint16_t* __res
 
 }  // namespace mk
 
+// ============================================================== static step scratch
+// Scratch for mk_decode_step_noalloc, for callers that cannot allocate device memory.
+// A file-scope device array: every GPU that loads the library holds it until exit.
+static __device__ __align__(256) uint8_t g_mk_static_scratch[mk::kStaticScratchBytes];
+
 // ============================================================== host-side launchers
 namespace mk {
+
+// Device address of the static scratch array on the current device, looked up once
+// per device (with that device current) and cached.  The host-side name of the array
+// is only a stand-in and must never be passed to a kernel.
+cudaError_t static_scratch_address(void** ptr) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mk_static_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
 
 cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, const void* src_c,
                         int n_rows_packed, int n_src_rows, int K, long long ld, int col0, int mode, int hd,
