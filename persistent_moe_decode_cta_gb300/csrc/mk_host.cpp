@@ -255,14 +255,28 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     std::vector<std::vector<int>> lists(n_sm);
     lists[0].push_back(t_embed);
     long long cursor = 0;
-    for (int l = 0; l < L; ++l)
+    std::vector<char> has_router(n_sm);
+    auto pos = [&](int w) { return (int)(std::find(order.begin(), order.end(), w) - order.begin()); };
+    for (int l = 0; l < L; ++l) {
+      std::fill(has_router.begin(), has_router.end(), 0);
       for (int w : order) {
         if (is_drain(w)) {
           for (int sm = 0; sm < n_sm; ++sm) lists[sm].push_back(drains[(size_t)l * W_COUNT + w]);
+        } else if (w == W_QKV && pos(W_ROUTER) < pos(W_QKV) && n_sm > s.n_router_tasks) {
+          // the router tiles head the MoE's critical path and the QKV tiles the
+          // attention's: keep the QKV tiles off the SMs that run this layer's router
+          for (int t : waves[(size_t)l * W_COUNT + w]) {
+            while (has_router[cursor % n_sm]) ++cursor;
+            lists[cursor++ % n_sm].push_back(t);
+          }
         } else {
-          for (int t : waves[(size_t)l * W_COUNT + w]) lists[cursor++ % n_sm].push_back(t);
+          for (int t : waves[(size_t)l * W_COUNT + w]) {
+            if (w == W_ROUTER) has_router[cursor % n_sm] = 1;
+            lists[cursor++ % n_sm].push_back(t);
+          }
         }
       }
+    }
     for (int t : lm) lists[cursor++ % n_sm].push_back(t);
     emit_segment(lists);
   }

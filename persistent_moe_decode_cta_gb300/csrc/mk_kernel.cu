@@ -40,7 +40,8 @@ __device__ __forceinline__ bool aborted(const Params& p) { return ld_volatile(&p
 //   record (16 x u64): [0] sm | op << 8 | layer << 16 | fan-in << 24, [1] item,
 //   [2] received, [3] dependency met (activation loads start), [4] first weight/KV
 //   chunk landed (activations built), [5] MMA loop done, [6] fan-in follow-up
-//   started (0 if none), [7] task done, [8..11] sub-steps of a fan-in follow-up.
+//   started (0 if none), [7] task done, [8..11] sub-steps of a fan-in follow-up,
+//   [12..15] sub-steps of the task's own epilogue (per opcode, see the marks).
 __device__ __forceinline__ unsigned long long* trace_slots(const Smem& S) {
   return reinterpret_cast<unsigned long long*>(S.small + 192);
 }
@@ -58,7 +59,7 @@ __device__ void trace_emit(const Params& p, const Smem& S, int op, int layer, in
   r[1] = (unsigned long long)(unsigned)item;
   r[2] = t[0]; r[3] = t[1]; r[4] = t[2]; r[5] = t[3]; r[6] = t[6]; r[7] = gtime();
   r[8] = t[8]; r[9] = t[9]; r[10] = t[10]; r[11] = t[11];
-  r[12] = r[13] = r[14] = r[15] = 0ull;
+  r[12] = t[12]; r[13] = t[13]; r[14] = t[14]; r[15] = t[15];
 }
 
 // Spin until ctr >= target, bounded by the timeout and the abort flag.  Polls are
@@ -142,7 +143,7 @@ __device__ __forceinline__ bool wait_full(const Params& p, const Smem& S, uint32
 }
 __device__ __forceinline__ void release_stage(const Smem& S, uint32_t seq) {
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(S.empty(seq % kStages));
+  if ((threadIdx.x & 31) == 0) mbar_arrive_relaxed(S.empty(seq % kStages));
 }
 // Consume n chunks without computing (error / abort path).
 __device__ bool drain_chunks(const Params& p, const Smem& S, uint32_t& cseq, int n) {
@@ -897,11 +898,13 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
     }
   }
 
+  trace_mark(p, S, 12);
   // ---- signal
   switch (op) {
     case OP_QKV:
     case OP_OPROJ:
       signal_async(p, S, sseq, T[D_SIG_CTR], 1u);
+      trace_mark(p, S, 13);
       break;
     case OP_ROUTER:
       if (signal_fanin(p, S, T[D_SIG_CTR], (unsigned)T[D_SIG_TARGET])) route_step(p, S, l);
@@ -974,7 +977,8 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
   const int nch1 = (ksw1 + gemv_jpc(nrb1) - 1) / gemv_jpc(nrb1);
   float v[4];
   if (!gemv_run<nrb1>(p, S, cseq, nch1, ksw1, fr, v)) return false;
-  uint16_t* a_s = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(S.scratch) + 16384);  // [8][fs]
+  trace_mark(p, S, 12);
+  uint16_t* a_s = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(S.scratch) + 28672);  // [8][fs]
   {
     const float rs0 = __shfl_sync(0xffffffffu, rs_have, 8 * c);
     const float rs1 = __shfl_sync(0xffffffffu, rs_have, 8 * c + 4);
@@ -991,6 +995,7 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
     }
   }
   bar_sync_consumers();
+  trace_mark(p, S, 13);
   // ---- phase 2: warp w owns output rows [w * rpw * 16, (w + 1) * rpw * 16), K = fs
   constexpr int k2 = FS / 16;
   uint32_t b2[k2][2];
@@ -999,37 +1004,71 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
     b2[ks][0] = *reinterpret_cast<const uint32_t*>(a_s + g8 * fs + 16 * ks + 2 * c);
     b2[ks][1] = *reinterpret_cast<const uint32_t*>(a_s + g8 * fs + 16 * ks + 8 + 2 * c);
   }
+  // The down slice is packed row-block-major (fragment (rb, ks) at (rb * k2 + ks) * 512 B),
+  // so every ring chunk holds rbc consecutive row blocks; all 8 warps share each chunk,
+  // rbw = rbc / 8 row blocks apiece, with independent accumulators for 4 at a time.
+  // The weighted outputs of those (up to 64 rows) are staged per warp as [token slot]
+  // [64 rows] (stride 68 floats: conflict-free stores) and added into the accumulator
+  // with 128-bit reductions, 16 lanes x 4 rows per token.
   const int rpw = p.d / 128;
-  const int region = rpw * k2 * kFragBytes;
-  const int wpc = moe_warps_per_chunk(region);
-  const int my_chunk = warp / wpc;
-  const int my_off = (warp % wpc) * region;
+  const int rbc = moe_warps_per_chunk(rpw * k2 * kFragBytes) * rpw;
+  const int rbw = rbc / kConsumerWarps;
   const int nch2 = nch - nch1;
-  float* out0 = bt[0] >= 0 ? p.moe + ((size_t)l * p.B + bt[0]) * p.d : nullptr;
-  float* out1 = bt[1] >= 0 ? p.moe + ((size_t)l * p.B + bt[1]) * p.d : nullptr;
+  constexpr int kStg = 68;
+  float* stg = S.scratch + warp * (kMaxBatch * kStg);
+  const int fq = (lane & 15) * 4;  // flush: this lane's 4 rows
   for (int ch = 0; ch < nch2; ++ch) {
     if (!wait_full(p, S, cseq)) return false;
-    if (ch == my_chunk) {
-      const uint32_t base = S.stage(cseq) + my_off + lane * 16;
-      for (int rb = 0; rb < rpw; ++rb) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ch == 0) trace_mark(p, S, 8);
+    if (ch == nch2 - 1) trace_mark(p, S, 10);
+    const uint32_t base = S.stage(cseq) + lane * 16;
+    for (int i0 = 0; i0 < rbw; i0 += 4) {
+      float acc[4][4];
 #pragma unroll
-        for (int ks = 0; ks < k2; ++ks) {
-          const uint4 a = lds128(base + (rb * k2 + ks) * kFragBytes);
-          mma_bf16(acc, a.x, a.y, a.z, a.w, b2[ks][0], b2[ks][1]);
+      for (int u = 0; u < 4; ++u) {
+        acc[u][0] = acc[u][1] = acc[u][2] = acc[u][3] = 0.f;
+        if (i0 + u < rbw) {
+          const int rbl = warp * rbw + i0 + u;
+#pragma unroll
+          for (int ks = 0; ks < k2; ++ks) {
+            const uint4 a = lds128(base + (rbl * k2 + ks) * kFragBytes);
+            mma_bf16(acc[u], a.x, a.y, a.z, a.w, b2[ks][0], b2[ks][1]);
+          }
         }
-        const int row = (warp * rpw + rb) * 16 + g8;
-        if (out0) { atomicAdd(out0 + row, wt[0] * acc[0]); atomicAdd(out0 + row + 8, wt[0] * acc[2]); }
-        if (out1) { atomicAdd(out1 + row, wt[1] * acc[1]); atomicAdd(out1 + row + 8, wt[1] * acc[3]); }
       }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int rl = u * 16 + g8;
+        stg[(2 * c) * kStg + rl] = wt[0] * acc[u][0];
+        stg[(2 * c) * kStg + rl + 8] = wt[0] * acc[u][2];
+        stg[(2 * c + 1) * kStg + rl] = wt[1] * acc[u][1];
+        stg[(2 * c + 1) * kStg + rl + 8] = wt[1] * acc[u][3];
+      }
+      __syncwarp();
+      const int nrow = min(4, rbw - i0) * 16;
+      const int row0 = (ch * rbc + warp * rbw + i0) * 16;
+      for (int n0 = 0; n0 < ntok; n0 += 2) {
+        const int n = n0 + (lane >> 4);
+        // batch index of token slot n: held as bt[n & 1] by lane n / 2
+        const int x0 = __shfl_sync(0xffffffffu, bt[0], (n >> 1) & 3);
+        const int x1 = __shfl_sync(0xffffffffu, bt[1], (n >> 1) & 3);
+        const int b = (n & 1) ? x1 : x0;
+        if (n < ntok && fq < nrow)
+          red_add_v4(p.moe + ((size_t)l * p.B + b) * p.d + row0 + fq,
+                     *reinterpret_cast<const float4*>(stg + n * kStg + fq));
+      }
+      __syncwarp();
     }
+    if (ch == 0) trace_mark(p, S, 9);
     release_stage(S, cseq);
     ++cseq;
   }
   trace_mark(p, S, 3);
   // ---- signal the layer's MoE-done counter (waited on by the ADD_RMSNORM tasks)
   signal_async(p, S, sseq, C_MD(p, l), 1u);
+  trace_mark(p, S, 14);
   bar_sync_consumers();
+  trace_mark(p, S, 15);
   return true;
 }
 
@@ -1270,10 +1309,13 @@ __device__ bool task_attention(const Params& p, const Smem& S, uint32_t& cseq, u
   } else {
     attention_self<HD>(p, l, it, ti);
   }
+  trace_mark(p, S, 12);
   if (signal_fanin(p, S, C_ATT(p, l, it.b, it.g), (unsigned)(it.ns + 1))) {
     attention_combine<HD>(p, l, it.b, it.g, it.ns);
+    trace_mark(p, S, 14);
     signal_async(p, S, sseq, C_OG(p, l, it.g), 1u);
   }
+  trace_mark(p, S, 13);
   bar_sync_consumers();
   return true;
 }
@@ -1338,6 +1380,7 @@ __device__ void consumer(const Params& p, const Smem& S) {
     if (p.trace && threadIdx.x == 0) {
       unsigned long long* t = trace_slots(S);
       t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = t[8] = t[9] = t[10] = t[11] = 0ull;
+      t[12] = t[13] = t[14] = t[15] = 0ull;
     }
     if (abort_now) skip = true;
     if (skip) {
