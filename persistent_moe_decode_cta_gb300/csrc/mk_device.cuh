@@ -20,7 +20,7 @@ struct Smem {
   uint32_t scratch_s;
   int* small;         // kSmallBytes
   uint32_t bars;      // full[kStages], empty[kStages], mfull[kMbox], mempty[kMbox], sfull[kSq], sempty[kSq]
-  int4* mbox;
+  int4* mbox;        // [kMbox][2] task entries
   int2* sq;           // signal requests [kSq]
 
   __device__ __forceinline__ uint32_t full(uint32_t s) const { return bars + 8u * s; }
@@ -55,7 +55,7 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
   S.bars = aligned + kStages * kStageBytes + kScratchBytes + kSmallBytes;
   S.mbox = reinterpret_cast<int4*>(g + kStages * kStageBytes + kScratchBytes + kSmallBytes +
                                    kBarBytes);
-  S.sq = reinterpret_cast<int2*>(S.mbox + kMbox);
+  S.sq = reinterpret_cast<int2*>(S.mbox + 2 * kMbox);
   return S;
 }
 
@@ -126,6 +126,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(bar), "l"(pol)
       : "memory");
 }
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
                                             uint32_t bar, uint64_t pol) {
   asm volatile(
@@ -180,6 +184,12 @@ __device__ __forceinline__ float2 ldg_cg_f2(const float* p) {
 __device__ __forceinline__ void ldg_cg_pred(uint32_t& v, const void* ptr, bool pred) {
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.cg.u32 %0, [%1];\n\t}"
+      : "+r"(v)
+      : "l"(ptr), "r"((int)pred));
+}
+__device__ __forceinline__ void ldg_cg_pred_i(int& v, const int* ptr, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.cg.s32 %0, [%1];\n\t}"
       : "+r"(v)
       : "l"(ptr), "r"((int)pred));
 }

@@ -130,7 +130,7 @@ enum Wave { W_QKV = 0, W_ROUTER, W_ATT, W_MOE, W_OPROJ, W_RESID, W_COUNT };
 
 struct PlanOut {
   int B = 0, maxa = 0, n_sm = 0;
-  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_done, n_ctr;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_oa, c_done, n_ctr;
   int rb_target;
   std::vector<int32_t> tasks;     // n_tasks * 32
   std::vector<int32_t> sm_off;    // n_segs * (n_sm + 1), absolute offsets into sm_list
@@ -161,7 +161,8 @@ bool parse_wave_order(const char* s, std::vector<int>& order) {
          pos(W_MOE) < pos(W_RESID) && pos(W_OPROJ) < pos(W_RESID);
 }
 
-int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, PlanOut& P, std::string* err) {
+int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, PlanOut& P, std::string* err,
+               bool prefetch = true) {
   if (B < 1 || B > s.max_batch) return fail(err, MK_ERR_INVALID, "batch %d not in [1, %d]", B, s.max_batch);
   if (n_sm < 1) return fail(err, MK_ERR_INVALID, "n_sms %d", n_sm);
   P = PlanOut();
@@ -177,6 +178,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   P.c_og = c; c += L * s.Hkv;
   P.c_md = c; c += L;
   P.c_rb = c; c += L * s.nrb_d;
+  P.c_oa = c; c += L;  // attention outputs complete per layer (target Hkv * B)
   P.c_done = c; c += 1;
   P.n_ctr = c;
   P.rb_target = s.Hkv * (kRowBlock / s.r_o);  // O-proj tiles of a residual row block
@@ -198,6 +200,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   const int t_embed = add(OP_EMBED, 0, 0, 0, 0, 0, 0, -1, 0, P.c_lr + 0, s.nrb_d, 0, 0, -1);
   std::vector<std::vector<int>> waves((size_t)L * W_COUNT);
   std::vector<int> drains((size_t)L * W_COUNT, -1);
+  std::vector<int> moe_oq(L, -1);  // megakernel MoE drains that also serve the O-proj queue
   for (int l = 0; l < L; ++l) {
     auto& wq = waves[(size_t)l * W_COUNT + W_QKV];
     for (int g = 0; g < s.Hkv; ++g)
@@ -215,6 +218,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
     drains[(size_t)l * W_COUNT + W_MOE] =
         add(OP_MOE_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
+    moe_oq[l] = add(OP_MOE_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
     auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
     for (int g = 0; g < s.Hkv; ++g)
       for (int t = 0; t < s.t_o; ++t)
@@ -257,10 +261,26 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     long long cursor = 0;
     std::vector<char> has_router(n_sm);
     auto pos = [&](int w) { return (int)(std::find(order.begin(), order.end(), w) - order.begin()); };
+    // With O-proj after the MoE drain, the O-proj tiles are not dealt: the MoE drain
+    // claims them from a queue, ahead of expert items once the layer's attention is
+    // complete and all remaining ones after the expert queue is empty, so that they
+    // run on whichever SMs are free instead of behind each SM's own expert items.
+    const bool oq = pos(W_OPROJ) > pos(W_MOE);
+    for (int l = 0; l < L && oq; ++l) {
+      const auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
+      int32_t* D = &P.tasks[(size_t)moe_oq[l] * kDescInts];
+      D[D_K0] = wo.empty() ? 0 : wo.front();
+      D[D_KLEN] = (int)wo.size();
+      for (size_t i = 1; i < wo.size(); ++i)
+        if (wo[i] != wo[0] + (int)i) return fail(err, MK_ERR_INVALID, "O-proj descriptors not contiguous");
+    }
     for (int l = 0; l < L; ++l) {
       std::fill(has_router.begin(), has_router.end(), 0);
       for (int w : order) {
-        if (is_drain(w)) {
+        if (oq && w == W_OPROJ) continue;
+        if (oq && w == W_MOE) {
+          for (int sm = 0; sm < n_sm; ++sm) lists[sm].push_back(moe_oq[l]);
+        } else if (is_drain(w)) {
           for (int sm = 0; sm < n_sm; ++sm) lists[sm].push_back(drains[(size_t)l * W_COUNT + w]);
         } else if (w == W_QKV && pos(W_ROUTER) < pos(W_QKV) && n_sm > s.n_router_tasks) {
           // the router tiles head the MoE's critical path and the QKV tiles the
@@ -278,6 +298,39 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
       }
     }
     for (int t : lm) lists[cursor++ % n_sm].push_back(t);
+    if (prefetch) {
+      // L2 prefetch entries around each layer's attention drain: before it, this
+      // layer's K/V pages (each SM a share) and the weights of this SM's own O-proj
+      // tiles of the layer; after it, the weights of its QKV and router tiles of the
+      // next layer.  The producer reaches the drain about when the layer's QKV tiles
+      // start, and the attention queue empties about when its MoE items start.
+      auto field = [&](int t, int f) { return P.tasks[(size_t)t * kDescInts + f]; };
+      auto pf_of = [&](int t) {
+        const size_t off = ((size_t)(uint32_t)field(t, D_WOFF_HI) << 32) | (uint32_t)field(t, D_WOFF_LO);
+        return add(OP_PREFETCH, field(t, D_LAYER), field(t, D_TASK_ID), 0, 0, 0, 0, -1, 0, -1, 0, off,
+                   field(t, D_WBYTES), -1);
+      };
+      std::vector<int> pf_kv(L);
+      for (int l = 0; l < L; ++l) pf_kv[l] = add(OP_PREFETCH_KV, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, -1);
+      for (int sm = 0; sm < n_sm; ++sm) {
+        const std::vector<int> in = lists[sm];
+        std::vector<int>& out = lists[sm];
+        out.clear();
+        for (size_t i = 0; i < in.size(); ++i) {
+          const int t = in[i];
+          if (field(t, D_OP) != OP_ATT_DRAIN) { out.push_back(t); continue; }
+          const int l = field(t, D_LAYER);
+          out.push_back(pf_kv[l]);
+          for (size_t j = i + 1; j < in.size() && field(in[j], D_LAYER) <= l; ++j)
+            if (field(in[j], D_OP) == OP_OPROJ) out.push_back(pf_of(in[j]));
+          out.push_back(t);
+          for (size_t j = i + 1; j < in.size() && field(in[j], D_LAYER) <= l + 1; ++j) {
+            const int op = field(in[j], D_OP);
+            if (field(in[j], D_LAYER) == l + 1 && (op == OP_QKV || op == OP_ROUTER)) out.push_back(pf_of(in[j]));
+          }
+        }
+      }
+    }
     emit_segment(lists);
   }
   // segments 1..: one launch per wave per layer (embed first, LM head last)
@@ -310,6 +363,14 @@ int choose_split_pages(int max_pages) {
   int sp = (max_pages + 31) / 32;
   sp = (sp + 7) / 8 * 8;
   return std::max(8, sp);
+}
+
+// L2 prefetch entries in the megakernel's lists, off by default (MK_PREFETCH=1 adds
+// them): at batch 1 the step is bound by its dependency latencies rather than by HBM,
+// and the extra early traffic measured slightly slower.
+bool prefetch_enabled() {
+  const char* e = getenv("MK_PREFETCH");
+  return e && e[0] == '1';
 }
 
 // Router first: its weights are then prefetched behind the previous layer's tasks
@@ -548,7 +609,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
   std::vector<int> order;
   parse_wave_order(default_order(), order);
   PlanOut P;
-  r = build_plan(s, batch, n_sms, order, P, nullptr);
+  r = build_plan(s, batch, n_sms, order, P, nullptr, prefetch_enabled());
   if (r) return r;
   const int list_len = P.sm_off[n_sms];  // segment 0 only
   if (info_out) {
@@ -557,7 +618,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
     I[5] = s.t_moe; I[6] = (int)(s.moe_item_bytes / 1024); I[7] = s.r_o; I[8] = s.moe_fs; I[9] = s.r_qkv; I[10] = s.qkv_tpg;
     I[11] = s.n_router_tasks; I[12] = P.rb_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
     I[16] = P.c_lr; I[17] = P.c_qkvg; I[18] = P.c_rt; I[19] = P.c_rr; I[20] = P.c_att; I[21] = P.c_og;
-    I[22] = P.c_md; I[23] = P.c_rb; I[24] = s.nrb_d; I[25] = s.gs;
+    I[22] = P.c_md; I[23] = P.c_rb; I[24] = s.nrb_d; I[25] = s.gs; I[26] = P.c_oa;
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
     return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
@@ -586,7 +647,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   const char* env = getenv("MK_WAVE_ORDER");
   if (!parse_wave_order(env && *env ? env : default_order(), order))
     return fail(&h->err, MK_ERR_INVALID, "bad wave order '%s'", env ? env : "");
-  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err);
+  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err, prefetch_enabled());
   if (r) return r;
   int occ = 0;
   megakernel_occupancy(&occ);
@@ -650,7 +711,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(h->d_trace_n, 1);
 #undef AL
   p.c_lr = P.c_lr; p.c_qkvg = P.c_qkvg; p.c_rt = P.c_rt; p.c_rr = P.c_rr; p.c_att = P.c_att; p.c_og = P.c_og;
-  p.c_md = P.c_md; p.c_rb = P.c_rb; p.c_done = P.c_done; p.n_ctr = P.n_ctr; p.n_queues = 3 * L;
+  p.c_md = P.c_md; p.c_rb = P.c_rb; p.c_oa = P.c_oa; p.c_done = P.c_done; p.n_ctr = P.n_ctr;
+  p.n_queues = 3 * L;
   p.rb_target = P.rb_target;
   p.tasks = h->d_tasks; p.sm_off = h->d_sm_off; p.sm_list = h->d_sm_list;
   p.trace = nullptr; p.trace_n = h->d_trace_n; p.trace_cap = 0;

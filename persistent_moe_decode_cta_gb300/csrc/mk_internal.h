@@ -35,7 +35,9 @@ constexpr int kFragsPerStage = kStageBytes / kFragBytes;
 constexpr int kMaxNrb = 8;                    // GEMV task rows <= 128
 constexpr int kMaxKsw = 16;                   // GEMV task K <= 2048 (16 k16-steps/warp)
 constexpr int kBarBytes = (2 * kStages + 2 * kMbox + 2 * kSq) * 8;
-constexpr int kMboxBytes = kMbox * 16 + kSq * 8;
+// mailbox entry: {task, item, chunks, n_tok} + {token bytes 0..3, 4..7, -, -} (MoE items
+// carry their expert's token list: byte n = b * 8 + j for the n-th token b, rank j)
+constexpr int kMboxBytes = kMbox * 32 + kSq * 8;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kScratchBytes +
                            kSmallBytes + kBarBytes + kMboxBytes;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
@@ -50,6 +52,7 @@ constexpr int kCtrStride = 32;
 // (every consumer of the normed input reads all of them).
 constexpr int kSsStride = 32;
 constexpr int kMaxBatch = 8;
+constexpr int kMaxActive = kMaxBatch * 8;     // active experts per layer <= batch * top_k
 constexpr int kRowBlock = 128;                // residual row block (rows of d_model)
 // j-groups per ring chunk of a GEMV tile with `nrb` 16-row blocks (chunk = jpc*nrb*4 KB)
 constexpr __host__ __device__ int gemv_jpc(int nrb) { return 8 / nrb > 0 ? 8 / nrb : 1; }
@@ -73,6 +76,9 @@ enum Op : int32_t {
   OP_LMHEAD = 8,     // final RMSNorm + LM_HEAD tile
   OP_RESID = 9,      // ADD_RMSNORM of one residual row block once the layer's O-proj
                      // tiles for it and all MoE items are done
+  OP_PREFETCH = 10,  // producer only: L2 prefetch of a weight range (D_WOFF, D_WBYTES)
+  OP_PREFETCH_KV = 11  // producer only: L2 prefetch of this SM's share of layer D_LAYER's
+                       // cached K/V pages
 };
 
 enum DescField : int {
@@ -87,8 +93,7 @@ enum PackMode : int { PACK_IDENT = 0, PACK_QKV = 1, PACK_GATE_UP = 2 };
 // MoE item (expert e, f-slice s = rows [FS s, FS s + FS) of d_ff, FS in {16, 32})
 // packed as one contiguous tile: the 2 FS interleaved gate/up rows x d_model (GEMV
 // fragment order, FS/8 row blocks), then the down slice W_down[:, FS s : FS s + FS]
-// with consumer warp w owning output rows [w d/8, (w+1) d/8) (fragment order
-// [w][row block][k16-step]).
+// row-block-major (fragment order [16-row block of d_model][k16-step]).
 
 // Device error word layout (int32[16]).
 enum ErrField : int { E_CODE = 0, E_TASK = 1, E_CTR = 2, E_OBS = 3, E_TARGET = 4,
@@ -141,7 +146,7 @@ struct Params {
   int* qhead;               // [3L]
   int* qcount;              // [3L]
   int* err;                 // [16]
-  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_done, n_ctr, n_queues;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_oa, c_done, n_ctr, n_queues;
   int rb_target;
   // optional task timeline (see trace_emit)
   unsigned long long* trace;

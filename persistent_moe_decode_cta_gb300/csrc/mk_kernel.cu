@@ -165,6 +165,7 @@ __device__ __forceinline__ int C_ATT(const Params& p, int l, int b, int g) {
 }
 __device__ __forceinline__ int C_OG(const Params& p, int l, int g) { return p.c_og + l * p.Hkv + g; }
 __device__ __forceinline__ int C_MD(const Params& p, int l) { return p.c_md + l; }
+__device__ __forceinline__ int C_OA(const Params& p, int l) { return p.c_oa + l; }
 __device__ __forceinline__ int C_RB(const Params& p, int l, int r) { return p.c_rb + l * p.nrb_d + r; }
 
 struct AttItem {
@@ -255,13 +256,15 @@ __device__ __forceinline__ int checked_page(const Params& p, int b, int logical,
 }
 
 // ============================================================== producer
-__device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int task, int item, int nch) {
+__device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int task, int item, int nch,
+                          int4 extra = make_int4(0, 0, 0, 0)) {
   const uint32_t slot = mseq % kMbox, use = mseq / kMbox;
   if (use > 0 && !mbar_wait(S.mempty(slot), (use - 1) & 1u, 8 * p.timeout_ns)) {
     raise_err(p, MK_ERR_TIMEOUT, task, -3, (int)mseq, 0);
     return false;
   }
-  S.mbox[slot] = make_int4(task, item, nch, 0);
+  S.mbox[2 * slot] = make_int4(task, item, nch, extra.x);
+  S.mbox[2 * slot + 1] = make_int4(extra.y, extra.z, 0, 0);
   mbar_arrive(S.mfull(slot));
   ++mseq;
   return true;
@@ -314,6 +317,44 @@ __device__ bool issue_linear(const Params& p, const Smem& S, uint32_t& cseq, con
   return true;
 }
 
+// L2 prefetches (no completion to wait for): they move HBM reads of data that a later
+// task on this SM will load -- its own O-proj, QKV and router tiles -- and this SM's
+// share of the layer's cached K/V pages into the periods when the layer's dependency
+// chain leaves HBM idle, so that the tasks later find their operands in L2.
+__device__ __forceinline__ void prefetch_range(const uint8_t* src, int bytes) {
+  constexpr int kPiece = 65536;
+  for (int off = 0; off < bytes; off += kPiece) prefetch_l2(src + off, (uint32_t)min(kPiece, bytes - off));
+}
+// This SM's share of layer l's cached pages (the pages attention reads this step,
+// counted over all sequences): per page id, the K and the V rows of all KV groups are
+// each one contiguous range (Hkv * 16 * hd bf16).
+__device__ void prefetch_kv_share(const Params& p, const Smem& S, int l) {
+  int total = 0;
+  for (int b = 0; b < p.B; ++b) {
+    int pos, lo, fp, npg, ns;
+    att_range(p, S, l, b, pos, lo, fp, npg, ns);
+    total += npg;
+  }
+  const int beg = (int)((long long)total * blockIdx.x / gridDim.x);
+  const int end = (int)((long long)total * (blockIdx.x + 1) / gridDim.x);
+  const uint32_t span = (uint32_t)p.Hkv * 16u * (uint32_t)p.hd * 2u;
+  int base = 0;
+  for (int b = 0; b < p.B && base < end; ++b) {
+    int pos, lo, fp, npg, ns;
+    att_range(p, S, l, b, pos, lo, fp, npg, ns);
+    for (int i = max(beg - base, 0); i < npg && base + i < end; ++i) {
+      const int logical = fp + i;
+      if (logical >= p.max_pages) break;
+      const int pg = p.page_table[b * p.max_pages + logical];
+      if (pg < 0 || pg >= p.n_pages) continue;  // reported by the tasks that use it
+      const size_t o = (((size_t)l * p.n_pages + pg) * p.Hkv) * 16 * p.hd;
+      prefetch_l2(p.kc + o, span);
+      prefetch_l2(p.vc + o, span);
+    }
+    base += npg;
+  }
+}
+
 // K pages then V pages of a split, 8 pages per ring stage.
 __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const CUtensorMap* tmK,
                          const CUtensorMap* tmV, int l, const AttItem& it, uint64_t pol, int task) {
@@ -321,14 +362,32 @@ __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const C
   const int nbox = p.hd / inner;
   const int box_bytes = 16 * inner * 2;
   const int page_bytes = 16 * p.hd * 2;
+  // page ids of the first chunk, then each chunk's ids are loaded (all 8 at once)
+  // while the previous chunk's copies are issued
+  int ids[8];
+  auto load_ids = [&](int c0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int logical = it.pg0 + c0 + i;
+      ids[i] = -1;
+      ldg_cg_pred_i(ids[i], p.page_table + it.b * p.max_pages + logical,
+                    c0 + i < it.np && logical >= 0 && logical < p.max_pages);
+    }
+  };
+  load_ids(0);
   for (int c0 = 0; c0 < it.np; c0 += 8) {
     const int n = min(8, it.np - c0);
     int rows[8];
-    for (int i = 0; i < n; ++i) {
-      int pg = checked_page(p, it.b, it.pg0 + c0 + i, task);
-      if (pg < 0) pg = 0;
-      rows[i] = ((l * p.n_pages + pg) * p.Hkv + it.g) * 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int pg = ids[i];
+      if (i < n && (pg < 0 || pg >= p.n_pages)) {
+        raise_err(p, MK_ERR_BAD_PAGE, task, -1, pg, it.pg0 + c0 + i);
+        pg = 0;
+      }
+      rows[i] = ((l * p.n_pages + max(pg, 0)) * p.Hkv + it.g) * 16;
     }
+    if (c0 + 8 < it.np) load_ids(c0 + 8);
     for (int kv = 0; kv < 2; ++kv) {
       if (!acquire_stage(p, S, cseq, task)) return false;
       const uint32_t s = cseq % kStages;
@@ -342,6 +401,18 @@ __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const C
     }
   }
   return true;
+}
+
+// A GEMV tile task: mailbox entry, then its weight chunks.
+__device__ __forceinline__ bool push_gemv(const Params& p, const Smem& S, uint32_t& mseq, uint32_t& cseq, int ti,
+                                          uint64_t pol) {
+  const int* T = p.tasks + ti * kDescInts;
+  const long long off = (long long)(((unsigned long long)(unsigned)T[D_WOFF_HI] << 32) | (unsigned)T[D_WOFF_LO]);
+  const int bytes = T[D_WBYTES];
+  const int nrb = T[D_NROWS] / 16;
+  const int cs = gemv_jpc(nrb) * nrb * 8 * kFragBytes;
+  const int nch = (bytes + cs - 1) / cs;
+  return mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs);
 }
 
 __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK, const CUtensorMap* tmV) {
@@ -360,19 +431,21 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
       case OP_RESID:
         ok = mbox_push(p, S, mseq, ti, 0, 0);
         break;
+      case OP_PREFETCH: {
+        const long long off = (long long)(((unsigned long long)(unsigned)T[D_WOFF_HI] << 32) |
+                                          (unsigned)T[D_WOFF_LO]);
+        prefetch_range(p.wblob + off, T[D_WBYTES]);
+        break;
+      }
+      case OP_PREFETCH_KV:
+        prefetch_kv_share(p, S, l);
+        break;
       case OP_QKV:
       case OP_ROUTER:
       case OP_OPROJ:
-      case OP_LMHEAD: {
-        const long long off = (long long)(((unsigned long long)(unsigned)T[D_WOFF_HI] << 32) |
-                                          (unsigned)T[D_WOFF_LO]);
-        const int bytes = T[D_WBYTES];
-        const int nrb = T[D_NROWS] / 16;
-        const int cs = gemv_jpc(nrb) * nrb * 8 * kFragBytes;
-        const int nch = (bytes + cs - 1) / cs;
-        ok = mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs);
+      case OP_LMHEAD:
+        ok = push_gemv(p, S, mseq, cseq, ti, pol);
         break;
-      }
       case OP_ATT_DRAIN: {
         const int count = att_item_count(p, S, l);
         int* head = p.qhead + l;
@@ -387,9 +460,34 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         break;
       }
       case OP_MOE_DRAIN: {
-        if (!wait_ge(p, C_RR(p, l), 1u, ti)) { ok = false; break; }
+        // The first claim is taken before the route step is known to be done (its
+        // round trip overlaps the wait); after the route the queue size and the whole
+        // active-expert list are fetched in one round trip.
         const int q = p.L + l;
+        if (!(ok = claim_gate(p, S, mseq, ti))) break;
+        int item = atomicAdd(p.qhead + q, 1);
+        if (!wait_ge(p, C_RR(p, l), 1u, ti)) { ok = false; break; }
+        int act[kMaxActive];
         const int count = ldg_cg(p.qcount + q);
+#pragma unroll
+        for (int a = 0; a < kMaxActive; ++a) {
+          act[a] = 0;
+          ldg_cg_pred_i(act[a], p.active + l * p.maxa + a, a < p.maxa);
+        }
+        // the token list of an item's expert slot goes to the consumers in the mailbox
+        // entry; the first item's list is fetched in the same round trip as the above
+        int tl_slot = -1, tl_cnt = 0, tl_tok[kMaxBatch];
+        auto load_tokens = [&](int a) {
+          tl_slot = a;
+          tl_cnt = 0;
+          ldg_cg_pred_i(tl_cnt, p.act_cnt + l * p.maxa + a, true);
+#pragma unroll
+          for (int n = 0; n < kMaxBatch; ++n) {
+            tl_tok[n] = 0;
+            ldg_cg_pred_i(tl_tok[n], p.act_tok + ((size_t)l * p.maxa + a) * p.B + n, n < p.B);
+          }
+        };
+        if (item < count) load_tokens(item / p.t_moe);
         // part 1 (gate/up tile) in whole k16-groups, part 2 (down slice) in warp regions
         const int nrb1 = p.moe_fs / 8;
         const int cs1 = gemv_jpc(nrb1) * nrb1 * 8 * kFragBytes;
@@ -398,15 +496,43 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         const int cs2 = moe_warps_per_chunk(region) * region;
         const int dn_bytes = (int)p.moe_item_bytes - gu_bytes;
         const int nch = (gu_bytes + cs1 - 1) / cs1 + (dn_bytes + cs2 - 1) / cs2;
-        while (ok) {
-          if (!(ok = claim_gate(p, S, mseq, ti))) break;
-          const int item = atomicAdd(p.qhead + q, 1);
+        // O-proj tiles of the layer as a queue (D_KLEN tiles from task D_K0; none when
+        // they are dealt statically): taken before expert items once all attention
+        // outputs of the layer are complete, and after the expert queue empties
+        const int qo = 2 * p.L + l, o_base = T[D_K0], n_o = T[D_KLEN];
+        bool o_left = n_o > 0;
+        auto claim_oproj = [&]() {
+          const int o = atomicAdd(p.qhead + qo, 1);
+          if (o >= n_o) { o_left = false; return false; }
+          ok = push_gemv(p, S, mseq, cseq, o_base + o, pol);
+          return true;
+        };
+        for (bool first = true; ok; first = false) {
+          if (!first) {
+            // read ahead: the count arrives while the claim gate waits for the consumers
+            const unsigned oa = o_left ? ld_relaxed(ctr_ptr(p, C_OA(p, l))) : 0u;
+            if (!(ok = claim_gate(p, S, mseq, ti))) break;
+            if (o_left && oa >= (unsigned)(p.Hkv * p.B) && claim_oproj()) continue;
+            item = atomicAdd(p.qhead + q, 1);
+          }
           if (item >= count) break;
           const int a = item / p.t_moe, t = item % p.t_moe;
-          const int e = ldg_cg(p.active + l * p.maxa + a);
+          const int e = act[a];
+          if (a != tl_slot) load_tokens(a);
+          int4 extra = make_int4(tl_cnt, 0, 0, 0);
+#pragma unroll
+          for (int n = 0; n < kMaxBatch; ++n) {
+            const int byte = ((tl_tok[n] >> 4) << 3) | (tl_tok[n] & 7);
+            if (n < 4) extra.y |= byte << (8 * n);
+            else extra.z |= byte << (8 * (n - 4));
+          }
           const uint8_t* src = p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
-          ok = mbox_push(p, S, mseq, ti, item, nch) && issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1) &&
+          ok = mbox_push(p, S, mseq, ti, item, nch, extra) && issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1) &&
                issue_linear(p, S, cseq, src + gu_bytes, dn_bytes, pol, ti, cs2);
+        }
+        while (ok && o_left) {
+          if (!(ok = claim_gate(p, S, mseq, ti))) break;
+          claim_oproj();
         }
         break;
       }
@@ -782,10 +908,10 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
     // the router's operand is hi + lo bf16 parts (hi is shared with the layer's QKV
     // tiles; the residue lo is loaded for the router only)
     const int n = lane >> 2;
+    BFrag lo;  // issued first: its loads share the round trip of the hi part and 1/rms
+    load_bfrag(lo, ksw, n < p.B ? p.XGL + ((size_t)l * p.B + n) * p.d : nullptr);
     if (!reuse) rs_have = build_norm_bfrag(p, S, fr, ksw, l, n < p.B ? n : -1);
     have = key;
-    BFrag lo;
-    load_bfrag(lo, ksw, n < p.B ? p.XGL + ((size_t)l * p.B + n) * p.d : nullptr);
     ran = (nrb == 1) ? gemv_run<1>(p, S, cseq, nch, ksw, fr, v, &lo) : gemv_run<2>(p, S, cseq, nch, ksw, fr, v, &lo);
   } else {
     if (!reuse) {
@@ -936,41 +1062,35 @@ __device__ bool task_resid(const Params& p, const Smem& S, uint32_t& sseq, const
 // by the route step).
 template <int FS>
 __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, const int* T,
-                                         int ti, int item, int nch, BFrag& fr, OperandKey& have, float& rs_have) {
+                                         int ti, int item, int nch, int ntok, int tok_lo, int tok_hi, BFrag& fr,
+                                         OperandKey& have, float& rs_have) {
   const int l = T[D_LAYER];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g8 = lane >> 2, c = lane & 3;
   const int a_slot = item / p.t_moe;
   const OperandKey key = {3, l, a_slot};
+  // The producer claimed this item after the layer's route step (acquire) and passed
+  // the expert's token list in the mailbox entry, so no dependency wait is needed here.
   const bool reuse = key == have;
-  if (reuse) {
-    trace_mark(p, S, 1);
-  } else if (!consumer_wait(p, S, C_RR(p, l), 1u, ti)) {
-    drain_chunks(p, S, cseq, nch);
-    return false;
-  }
-  const int ntok = ldg_cg(p.act_cnt + l * p.maxa + a_slot);
-  const int* tok_list = p.act_tok + ((size_t)l * p.maxa + a_slot) * p.B;
-  const int ksw1 = p.d / 128;
-  if (!reuse) {
-    const int n = lane >> 2;
-    const int b = (n < ntok) ? (ldg_cg(tok_list + n) >> 4) : -1;
-    rs_have = build_norm_bfrag(p, S, fr, ksw1, l, b);
-    have = key;
-  }
-  // this lane's two epilogue tokens (2c, 2c+1): batch index and routing weight
+  trace_mark(p, S, 1);
+  auto tok_byte = [&](int n) { return ((n < 4 ? tok_lo : tok_hi) >> (8 * (n & 3))) & 0xff; };
+  // this lane's two epilogue tokens (2c, 2c+1): batch index and routing weight (the
+  // weight loads share the round trip of the operand loads below)
   int bt[2];
   float wt[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int n = 2 * c + e;
-    bt[e] = -1;
+    const int tb = tok_byte(n);
+    bt[e] = (n < ntok) ? (tb >> 3) : -1;
     wt[e] = 0.f;
-    if (n < ntok) {
-      const int pk = ldg_cg(tok_list + n);
-      bt[e] = pk >> 4;
-      wt[e] = ldg_cg(p.rw + ((size_t)l * p.B + bt[e]) * p.topk + (pk & 15));
-    }
+    ldg_cg_pred(wt[e], p.rw + ((size_t)l * p.B + (tb >> 3)) * p.topk + (tb & 7), n < ntok);
+  }
+  const int ksw1 = p.d / 128;
+  if (!reuse) {
+    const int n = lane >> 2;
+    rs_have = build_norm_bfrag(p, S, fr, ksw1, l, (n < ntok) ? (tok_byte(n) >> 3) : -1);
+    have = key;
   }
   // ---- phase 1: 2*FS interleaved gate/up rows = FS/8 row blocks
   constexpr int fs = FS, nrb1 = FS / 8;
@@ -1314,6 +1434,7 @@ __device__ bool task_attention(const Params& p, const Smem& S, uint32_t& cseq, u
     attention_combine<HD>(p, l, it.b, it.g, it.ns);
     trace_mark(p, S, 14);
     signal_async(p, S, sseq, C_OG(p, l, it.g), 1u);
+    signal_async(p, S, sseq, C_OA(p, l), 1u);
   }
   trace_mark(p, S, 13);
   bar_sync_consumers();
@@ -1370,7 +1491,8 @@ __device__ void consumer(const Params& p, const Smem& S) {
     bar_sync_consumers();
     const bool got = S.small[3] != 0;
     const bool abort_now = S.small[4] != 0;
-    const int4 ent = got ? S.mbox[slot] : make_int4(-1, 0, 0, 0);
+    const int4 ent = got ? S.mbox[2 * slot] : make_int4(-1, 0, 0, 0);
+    const int4 ent2 = got ? S.mbox[2 * slot + 1] : make_int4(0, 0, 0, 0);
     bar_sync_consumers();
     if (got && threadIdx.x == 0) mbar_arrive(S.mempty(slot));
     ++mseq;
@@ -1406,8 +1528,9 @@ __device__ void consumer(const Params& p, const Smem& S) {
         for (int j = 0; j < kMaxKsw; ++j) fr.b0[j] = fr.b1[j] = 0u;
         break;
       case OP_MOE_DRAIN:
-        ok = (p.moe_fs == 32) ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, fr, have, rs_have)
-                              : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, fr, have, rs_have);
+        ok = (p.moe_fs == 32)
+                 ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, fr, have, rs_have)
+                 : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, fr, have, rs_have);
         break;
       default:
         ok = task_gemv(p, S, cseq, sseq, T, ent.x, nch, fr, have, rs_have);

@@ -16,7 +16,8 @@ import synth
 from persistent_moe_decode_cta_gb300 import binding as B
 
 OP_EMBED, OP_QKV, OP_ROUTER, OP_ATT, OP_MOE, OP_OPROJ, OP_LM, OP_RESID = 1, 2, 3, 4, 5, 7, 8, 9
-D_OP, D_LAYER, D_AUX, D_ROW0 = 0, 1, 2, 3
+OP_PREFETCH, OP_PREFETCH_KV = 10, 11
+D_OP, D_LAYER, D_AUX, D_ROW0, D_K0, D_KLEN = 0, 1, 2, 3, 5, 6
 D_WAIT, D_WAIT_T, D_SIG, D_SIG_T, D_WAIT2, D_WAIT2_T = 7, 8, 9, 10, 17, 18
 PAGE = 16
 
@@ -44,6 +45,8 @@ class Sim:
         (self.c_lr, self.c_qkvg, self.c_rt, self.c_rr, self.c_att, self.c_og, self.c_md,
          self.c_rb) = I[16:24]
         self.nrb_d, self.L, self.Hkv = I[24], cfg["n_layers"], cfg["n_kv_heads"]
+        self.c_oa = I[26]
+        self.pending = [None] * n_sm   # a claimed O-proj tile waiting for its group
         # queues
         self.att_items = {}
         self.moe_count = {}
@@ -88,11 +91,21 @@ class Sim:
 
     def step_task(self, sm):
         """Try to advance SM `sm` by one task or one claimed item; True if it did."""
+        if self.pending[sm] is not None:
+            T = self.T[self.pending[sm]]
+            if not self.ready(T[D_WAIT], T[D_WAIT_T]):
+                return False
+            self.ctr[T[D_SIG]] += 1
+            self.pending[sm] = None
+            return True
         if not self.lists[sm]:
             return False
         ti = self.lists[sm][0]
         T = self.T[ti]
         op, l = T[D_OP], T[D_LAYER]
+        if op in (OP_PREFETCH, OP_PREFETCH_KV):   # producer-only, no dependency
+            self.lists[sm].pop(0)
+            return True
         if op in (OP_QKV, OP_ROUTER, OP_OPROJ, OP_LM, OP_RESID, OP_EMBED):
             if T[D_WAIT] >= 0 and not self.ready(T[D_WAIT], T[D_WAIT_T]):
                 return False
@@ -125,22 +138,36 @@ class Sim:
             self.targets.setdefault(ca, set()).add(ns + 1)
             if self.ctr[ca] == ns + 1:
                 self.ctr[self.C(self.c_og, l, g)] += 1
+                self.ctr[self.c_oa + l] += 1
             return True
         if op == OP_MOE:
+            # the drain also serves the layer's O-proj tiles (D_KLEN from task D_K0): ahead
+            # of expert items once every attention output is complete, and all the
+            # remaining ones (waiting for their group if needed) once the items are gone
+            n_o, o_base = T[D_KLEN], T[D_K0]
+            ho = self.heads[("oproj", l)]
+            if n_o and ho < n_o and self.ready(self.c_oa + l, self.Hkv * self.B):
+                self.heads[("oproj", l)] += 1
+                self.pending[sm] = o_base + ho
+                return True
             if not self.ready(self.c_rr + l, 1):
                 return False
             h = self.heads[("moe", l)]
-            if h >= self.moe_count[l]:
-                self.lists[sm].pop(0)
+            if h < self.moe_count[l]:
+                self.heads[("moe", l)] += 1
+                self.ctr[self.c_md + l] += 1
                 return True
-            self.heads[("moe", l)] += 1
-            self.ctr[self.c_md + l] += 1
+            if n_o and ho < n_o:
+                self.heads[("oproj", l)] += 1
+                self.pending[sm] = o_base + ho
+                return True
+            self.lists[sm].pop(0)
             return True
         raise AssertionError(f"unknown op {op}")
 
     def run(self):
         n = len(self.lists)
-        while any(self.lists):
+        while any(self.lists) or any(x is not None for x in self.pending):
             order = self.rng.permutation(n)
             progressed = False
             for sm in order:
@@ -180,9 +207,11 @@ def test_tasks_are_dealt_round_robin_within_waves():
     owner = {}
     for s in range(7):
         for t in lst[off[s]:off[s + 1]]:
-            if T[t][0] not in (OP_ATT, OP_MOE):
+            if T[t][0] not in (OP_ATT, OP_MOE, OP_PREFETCH_KV):
                 assert t not in owner
                 owner[t] = s
+    # the O-proj tiles are served by the MoE drains, not dealt
+    assert not any(T[t][0] == OP_OPROJ for t in owner)
     router0 = [t for t in range(len(T)) if T[t][0] == OP_ROUTER and T[t][1] == 0]
     assert [owner[t] for t in router0] == [k % 7 for k in range(len(router0))]
     # claimer tasks: one per SM per layer
