@@ -48,7 +48,7 @@ typedef enum mk_status {
  * (n_q_heads / n_kv_heads) * head_dim multiples of 128; n_q_heads divisible by
  * n_kv_heads (at most 8) with a group of at most 8 query heads and
  * group*head_dim <= 1024;
- * n_experts <= 256; top_k <= 8; page_size == 16; max_batch <= 8; n_layers <= 64.
+ * n_experts a multiple of 8 in [8, 256]; top_k <= 8; page_size == 16; max_batch <= 8; n_layers <= 64.
  * swa_layer_mask bit l set = layer l uses a sliding window of sliding_window keys
  * (the window holds the new token and the sliding_window - 1 keys before it).
  * timeout_ms bounds every dependency wait inside the kernel (0 = 2000 ms). */

@@ -20,7 +20,7 @@ struct Smem {
   uint32_t scratch_s;
   int* small;         // kSmallBytes
   uint32_t bars;      // full[kStages], empty[kStages], mfull[kMbox], mempty[kMbox], sfull[kSq], sempty[kSq]
-  int4* mbox;        // [kMbox][2] task entries
+  int4* mbox;        // [kMbox][4] task entries
   int2* sq;           // signal requests [kSq]
 
   __device__ __forceinline__ uint32_t full(uint32_t s) const { return bars + 8u * s; }
@@ -55,7 +55,7 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
   S.bars = aligned + kStages * kStageBytes + kScratchBytes + kSmallBytes;
   S.mbox = reinterpret_cast<int4*>(g + kStages * kStageBytes + kScratchBytes + kSmallBytes +
                                    kBarBytes);
-  S.sq = reinterpret_cast<int2*>(S.mbox + 2 * kMbox);
+  S.sq = reinterpret_cast<int2*>(S.mbox + 4 * kMbox);
   return S;
 }
 
@@ -149,6 +149,29 @@ __device__ __forceinline__ unsigned ld_relaxed(const unsigned* p) {
   unsigned v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Predicated relaxed 64-bit load: `v` keeps its value when `pred` is false.
+__device__ __forceinline__ void ld_relaxed_u64_pred(uint64_t& v, const uint64_t* ptr, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.relaxed.gpu.global.u64 %0, [%1];\n\t}"
+      : "+l"(v)
+      : "l"(ptr), "r"((int)pred)
+      : "memory");
+}
+// OR-reduction barrier of the 256 consumer threads (named barrier 1).
+__device__ __forceinline__ bool bar_or_consumers(bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((int)pred)
+      : "memory");
+  return r != 0;
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {

@@ -82,7 +82,8 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   if (s.gs > 8) return fail(err, MK_ERR_UNSUPPORTED, "query group %d > 8", s.gs);
   if (s.Hkv > 8) return fail(err, MK_ERR_UNSUPPORTED, "n_kv_heads %d > 8", s.Hkv);
   if ((s.gs * s.hd) % 128 || s.gs * s.hd > 1024) return fail(err, MK_ERR_UNSUPPORTED, "group*head_dim %d must be a multiple of 128 <= 1024", s.gs * s.hd);
-  if (s.E < 1 || s.E > 256) return fail(err, MK_ERR_UNSUPPORTED, "n_experts %d not in [1, 256]", s.E);
+  if (s.E < 8 || s.E > 256 || s.E % 8)
+    return fail(err, MK_ERR_UNSUPPORTED, "n_experts %d: need a multiple of 8 in [8, 256]", s.E);
   if (s.topk < 1 || s.topk > 8 || s.topk > s.E) return fail(err, MK_ERR_UNSUPPORTED, "top_k %d not in [1, min(8, E)]", s.topk);
   if (c->page_size != 16) return fail(err, MK_ERR_UNSUPPORTED, "page_size %d != 16", c->page_size);
   if (s.max_batch < 1 || s.max_batch > kMaxBatch) return fail(err, MK_ERR_UNSUPPORTED, "max_batch %d not in [1, 8]", s.max_batch);
@@ -211,8 +212,10 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
                              (size_t)t * s.r_qkv * s.d * 2,
                          s.r_qkv * s.d * 2, W_QKV));
     auto& wr = waves[(size_t)l * W_COUNT + W_ROUTER];
+    // the last tile (dealt last on its SM) collects all tiles' logits and routes
     for (int t = 0; t < s.n_router_tasks; ++t)
-      wr.push_back(add(OP_ROUTER, l, 0, t * s.r_router, s.r_router, 0, s.d, P.c_lr + l, s.nrb_d, P.c_rt + l,
+      wr.push_back(add(OP_ROUTER, l, t == s.n_router_tasks - 1 ? 1 : 0, t * s.r_router, s.r_router, 0, s.d,
+                       P.c_lr + l, s.nrb_d, P.c_rt + l,
                        s.n_router_tasks, s.off_router + l * s.router_layer_bytes + (size_t)t * s.r_router * s.d * 2,
                        s.r_router * s.d * 2, W_ROUTER));
     drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
@@ -675,6 +678,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.timeout_ns = (long long)h->cfg.timeout_ms * 1000000ll;
   p.inflight = 2;
   if (const char* fl = getenv("MK_INFLIGHT")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight = v; }
+  p.inflight_moe = p.inflight;
+  if (const char* fl = getenv("MK_INFLIGHT_MOE")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight_moe = v; }
   p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
   p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
   p.rope_turns = h->rope_turns;
@@ -692,6 +697,9 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(p.atto, (size_t)L * B * s.Hq * s.hd);
   AL(p.opart, (size_t)L * s.Hkv * B * s.d);
   AL(p.rlog, (size_t)L * B * s.E);
+  p.rw_stride = (int)(1 + 2 * maxa + 2 * maxa * B);
+  AL(p.rword, (size_t)L * p.rw_stride);
+  AL(p.epoch, 1);
   AL(p.ridx, (size_t)L * B * s.topk);
   AL(p.rw, (size_t)L * B * s.topk);
   AL(p.active, (size_t)L * maxa);
@@ -720,6 +728,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   CK(h, cudaMemcpy(h->d_sm_off, P.sm_off.data(), P.sm_off.size() * 4, cudaMemcpyHostToDevice));
   CK(h, cudaMemcpy(h->d_sm_list, P.sm_list.data(), P.sm_list.size() * 4, cudaMemcpyHostToDevice));
   CK(h, cudaMemcpy(p.seq_lens, seq_lens_host, (size_t)B * 4, cudaMemcpyHostToDevice));
+  const unsigned first_epoch = 1;  // the cleared tagged words carry epoch 0
+  CK(h, cudaMemcpy(p.epoch, &first_epoch, 4, cudaMemcpyHostToDevice));
   h->planned = true;
   return MK_OK;
 }
@@ -752,7 +762,6 @@ static size_t step_scratch_layout(const mk_handle* h, uint8_t* base, Params* p, 
   q = take(L * s.Hkv * B * (size_t)h->max_items_bg * s.gs * (s.hd + 2) * 4); if (p) p->attp = (float*)q;
   q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->atto = (uint16_t*)q;
   q = take(L * s.Hkv * B * s.d * 4);                            if (p) p->opart = (float*)q;
-  q = take(L * B * s.E * 4);                                    if (p) p->rlog = (float*)q;
   q = take(L * B * s.topk * 4);                                 if (p) p->ridx = (int*)q;
   q = take(L * B * s.topk * 4);                                 if (p) p->rw = (float*)q;
   q = take(L * maxa * 4);                                       if (p) p->active = (int*)q;
@@ -760,7 +769,11 @@ static size_t step_scratch_layout(const mk_handle* h, uint8_t* base, Params* p, 
   q = take(L * maxa * 4);                                       if (p) p->act_cnt = (int*)q;
   q = take(L * maxa * B * 4);                                   if (p) p->act_tok = (int*)q;
   q = take(L * B * s.d * 4);                                    if (p) p->moe = (float*)q;
+  // cleared each call: the counters and queues, and the epoch-tagged words (other
+  // handles' calls share this array and may have used the same epochs)
   const size_t z0 = o;
+  q = take(L * B * s.E * 8);                                    if (p) p->rlog = (uint64_t*)q;
+  q = take(L * (1 + 2 * maxa + 2 * maxa * B) * 8);              if (p) { p->rword = (uint64_t*)q; p->rw_stride = (int)(1 + 2 * maxa + 2 * maxa * B); }
   q = take((size_t)h->P.n_ctr * kCtrStride * 4);                if (p) p->ctr = (unsigned*)q;
   q = take(3 * L * 4);                                          if (p) p->qhead = (int*)q;
   q = take(3 * L * 4);                                          if (p) p->qcount = (int*)q;
@@ -784,7 +797,7 @@ int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cach
   size_t z_off = 0, z_bytes = 0;
   step_scratch_layout(h, static_cast<uint8_t*>(base), &p, &z_off, &z_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // counters and queues must start at zero; everything else is written before it is read
+  // counters, queues and tagged words must start at zero; the rest is written before it is read
   CK(h, cudaMemsetAsync(static_cast<uint8_t*>(base) + z_off, 0, z_bytes, st));
   h->last_stream = st;
   p.sm_off = h->d_sm_off;
@@ -924,7 +937,14 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
       for (int i = 0; i < p.n_ctr; ++i) o[i] = raw[(size_t)i * kCtrStride];
       return MK_OK;
     }
-    case MK_READ_ROUTER_LOGITS: return copy(p.rlog, L * B * s.E * 4);
+    case MK_READ_ROUTER_LOGITS: {  // stored tagged with the step epoch: return the values
+      if (bytes != L * B * s.E * 4) return fail(&h->err, MK_ERR_INVALID, "mk_read(ROUTER_LOGITS): need %zu bytes", L * B * s.E * 4);
+      std::vector<uint64_t> raw(L * B * s.E);
+      CK(h, cudaMemcpy(raw.data(), p.rlog, raw.size() * 8, cudaMemcpyDeviceToHost));
+      uint32_t* o = static_cast<uint32_t*>(host_out);
+      for (size_t i = 0; i < raw.size(); ++i) o[i] = (uint32_t)raw[i];
+      return MK_OK;
+    }
     case MK_READ_TRACE_COUNT: return copy(h->d_trace_n, 4);
     case MK_READ_ACTIVE: {
       const size_t maxa = p.maxa, per = 1 + maxa * (2 + B);

@@ -35,9 +35,10 @@ constexpr int kFragsPerStage = kStageBytes / kFragBytes;
 constexpr int kMaxNrb = 8;                    // GEMV task rows <= 128
 constexpr int kMaxKsw = 16;                   // GEMV task K <= 2048 (16 k16-steps/warp)
 constexpr int kBarBytes = (2 * kStages + 2 * kMbox + 2 * kSq) * 8;
-// mailbox entry: {task, item, chunks, n_tok} + {token bytes 0..3, 4..7, -, -} (MoE items
-// carry their expert's token list: byte n = b * 8 + j for the n-th token b, rank j)
-constexpr int kMboxBytes = kMbox * 32 + kSq * 8;
+// mailbox entry: {task, item, chunks, n_tok}, {token bytes 0..3, 4..7, -, -}, {weights
+// 0..3}, {weights 4..7} (MoE items carry their expert's token list -- byte n = b * 8 + j
+// for the n-th token b, rank j -- and the tokens' routing weights as f32 bits)
+constexpr int kMboxBytes = kMbox * 64 + kSq * 8;
 constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kScratchBytes +
                            kSmallBytes + kBarBytes + kMboxBytes;
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB per-block shared memory limit");
@@ -110,6 +111,7 @@ struct Params {
   long long timeout_ns;
   int fixed, do_reset;
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
+  int inflight_moe;         // the same for the chunks of expert items
   // weights
   const uint8_t* wblob;
   long long off_moe, moe_item_bytes;  // item (l, e, s) at off_moe + ((l*E + e)*t_moe + s) * item_bytes
@@ -133,7 +135,12 @@ struct Params {
   float* attp;              // [L][Hkv][B][max_items_bg][gs*(hd+2)]
   uint16_t* atto;           // [L][B][Hq*hd]
   float* opart;             // [L][Hkv][B][d]
-  float* rlog;              // [L][B][E]
+  uint64_t* rlog;           // [L][B][E] router logits as (step epoch << 32 | f32 bits)
+  uint64_t* rword;          // [L][rw_stride] route words (epoch << 32 | value): n_active,
+                            // active ids [maxa], token counts [maxa], tokens [maxa][B]
+                            // (b * 16 + j), token weights [maxa][B] (f32 bits)
+  unsigned* epoch;          // step epoch (device word; the step's last launch advances it)
+  int rw_stride;
   int* ridx;                // [L][B][topk]
   float* rw;                // [L][B][topk]
   int* active;              // [L][maxa]

@@ -178,6 +178,10 @@ struct AttItem {
 
 // seq_lens are constant during a step: the kernel prologue copies them to smem.
 __device__ __forceinline__ const int* seq_lens_s(const Smem& S) { return S.small + 224; }
+// The step's epoch (read from device memory at launch): tags the router logits and the
+// route words of this step, so that a reader can tell them from the previous step's.
+__device__ __forceinline__ unsigned step_epoch(const Smem& S) { return (unsigned)S.small[248]; }
+__device__ __forceinline__ uint64_t tagged(unsigned ep, unsigned v) { return ((uint64_t)ep << 32) | v; }
 
 __device__ __forceinline__ int layer_window(const Params& p, int l) {
   return ((p.swa_mask >> l) & 1ull) ? p.window : 0;
@@ -257,14 +261,17 @@ __device__ __forceinline__ int checked_page(const Params& p, int b, int logical,
 
 // ============================================================== producer
 __device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int task, int item, int nch,
-                          int4 extra = make_int4(0, 0, 0, 0)) {
+                          int4 extra = make_int4(0, 0, 0, 0), int4 w_lo = make_int4(0, 0, 0, 0),
+                          int4 w_hi = make_int4(0, 0, 0, 0)) {
   const uint32_t slot = mseq % kMbox, use = mseq / kMbox;
   if (use > 0 && !mbar_wait(S.mempty(slot), (use - 1) & 1u, 8 * p.timeout_ns)) {
     raise_err(p, MK_ERR_TIMEOUT, task, -3, (int)mseq, 0);
     return false;
   }
-  S.mbox[2 * slot] = make_int4(task, item, nch, extra.x);
-  S.mbox[2 * slot + 1] = make_int4(extra.y, extra.z, 0, 0);
+  S.mbox[4 * slot] = make_int4(task, item, nch, extra.x);
+  S.mbox[4 * slot + 1] = make_int4(extra.y, extra.z, 0, 0);
+  S.mbox[4 * slot + 2] = w_lo;
+  S.mbox[4 * slot + 3] = w_hi;
   mbar_arrive(S.mfull(slot));
   ++mseq;
   return true;
@@ -275,14 +282,15 @@ __device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int ta
 // landed chunks ahead of the consumers, but only a few are requested at a time:
 // that is enough to keep HBM busy, and keeps the memory queues -- which every
 // other load of the step also waits in -- short.
-__device__ __forceinline__ bool acquire_stage(const Params& p, const Smem& S, uint32_t seq, int task) {
+__device__ __forceinline__ bool acquire_stage(const Params& p, const Smem& S, uint32_t seq, int task,
+                                              int inflight) {
   const uint32_t use = seq / kStages;
   if (use > 0 && !mbar_wait(S.empty(seq % kStages), (use - 1) & 1u, 8 * p.timeout_ns)) {
     raise_err(p, MK_ERR_TIMEOUT, task, -4, (int)seq, 0);
     return false;
   }
-  if (seq >= (uint32_t)p.inflight) {
-    const uint32_t q = seq - p.inflight;
+  if (seq >= (uint32_t)inflight) {
+    const uint32_t q = seq - inflight;
     if (!mbar_wait(S.full(q % kStages), (q / kStages) & 1u, 8 * p.timeout_ns)) {
       raise_err(p, MK_ERR_TIMEOUT, task, -6, (int)q, 0);
       return false;
@@ -305,10 +313,10 @@ __device__ __forceinline__ bool claim_gate(const Params& p, const Smem& S, uint3
 }
 
 __device__ bool issue_linear(const Params& p, const Smem& S, uint32_t& cseq, const uint8_t* src,
-                             int bytes, uint64_t pol, int task, int chunk = kStageBytes) {
+                             int bytes, uint64_t pol, int task, int chunk, int inflight) {
   for (int off = 0; off < bytes; off += chunk) {
     const int n = min(chunk, bytes - off);
-    if (!acquire_stage(p, S, cseq, task)) return false;
+    if (!acquire_stage(p, S, cseq, task, inflight)) return false;
     const uint32_t s = cseq % kStages;
     mbar_expect_tx(S.full(s), (uint32_t)n);
     bulk_g2s(S.stage(cseq), src + off, (uint32_t)n, S.full(s), pol);
@@ -389,7 +397,7 @@ __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const C
     }
     if (c0 + 8 < it.np) load_ids(c0 + 8);
     for (int kv = 0; kv < 2; ++kv) {
-      if (!acquire_stage(p, S, cseq, task)) return false;
+      if (!acquire_stage(p, S, cseq, task, p.inflight)) return false;
       const uint32_t s = cseq % kStages;
       mbar_expect_tx(S.full(s), (uint32_t)(n * page_bytes));
       const uint32_t dst = S.stage(cseq);
@@ -412,7 +420,7 @@ __device__ __forceinline__ bool push_gemv(const Params& p, const Smem& S, uint32
   const int nrb = T[D_NROWS] / 16;
   const int cs = gemv_jpc(nrb) * nrb * 8 * kFragBytes;
   const int nch = (bytes + cs - 1) / cs;
-  return mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs);
+  return mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs, p.inflight);
 }
 
 __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK, const CUtensorMap* tmV) {
@@ -460,34 +468,67 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         break;
       }
       case OP_MOE_DRAIN: {
-        // The first claim is taken before the route step is known to be done (its
-        // round trip overlaps the wait); after the route the queue size and the whole
-        // active-expert list are fetched in one round trip.
+        // The first claim is taken before the layer's route is known (its round trip
+        // overlaps the wait).  The route words an item needs -- n_active, the expert of
+        // its slot, the slot's tokens and their weights -- are polled until they carry
+        // this step's epoch: the detection and the data come with the same loads, and
+        // the consumers get tokens and weights in the mailbox entry.
         const int q = p.L + l;
         if (!(ok = claim_gate(p, S, mseq, ti))) break;
         int item = atomicAdd(p.qhead + q, 1);
-        if (!wait_ge(p, C_RR(p, l), 1u, ti)) { ok = false; break; }
-        int act[kMaxActive];
-        const int count = ldg_cg(p.qcount + q);
+        const uint64_t* rw = p.rword + (size_t)l * p.rw_stride;
+        const unsigned ep = step_epoch(S);
+        const int maxa = p.maxa;
+        int nact = -1, tl_slot = -1, tl_e = 0, tl_cnt = 0, tl_tok[kMaxBatch], tl_w[kMaxBatch];
+        auto fetch = [&](int a) -> bool {  // slot a's words (and n_active while unknown)
+          const uint64_t t0 = gtime();
+          unsigned ns = 32;
+          for (int it = 0;; ++it) {
+            const bool sl = a >= 0 && a < maxa;
+            const int as = sl ? a : 0;
+            uint64_t wn = 0, we = 0, wc = 0, wt[kMaxBatch], ww[kMaxBatch];
+            ld_relaxed_u64_pred(wn, rw, nact < 0);
+            ld_relaxed_u64_pred(we, rw + 1 + as, sl);
+            ld_relaxed_u64_pred(wc, rw + 1 + maxa + as, sl);
 #pragma unroll
-        for (int a = 0; a < kMaxActive; ++a) {
-          act[a] = 0;
-          ldg_cg_pred_i(act[a], p.active + l * p.maxa + a, a < p.maxa);
-        }
-        // the token list of an item's expert slot goes to the consumers in the mailbox
-        // entry; the first item's list is fetched in the same round trip as the above
-        int tl_slot = -1, tl_cnt = 0, tl_tok[kMaxBatch];
-        auto load_tokens = [&](int a) {
-          tl_slot = a;
-          tl_cnt = 0;
-          ldg_cg_pred_i(tl_cnt, p.act_cnt + l * p.maxa + a, true);
+            for (int n = 0; n < kMaxBatch; ++n) {
+              wt[n] = ww[n] = 0;
+              ld_relaxed_u64_pred(wt[n], rw + 1 + 2 * maxa + as * p.B + n, sl && n < p.B);
+              ld_relaxed_u64_pred(ww[n], rw + 1 + 2 * maxa + maxa * p.B + as * p.B + n, sl && n < p.B);
+            }
+            if (nact < 0 && (unsigned)(wn >> 32) == ep) nact = (int)(unsigned)wn;
+            if (nact >= 0) {
+              if (!sl || a >= nact) return true;  // no such item
+              const int c2 = (int)(unsigned)wc;
+              bool good = (unsigned)(we >> 32) == ep && (unsigned)(wc >> 32) == ep;
 #pragma unroll
-          for (int n = 0; n < kMaxBatch; ++n) {
-            tl_tok[n] = 0;
-            ldg_cg_pred_i(tl_tok[n], p.act_tok + ((size_t)l * p.maxa + a) * p.B + n, n < p.B);
+              for (int n = 0; n < kMaxBatch; ++n)
+                if (n < c2 && ((unsigned)(wt[n] >> 32) != ep || (unsigned)(ww[n] >> 32) != ep)) good = false;
+              if (good) {
+                tl_slot = a;
+                tl_e = (int)(unsigned)we;
+                tl_cnt = c2;
+#pragma unroll
+                for (int n = 0; n < kMaxBatch; ++n) {
+                  tl_tok[n] = (n < c2) ? (int)(unsigned)wt[n] : 0;
+                  tl_w[n] = (n < c2) ? (int)(unsigned)ww[n] : 0;
+                }
+                return true;
+              }
+            }
+            __nanosleep(ns);
+            ns = ns < 256 ? ns * 2 : 256;
+            if ((it & 7) == 7) {
+              if (aborted(p)) return false;
+              if ((long long)(gtime() - t0) > p.timeout_ns) {
+                raise_err(p, MK_ERR_TIMEOUT, ti, -12, a, (int)ep);
+                return false;
+              }
+            }
           }
         };
-        if (item < count) load_tokens(item / p.t_moe);
+        if (!fetch(item / p.t_moe)) { ok = false; break; }
+        const int count = nact * p.t_moe;
         // part 1 (gate/up tile) in whole k16-groups, part 2 (down slice) in warp regions
         const int nrb1 = p.moe_fs / 8;
         const int cs1 = gemv_jpc(nrb1) * nrb1 * 8 * kFragBytes;
@@ -517,8 +558,8 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
           }
           if (item >= count) break;
           const int a = item / p.t_moe, t = item % p.t_moe;
-          const int e = act[a];
-          if (a != tl_slot) load_tokens(a);
+          if (a != tl_slot && !fetch(a)) { ok = false; break; }
+          const int e = tl_e;
           int4 extra = make_int4(tl_cnt, 0, 0, 0);
 #pragma unroll
           for (int n = 0; n < kMaxBatch; ++n) {
@@ -527,8 +568,11 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
             else extra.z |= byte << (8 * (n - 4));
           }
           const uint8_t* src = p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
-          ok = mbox_push(p, S, mseq, ti, item, nch, extra) && issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1) &&
-               issue_linear(p, S, cseq, src + gu_bytes, dn_bytes, pol, ti, cs2);
+          const int fl = p.inflight_moe;
+          ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
+                         make_int4(tl_w[4], tl_w[5], tl_w[6], tl_w[7])) &&
+               issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1, fl) &&
+               issue_linear(p, S, cseq, src + gu_bytes, dn_bytes, pol, ti, cs2, fl);
         }
         while (ok && o_left) {
           if (!(ok = claim_gate(p, S, mseq, ti))) break;
@@ -684,55 +728,95 @@ __device__ __forceinline__ float build_norm_bfrag(const Params& p, const Smem& S
 // per-expert token lists in (token, slot) order, and the layer's MoE queue sizes.
 // Top-k by counting: thread (b, e) finds the rank of logit e = how many logits of
 // token b beat it; ranks below top_k are the selection, in descending order.
-__device__ void route_step(const Params& p, const Smem& S, int l) {
+__device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int* sel = S.small + 16;                               // [B][topk] expert ids (<= 64)
   float* lg = S.scratch;                                 // [B][E] logits
   int* slot_of = reinterpret_cast<int*>(S.scratch) + kMaxBatch * 256;  // [E]
   int* act_s = slot_of + 256;                            // [maxa] active expert ids
+  int* cnt_s = act_s + kMaxActive;                       // [maxa] tokens per active expert
+  int* tok_s = cnt_s + kMaxActive;                       // [maxa][B] b * 16 + j
   const int BE = p.B * p.E;
-  for (int i = tid; i < BE; i += kConsumerThreads) lg[i] = ldg_cg(p.rlog + (size_t)l * BE + i);
-  for (int e = tid; e < p.E; e += kConsumerThreads) slot_of[e] = 0;
-  bar_sync_consumers();
-  for (int i = tid; i < BE; i += kConsumerThreads) {
-    const int b = i / p.E, e = i % p.E;
-    const float* r = lg + b * p.E;
-    const float ve = r[e];
-    int rank = 0;
-#pragma unroll 8
-    for (int f = 0; f < p.E; ++f) {
-      const float vf = r[f];
-      rank += (vf > ve || (vf == ve && f < e)) ? 1 : 0;
+  const unsigned ep = step_epoch(S);
+  // the logits of every router tile, polled until all carry this step's epoch (the
+  // poll's loads are the data: no separate fan-in counter and reload)
+  const uint64_t* src = p.rlog + (size_t)l * BE;
+  const uint64_t t0 = gtime();
+  unsigned ns = 32;
+  for (int it = 0;; ++it) {
+    bool stale = false;
+    for (int i = tid; i < BE; i += kConsumerThreads) {
+      const uint64_t w = ld_relaxed_u64(src + i);
+      if ((unsigned)(w >> 32) != ep) stale = true;
+      else lg[i] = __uint_as_float((unsigned)w);
     }
-    if (rank < p.topk) sel[b * p.topk + rank] = e;
+    if (!bar_or_consumers(stale)) break;
+    if (tid == 0) __nanosleep(ns);
+    ns = ns < 256 ? ns * 2 : 256;
+    if ((it & 7) == 7 && bar_or_consumers(tid == 0 && (aborted(p) || (long long)(gtime() - t0) > p.timeout_ns))) {
+      if (tid == 0 && !aborted(p)) raise_err(p, MK_ERR_TIMEOUT, ti, -11, l, 0);
+      return false;
+    }
+  }
+  if (p.trace && tid == 0) trace_slots(S)[6] = gtime();
+  float* wsel = reinterpret_cast<float*>(tok_s + kMaxActive * kMaxBatch);  // [B][topk] weights
+  int* prk = reinterpret_cast<int*>(wsel + kMaxActive);                    // [2][B*E] partial ranks
+  int* tot_s = prk + 256;                                                 // n_active
+  const int E = p.E, K = p.topk, B = p.B;
+  for (int e = tid; e < E; e += kConsumerThreads) slot_of[e] = 0;
+  // rank of logit (b, e) = how many logits of token b beat it (ties to the lower id),
+  // by 128-bit shared-memory reads; with few logits two threads split the range
+  const int H = (2 * BE <= kConsumerThreads) ? 2 : 1;
+  for (int t = tid; t < H * BE; t += kConsumerThreads) {
+    const int i = t % BE, h = t / BE;
+    const int b = i / E, e = i % E;
+    const float* r = lg + b * E;
+    const float ve = r[e];
+    const int f0 = h * (E / H), f1 = f0 + E / H;
+    int rank = 0;
+#pragma unroll 4
+    for (int f = f0; f < f1; f += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(r + f);
+      rank += (q.x > ve || (q.x == ve && f < e)) ? 1 : 0;
+      rank += (q.y > ve || (q.y == ve && f + 1 < e)) ? 1 : 0;
+      rank += (q.z > ve || (q.z == ve && f + 2 < e)) ? 1 : 0;
+      rank += (q.w > ve || (q.w == ve && f + 3 < e)) ? 1 : 0;
+    }
+    if (H == 1) {
+      if (rank < K) sel[b * K + rank] = e;
+    } else {
+      prk[t] = rank;
+    }
+  }
+  if (H == 2) {
+    bar_sync_consumers();
+    for (int i = tid; i < BE; i += kConsumerThreads) {
+      const int rank = prk[i] + prk[BE + i];
+      if (rank < K) sel[(i / E) * K + rank] = i % E;
+    }
   }
   bar_sync_consumers();
-  if (warp < p.B) {
+  if (warp < B) {  // softmax over the selected logits of token `warp`
     const int b = warp;
-    const float* r = lg + b * p.E;
-    const int ej = (lane < p.topk) ? sel[b * p.topk + lane] : 0;
-    const float mx = r[sel[b * p.topk]];
-    const float w = (lane < p.topk) ? __expf(r[ej] - mx) : 0.f;
+    const float* r = lg + b * E;
+    const int ej = (lane < K) ? sel[b * K + lane] : 0;
+    const float mx = r[sel[b * K]];
+    const float w = (lane < K) ? __expf(r[ej] - mx) : 0.f;
     float sum = w;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane < p.topk) {
-      p.ridx[((size_t)l * p.B + b) * p.topk + lane] = ej;
-      p.rw[((size_t)l * p.B + b) * p.topk + lane] = w / sum;
-    }
+    if (lane < K) wsel[b * K + lane] = w / sum;
   }
   trace_mark(p, S, 8);
-  trace_mark(p, S, 9);
-  if (warp == 0) {
-    const int nsel = p.B * p.topk;  // <= 64
+  const int nsel = B * K;  // <= 64
+  if (warp == 0) {  // active experts (ascending id) and per active expert its tokens
     for (int i = lane; i < nsel; i += 32) slot_of[sel[i]] = 1;  // mark used
     __syncwarp();
-    // ascending-id slots: exclusive prefix count of used experts
-    const int per = (p.E + 31) / 32;
+    const int per = (E + 31) / 32;
     int cnt = 0;
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
-      if (e < p.E && slot_of[e]) ++cnt;
+      if (e < E && slot_of[e]) ++cnt;
     }
     int incl = cnt;
 #pragma unroll
@@ -745,47 +829,61 @@ __device__ void route_step(const Params& p, const Smem& S, int l) {
     __syncwarp();
     for (int i = 0; i < per; ++i) {
       const int e = lane * per + i;
-      if (e < p.E && slot_of[e]) {
-        p.active[l * p.maxa + slot] = e;
+      if (e < E && slot_of[e]) {
         act_s[slot] = e;
+        cnt_s[slot] = 0;
         slot_of[e] = slot + 1;  // 1-based; only this lane touches expert e here
         ++slot;
       }
     }
     __syncwarp();
-    // token lists: selection i = b*topk + j goes to slot slot_of[sel[i]] - 1 at
-    // position = earlier selections of the same expert (at most one per token)
-    for (int i0 = 0; i0 < nsel; i0 += 32) {
-      const int i = i0 + lane;
-      const bool on = i < nsel;
-      const int e = on ? sel[i] : -1 - lane;
-      const unsigned same = __match_any_sync(0xffffffffu, e);
-      int pos = __popc(same & ((1u << lane) - 1u));
-      for (int q = 0; q < i0; ++q) pos += (on && sel[q] == e) ? 1 : 0;
-      if (on)
-        p.act_tok[((size_t)l * p.maxa + slot_of[e] - 1) * p.B + pos] = (i / p.topk) * 16 + (i % p.topk);
+    // token lists in ascending (b, j): one pass per token (a token picks an expert once)
+    for (int b = 0; b < B; ++b) {
+      if (lane < K) {
+        const int a = slot_of[sel[b * K + lane]] - 1;
+        tok_s[a * B + cnt_s[a]] = b * 16 + lane;
+        ++cnt_s[a];
+      }
+      __syncwarp();
     }
-    for (int a = lane; a < total; a += 32) {
-      const int e = act_s[a];
-      int c2 = 0;
-      for (int i = 0; i < nsel; ++i) c2 += (sel[i] == e) ? 1 : 0;
-      p.act_cnt[l * p.maxa + a] = c2;
-    }
-    if (lane == 0) {
-      p.nact[l] = total;
-      p.qcount[p.L + l] = total * p.t_moe;
-      // the MoE-done fan-in counts maxa * t_moe arrivals: the inactive slots' share
-      // arrives here (before any item can, since items need this route)
-      const unsigned pad = (unsigned)((p.maxa - total) * p.t_moe);
-      if (pad > 0) atomicAdd(ctr_ptr(p, C_MD(p, l)), pad);
-    }
-    __syncwarp();
-    if (lane == 0) {
-      if (p.trace) trace_slots(S)[10] = gtime();
-      red_release(ctr_ptr(p, C_RR(p, l)), 1u);
-      if (p.trace) trace_slots(S)[11] = gtime();
-    }
+    if (lane == 0) *tot_s = total;
   }
+  bar_sync_consumers();
+  trace_mark(p, S, 9);
+  // route words for the expert-item claimers (each carries the epoch: no ordering needed)
+  const int total = *tot_s, maxa = p.maxa;
+  uint64_t* rw = p.rword + (size_t)l * p.rw_stride;
+  for (int a = tid; a < total; a += kConsumerThreads) {
+    const int c2 = cnt_s[a];
+    for (int n = 0; n < c2; ++n) {
+      const int tk = tok_s[a * B + n];
+      rw[1 + 2 * maxa + a * B + n] = tagged(ep, (unsigned)tk);
+      rw[1 + 2 * maxa + maxa * B + a * B + n] = tagged(ep, __float_as_uint(wsel[(tk >> 4) * K + (tk & 15)]));
+    }
+    rw[1 + a] = tagged(ep, (unsigned)act_s[a]);
+    rw[1 + maxa + a] = tagged(ep, (unsigned)c2);
+  }
+  if (tid == 0) rw[0] = tagged(ep, (unsigned)total);
+  if (p.trace && tid == 0) trace_slots(S)[10] = gtime();
+  // the routing in plain arrays (host-side readers), and the MoE-done padding: the
+  // inactive slots' share of the maxa * t_moe arrivals the ADD_RMSNORM tasks wait for
+  for (int i = tid; i < nsel; i += kConsumerThreads) {
+    p.ridx[(size_t)l * nsel + i] = sel[i];
+    p.rw[(size_t)l * nsel + i] = wsel[i];
+  }
+  for (int a = tid; a < total; a += kConsumerThreads) {
+    p.active[l * maxa + a] = act_s[a];
+    p.act_cnt[l * maxa + a] = cnt_s[a];
+    for (int n = 0; n < cnt_s[a]; ++n) p.act_tok[((size_t)l * maxa + a) * B + n] = tok_s[a * B + n];
+  }
+  if (tid == 0) {
+    p.nact[l] = total;
+    p.qcount[p.L + l] = total * p.t_moe;
+    const unsigned pad = (unsigned)((maxa - total) * p.t_moe);
+    if (pad > 0) atomicAdd(ctr_ptr(p, C_MD(p, l)), pad);
+    if (p.trace) trace_slots(S)[11] = gtime();
+  }
+  return true;
 }
 
 // ADD_RMSNORM for the residual row blocks in `mask` (bit r = rows [128 r, 128 r + 128))
@@ -990,9 +1088,10 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
         for (int e = 0; e < 2; ++e) {
           const int n = 2 * c + e;
           if (n >= p.B) continue;
-          float* out = p.rlog + ((size_t)l * p.B + n) * p.E;
-          if (r0 < p.E) out[r0] = v[e];
-          if (r0 + 8 < p.E) out[r0 + 8] = v[2 + e];
+          uint64_t* out = p.rlog + ((size_t)l * p.B + n) * p.E;
+          const unsigned ep = step_epoch(S);
+          if (r0 < p.E) out[r0] = tagged(ep, __float_as_uint(v[e]));
+          if (r0 + 8 < p.E) out[r0 + 8] = tagged(ep, __float_as_uint(v[2 + e]));
         }
         break;
       }
@@ -1033,7 +1132,9 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
       trace_mark(p, S, 13);
       break;
     case OP_ROUTER:
-      if (signal_fanin(p, S, T[D_SIG_CTR], (unsigned)T[D_SIG_TARGET])) route_step(p, S, l);
+      // no fan-in: the layer's last router tile (D_AUX = 1) collects every tile's
+      // tagged logits itself and runs the route step
+      if (T[D_AUX] == 1 && !route_step(p, S, l, ti)) return false;
       break;
     default:
       break;
@@ -1062,29 +1163,31 @@ __device__ bool task_resid(const Params& p, const Smem& S, uint32_t& sseq, const
 // by the route step).
 template <int FS>
 __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, const int* T,
-                                         int ti, int item, int nch, int ntok, int tok_lo, int tok_hi, BFrag& fr,
-                                         OperandKey& have, float& rs_have) {
+                                         int ti, int item, int nch, int ntok, int tok_lo, int tok_hi, int4 w_lo,
+                                         int4 w_hi, BFrag& fr, OperandKey& have, float& rs_have) {
   const int l = T[D_LAYER];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g8 = lane >> 2, c = lane & 3;
   const int a_slot = item / p.t_moe;
   const OperandKey key = {3, l, a_slot};
-  // The producer claimed this item after the layer's route step (acquire) and passed
-  // the expert's token list in the mailbox entry, so no dependency wait is needed here.
+  // The producer claimed this item from the layer's route words and passed the
+  // expert's token list and weights in the mailbox entry: no dependency wait here.
   const bool reuse = key == have;
   trace_mark(p, S, 1);
   auto tok_byte = [&](int n) { return ((n < 4 ? tok_lo : tok_hi) >> (8 * (n & 3))) & 0xff; };
-  // this lane's two epilogue tokens (2c, 2c+1): batch index and routing weight (the
-  // weight loads share the round trip of the operand loads below)
+  // this lane's two epilogue tokens (2c, 2c+1): batch index and routing weight (both
+  // from the mailbox entry)
+  const int wbits[8] = {w_lo.x, w_lo.y, w_lo.z, w_lo.w, w_hi.x, w_hi.y, w_hi.z, w_hi.w};
   int bt[2];
   float wt[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int n = 2 * c + e;
-    const int tb = tok_byte(n);
-    bt[e] = (n < ntok) ? (tb >> 3) : -1;
-    wt[e] = 0.f;
-    ldg_cg_pred(wt[e], p.rw + ((size_t)l * p.B + (tb >> 3)) * p.topk + (tb & 7), n < ntok);
+    int wb = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wb = (k == n) ? wbits[k] : wb;
+    bt[e] = (n < ntok) ? (tok_byte(n) >> 3) : -1;
+    wt[e] = (n < ntok) ? __int_as_float(wb) : 0.f;
   }
   const int ksw1 = p.d / 128;
   if (!reuse) {
@@ -1491,8 +1594,10 @@ __device__ void consumer(const Params& p, const Smem& S) {
     bar_sync_consumers();
     const bool got = S.small[3] != 0;
     const bool abort_now = S.small[4] != 0;
-    const int4 ent = got ? S.mbox[2 * slot] : make_int4(-1, 0, 0, 0);
-    const int4 ent2 = got ? S.mbox[2 * slot + 1] : make_int4(0, 0, 0, 0);
+    const int4 ent = got ? S.mbox[4 * slot] : make_int4(-1, 0, 0, 0);
+    const int4 ent2 = got ? S.mbox[4 * slot + 1] : make_int4(0, 0, 0, 0);
+    const int4 ew_lo = got ? S.mbox[4 * slot + 2] : make_int4(0, 0, 0, 0);
+    const int4 ew_hi = got ? S.mbox[4 * slot + 3] : make_int4(0, 0, 0, 0);
     bar_sync_consumers();
     if (got && threadIdx.x == 0) mbar_arrive(S.mempty(slot));
     ++mseq;
@@ -1529,8 +1634,8 @@ __device__ void consumer(const Params& p, const Smem& S) {
         break;
       case OP_MOE_DRAIN:
         ok = (p.moe_fs == 32)
-                 ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, fr, have, rs_have)
-                 : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, fr, have, rs_have);
+                 ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have)
+                 : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have);
         break;
       default:
         ok = task_gemv(p, S, cseq, sseq, T, ent.x, nch, fr, have, rs_have);
@@ -1565,6 +1670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (threadIdx.x < p.B) S.small[224 + threadIdx.x] = p.seq_lens[threadIdx.x];
+  if (threadIdx.x == 0) S.small[248] = (int)ld_volatile(reinterpret_cast<const int*>(p.epoch));
   __syncthreads();
   const int warp = threadIdx.x >> 5;
   if (warp == kProducerWarp) {
@@ -1590,6 +1696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
       if (!p.fixed)
         for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.seq_lens[b] += 1;
+      // the next step's epoch (never 0: freshly cleared words must not look current)
+      if (threadIdx.x == 0) {
+        const unsigned ep = step_epoch(S) + 1u;
+        *p.epoch = ep ? ep : 1u;
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {

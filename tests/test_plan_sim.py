@@ -111,12 +111,16 @@ class Sim:
                 return False
             if op == OP_RESID and not self.ready(T[D_WAIT2], T[D_WAIT2_T]):
                 return False
+            # the layer's last router tile (D_AUX = 1) collects every tile's logits
+            if op == OP_ROUTER and T[D_AUX] == 1 and self.ctr[T[D_SIG]] < T[D_SIG_T] - 1:
+                return False
             self.lists[sm].pop(0)
             if op == OP_EMBED:
                 self.ctr[T[D_SIG]] += self.nrb_d
             elif op == OP_ROUTER:
                 self.ctr[T[D_SIG]] += 1
-                if self.ctr[T[D_SIG]] == T[D_SIG_T]:
+                if T[D_AUX] == 1:
+                    assert self.ctr[T[D_SIG]] == T[D_SIG_T]
                     self.route(l)
             elif op == OP_RESID:
                 self.ctr[self.c_lr + l + 1] += 1
@@ -150,7 +154,7 @@ class Sim:
                 self.heads[("oproj", l)] += 1
                 self.pending[sm] = o_base + ho
                 return True
-            if not self.ready(self.c_rr + l, 1):
+            if not self.ready(self.c_rr + l, 1):   # the route words of the layer
                 return False
             h = self.heads[("moe", l)]
             if h < self.moe_count[l]:
