@@ -131,8 +131,8 @@ enum Wave { W_QKV = 0, W_ROUTER, W_ATT, W_MOE, W_OPROJ, W_RESID, W_COUNT };
 
 struct PlanOut {
   int B = 0, maxa = 0, n_sm = 0;
-  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_oa, c_done, n_ctr;
-  int rb_target;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_od, c_oa, c_done, n_ctr;
+  int od_target;
   std::vector<int32_t> tasks;     // n_tasks * 32
   std::vector<int32_t> sm_off;    // n_segs * (n_sm + 1), absolute offsets into sm_list
   std::vector<int32_t> sm_list;
@@ -178,11 +178,11 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   P.c_att = c; c += L * B * s.Hkv;
   P.c_og = c; c += L * s.Hkv;
   P.c_md = c; c += L;
-  P.c_rb = c; c += L * s.nrb_d;
+  P.c_od = c; c += L;  // O-proj tiles done per layer (target od_target)
   P.c_oa = c; c += L;  // attention outputs complete per layer (target Hkv * B)
   P.c_done = c; c += 1;
   P.n_ctr = c;
-  P.rb_target = s.Hkv * (kRowBlock / s.r_o);  // O-proj tiles of a residual row block
+  P.od_target = s.Hkv * s.t_o;  // O-proj tiles of a layer
 
   auto add = [&](int op, int layer, int aux, int row0, int nrows, int k0, int klen, int wc, int wt, int sc,
                  int st, size_t woff, int wbytes, int wave) {
@@ -193,7 +193,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     T[D_K0] = k0; T[D_KLEN] = klen; T[D_WAIT_CTR] = wc; T[D_WAIT_TARGET] = wt; T[D_SIG_CTR] = sc;
     T[D_SIG_TARGET] = st; T[D_WOFF_LO] = (int32_t)(uint32_t)(woff & 0xffffffffull);
     T[D_WOFF_HI] = (int32_t)(uint32_t)(woff >> 32); T[D_WBYTES] = wbytes; T[D_QUEUE] = -1;
-    T[D_TASK_ID] = id; T[D_WAVE] = wave;
+    T[D_TASK_ID] = id; T[D_WAVE] = wave; T[D_WAIT2_CTR] = -1;
     return id;
   };
 
@@ -203,21 +203,32 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   std::vector<int> drains((size_t)L * W_COUNT, -1);
   std::vector<int> moe_oq(L, -1);  // megakernel MoE drains that also serve the O-proj queue
   for (int l = 0; l < L; ++l) {
+    // layer 0's QKV and router tiles wait for the embedding (its operand); the later
+    // layers' wait for the previous layer's experts and O-proj tiles and build their
+    // operand from its parts
+    const int w1 = l == 0 ? P.c_lr : P.c_md + l - 1;
+    const int t1 = l == 0 ? s.nrb_d : P.maxa * s.t_moe;
+    auto wait2 = [&](int t) {
+      if (l == 0) return t;
+      P.tasks[(size_t)t * kDescInts + D_WAIT2_CTR] = P.c_od + l - 1;
+      P.tasks[(size_t)t * kDescInts + D_WAIT2_TARGET] = P.od_target;
+      return t;
+    };
     auto& wq = waves[(size_t)l * W_COUNT + W_QKV];
     for (int g = 0; g < s.Hkv; ++g)
       for (int t = 0; t < s.qkv_tpg; ++t)
-        wq.push_back(add(OP_QKV, l, g, t * s.r_qkv, s.r_qkv, 0, s.d, P.c_lr + l, s.nrb_d,
-                         P.c_qkvg + l * s.Hkv + g, s.qkv_tpg,
-                         s.off_qkv + l * s.qkv_layer_bytes + (size_t)g * s.qkv_rows_group * s.d * 2 +
-                             (size_t)t * s.r_qkv * s.d * 2,
-                         s.r_qkv * s.d * 2, W_QKV));
+        wq.push_back(wait2(add(OP_QKV, l, g, t * s.r_qkv, s.r_qkv, 0, s.d, w1, t1, P.c_qkvg + l * s.Hkv + g,
+                               s.qkv_tpg,
+                               s.off_qkv + l * s.qkv_layer_bytes + (size_t)g * s.qkv_rows_group * s.d * 2 +
+                                   (size_t)t * s.r_qkv * s.d * 2,
+                               s.r_qkv * s.d * 2, W_QKV)));
     auto& wr = waves[(size_t)l * W_COUNT + W_ROUTER];
     // the last tile (dealt last on its SM) collects all tiles' logits and routes
     for (int t = 0; t < s.n_router_tasks; ++t)
-      wr.push_back(add(OP_ROUTER, l, t == s.n_router_tasks - 1 ? 1 : 0, t * s.r_router, s.r_router, 0, s.d,
-                       P.c_lr + l, s.nrb_d, P.c_rt + l,
-                       s.n_router_tasks, s.off_router + l * s.router_layer_bytes + (size_t)t * s.r_router * s.d * 2,
-                       s.r_router * s.d * 2, W_ROUTER));
+      wr.push_back(wait2(add(OP_ROUTER, l, t == s.n_router_tasks - 1 ? 1 : 0, t * s.r_router, s.r_router, 0, s.d,
+                             w1, t1, P.c_rt + l, s.n_router_tasks,
+                             s.off_router + l * s.router_layer_bytes + (size_t)t * s.r_router * s.d * 2,
+                             s.r_router * s.d * 2, W_ROUTER)));
     drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
     drains[(size_t)l * W_COUNT + W_MOE] =
         add(OP_MOE_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
@@ -226,14 +237,14 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     for (int g = 0; g < s.Hkv; ++g)
       for (int t = 0; t < s.t_o; ++t)
         wo.push_back(add(OP_OPROJ, l, g, t * s.r_o, s.r_o, g * s.k_o, s.k_o, P.c_og + l * s.Hkv + g, B,
-                         P.c_rb + l * s.nrb_d + (t * s.r_o) / kRowBlock, P.rb_target,
+                         P.c_od + l, P.od_target,
                          s.off_o + l * s.o_layer_bytes + (size_t)g * s.d * s.k_o * 2 + (size_t)t * s.r_o * s.k_o * 2,
                          s.r_o * s.k_o * 2, W_OPROJ));
   }
   for (int l = 0; l < L; ++l) {
     auto& wx = waves[(size_t)l * W_COUNT + W_RESID];
     for (int r = 0; r < s.nrb_d; ++r) {
-      const int t = add(OP_RESID, l, r, r * kRowBlock, kRowBlock, 0, 0, P.c_rb + l * s.nrb_d + r, P.rb_target,
+      const int t = add(OP_RESID, l, r, r * kRowBlock, kRowBlock, 0, 0, P.c_od + l, P.od_target,
                         P.c_lr + l + 1, s.nrb_d, 0, 0, W_RESID);
       P.tasks[(size_t)t * kDescInts + D_WAIT2_CTR] = P.c_md + l;
       P.tasks[(size_t)t * kDescInts + D_WAIT2_TARGET] = P.maxa * s.t_moe;
@@ -619,9 +630,9 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
     int32_t* I = info_out;
     I[0] = P.n_tasks(); I[1] = list_len; I[2] = P.n_ctr; I[3] = P.maxa; I[4] = 0;
     I[5] = s.t_moe; I[6] = (int)(s.moe_item_bytes / 1024); I[7] = s.r_o; I[8] = s.moe_fs; I[9] = s.r_qkv; I[10] = s.qkv_tpg;
-    I[11] = s.n_router_tasks; I[12] = P.rb_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
+    I[11] = s.n_router_tasks; I[12] = P.od_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
     I[16] = P.c_lr; I[17] = P.c_qkvg; I[18] = P.c_rt; I[19] = P.c_rr; I[20] = P.c_att; I[21] = P.c_og;
-    I[22] = P.c_md; I[23] = P.c_rb; I[24] = s.nrb_d; I[25] = s.gs; I[26] = P.c_oa;
+    I[22] = P.c_md; I[23] = P.c_od; I[24] = s.nrb_d; I[25] = s.gs; I[26] = P.c_oa;
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
     return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
@@ -695,7 +706,6 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(p.Q, (size_t)L * B * s.Hq * s.hd);
   AL(p.attp, (size_t)L * s.Hkv * B * h->max_items_bg * s.gs * (s.hd + 2));
   AL(p.atto, (size_t)L * B * s.Hq * s.hd);
-  AL(p.opart, (size_t)L * s.Hkv * B * s.d);
   AL(p.rlog, (size_t)L * B * s.E);
   p.rw_stride = (int)(1 + 2 * maxa + 2 * maxa * B);
   AL(p.rword, (size_t)L * p.rw_stride);
@@ -719,9 +729,9 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(h->d_trace_n, 1);
 #undef AL
   p.c_lr = P.c_lr; p.c_qkvg = P.c_qkvg; p.c_rt = P.c_rt; p.c_rr = P.c_rr; p.c_att = P.c_att; p.c_og = P.c_og;
-  p.c_md = P.c_md; p.c_rb = P.c_rb; p.c_oa = P.c_oa; p.c_done = P.c_done; p.n_ctr = P.n_ctr;
+  p.c_md = P.c_md; p.c_od = P.c_od; p.c_oa = P.c_oa; p.c_done = P.c_done; p.n_ctr = P.n_ctr;
   p.n_queues = 3 * L;
-  p.rb_target = P.rb_target;
+  p.od_target = P.od_target;
   p.tasks = h->d_tasks; p.sm_off = h->d_sm_off; p.sm_list = h->d_sm_list;
   p.trace = nullptr; p.trace_n = h->d_trace_n; p.trace_cap = 0;
   CK(h, cudaMemcpy(h->d_tasks, P.tasks.data(), P.tasks.size() * 4, cudaMemcpyHostToDevice));
@@ -761,17 +771,17 @@ static size_t step_scratch_layout(const mk_handle* h, uint8_t* base, Params* p, 
   q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->Q = (uint16_t*)q;
   q = take(L * s.Hkv * B * (size_t)h->max_items_bg * s.gs * (s.hd + 2) * 4); if (p) p->attp = (float*)q;
   q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->atto = (uint16_t*)q;
-  q = take(L * s.Hkv * B * s.d * 4);                            if (p) p->opart = (float*)q;
   q = take(L * B * s.topk * 4);                                 if (p) p->ridx = (int*)q;
   q = take(L * B * s.topk * 4);                                 if (p) p->rw = (float*)q;
   q = take(L * maxa * 4);                                       if (p) p->active = (int*)q;
   q = take(L * 4);                                              if (p) p->nact = (int*)q;
   q = take(L * maxa * 4);                                       if (p) p->act_cnt = (int*)q;
   q = take(L * maxa * B * 4);                                   if (p) p->act_tok = (int*)q;
-  q = take(L * B * s.d * 4);                                    if (p) p->moe = (float*)q;
-  // cleared each call: the counters and queues, and the epoch-tagged words (other
-  // handles' calls share this array and may have used the same epochs)
+  // cleared each call: the layer accumulators, the counters and queues, and the
+  // epoch-tagged words (other handles' calls share this array and may have used the
+  // same epochs)
   const size_t z0 = o;
+  q = take(L * B * s.d * 4);                                    if (p) p->moe = (float*)q;
   q = take(L * B * s.E * 8);                                    if (p) p->rlog = (uint64_t*)q;
   q = take(L * (1 + 2 * maxa + 2 * maxa * B) * 8);              if (p) { p->rword = (uint64_t*)q; p->rw_stride = (int)(1 + 2 * maxa + 2 * maxa * B); }
   q = take((size_t)h->P.n_ctr * kCtrStride * 4);                if (p) p->ctr = (unsigned*)q;

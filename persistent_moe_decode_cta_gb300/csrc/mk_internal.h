@@ -134,7 +134,6 @@ struct Params {
   uint16_t* Q;              // [L][B][Hq*hd]
   float* attp;              // [L][Hkv][B][max_items_bg][gs*(hd+2)]
   uint16_t* atto;           // [L][B][Hq*hd]
-  float* opart;             // [L][Hkv][B][d]
   uint64_t* rlog;           // [L][B][E] router logits as (step epoch << 32 | f32 bits)
   uint64_t* rword;          // [L][rw_stride] route words (epoch << 32 | value): n_active,
                             // active ids [maxa], token counts [maxa], tokens [maxa][B]
@@ -147,14 +146,15 @@ struct Params {
   int* nact;                // [L]
   int* act_cnt;             // [L][maxa]
   int* act_tok;             // [L][maxa][B]  (b*16 + j)
-  float* moe;               // [L][B][d] routing-weighted sum of the layer's expert outputs
+  float* moe;               // [L][B][d] layer accumulator: the routing-weighted expert outputs
+                            // plus the O-proj outputs of every KV group
   // synchronisation
   unsigned* ctr;
   int* qhead;               // [3L]
   int* qcount;              // [3L]
   int* err;                 // [16]
-  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_rb, c_oa, c_done, n_ctr, n_queues;
-  int rb_target;
+  int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_od, c_oa, c_done, n_ctr, n_queues;
+  int od_target;
   // optional task timeline (see trace_emit)
   unsigned long long* trace;
   unsigned* trace_n;

@@ -166,7 +166,7 @@ __device__ __forceinline__ int C_ATT(const Params& p, int l, int b, int g) {
 __device__ __forceinline__ int C_OG(const Params& p, int l, int g) { return p.c_og + l * p.Hkv + g; }
 __device__ __forceinline__ int C_MD(const Params& p, int l) { return p.c_md + l; }
 __device__ __forceinline__ int C_OA(const Params& p, int l) { return p.c_oa + l; }
-__device__ __forceinline__ int C_RB(const Params& p, int l, int r) { return p.c_rb + l * p.nrb_d + r; }
+__device__ __forceinline__ int C_OD(const Params& p, int l) { return p.c_od + l; }
 
 struct AttItem {
   int b, g, s, ns;      // sequence, KV group, split (s == ns: the new token itself)
@@ -480,12 +480,18 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         const unsigned ep = step_epoch(S);
         const int maxa = p.maxa;
         int nact = -1, tl_slot = -1, tl_e = 0, tl_cnt = 0, tl_tok[kMaxBatch], tl_w[kMaxBatch];
+        // the items' operand (bf16(x_l * gain), 1/rms) is written by the previous layer's
+        // ADD_RMSNORM tasks: their counter is read (and acquired) in the same batch
+        bool lr_done = false;
+        const unsigned* lr_ctr = ctr_ptr(p, C_LR(p, l));
+        const unsigned lr_target = (unsigned)p.nrb_d;
         auto fetch = [&](int a) -> bool {  // slot a's words (and n_active while unknown)
           const uint64_t t0 = gtime();
           unsigned ns = 32;
           for (int it = 0;; ++it) {
             const bool sl = a >= 0 && a < maxa;
             const int as = sl ? a : 0;
+            const unsigned lr = lr_done ? lr_target : ld_relaxed(lr_ctr);
             uint64_t wn = 0, we = 0, wc = 0, wt[kMaxBatch], ww[kMaxBatch];
             ld_relaxed_u64_pred(wn, rw, nact < 0);
             ld_relaxed_u64_pred(we, rw + 1 + as, sl);
@@ -497,7 +503,11 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
               ld_relaxed_u64_pred(ww[n], rw + 1 + 2 * maxa + maxa * p.B + as * p.B + n, sl && n < p.B);
             }
             if (nact < 0 && (unsigned)(wn >> 32) == ep) nact = (int)(unsigned)wn;
-            if (nact >= 0) {
+            if (!lr_done && lr >= lr_target) {
+              fence_acq_rel_gpu();  // acquire: the ADD_RMSNORM outputs are visible
+              lr_done = true;
+            }
+            if (nact >= 0 && lr_done) {
               if (!sl || a >= nact) return true;  // no such item
               const int c2 = (int)(unsigned)wc;
               bool good = (unsigned)(we >> 32) == ep && (unsigned)(wc >> 32) == ep;
@@ -721,6 +731,110 @@ __device__ __forceinline__ float build_norm_bfrag(const Params& p, const Smem& S
   return b < 0 ? 0.f : rstd_smem(S)[b];
 }
 
+// Normed operand of layer l >= 1 straight from its parts, without waiting for the
+// ADD_RMSNORM step: x_l = x_{l-1} + the accumulator of layer l-1 (expert and O-proj
+// outputs).  The B fragments get bf16(x_l * gain) (and, with `lo`, the bf16 residue of
+// the product); the returned value is 1/rms of this lane's token row (lane / 4).  The
+// products are staged in scratch as bf16 rows [token][d] whose 16-byte chunks are
+// XOR-swizzled by the token index (conflict-free fragment reads); with `lo`, hi rows
+// sit at 0 and lo rows at 16 KB, four tokens per pass.
+__device__ float build_operand_parts(const Params& p, const Smem& S, BFrag& fr, BFrag* lo, int ksw, int l) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = lane & 3, nl = lane >> 2;
+  const int d = p.d, B = p.B, d4 = d / 4;
+  const float* xa = p.X + (size_t)(l - 1) * B * d;
+  const float* ma = p.moe + (size_t)(l - 1) * B * d;
+  const float4* gain4 = reinterpret_cast<const float4*>(p.attn_norm + (size_t)l * d);
+  uint8_t* st = reinterpret_cast<uint8_t*>(S.scratch);
+  float* ssw = reinterpret_cast<float*>(S.small + 16);  // [8 warps][8 tokens] partial sums
+  const int row_bytes = 2 * d;
+  const int per_pass = lo ? 4 : 8;
+#pragma unroll
+  for (int j = 0; j < kMaxKsw; ++j) {
+    fr.b0[j] = fr.b1[j] = 0u;
+    if (lo) lo->b0[j] = lo->b1[j] = 0u;
+  }
+  constexpr int kG = 2048 / 4 / kConsumerThreads;  // float4 groups per thread (d <= 2048)
+  constexpr int kU = 2;                             // tokens whose loads are in flight together
+  float4 gv[kG];
+#pragma unroll
+  for (int q = 0; q < kG; ++q) {
+    const int g = tid + q * kConsumerThreads;
+    gv[q] = g < d4 ? gain4[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int t0 = 0; t0 < B; t0 += per_pass) {
+    const int t1 = min(B, t0 + per_pass);
+    for (int u0 = t0; u0 < t1; u0 += kU) {
+      // loads of kU tokens in flight together
+      float4 av[kU][kG], mv[kU][kG];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int q = 0; q < kG; ++q) {
+          const int n = u0 + u, g = tid + q * kConsumerThreads;
+          av[u][q] = mv[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (n < t1 && g < d4) {
+            av[u][q] = __ldcg(reinterpret_cast<const float4*>(xa + (size_t)n * d) + g);
+            mv[u][q] = __ldcg(reinterpret_cast<const float4*>(ma + (size_t)n * d) + g);
+          }
+        }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int n = u0 + u;
+        float s2 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kG; ++q) {
+          const int g = tid + q * kConsumerThreads;
+          if (n < t1 && g < d4) {
+            const float x0 = av[u][q].x + mv[u][q].x, x1 = av[u][q].y + mv[u][q].y;
+            const float x2 = av[u][q].z + mv[u][q].z, x3 = av[u][q].w + mv[u][q].w;
+            s2 += x0 * x0 + x1 * x1 + x2 * x2 + x3 * x3;
+            const float y0 = x0 * gv[q].x, y1 = x1 * gv[q].y, y2 = x2 * gv[q].z, y3 = x3 * gv[q].w;
+            const uint16_t h0 = to_bf16(y0), h1 = to_bf16(y1), h2 = to_bf16(y2), h3 = to_bf16(y3);
+            const int off = (n - t0) * row_bytes + ((((g >> 1) ^ (n & 7))) << 4) + (g & 1) * 8;
+            *reinterpret_cast<uint2*>(st + off) =
+                make_uint2((uint32_t)h0 | ((uint32_t)h1 << 16), (uint32_t)h2 | ((uint32_t)h3 << 16));
+            if (lo) {
+              const uint16_t l0 = to_bf16(y0 - bf16_to_f(h0)), l1 = to_bf16(y1 - bf16_to_f(h1));
+              const uint16_t l2 = to_bf16(y2 - bf16_to_f(h2)), l3 = to_bf16(y3 - bf16_to_f(h3));
+              *reinterpret_cast<uint2*>(st + 16384 + off) =
+                  make_uint2((uint32_t)l0 | ((uint32_t)l1 << 16), (uint32_t)l2 | ((uint32_t)l3 << 16));
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+        if (lane == 0 && n < t1) ssw[warp * 8 + n] = s2;
+      }
+    }
+    bar_sync_consumers();
+    if (tid >= t0 && tid < t1) {
+      float s2 = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) s2 += ssw[w * 8 + tid];
+      rstd_smem(S)[tid] = rsqrtf(s2 / (float)d + p.eps);
+    }
+    if (nl >= t0 && nl < t1) {
+      const uint8_t* row = st + (nl - t0) * row_bytes;
+#pragma unroll
+      for (int j = 0; j < kMaxKsw; ++j) {
+        if (j < ksw) {
+          const int ks = warp + 8 * j;
+          const int o0 = (((2 * ks) ^ (nl & 7)) << 4) + 4 * c, o1 = (((2 * ks + 1) ^ (nl & 7)) << 4) + 4 * c;
+          fr.b0[j] = *reinterpret_cast<const uint32_t*>(row + o0);
+          fr.b1[j] = *reinterpret_cast<const uint32_t*>(row + o1);
+          if (lo) {
+            lo->b0[j] = *reinterpret_cast<const uint32_t*>(row + 16384 + o0);
+            lo->b1[j] = *reinterpret_cast<const uint32_t*>(row + 16384 + o1);
+          }
+        }
+      }
+    }
+    bar_sync_consumers();
+  }
+  return nl < B ? rstd_smem(S)[nl] : 0.f;
+}
+
 // ============================================================== epilogues / fan-in steps
 
 // Route step: top-k of the router logits per token (ties to the lower expert id),
@@ -887,10 +1001,11 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
 }
 
 // ADD_RMSNORM for the residual row blocks in `mask` (bit r = rows [128 r, 128 r + 128))
-// of layer l, in one pass over the CTA: x_{l+1} = x_l + sum_g O-proj partial_g + MoE
-// accumulator; the next layer's operand bf16(x_{l+1} * gain_{l+1}) as hi/lo parts; the
-// blocks' per-token sums of squares; the next layer's MoE accumulator rows zeroed.
-// Then LR(l+1) += number of blocks.
+// of layer l, in one pass over the CTA: x_{l+1} = x_l + the layer accumulator (expert and
+// O-proj outputs); the next layer's operand bf16(x_{l+1} * gain_{l+1}) as hi/lo parts (for
+// the expert items and the LM head) and the blocks' per-token sums of squares.  Then
+// LR(l+1) += number of blocks.  (The next layer's router and QKV tiles do not wait for
+// this: they build their operand from x_l and the accumulator themselves.)
 __device__ void residual_blocks(const Params& p, const Smem& S, uint32_t& sseq, int l, unsigned mask) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int* rbl = S.small + 16;  // list of the blocks (<= 16)
@@ -910,25 +1025,13 @@ __device__ void residual_blocks(const Params& p, const Smem& S, uint32_t& sseq, 
     const int blk = q >> 2;                      // (block index, token)
     const int r = rbl[blk / p.B], b = blk % p.B;
     const int row = r * kRowBlock + (q & 3) * 32 + lane;
-    constexpr int kMaxG = 8;
-    float part[2 + kMaxG];
-    part[0] = ldg_cg(p.X + ((size_t)l * p.B + b) * p.d + row);
-    part[1] = ldg_cg(p.moe + ((size_t)l * p.B + b) * p.d + row);
-#pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
-      part[2 + g] = 0.f;
-      ldg_cg_pred(part[2 + g], p.opart + (((size_t)l * p.Hkv + g) * p.B + b) * p.d + row, g < p.Hkv);
-    }
-    float x = 0.f;
-#pragma unroll
-    for (int k = 0; k < 2 + kMaxG; ++k) x += part[k];
+    const float x = ldg_cg(p.X + ((size_t)l * p.B + b) * p.d + row) + ldg_cg(p.moe + ((size_t)l * p.B + b) * p.d + row);
     const size_t o = ((size_t)(l + 1) * p.B + b) * p.d + row;
     p.X[o] = x;
     const float xg = x * gain_next[row];
     const uint16_t hi = to_bf16(xg);
     p.XG[o] = hi;
     p.XGL[o] = to_bf16(xg - bf16_to_f(hi));
-    if (l + 1 < p.L) p.moe[o] = 0.f;
     float sq = x * x;
 #pragma unroll
     for (int s2 = 16; s2 > 0; s2 >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, s2);
@@ -993,10 +1096,15 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
   const bool reuse = key == have;
   if (reuse) {
     trace_mark(p, S, 1);
-  } else if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti)) {
+  } else if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti) ||
+             !consumer_wait(p, S, T[D_WAIT2_CTR], (unsigned)T[D_WAIT2_TARGET], ti)) {
     drain_chunks(p, S, cseq, nch);
     return false;
   }
+  // QKV and router tiles of layers >= 1 build their operand from the previous layer's
+  // residual stream and accumulator (they wait for the layer's experts and O-proj, not
+  // for its ADD_RMSNORM step)
+  const bool from_parts = (op == OP_QKV || op == OP_ROUTER) && l >= 1;
   const int nrb = nrows / 16;
   const int ksw = klen / 16 / kConsumerWarps;
 
@@ -1006,9 +1114,15 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
     // the router's operand is hi + lo bf16 parts (hi is shared with the layer's QKV
     // tiles; the residue lo is loaded for the router only)
     const int n = lane >> 2;
-    BFrag lo;  // issued first: its loads share the round trip of the hi part and 1/rms
-    load_bfrag(lo, ksw, n < p.B ? p.XGL + ((size_t)l * p.B + n) * p.d : nullptr);
-    if (!reuse) rs_have = build_norm_bfrag(p, S, fr, ksw, l, n < p.B ? n : -1);
+    BFrag lo;
+    if (from_parts) {
+      // the hi part is rebuilt as well (it is the shared QKV operand)
+      rs_have = build_operand_parts(p, S, fr, &lo, ksw, l);
+    } else {
+      // issued first: its loads share the round trip of the hi part and 1/rms
+      load_bfrag(lo, ksw, n < p.B ? p.XGL + ((size_t)l * p.B + n) * p.d : nullptr);
+      if (!reuse) rs_have = build_norm_bfrag(p, S, fr, ksw, l, n < p.B ? n : -1);
+    }
     have = key;
     ran = (nrb == 1) ? gemv_run<1>(p, S, cseq, nch, ksw, fr, v, &lo) : gemv_run<2>(p, S, cseq, nch, ksw, fr, v, &lo);
   } else {
@@ -1016,6 +1130,8 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
       const int n = lane >> 2;
       if (op == OP_OPROJ) {
         load_bfrag(fr, ksw, n < p.B ? p.atto + ((size_t)l * p.B + n) * p.Hq * p.hd + T[D_K0] : nullptr);
+      } else if (from_parts) {
+        rs_have = build_operand_parts(p, S, fr, nullptr, ksw, l);
       } else {
         // RMSNorm operand of QKV (layer input) and LM_HEAD (final norm)
         rs_have = build_norm_bfrag(p, S, fr, ksw, op == OP_LMHEAD ? p.L : l, n < p.B ? n : -1);
@@ -1095,15 +1211,14 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
         }
         break;
       }
-      case OP_OPROJ: {
-        const int g = T[D_AUX];
+      case OP_OPROJ: {  // added into the layer accumulator (with the expert outputs)
         const int r0 = T[D_ROW0] + rlo;
         for (int e = 0; e < 2; ++e) {
           const int n = 2 * c + e;
           if (n >= p.B) continue;
-          float* out = p.opart + (((size_t)l * p.Hkv + g) * p.B + n) * p.d;
-          out[r0] = v[e];
-          out[r0 + 8] = v[2 + e];
+          float* out = p.moe + ((size_t)l * p.B + n) * p.d;
+          atomicAdd(out + r0, v[e]);
+          atomicAdd(out + r0 + 8, v[2 + e]);
         }
         break;
       }
@@ -1556,7 +1671,6 @@ __device__ void task_embed(const Params& p, const Smem& S, uint32_t& sseq, int t
     }
     const float x = bf16_to_f(p.embed[(size_t)t * p.d + k]);
     p.X[(size_t)b * p.d + k] = x;
-    p.moe[(size_t)b * p.d + k] = 0.f;
     const float xg = x * p.attn_norm[k];
     const uint16_t hi = to_bf16(xg);
     p.XG[(size_t)b * p.d + k] = hi;
@@ -1694,6 +1808,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x)
         if (i != p.c_done) *ctr_ptr(p, i) = 0u;
       for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
+      // the layer accumulators start the next step at zero (nothing reads them now)
+      float4* acc = reinterpret_cast<float4*>(p.moe);
+      const size_t n4 = (size_t)p.L * p.B * p.d / 4;
+      for (size_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (!p.fixed)
         for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.seq_lens[b] += 1;
       // the next step's epoch (never 0: freshly cleared words must not look current)

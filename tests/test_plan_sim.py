@@ -43,7 +43,7 @@ class Sim:
         I = self.I
         self.maxa, self.t_moe, self.qkv_tpg, self.n_router = I[3], I[5], I[10], I[11]
         (self.c_lr, self.c_qkvg, self.c_rt, self.c_rr, self.c_att, self.c_og, self.c_md,
-         self.c_rb) = I[16:24]
+         self.c_od) = I[16:24]
         self.nrb_d, self.L, self.Hkv = I[24], cfg["n_layers"], cfg["n_kv_heads"]
         self.c_oa = I[26]
         self.pending = [None] * n_sm   # a claimed O-proj tile waiting for its group
@@ -61,9 +61,6 @@ class Sim:
         if base in (self.c_qkvg, self.c_og):
             l, g = idx
             return base + l * self.Hkv + g
-        if base == self.c_rb:
-            l, r = idx
-            return self.c_rb + l * self.nrb_d + r
         return base + idx[0]
 
     def att_queue(self, l):
@@ -109,7 +106,7 @@ class Sim:
         if op in (OP_QKV, OP_ROUTER, OP_OPROJ, OP_LM, OP_RESID, OP_EMBED):
             if T[D_WAIT] >= 0 and not self.ready(T[D_WAIT], T[D_WAIT_T]):
                 return False
-            if op == OP_RESID and not self.ready(T[D_WAIT2], T[D_WAIT2_T]):
+            if T[D_WAIT2] >= 0 and not self.ready(T[D_WAIT2], T[D_WAIT2_T]):
                 return False
             # the layer's last router tile (D_AUX = 1) collects every tile's logits
             if op == OP_ROUTER and T[D_AUX] == 1 and self.ctr[T[D_SIG]] < T[D_SIG_T] - 1:
@@ -154,7 +151,8 @@ class Sim:
                 self.heads[("oproj", l)] += 1
                 self.pending[sm] = o_base + ho
                 return True
-            if not self.ready(self.c_rr + l, 1):   # the route words of the layer
+            # the route words of the layer, and the ADD_RMSNORM outputs (the items' operand)
+            if not self.ready(self.c_rr + l, 1) or not self.ready(self.c_lr + l, self.nrb_d):
                 return False
             h = self.heads[("moe", l)]
             if h < self.moe_count[l]:
