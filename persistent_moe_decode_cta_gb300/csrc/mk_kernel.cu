@@ -91,14 +91,41 @@ __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
 
 __device__ __forceinline__ unsigned* ctr_ptr(const Params& p, int ci) { return p.ctr + (size_t)ci * kCtrStride; }
 
+// Two counters polled in the same loop (one detection instead of two in sequence).
+__device__ bool wait_ge2(const Params& p, int c1, unsigned t1, int c2, unsigned t2, int task) {
+  if (c2 < 0) return wait_ge(p, c1, t1, task);
+  const unsigned* a = ctr_ptr(p, c1);
+  const unsigned* b = ctr_ptr(p, c2);
+  const uint64_t t0 = gtime();
+  unsigned ns = 32;
+  for (int it = 0;; ++it) {
+    const unsigned va = ld_relaxed(a), vb = ld_relaxed(b);
+    if (va >= t1 && vb >= t2) {
+      fence_acq_rel_gpu();
+      return true;
+    }
+    __nanosleep(ns);
+    ns = ns < 256 ? ns * 2 : 256;
+    if ((it & 7) == 7) {
+      if (aborted(p)) return false;
+      if ((long long)(gtime() - t0) > p.timeout_ns) {
+        if (va < t1) raise_err(p, MK_ERR_TIMEOUT, task, c1, (int)va, (int)t1);
+        else raise_err(p, MK_ERR_TIMEOUT, task, c2, (int)vb, (int)t2);
+        return false;
+      }
+    }
+  }
+}
+
 // Consumer-side wait: thread 0 polls, the others learn the result at a barrier.
-__device__ bool consumer_wait(const Params& p, const Smem& S, int ci, unsigned target, int task) {
+__device__ bool consumer_wait(const Params& p, const Smem& S, int ci, unsigned target, int task, int ci2 = -1,
+                              unsigned target2 = 0) {
   if (ci < 0) {
     trace_mark(p, S, 1);
     return true;
   }
   if (threadIdx.x == 0) {
-    S.small[0] = wait_ge(p, ci, target, task) ? 1 : 0;
+    S.small[0] = wait_ge2(p, ci, target, ci2, target2, task) ? 1 : 0;
     if (p.trace) trace_slots(S)[1] = gtime();
   }
   bar_sync_consumers();
@@ -527,8 +554,8 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
               }
             }
             __nanosleep(ns);
-            ns = ns < 256 ? ns * 2 : 256;
-            if ((it & 7) == 7) {
+            ns = ns < 64 ? ns * 2 : 64;
+            if ((it & 15) == 15) {
               if (aborted(p)) return false;
               if ((long long)(gtime() - t0) > p.timeout_ns) {
                 raise_err(p, MK_ERR_TIMEOUT, ti, -12, a, (int)ep);
@@ -866,7 +893,7 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     }
     if (!bar_or_consumers(stale)) break;
     if (tid == 0) __nanosleep(ns);
-    ns = ns < 256 ? ns * 2 : 256;
+    ns = ns < 64 ? ns * 2 : 64;
     if ((it & 7) == 7 && bar_or_consumers(tid == 0 && (aborted(p) || (long long)(gtime() - t0) > p.timeout_ns))) {
       if (tid == 0 && !aborted(p)) raise_err(p, MK_ERR_TIMEOUT, ti, -11, l, 0);
       return false;
@@ -882,20 +909,21 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
   // by 128-bit shared-memory reads; with few logits two threads split the range
   const int H = (2 * BE <= kConsumerThreads) ? 2 : 1;
   for (int t = tid; t < H * BE; t += kConsumerThreads) {
-    const int i = t % BE, h = t / BE;
-    const int b = i / E, e = i % E;
+    const int h = t >= BE ? 1 : 0, i = t - h * BE;
+    const int b = i / E, e = i - b * E;
     const float* r = lg + b * E;
     const float ve = r[e];
     const int f0 = h * (E / H), f1 = f0 + E / H;
-    int rank = 0;
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // independent counts (no serial add chain)
 #pragma unroll 4
     for (int f = f0; f < f1; f += 4) {
       const float4 q = *reinterpret_cast<const float4*>(r + f);
-      rank += (q.x > ve || (q.x == ve && f < e)) ? 1 : 0;
-      rank += (q.y > ve || (q.y == ve && f + 1 < e)) ? 1 : 0;
-      rank += (q.z > ve || (q.z == ve && f + 2 < e)) ? 1 : 0;
-      rank += (q.w > ve || (q.w == ve && f + 3 < e)) ? 1 : 0;
+      r0 += (q.x > ve || (q.x == ve && f < e)) ? 1 : 0;
+      r1 += (q.y > ve || (q.y == ve && f + 1 < e)) ? 1 : 0;
+      r2 += (q.z > ve || (q.z == ve && f + 2 < e)) ? 1 : 0;
+      r3 += (q.w > ve || (q.w == ve && f + 3 < e)) ? 1 : 0;
     }
+    const int rank = (r0 + r1) + (r2 + r3);
     if (H == 1) {
       if (rank < K) sel[b * K + rank] = e;
     } else {
@@ -922,45 +950,35 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     if (lane < K) wsel[b * K + lane] = w / sum;
   }
   trace_mark(p, S, 8);
+  // active experts (ascending id) and per active expert its tokens in ascending b, in
+  // parallel: a bitmap of the selected experts and per expert a mask of its tokens
   const int nsel = B * K;  // <= 64
-  if (warp == 0) {  // active experts (ascending id) and per active expert its tokens
-    for (int i = lane; i < nsel; i += 32) slot_of[sel[i]] = 1;  // mark used
-    __syncwarp();
-    const int per = (E + 31) / 32;
-    int cnt = 0;
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e < E && slot_of[e]) ++cnt;
+  unsigned* emask = reinterpret_cast<unsigned*>(slot_of);  // [E / 32] selected experts
+  unsigned* tmask = reinterpret_cast<unsigned*>(prk);      // [E] tokens per expert (ranks done)
+  if (tid < 8) emask[tid] = 0u;
+  for (int e = tid; e < E; e += kConsumerThreads) tmask[e] = 0u;
+  bar_sync_consumers();
+  if (tid < nsel) {
+    const int e = sel[tid];
+    atomicOr(&emask[e >> 5], 1u << (e & 31));
+    atomicOr(&tmask[e], 1u << (tid / K));
+  }
+  bar_sync_consumers();
+  if (tid < nsel) {
+    const int e = sel[tid], b = tid / K;
+    int slot = __popc(emask[e >> 5] & ((1u << (e & 31)) - 1u));
+    for (int w = 0; w < (e >> 5); ++w) slot += __popc(emask[w]);
+    const unsigned tm = tmask[e];
+    tok_s[slot * B + __popc(tm & ((1u << b) - 1u))] = b * 16 + (tid % K);
+    if ((tm & ((1u << b) - 1u)) == 0u) {  // the expert's first token fills its slot
+      act_s[slot] = e;
+      cnt_s[slot] = __popc(tm);
     }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    int slot = incl - cnt;
-    __syncwarp();
-    for (int i = 0; i < per; ++i) {
-      const int e = lane * per + i;
-      if (e < E && slot_of[e]) {
-        act_s[slot] = e;
-        cnt_s[slot] = 0;
-        slot_of[e] = slot + 1;  // 1-based; only this lane touches expert e here
-        ++slot;
-      }
-    }
-    __syncwarp();
-    // token lists in ascending (b, j): one pass per token (a token picks an expert once)
-    for (int b = 0; b < B; ++b) {
-      if (lane < K) {
-        const int a = slot_of[sel[b * K + lane]] - 1;
-        tok_s[a * B + cnt_s[a]] = b * 16 + lane;
-        ++cnt_s[a];
-      }
-      __syncwarp();
-    }
-    if (lane == 0) *tot_s = total;
+  }
+  if (tid == 0) {
+    int total = 0;
+    for (int w = 0; w < (E + 31) / 32; ++w) total += __popc(emask[w]);
+    *tot_s = total;
   }
   bar_sync_consumers();
   trace_mark(p, S, 9);
@@ -1096,8 +1114,8 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
   const bool reuse = key == have;
   if (reuse) {
     trace_mark(p, S, 1);
-  } else if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti) ||
-             !consumer_wait(p, S, T[D_WAIT2_CTR], (unsigned)T[D_WAIT2_TARGET], ti)) {
+  } else if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti, T[D_WAIT2_CTR],
+                            (unsigned)T[D_WAIT2_TARGET])) {
     drain_chunks(p, S, cseq, nch);
     return false;
   }
