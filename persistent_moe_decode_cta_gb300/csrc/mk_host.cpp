@@ -163,7 +163,7 @@ bool parse_wave_order(const char* s, std::vector<int>& order) {
 }
 
 int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, PlanOut& P, std::string* err,
-               bool prefetch = true) {
+               int prefetch = 0) {
   if (B < 1 || B > s.max_batch) return fail(err, MK_ERR_INVALID, "batch %d not in [1, %d]", B, s.max_batch);
   if (n_sm < 1) return fail(err, MK_ERR_INVALID, "n_sms %d", n_sm);
   P = PlanOut();
@@ -334,14 +334,23 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
           const int t = in[i];
           if (field(t, D_OP) != OP_ATT_DRAIN) { out.push_back(t); continue; }
           const int l = field(t, D_LAYER);
-          out.push_back(pf_kv[l]);
-          for (size_t j = i + 1; j < in.size() && field(in[j], D_LAYER) <= l; ++j)
-            if (field(in[j], D_OP) == OP_OPROJ) out.push_back(pf_of(in[j]));
-          out.push_back(t);
-          for (size_t j = i + 1; j < in.size() && field(in[j], D_LAYER) <= l + 1; ++j) {
-            const int op = field(in[j], D_OP);
-            if (field(in[j], D_LAYER) == l + 1 && (op == OP_QKV || op == OP_ROUTER)) out.push_back(pf_of(in[j]));
+          if (prefetch & 1) out.push_back(pf_kv[l]);
+          if (prefetch & 4) {  // this SM's share of the layer's O-proj weights (512-byte units)
+            const size_t units = s.o_layer_bytes / 512;
+            const size_t u0 = units * sm / n_sm, u1 = units * (sm + 1) / n_sm;
+            if (u1 > u0)
+              out.push_back(add(OP_PREFETCH, l, 0, 0, 0, 0, 0, -1, 0, -1, 0,
+                                s.off_o + l * s.o_layer_bytes + u0 * 512, (int)((u1 - u0) * 512), -1));
           }
+          if (prefetch & 2)
+            for (size_t j = i + 1; j < in.size() && field(in[j], D_LAYER) <= l; ++j)
+              if (field(in[j], D_OP) == OP_OPROJ) out.push_back(pf_of(in[j]));
+          out.push_back(t);
+          if (prefetch & 2)
+            for (size_t j = i + 1; j < in.size() && field(in[j], D_LAYER) <= l + 1; ++j) {
+              const int op = field(in[j], D_OP);
+              if (field(in[j], D_LAYER) == l + 1 && (op == OP_QKV || op == OP_ROUTER)) out.push_back(pf_of(in[j]));
+            }
         }
       }
     }
@@ -379,12 +388,15 @@ int choose_split_pages(int max_pages) {
   return std::max(8, sp);
 }
 
-// L2 prefetch entries in the megakernel's lists, off by default (MK_PREFETCH=1 adds
-// them): at batch 1 the step is bound by its dependency latencies rather than by HBM,
-// and the extra early traffic measured slightly slower.
-bool prefetch_enabled() {
+constexpr int kDefaultPrefetch = 0;
+
+// L2 prefetch entries in the megakernel's lists, as a bit mask (MK_PREFETCH): 1 = each
+// SM's share of the layer's cached K/V pages, 2 = the weights of the SM's own later
+// static tiles (next layer's QKV and router), 4 = each SM's share of the layer's O-proj
+// weights (the O-proj tiles are claimed later, from a queue).
+int prefetch_mask() {
   const char* e = getenv("MK_PREFETCH");
-  return e && e[0] == '1';
+  return e ? atoi(e) : kDefaultPrefetch;
 }
 
 // Router first: its weights are then prefetched behind the previous layer's tasks
@@ -623,7 +635,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
   std::vector<int> order;
   parse_wave_order(default_order(), order);
   PlanOut P;
-  r = build_plan(s, batch, n_sms, order, P, nullptr, prefetch_enabled());
+  r = build_plan(s, batch, n_sms, order, P, nullptr, prefetch_mask());
   if (r) return r;
   const int list_len = P.sm_off[n_sms];  // segment 0 only
   if (info_out) {
@@ -661,7 +673,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   const char* env = getenv("MK_WAVE_ORDER");
   if (!parse_wave_order(env && *env ? env : default_order(), order))
     return fail(&h->err, MK_ERR_INVALID, "bad wave order '%s'", env ? env : "");
-  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err, prefetch_enabled());
+  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err, prefetch_mask());
   if (r) return r;
   int occ = 0;
   megakernel_occupancy(&occ);
