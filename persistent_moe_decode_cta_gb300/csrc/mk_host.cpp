@@ -487,15 +487,27 @@ int encode_kv_map(mk_handle* h, CUtensorMap* tm, void* base) {
   if (!fn) return fail(&h->err, MK_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   const Shape& s = h->s;
   const cuuint64_t rows = (cuuint64_t)s.L * h->n_pages * s.Hkv * 16;
-  const int inner = s.hd < 64 ? s.hd : 64;
-  cuuint64_t dims[2] = {(cuuint64_t)s.hd, rows};
-  cuuint64_t strides[1] = {(cuuint64_t)s.hd * 2};
-  cuuint32_t box[2] = {(cuuint32_t)inner, 16};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  inner == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  // One box per (page, KV head): all 16 keys x head_dim.  A 128-byte swizzle span
+  // holds 64 bf16, so a 128-wide row is addressed as two 64-column halves (a 3-D map:
+  // column, half, row) and the box lands as 32 swizzled 128-byte lines, row-major.
+  CUresult r;
+  if (s.hd == 128) {
+    cuuint64_t dims[3] = {64, 2, rows};
+    cuuint64_t strides[2] = {128, (cuuint64_t)s.hd * 2};
+    cuuint32_t box[3] = {64, 2, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {(cuuint64_t)s.hd, rows};
+    cuuint64_t strides[1] = {(cuuint64_t)s.hd * 2};
+    cuuint32_t box[2] = {(cuuint32_t)s.hd, 16};
+    cuuint32_t estr[2] = {1, 1};
+    r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, s.hd == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return fail(&h->err, MK_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return MK_OK;
 }

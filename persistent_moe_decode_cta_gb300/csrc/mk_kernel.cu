@@ -390,12 +390,9 @@ __device__ void prefetch_kv_share(const Params& p, const Smem& S, int l) {
   }
 }
 
-// K pages then V pages of a split, 8 pages per ring stage.
+// K pages then V pages of a split, 8 pages per ring stage, one tensor-map copy per page.
 __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const CUtensorMap* tmK,
                          const CUtensorMap* tmV, int l, const AttItem& it, uint64_t pol, int task) {
-  const int inner = p.hd < 64 ? p.hd : 64;
-  const int nbox = p.hd / inner;
-  const int box_bytes = 16 * inner * 2;
   const int page_bytes = 16 * p.hd * 2;
   // page ids of the first chunk, then each chunk's ids are loaded (all 8 at once)
   // while the previous chunk's copies are issued
@@ -429,9 +426,12 @@ __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const C
       mbar_expect_tx(S.full(s), (uint32_t)(n * page_bytes));
       const uint32_t dst = S.stage(cseq);
       const CUtensorMap* tm = kv ? tmV : tmK;
-      for (int i = 0; i < n; ++i)
-        for (int j = 0; j < nbox; ++j)
-          tma_load_2d(dst + i * page_bytes + j * box_bytes, tm, j * inner, rows[i], S.full(s), pol);
+      for (int i = 0; i < n; ++i) {  // one box per page
+        if (p.hd == 128)
+          tma_load_3d(dst + i * page_bytes, tm, 0, 0, rows[i], S.full(s), pol);
+        else
+          tma_load_2d(dst + i * page_bytes, tm, 0, rows[i], S.full(s), pol);
+      }
       ++cseq;
     }
   }
@@ -1430,17 +1430,16 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
 
 // ============================================================== attention
 // Address of the 16-byte chunk `ch` (8 dims) of key row `key` inside a page of the
-// stage, laid out by the tensor-map copy with 128-byte (hd >= 64) or 64-byte (hd = 32)
-// swizzle: boxes of 16 keys x min(hd, 64) dims.
+// stage, as the tensor-map copy lays it out: 16 keys x hd dims, row-major, cut into
+// lines of min(hd, 64) dims (two lines a key at hd = 128), with the 128-byte swizzle
+// (hd >= 64: chunk ^= line % 8) or the 64-byte one (hd = 32: chunk ^= (line / 2) % 4).
 template <int HD>
 __device__ __forceinline__ uint32_t kv_addr(uint32_t page_base, int key, int ch) {
-  constexpr int kInner = HD < 64 ? HD : 64;
-  constexpr int kRowB = kInner * 2;
-  constexpr int kCpr = kRowB / 16;
-  constexpr int kBoxB = 16 * kRowB;
-  const int box = ch / kCpr, q = ch % kCpr;
-  const int swz = (kRowB == 128) ? (key & 7) : ((key >> 1) & 3);
-  return page_base + box * kBoxB + key * kRowB + ((q ^ swz) << 4);
+  constexpr int kLineB = (HD < 64 ? HD : 64) * 2;
+  constexpr int kCpl = kLineB / 16;
+  const int line = key * (HD * 2 / kLineB) + ch / kCpl;
+  const int swz = (kLineB == 128) ? (line & 7) : ((line >> 1) & 3);
+  return page_base + line * kLineB + (((ch % kCpl) ^ swz) << 4);
 }
 
 template <int HD>
