@@ -611,8 +611,15 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
                issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1, fl) &&
                issue_linear(p, S, cseq, src + gu_bytes, dn_bytes, pol, ti, cs2, fl);
         }
+        // after the expert queue empties: while the layer's attention outputs are
+        // incomplete a producer holds at most one O-proj tile (its weights land while
+        // it waits); the rest go to whichever SMs are free once they are complete,
+        // instead of queueing behind the first on the SMs that emptied the queue
+        bool held = false;
         while (ok && o_left) {
           if (!(ok = claim_gate(p, S, mseq, ti))) break;
+          if (held && !(ok = wait_ge(p, C_OA(p, l), (unsigned)(p.Hkv * p.B), ti))) break;
+          held = ld_relaxed(ctr_ptr(p, C_OA(p, l))) < (unsigned)(p.Hkv * p.B);
           claim_oproj();
         }
         break;
@@ -1599,48 +1606,67 @@ __device__ void attention_self(const Params& p, int l, const AttItem& it, int ta
 }
 
 // ATTN_COMBINE: log-sum-exp merge of the (ns + 1) partials of (b, g) -> o (bf16).
-// Warp h merges head h: lanes hold the items' (m, l) to form the weights, then every
-// lane accumulates HD/32 contiguous dims of each item's o with vector loads.
+// Warp h merges head h over batches of KB partials: lane t < KB loads partial t's
+// (m, l) and every lane its HD/32 dims of all KB partials' o, all loads of a batch in
+// flight together (one L2 round trip per batch); the running sums are rescaled to the
+// running maximum between batches (the split-softmax merge applied batch by batch).
 template <int HD>
 __device__ void attention_combine(const Params& p, int l, int b, int g, int ns) {
   constexpr int V = HD / 32;  // dims per lane: 4 (128), 2 (64), 1 (32)
+  constexpr int KB = 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gs = p.gs;
   const size_t stride = (size_t)gs * (HD + 2);
   const float* base = p.attp + ((size_t)l * p.Hkv * p.B * p.max_items_bg + (size_t)(g * p.B + b) * p.max_items_bg) * stride;
   const int n = ns + 1;
   for (int h = warp; h < gs; h += kConsumerWarps) {
-    float M = -INFINITY;
-    for (int s = lane; s < n; s += 32) M = fmaxf(M, ldg_cg(base + s * stride + gs * HD + h));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Ls = 0.f;
+    float M = -INFINITY, Ls = 0.f;
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    for (int s0 = 0; s0 < n; s0 += 32) {
-      const int s = s0 + lane;
-      float wgt = 0.f;
-      if (s < n) {
-        wgt = exp2f(ldg_cg(base + s * stride + gs * HD + h) - M);
-        Ls += wgt * ldg_cg(base + s * stride + gs * HD + gs + h);
+    for (int s0 = 0; s0 < n; s0 += KB) {
+      const int cnt = min(KB, n - s0);
+      const float* bs = base + (size_t)s0 * stride;
+      float mt = -INFINITY, lt = 0.f;
+      if (lane < cnt) {
+        mt = ldg_cg(bs + lane * stride + gs * HD + h);
+        lt = ldg_cg(bs + lane * stride + gs * HD + gs + h);
       }
-      const int cnt = min(32, n - s0);
-#pragma unroll 8
-      for (int t = 0; t < cnt; ++t) {
-        const float wt = __shfl_sync(0xffffffffu, wgt, t);
-        const float* o = base + (s0 + t) * stride + h * HD + lane * V;
-        if (V == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(o));
-          acc[0] += wt * x.x; acc[V > 1 ? 1 : 0] += wt * x.y;
-          acc[V > 2 ? 2 : 0] += wt * x.z; acc[V > 3 ? 3 : 0] += wt * x.w;
-        } else if (V == 2) {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(o));
-          acc[0] += wt * x.x; acc[V > 1 ? 1 : 0] += wt * x.y;
+      float x[KB][V];
+#pragma unroll
+      for (int t = 0; t < KB; ++t) {
+        const float* o = bs + t * stride + h * HD + lane * V;
+        if (t < cnt) {
+          if (V == 4) {
+            const float4 q = __ldcg(reinterpret_cast<const float4*>(o));
+            x[t][0] = q.x; x[t][V > 1 ? 1 : 0] = q.y; x[t][V > 2 ? 2 : 0] = q.z; x[t][V > 3 ? 3 : 0] = q.w;
+          } else if (V == 2) {
+            const float2 q = __ldcg(reinterpret_cast<const float2*>(o));
+            x[t][0] = q.x; x[t][V > 1 ? 1 : 0] = q.y;
+          } else {
+            x[t][0] = __ldcg(o);
+          }
         } else {
-          acc[0] += wt * __ldcg(o);
+#pragma unroll
+          for (int i = 0; i < V; ++i) x[t][i] = 0.f;
         }
       }
+      float mb = mt;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      const float Mn = fmaxf(M, mb);
+      const float sc = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+      const float w = (mt == -INFINITY) ? 0.f : exp2f(mt - Mn);
+      Ls = Ls * sc + w * lt;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] *= sc;
+#pragma unroll
+      for (int t = 0; t < KB; ++t) {
+        const float wt = __shfl_sync(0xffffffffu, w, t);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += wt * x[t][i];
+      }
+      M = Mn;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);

@@ -47,6 +47,7 @@ class Sim:
         self.nrb_d, self.L, self.Hkv = I[24], cfg["n_layers"], cfg["n_kv_heads"]
         self.c_oa = I[26]
         self.pending = [None] * n_sm   # a claimed O-proj tile waiting for its group
+        self.held = [None] * n_sm      # layer of an O-proj tile claimed before C_OA was full
         # queues
         self.att_items = {}
         self.moe_count = {}
@@ -143,8 +144,8 @@ class Sim:
             return True
         if op == OP_MOE:
             # the drain also serves the layer's O-proj tiles (D_KLEN from task D_K0): ahead
-            # of expert items once every attention output is complete, and all the
-            # remaining ones (waiting for their group if needed) once the items are gone
+            # of expert items once every attention output is complete, and the remaining
+            # ones once the items are gone
             n_o, o_base = T[D_KLEN], T[D_K0]
             ho = self.heads[("oproj", l)]
             if n_o and ho < n_o and self.ready(self.c_oa + l, self.Hkv * self.B):
@@ -160,6 +161,12 @@ class Sim:
                 self.ctr[self.c_md + l] += 1
                 return True
             if n_o and ho < n_o:
+                # while the layer's attention outputs are incomplete a drain holds at
+                # most one O-proj tile
+                full = self.Hkv * self.B
+                if self.held[sm] == l and not self.ready(self.c_oa + l, full):
+                    return False
+                self.held[sm] = l if self.ctr[self.c_oa + l] < full else None
                 self.heads[("oproj", l)] += 1
                 self.pending[sm] = o_base + ho
                 return True
