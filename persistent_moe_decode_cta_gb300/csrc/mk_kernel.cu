@@ -63,9 +63,10 @@ __device__ void trace_emit(const Params& p, const Smem& S, int op, int layer, in
 }
 
 // Spin until ctr >= target, bounded by the timeout and the abort flag.  Polls are
-// relaxed loads with a growing back-off (32 ns .. 256 ns) so that the many waiters
-// of a layer boundary do not saturate the counter's L2 line; the final observation
-// is followed by an acquire fence.
+// acquire loads with a growing back-off (32 ns .. 256 ns) so that the many waiters
+// of a layer boundary do not saturate the counter's L2 line.  The load that sees the
+// target is itself the acquire: no trailing fence, which would also wait for this
+// thread's unrelated earlier stores (the previous task's outputs) to drain.
 __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
   const unsigned* c = p.ctr + (size_t)ci * kCtrStride;
   if (ld_acquire(c) >= target) return true;
@@ -74,11 +75,8 @@ __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
   for (int it = 0;; ++it) {
     __nanosleep(ns);
     ns = ns < 256 ? ns * 2 : 256;
-    const unsigned v = ld_relaxed(c);
-    if (v >= target) {
-      fence_acq_rel_gpu();
-      return true;
-    }
+    const unsigned v = ld_acquire(c);
+    if (v >= target) return true;
     if ((it & 7) == 7) {
       if (aborted(p)) return false;
       if ((long long)(gtime() - t0) > p.timeout_ns) {
@@ -99,11 +97,8 @@ __device__ bool wait_ge2(const Params& p, int c1, unsigned t1, int c2, unsigned 
   const uint64_t t0 = gtime();
   unsigned ns = 32;
   for (int it = 0;; ++it) {
-    const unsigned va = ld_relaxed(a), vb = ld_relaxed(b);
-    if (va >= t1 && vb >= t2) {
-      fence_acq_rel_gpu();
-      return true;
-    }
+    const unsigned va = ld_acquire(a), vb = ld_acquire(b);
+    if (va >= t1 && vb >= t2) return true;
     __nanosleep(ns);
     ns = ns < 256 ? ns * 2 : 256;
     if ((it & 7) == 7) {
@@ -518,7 +513,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
           for (int it = 0;; ++it) {
             const bool sl = a >= 0 && a < maxa;
             const int as = sl ? a : 0;
-            const unsigned lr = lr_done ? lr_target : ld_relaxed(lr_ctr);
+            const unsigned lr = lr_done ? lr_target : ld_acquire(lr_ctr);  // acquire: the ADD_RMSNORM outputs
             uint64_t wn = 0, we = 0, wc = 0, wt[kMaxBatch], ww[kMaxBatch];
             ld_relaxed_u64_pred(wn, rw, nact < 0);
             ld_relaxed_u64_pred(we, rw + 1 + as, sl);
@@ -530,10 +525,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
               ld_relaxed_u64_pred(ww[n], rw + 1 + 2 * maxa + maxa * p.B + as * p.B + n, sl && n < p.B);
             }
             if (nact < 0 && (unsigned)(wn >> 32) == ep) nact = (int)(unsigned)wn;
-            if (!lr_done && lr >= lr_target) {
-              fence_acq_rel_gpu();  // acquire: the ADD_RMSNORM outputs are visible
-              lr_done = true;
-            }
+            if (!lr_done && lr >= lr_target) lr_done = true;
             if (nact >= 0 && lr_done) {
               if (!sl || a >= nact) return true;  // no such item
               const int c2 = (int)(unsigned)wc;
