@@ -949,6 +949,40 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     if (lane < K) wsel[b * K + lane] = w / sum;
   }
   trace_mark(p, S, 8);
+  if (B == 1) {
+    // one token: the active experts are its selection (maxa = top_k); warp 0 places
+    // each in its slot (the number of selected ids below it) and writes everything
+    if (warp == 0) {
+      __syncwarp();
+      const int maxa = p.maxa;
+      const int e = lane < K ? sel[lane] : 0x7fffffff;
+      int slot = 0;
+      for (int j = 0; j < K; ++j) slot += __shfl_sync(0xffffffffu, e, j) < e ? 1 : 0;
+      uint64_t* rw = p.rword + (size_t)l * p.rw_stride;
+      if (lane < K) {
+        const float w = wsel[lane];
+        rw[1 + 2 * maxa + slot] = tagged(ep, (unsigned)lane);  // token 0, selection rank
+        rw[1 + 2 * maxa + maxa + slot] = tagged(ep, __float_as_uint(w));
+        rw[1 + slot] = tagged(ep, (unsigned)e);
+        rw[1 + maxa + slot] = tagged(ep, 1u);
+        p.ridx[(size_t)l * K + lane] = e;
+        p.rw[(size_t)l * K + lane] = w;
+        p.active[l * maxa + slot] = e;
+        p.act_cnt[l * maxa + slot] = 1;
+        p.act_tok[(size_t)l * maxa + slot] = lane;
+      }
+      if (lane == 0) {
+        rw[0] = tagged(ep, (unsigned)K);
+        if (p.trace) trace_slots(S)[10] = gtime();
+        p.nact[l] = K;
+        p.qcount[p.L + l] = K * p.t_moe;
+        const unsigned pad = (unsigned)((maxa - K) * p.t_moe);
+        if (pad > 0) atomicAdd(ctr_ptr(p, C_MD(p, l)), pad);
+        if (p.trace) trace_slots(S)[11] = gtime();
+      }
+    }
+    return true;
+  }
   // active experts (ascending id) and per active expert its tokens in ascending b, in
   // parallel: a bitmap of the selected experts and per expert a mask of its tokens
   const int nsel = B * K;  // <= 64
