@@ -238,11 +238,13 @@ __device__ int att_item_count(const Params& p, const Smem& S, int l) {
 
 // Items are ordered by (group, sequence, split): group 0's items come first, in
 // step with the QKV tiles, which are dealt group by group.
+// Queue order: the KV groups interleaved (item = rem * Hkv + g), so that all groups'
+// splits are claimed, and their combines finish, at about the same time (the O-proj
+// tiles go ahead of expert items once every group is complete).
 __device__ AttItem att_decode(const Params& p, const Smem& S, int l, int item) {
-  const int per_g = att_item_count(p, S, l) / p.Hkv;
   AttItem it;
-  it.g = item / per_g;
-  int rem = item % per_g;
+  it.g = item % p.Hkv;
+  int rem = item / p.Hkv;
   for (int b = 0; b < p.B; ++b) {
     int pos, lo, fp, npg, ns;
     att_range(p, S, l, b, pos, lo, fp, npg, ns);

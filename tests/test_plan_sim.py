@@ -66,12 +66,12 @@ class Sim:
 
     def att_queue(self, l):
         if l not in self.att_items:
-            items = []
-            for g in range(self.Hkv):
-                for b in range(self.B):
-                    ns = att_splits(self.cfg, l, self.seq[b], self.split_pages)
-                    items += [(g, b, s, ns) for s in range(ns + 1)]
-            self.att_items[l] = items
+            per_g = []
+            for b in range(self.B):
+                ns = att_splits(self.cfg, l, self.seq[b], self.split_pages)
+                per_g += [(b, s, ns) for s in range(ns + 1)]
+            # the kernel's queue order: KV groups interleaved
+            self.att_items[l] = [(g, b, s, ns) for (b, s, ns) in per_g for g in range(self.Hkv)]
         return self.att_items[l]
 
     def route(self, l):
