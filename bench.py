@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--no-bs8", action="store_true", help="skip the batch-8 ragged measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--multistep", type=int, default=16,
+                    help="also time greedy decode with this many steps per launch (tokens fed "
+                         "back on the device); 0 skips it")
     ap.add_argument("--trace", default="",
                     help="after timing, record one step's task timeline and write a per-opcode "
                          "summary (JSON) to this path")
@@ -434,6 +437,41 @@ def main():
         barrier(ws)
         line["e2e"] = {"value": ws * B * args.steps / el, "unit": UNIT,
                        "h2d_bytes_per_step": B * 4, "d2h_bytes_per_step": B * cfg["vocab"] * 4}
+
+    # ---- greedy multi-step decode: n steps per launch, each step's token fed to the next
+    # on the device (fixed positions, as above, so every step moves the same bytes)
+    if args.multistep > 0 and args.mode == "mega":
+        n = args.multistep
+        tok_out = torch.empty(n, B, dtype=torch.int32, device=device)
+
+        def step_multi():
+            mk.steps(st["tokens"], n, st["k"], st["v"], st["logits"], tok_out)
+
+        k2 = max(3, args.steps // n)
+        t, _ = time_device(step_multi, k2, 2, ws, stream)
+        t = max_over_ranks(t, ws, device)
+        if mk.status()["code"] != 0:
+            raise RuntimeError("device error in the multi-step arm")
+        ms = {"steps_per_launch": n, "launches": k2, "value": ws * B * n * k2 / t, "unit": UNIT,
+              "ms_per_step": t / (n * k2) * 1e3}
+        if not args.no_e2e:
+            # end to end: host tokens in and the n greedy tokens back, once per launch
+            tok_h = st["tokens"].cpu().pin_memory()
+            out_h = torch.empty(n, B, dtype=torch.int32).pin_memory()
+            tok_d = torch.empty_like(st["tokens"])
+            barrier(ws)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(k2):
+                tok_d.copy_(tok_h, non_blocking=True)
+                mk.steps(tok_d, n, st["k"], st["v"], st["logits"], tok_out)
+                out_h.copy_(tok_out, non_blocking=True)
+                torch.cuda.synchronize()
+            el = max_over_ranks(time.perf_counter() - t0, ws, device)
+            barrier(ws)
+            ms["e2e"] = {"value": ws * B * n * k2 / el, "unit": UNIT, "h2d_bytes_per_launch": B * 4,
+                         "d2h_bytes_per_launch": n * B * 4}
+        line["multistep"] = ms
 
     if args.trace:
         line["trace"] = task_trace_summary(mk, st, args.trace)

@@ -28,7 +28,7 @@ MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT =
  MK_Q_NUM_STAGES) = range(1, 12)
 
 # exported symbols (kept equal to the declarations of include/mk.h)
-EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_step_host", "mk_decode_step_noalloc",
+EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_decode_step_noalloc",
            "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace",
            "mk_plan_drop_signal", "mk_read", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                               ctypes.POINTER(H)]
     lib.mk_plan.argtypes = [H, i32, ctypes.POINTER(ctypes.c_int32), vp, i32, i32]
     lib.mk_decode_step.argtypes = [H, vp, vp, vp, vp, vp]
+    lib.mk_decode_steps.argtypes = [H, vp, i32, vp, vp, vp, vp, vp]
     lib.mk_decode_step_host.argtypes = [H, vp, vp, vp, vp, vp]
     lib.mk_decode_step_noalloc.argtypes = [H, vp, vp, vp, vp, vp]
     lib.mk_decode_step_perop.argtypes = [H, vp, vp, vp, vp, vp, i32]
@@ -181,6 +182,13 @@ def mk_decode_step(h, tokens, k_cache, v_cache, logits, stream=None):
                                          _stream_ptr(stream)), h)
 
 
+def mk_decode_steps(h, tokens, n_steps, k_cache, v_cache, logits, tokens_out, stream=None):
+    """n_steps greedy steps in one launch; tokens_out: device int32 [n_steps, batch]."""
+    _check(load_library().mk_decode_steps(h, tokens.data_ptr(), int(n_steps), k_cache.data_ptr(),
+                                          v_cache.data_ptr(), logits.data_ptr(), tokens_out.data_ptr(),
+                                          _stream_ptr(stream)), h)
+
+
 def mk_decode_step_noalloc(h, tokens, k_cache, v_cache, logits, stream=None):
     """mk_decode_step with the step scratch in the library's static device buffer."""
     _check(load_library().mk_decode_step_noalloc(h, tokens.data_ptr(), k_cache.data_ptr(),
@@ -276,6 +284,15 @@ class Megakernel:
 
     def step(self, tokens, k_cache, v_cache, logits, stream=None):
         mk_decode_step(self.h, tokens, k_cache, v_cache, logits, stream)
+
+    def steps(self, tokens, n_steps, k_cache, v_cache, logits, tokens_out=None, stream=None):
+        """n_steps greedy decode steps in one launch (device-side token feedback).
+        Returns the int32 [n_steps, batch] tensor of each step's greedy token."""
+        import torch
+        if tokens_out is None:
+            tokens_out = torch.empty(n_steps, tokens.shape[0], dtype=torch.int32, device=tokens.device)
+        mk_decode_steps(self.h, tokens, n_steps, k_cache, v_cache, logits, tokens_out, stream)
+        return tokens_out
 
     def step_host(self, tokens_host, k_cache, v_cache, logits_host, stream=None):
         mk_decode_step_host(self.h, tokens_host, k_cache, v_cache, logits_host, stream)

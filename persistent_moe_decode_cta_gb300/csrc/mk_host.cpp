@@ -711,6 +711,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.moe_fs = s.moe_fs; p.t_moe = s.t_moe; p.qkv_tpg = s.qkv_tpg;
   p.n_router_tasks = s.n_router_tasks;
   p.timeout_ns = (long long)h->cfg.timeout_ms * 1000000ll;
+  p.n_steps = 1; p.tok_out = nullptr;  // one step, no greedy tokens (mk_decode_steps sets both)
   p.inflight = 2;
   if (const char* fl = getenv("MK_INFLIGHT")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight = v; }
   p.inflight_moe = p.inflight;
@@ -745,6 +746,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(p.qhead, (size_t)3 * L);
   AL(p.qcount, (size_t)3 * L);
   AL(p.err, 16);
+  AL(p.amax, (size_t)kAmaxReplicas * B);
+  AL(p.gen, 2);
   AL(h->d_tasks, P.tasks.size());
   AL(h->d_sm_off, P.sm_off.size());
   AL(h->d_sm_list, P.sm_list.size());
@@ -775,6 +778,25 @@ int mk_decode_step(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   return launch_segment(h, 0, true, true, st);
+}
+
+int mk_decode_steps(mk_handle* h, const int32_t* tokens_dev, int n_steps, void* k_cache, void* v_cache,
+                    float* logits_dev, int32_t* tokens_out_dev, void* stream) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (n_steps < 1 || n_steps > 4096) return fail(&h->err, MK_ERR_INVALID, "n_steps %d not in [1, 4096]", n_steps);
+  if (!tokens_out_dev) return fail(&h->err, MK_ERR_INVALID, "tokens_out is NULL");
+  int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
+  if (r) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  Params p = h->prm;
+  p.sm_off = h->d_sm_off;  // the megakernel segment
+  p.do_reset = 1;
+  p.n_steps = n_steps;
+  p.tok_out = tokens_out_dev;
+  cudaError_t e = launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
+  if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch (multi-step)");
+  return MK_OK;
 }
 
 // The step's scratch buffers (everything mk_plan allocates per step except the plan

@@ -53,6 +53,10 @@ constexpr int kCtrStride = 32;
 // (every consumer of the normed input reads all of them).
 constexpr int kSsStride = 32;
 constexpr int kMaxBatch = 8;
+// Replicas of the per-token greedy-argmax key (multi-step decode): the LM head tiles
+// of a step add into replica (SM index mod kAmaxReplicas) so that ~2400 tiles do not
+// serialise on one word; the step's last CTA reduces them.
+constexpr int kAmaxReplicas = 32;
 constexpr int kMaxActive = kMaxBatch * 8;     // active experts per layer <= batch * top_k
 constexpr int kRowBlock = 128;                // residual row block (rows of d_model)
 // j-groups per ring chunk of a GEMV tile with `nrb` 16-row blocks (chunk = jpc*nrb*4 KB)
@@ -112,6 +116,12 @@ struct Params {
   int fixed, do_reset;
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   int inflight_moe;         // the same for the chunks of expert items
+  // multi-step decode: n_steps steps per launch, each step's greedy token (argmax of its
+  // logits, lowest index on ties) written to tok_out[step][B] and fed to the next step
+  int n_steps;
+  int32_t* tok_out;               // [n_steps][B] or null (then no argmax)
+  unsigned long long* amax;       // [kAmaxReplicas][B] (value key << 32 | ~row), zero between steps
+  unsigned* gen;                  // step generation word of the grid barrier between steps
   // weights
   const uint8_t* wblob;
   long long off_moe, moe_item_bytes;  // item (l, e, s) at off_moe + ((l*E + e)*t_moe + s) * item_bytes

@@ -89,6 +89,14 @@ __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
 
 __device__ __forceinline__ unsigned* ctr_ptr(const Params& p, int ci) { return p.ctr + (size_t)ci * kCtrStride; }
 
+// Greedy-token key: larger for a larger logit, then for a lower row (ties go to the
+// lowest index); -0 and +0 compare equal; 0 is below every key of a real logit.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
+  const unsigned u = __float_as_uint(v + 0.f);
+  const unsigned k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)k << 32) | (unsigned)~(unsigned)row;
+}
+
 // Two counters polled in the same loop (one detection instead of two in sequence).
 __device__ bool wait_ge2(const Params& p, int c1, unsigned t1, int c2, unsigned t2, int task) {
   if (c2 < 0) return wait_ge(p, c1, t1, task);
@@ -1284,6 +1292,26 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
           if (r0 < p.V) out[r0] = v[e];
           if (r0 + 8 < p.V) out[r0 + 8] = v[2 + e];
         }
+        if (p.tok_out) {
+          // greedy token: the tile's best (value, lowest row) per token over the 8 lanes
+          // of a row group, then one max into this SM's replica of the step's key
+          unsigned long long best[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const unsigned long long k0 = r0 < p.V ? argmax_key(v[e], r0) : 0ull;
+            const unsigned long long k1 = r0 + 8 < p.V ? argmax_key(v[2 + e], r0 + 8) : 0ull;
+            best[e] = k0 > k1 ? k0 : k1;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              const unsigned long long x = __shfl_xor_sync(0xffffffffu, best[e], o);
+              best[e] = x > best[e] ? x : best[e];
+            }
+          }
+          if (g8 == 0)
+            for (int e = 0; e < 2; ++e)
+              if (2 * c + e < p.B)
+                atomicMax(p.amax + (size_t)(blockIdx.x % kAmaxReplicas) * p.B + 2 * c + e, best[e]);
+        }
         break;
       }
       default:
@@ -1735,7 +1763,10 @@ __device__ void task_embed(const Params& p, const Smem& S, uint32_t& sseq, int t
   const int tid = threadIdx.x;
   for (int i = tid; i < p.B * p.d; i += kConsumerThreads) {
     const int b = i / p.d, k = i % p.d;
-    int t = p.tokens[b];
+    // step 0 reads the caller's tokens, later steps (multi-step decode) the previous
+    // step's greedy tokens
+    const int step = S.small[249];
+    int t = step == 0 ? p.tokens[b] : ld_volatile(p.tok_out + (size_t)(step - 1) * p.B + b);
     if (t < 0 || t >= p.V) {
       if (k == 0) raise_err(p, MK_ERR_BAD_TOKEN, ti, -1, t, b);
       t = 0;
@@ -1838,64 +1869,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t smem_raw[];
   const Smem S = carve_smem(smem_raw);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(S.full(s), 1);
-      mbar_init(S.empty(s), kConsumerWarps);
-    }
-    for (int m = 0; m < kMbox; ++m) {
-      mbar_init(S.mfull(m), 1);
-      mbar_init(S.mempty(m), 1);
-    }
-    for (int q = 0; q < kSq; ++q) {
-      mbar_init(S.sfull(q), kConsumerWarps);
-      mbar_init(S.sempty(q), 1);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (threadIdx.x < p.B) S.small[224 + threadIdx.x] = p.seq_lens[threadIdx.x];
-  if (threadIdx.x == 0) S.small[248] = (int)ld_volatile(reinterpret_cast<const int*>(p.epoch));
-  __syncthreads();
-  const int warp = threadIdx.x >> 5;
-  if (warp == kProducerWarp) {
-    if ((threadIdx.x & 31) == 0) producer(p, S, &tmK, &tmV);
-  } else if (warp == kStorerWarp) {
-    if ((threadIdx.x & 31) == 0) storer(p, S);
-  } else {
-    consumer(p, S);
-  }
-  __syncthreads();
-  // last CTA out resets the counters and queues for the next launch
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atom_add_acq_rel(ctr_ptr(p, p.c_done), 1u);
-    S.small[2] = (old == gridDim.x - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (S.small[2]) {
-    __threadfence();
-    if (p.do_reset) {
-      for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x)
-        if (i != p.c_done) *ctr_ptr(p, i) = 0u;
-      for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
-      // the layer accumulators start the next step at zero (nothing reads them now)
-      float4* acc = reinterpret_cast<float4*>(p.moe);
-      const size_t n4 = (size_t)p.L * p.B * p.d / 4;
-      for (size_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!p.fixed)
-        for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.seq_lens[b] += 1;
-      // the next step's epoch (never 0: freshly cleared words must not look current)
-      if (threadIdx.x == 0) {
-        const unsigned ep = step_epoch(S) + 1u;
-        *p.epoch = ep ? ep : 1u;
+  // multi-step decode: the generation word of the grid barrier between steps, read
+  // before any CTA can advance it (the first advance waits for every CTA's arrival)
+  if (threadIdx.x == 0 && p.n_steps > 1) S.small[250] = (int)ld_volatile(reinterpret_cast<const int*>(p.gen));
+  for (int step = 0; step < p.n_steps; ++step) {
+    if (threadIdx.x == 0) {  // (re)initialised per step: no copy or arrival is pending here
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(S.full(s), 1);
+        mbar_init(S.empty(s), kConsumerWarps);
       }
+      for (int m = 0; m < kMbox; ++m) {
+        mbar_init(S.mfull(m), 1);
+        mbar_init(S.mempty(m), 1);
+      }
+      for (int q = 0; q < kSq; ++q) {
+        mbar_init(S.sfull(q), kConsumerWarps);
+        mbar_init(S.sempty(q), 1);
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (threadIdx.x < p.B) S.small[224 + threadIdx.x] = ld_volatile(p.seq_lens + threadIdx.x);
+    if (threadIdx.x == 0) {
+      S.small[248] = (int)ld_volatile(reinterpret_cast<const int*>(p.epoch));
+      S.small[249] = step;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      *ctr_ptr(p, p.c_done) = 0u;
-      __threadfence();
+    const int warp = threadIdx.x >> 5;
+    if (warp == kProducerWarp) {
+      if ((threadIdx.x & 31) == 0) producer(p, S, &tmK, &tmV);
+    } else if (warp == kStorerWarp) {
+      if ((threadIdx.x & 31) == 0) storer(p, S);
+    } else {
+      consumer(p, S);
     }
+    __syncthreads();
+    // last CTA out resets the counters and queues for the next step or launch
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned old = atom_add_acq_rel(ctr_ptr(p, p.c_done), 1u);
+      S.small[2] = (old == gridDim.x - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    const bool more = step + 1 < p.n_steps;
+    if (S.small[2]) {
+      __threadfence();
+      if (p.tok_out && threadIdx.x < p.B) {
+        // the step's greedy tokens from the replicas of the argmax key
+        const int b = threadIdx.x;
+        unsigned long long best = 0ull;
+        for (int r = 0; r < kAmaxReplicas; ++r) {
+          const unsigned long long k = p.amax[(size_t)r * p.B + b];
+          best = k > best ? k : best;
+          p.amax[(size_t)r * p.B + b] = 0ull;
+        }
+        p.tok_out[(size_t)step * p.B + b] = best ? (int)~(unsigned)best : 0;
+      }
+      if (p.do_reset) {
+        for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x)
+          if (i != p.c_done) *ctr_ptr(p, i) = 0u;
+        for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
+        // the layer accumulators start the next step at zero (nothing reads them now)
+        float4* acc = reinterpret_cast<float4*>(p.moe);
+        const size_t n4 = (size_t)p.L * p.B * p.d / 4;
+        for (size_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!p.fixed)
+          for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.seq_lens[b] += 1;
+        // the next step's epoch (never 0: freshly cleared words must not look current)
+        if (threadIdx.x == 0) {
+          const unsigned ep = step_epoch(S) + 1u;
+          *p.epoch = ep ? ep : 1u;
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        *ctr_ptr(p, p.c_done) = 0u;
+        __threadfence();
+        if (more) {  // release the next step (and say whether to stop)
+          p.gen[1] = aborted(p) ? 1u : 0u;
+          __threadfence();
+          st_release(p.gen, (unsigned)S.small[250] + (unsigned)step + 1u);
+        }
+      }
+    }
+    if (!more) break;
+    if (threadIdx.x == 0) {
+      // grid barrier: wait (bounded) for the last CTA of this step
+      const unsigned target = (unsigned)S.small[250] + (unsigned)step + 1u;
+      const uint64_t t0 = gtime();
+      bool stop = false;
+      while ((int)(ld_acquire(p.gen) - target) < 0) {
+        __nanosleep(256);
+        if ((long long)(gtime() - t0) > p.timeout_ns) {
+          raise_err(p, MK_ERR_TIMEOUT, -20, -1, (int)ld_acquire(p.gen), (int)target);
+          stop = true;
+          break;
+        }
+      }
+      S.small[251] = (stop || ld_volatile(reinterpret_cast<const int*>(p.gen + 1)) != 0) ? 1 : 0;
+    }
+    __syncthreads();
+    if (S.small[251]) break;
   }
 }
 
