@@ -47,6 +47,10 @@ def parse_args():
     ap.add_argument("--no-bs8", action="store_true", help="skip the batch-8 ragged measurement")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ablate-orders", default="",
+                    help="comma-separated wave orders (letters r q a m o x: router, QKV, "
+                         "attention, MoE items, O-proj, ADD_RMSNORM) to time one after another "
+                         "on the same buffers, e.g. rqamox,qramox,rqaomx")
     ap.add_argument("--multistep", type=int, default=16,
                     help="also time greedy decode with this many steps per launch (tokens fed "
                          "back on the device); 0 skips it")
@@ -472,6 +476,25 @@ def main():
             ms["e2e"] = {"value": ws * B * n * k2 / el, "unit": UNIT, "h2d_bytes_per_launch": B * 4,
                          "d2h_bytes_per_launch": n * B * 4}
         line["multistep"] = ms
+
+    # ---- wave-order ablation: the same step re-planned with each order (the order is a
+    # plan-time property of the per-SM lists; outputs do not depend on it)
+    if args.ablate_orders and args.mode == "mega":
+        abl = {}
+        k2 = max(5, args.steps // 4)
+        for order in [o for o in args.ablate_orders.split(",") if o]:
+            os.environ["MK_WAVE_ORDER"] = order
+            mk.plan(st["seq"], st["pt"], st["npages"])
+            mk.set_fixed(True)
+            t, _ = time_device(step_mega, k2, 2, ws, stream)
+            t = max_over_ranks(t, ws, device)
+            if mk.status()["code"] != 0:
+                raise RuntimeError(f"device error with wave order {order}")
+            abl[order] = {"value": ws * B * k2 / t, "ms_per_step": t / k2 * 1e3}
+        os.environ.pop("MK_WAVE_ORDER", None)
+        mk.plan(st["seq"], st["pt"], st["npages"])
+        mk.set_fixed(True)
+        line["wave_order_ablation"] = abl
 
     if args.trace:
         line["trace"] = task_trace_summary(mk, st, args.trace)
