@@ -29,7 +29,9 @@ rotate-half RoPE with inv_freq_i = theta^(-2i/hd) over the full head; cached K i
 already rotated; the new token sits at position L_b and attends to itself; the
 attention window of a sliding-window layer is {j : p - W < j <= p}; q head i uses
 KV head floor(i * Hkv / Hq); top-k ties go to the lower expert index; argmax ties
-to the lower token id; norm gains multiply after the normalisation.
+to the lower token id; norm gains multiply after the normalisation; a dense layer of
+a mixed stack (cfg["dense_layers"]) replaces the routed experts by one SwiGLU FFN of
+width cfg["dense_ff"] applied to every token with weight 1, sharing the layer's pre-norm.
 
 Parity status: every building block below is pinned by tests/test_oracle_pins.py
 (closed forms, invariants, special cases, library routines for bf16 rounding and
@@ -203,9 +205,9 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
     k_top, eps, theta = cfg["top_k"], cfg["rms_eps"], cfg["rope_theta"]
     window = cfg["sliding_window"] if l in tuple(cfg.get("swa_layers", ())) else 0
 
+    dense = l in tuple(cfg.get("dense_layers", ()))
     g = bf16_to_f64(W.attn_norm(l))
-    Wq, Wk, Wv, Wo, Wr = (_mat(W.wq(l)), _mat(W.wk(l)), _mat(W.wv(l)), _mat(W.wo(l)),
-                          _mat(W.router(l)))
+    Wq, Wk, Wv, Wo = (_mat(W.wq(l)), _mat(W.wk(l)), _mat(W.wv(l)), _mat(W.wo(l)))
     h = rms_norm(x, g, eps)                                   # [B, d]
 
     info = dict(router_logits=np.empty((B, cfg["n_experts"])), idx=[], w=[], margin=[],
@@ -235,6 +237,20 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
         o = attention(q, keys, vals)
         attn_out[b] = Wo @ o.reshape(-1)
 
+    if dense:
+        # a dense layer of a mixed stack: one SwiGLU FFN for every token, no router
+        # [Cohere open-sources fused LLM decode kernel with 1.58x vLLM claim: the dense
+        # GEMM task types FFN_UPGATE_ACT and FFN_DOWN]
+        wg, wu, wd = (_mat(a) for a in W.dense_ffn(l))
+        ffn_out = np.stack([swiglu_expert(h[b], wg, wu, wd) for b in range(B)])
+        info["router_logits"] = None
+        info["experts"] = {}
+        info["idx"] = np.zeros((B, 0), dtype=np.int64)
+        info["w"] = np.zeros((B, 0))
+        info["margin"] = np.full(B, np.inf)
+        return x + attn_out + ffn_out, info
+
+    Wr = _mat(W.router(l))
     r = h @ Wr.T                                              # [B, E]
     info["router_logits"][:] = r
     moe_out = np.zeros((B, d))

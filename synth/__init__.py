@@ -33,6 +33,10 @@ MODELS = {
                   n_experts=128, top_k=8, d_ff=768, vocab=151936, rope_theta=1e6,
                   rms_eps=1e-6, sliding_window=0, swa_layers=()),
 }
+# Mixed dense/MoE stacks (a dense layer: one SwiGLU FFN of width dense_ff for every
+# token, no router): the tiny and small parity models with some layers dense.
+MODELS["tiny_dense"] = dict(MODELS["tiny"], dense_layers=(0,), dense_ff=256)
+MODELS["small_dense"] = dict(MODELS["small"], dense_layers=(0, 5), dense_ff=1024)
 # Two layers of the pages-scale shape: small enough (3.7 GB) for profiler captures
 # and for the oracle to run in seconds, with every tile size of the full model.
 MODELS["pages_l2"] = dict(MODELS["pages"], n_layers=2)
@@ -50,6 +54,8 @@ WORKLOADS = {
     "pages_l1_b1_8k": dict(model="pages_l1", batch=1, lens=("fixed", 8192)),
     "pages_l2_b8_ragged_swa": dict(model="pages_l2", batch=8, lens=("uniform", 1024, 32768),
                                    sliding_window=4096, swa="odd"),
+    "tiny_dense_b1_64": dict(model="tiny_dense", batch=1, lens=("fixed", 64)),
+    "small_dense_b1_2k": dict(model="small_dense", batch=1, lens=("fixed", 2048)),
 }
 
 
@@ -130,6 +136,16 @@ def make_weights(cfg: dict, seed: int = 0, device="cpu", gain_jitter: float = 0.
         return g.to(bf)
     W["attn_norm"] = gains("attn_norm", (L, d))
     W["final_norm"] = gains("final_norm", (d,))
+    dense = tuple(cfg.get("dense_layers", ()))
+    if dense:
+        # the dense FFNs of a mixed stack: ffn_gate/ffn_up [L, Fd, d], ffn_down [L, d, Fd]
+        # (drawn for the dense layers, zero elsewhere)
+        fd = cfg["dense_ff"]
+        for name, shp in (("ffn_gate", (fd, d)), ("ffn_up", (fd, d)), ("ffn_down", (d, fd))):
+            t = torch.zeros((L,) + shp, dtype=bf, device=device)
+            for l in dense:
+                t[l].normal_(0.0, std, generator=_gen(device, seed, name, l))
+            W[name] = t
     return W
 
 
@@ -209,6 +225,9 @@ class HostWeights:
     def expert(self, l, e):
         return (_u16(self.W["w_gate"][l, e]), _u16(self.W["w_up"][l, e]),
                 _u16(self.W["w_down"][l, e]))
+
+    def dense_ffn(self, l):
+        return (_u16(self.W["ffn_gate"][l]), _u16(self.W["ffn_up"][l]), _u16(self.W["ffn_down"][l]))
 
     def final_norm(self): return self._get(("fn",), lambda: _u16(self.W["final_norm"]))
     def lm_head(self): return self._get(("lm",), lambda: _u16(self.W["lm_head"]))

@@ -225,6 +225,28 @@ def test_all_experts_with_identical_weights_equal_dense_swiglu():
         assert sorted(info["idx"][b]) == [0, 1, 2, 3]
 
 
+def test_dense_layer_equals_moe_layer_of_identical_experts():
+    """A dense layer of a mixed stack (one SwiGLU FFN for every token) equals an MoE
+    layer whose experts are all copies of that FFN, whatever the routing (the weights
+    sum to 1); the dense layer does not use the router."""
+    cfg = dict(TINY, top_k=2)
+    W, pt, k, v = _setup(cfg)
+    for name in ("w_gate", "w_up", "w_down"):
+        W[name][:, 1:] = W[name][:, :1]
+    dcfg = dict(cfg, dense_layers=(0,), dense_ff=cfg["d_ff"])
+    Wd = dict(W, ffn_gate=W["w_gate"][:, 0].clone(), ffn_up=W["w_up"][:, 0].clone(),
+              ffn_down=W["w_down"][:, 0].clone(), router=torch.zeros_like(W["router"]))
+    x = _x(2, 32)
+    kv = synth.HostKV(k, v)
+    y_moe, _ = O.layer_step(cfg, synth.HostWeights(W), kv, 0, x, [37, 5], pt)
+    y_dense, info = O.layer_step(dcfg, synth.HostWeights(Wd), kv, 0, x, [37, 5], pt)
+    assert np.allclose(y_dense, y_moe, atol=1e-13)
+    assert info["experts"] == {} and info["idx"].shape == (2, 0)
+    # layer 1 of the same stack is still routed
+    _, info1 = O.layer_step(dcfg, synth.HostWeights(Wd), kv, 1, x, [37, 5], pt)
+    assert info1["idx"].shape == (2, 2)
+
+
 def test_first_token_attends_only_to_itself():
     W, pt, k, v = _setup(lens=(0,))
     W["w_down"] = torch.zeros_like(W["w_down"])
