@@ -51,7 +51,12 @@ typedef enum mk_status {
  * n_experts a multiple of 8 in [8, 256]; top_k <= 8; page_size == 16; max_batch <= 8; n_layers <= 64.
  * swa_layer_mask bit l set = layer l uses a sliding window of sliding_window keys
  * (the window holds the new token and the sliding_window - 1 keys before it).
- * timeout_ms bounds every dependency wait inside the kernel (0 = 2000 ms). */
+ * timeout_ms bounds every dependency wait inside the kernel (0 = 2000 ms).
+ * dense_layer_mask bit l set = layer l is dense (a mixed dense/MoE stack): one SwiGLU
+ * FFN of width dense_ff (a multiple of 128, <= 4096) for every token, no router, in
+ * place of the routed experts; 0 = every layer routed (dense_ff ignored).
+ * [Cohere open-sources fused LLM decode kernel with 1.58x vLLM claim: the dense GEMM
+ * task types FFN_UPGATE_ACT and FFN_DOWN] */
 typedef struct mk_config {
   int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim;
   int32_t n_experts, top_k, d_ff, vocab, page_size, max_batch;
@@ -59,6 +64,8 @@ typedef struct mk_config {
   uint64_t swa_layer_mask;
   float rope_theta, rms_eps;
   int32_t timeout_ms;
+  uint64_t dense_layer_mask;
+  int32_t dense_ff;
 } mk_config;
 
 /* Model weights, all bf16 DEVICE pointers, row-major [out][in]:
@@ -68,8 +75,11 @@ typedef struct mk_config {
  *   wq[l] [Hq*hd][d]   wk[l], wv[l] [Hkv*hd][d]       wo[l] [d][Hq*hd]
  *   router[l]          [n_experts][d]
  *   w_gate[l*E+e], w_up[l*E+e] [d_ff][d];  w_down[l*E+e] [d][d_ff]
- * The arrays of pointers are HOST arrays.  mk_create copies everything into a
- * handle-owned packed blob, so the caller may free its tensors afterwards. */
+ *   ffn_gate[l], ffn_up[l] [dense_ff][d];  ffn_down[l] [d][dense_ff]  (dense layers)
+ * The arrays of pointers are HOST arrays.  On a dense layer router[l] and the
+ * layer's expert pointers may be NULL; ffn_* may be NULL (the arrays themselves too)
+ * when no layer is dense.  mk_create copies everything into a handle-owned packed
+ * blob, so the caller may free its tensors afterwards. */
 typedef struct mk_weights {
   const void* embed;
   const void* lm_head;
@@ -83,6 +93,9 @@ typedef struct mk_weights {
   const void* const* w_gate;
   const void* const* w_up;
   const void* const* w_down;
+  const void* const* ffn_gate;
+  const void* const* ffn_up;
+  const void* const* ffn_down;
 } mk_weights;
 
 typedef struct mk_handle mk_handle;
@@ -249,11 +262,14 @@ int mk_query(mk_handle* h, int what, int64_t* out);
  *     [0] tasks  [1] list length  [2] counters  [3] max active experts  [4] 0
  *     [5] MoE items per expert  [6] MoE item KiB  [7] O-proj tile rows
  *     [8] MoE f-slice rows  [9] QKV tile rows  [10] QKV tiles per KV group
- *     [11] router tiles  [12] residual row-block target  [13] done-counter index
+ *     [11] router tiles (per routed layer)  [12] O-proj tiles of a layer (the O-proj-done
+ *     target)  [13] done-counter index
  *     [14] plan segments (1 + per-op launches)  [15] LM-head tiles
  *     [16..23] counter bases: layer-ready, QKV-group, router-tiles, route-ready,
  *              attention (layer, seq, group), O-group, MoE-done, row-block
  *     [24] residual row blocks  [25] query heads per KV group
+ *     [26] attention-complete counter base  [27] items of a dense layer's FFN
+ *     [28], [29] dense-layer mask, low and high 32 bits
  * Returns MK_ERR_INVALID if a cap is too small (info_out[0..1] still hold the sizes
  * needed). */
 int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out,

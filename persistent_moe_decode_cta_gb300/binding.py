@@ -48,7 +48,8 @@ class mk_config(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("max_batch", ctypes.c_int32),
                 ("sliding_window", ctypes.c_int32), ("swa_layer_mask", ctypes.c_uint64),
                 ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
-                ("timeout_ms", ctypes.c_int32)]
+                ("timeout_ms", ctypes.c_int32), ("dense_layer_mask", ctypes.c_uint64),
+                ("dense_ff", ctypes.c_int32)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -58,7 +59,7 @@ class mk_weights(ctypes.Structure):
     _fields_ = [("embed", ctypes.c_void_p), ("lm_head", ctypes.c_void_p),
                 ("final_norm", ctypes.c_void_p), ("attn_norm", _PP), ("wq", _PP), ("wk", _PP),
                 ("wv", _PP), ("wo", _PP), ("router", _PP), ("w_gate", _PP), ("w_up", _PP),
-                ("w_down", _PP)]
+                ("w_down", _PP), ("ffn_gate", _PP), ("ffn_up", _PP), ("ffn_down", _PP)]
 
 
 class mk_error_info(ctypes.Structure):
@@ -118,10 +119,14 @@ def make_config(cfg: dict, max_batch: int = 8, timeout_ms: int = 2000) -> mk_con
     mask = 0
     for l in cfg.get("swa_layers", ()):
         mask |= 1 << int(l)
+    dense = 0
+    for l in cfg.get("dense_layers", ()):
+        dense |= 1 << int(l)
     return mk_config(cfg["n_layers"], cfg["d_model"], cfg["n_q_heads"], cfg["n_kv_heads"],
                      cfg["head_dim"], cfg["n_experts"], cfg["top_k"], cfg["d_ff"], cfg["vocab"],
                      cfg.get("page_size", 16), max_batch, cfg.get("sliding_window", 0), mask,
-                     cfg["rope_theta"], cfg["rms_eps"], timeout_ms)
+                     cfg["rope_theta"], cfg["rms_eps"], timeout_ms, dense,
+                     cfg.get("dense_ff", 0) if dense else 0)
 
 
 def _ptrs(t, n):
@@ -142,9 +147,13 @@ def make_weights(W: dict, cfg: dict):
                 w_gate=_ptrs(W["w_gate"].view(L * E, *W["w_gate"].shape[2:]), L * E),
                 w_up=_ptrs(W["w_up"].view(L * E, *W["w_up"].shape[2:]), L * E),
                 w_down=_ptrs(W["w_down"].view(L * E, *W["w_down"].shape[2:]), L * E))
+    names = ["attn_norm", "wq", "wk", "wv", "wo", "router", "w_gate", "w_up", "w_down"]
+    if "ffn_gate" in W:  # the dense FFNs of a mixed stack
+        for k in ("ffn_gate", "ffn_up", "ffn_down"):
+            arrs[k] = _ptrs(W[k], L)
+        names += ["ffn_gate", "ffn_up", "ffn_down"]
     s = mk_weights(W["embed"].data_ptr(), W["lm_head"].data_ptr(), W["final_norm"].data_ptr(),
-                   *[ctypes.cast(arrs[k], _PP) for k in ("attn_norm", "wq", "wk", "wv", "wo",
-                                                         "router", "w_gate", "w_up", "w_down")])
+                   *[ctypes.cast(arrs[k], _PP) for k in names])
     return s, arrs
 
 

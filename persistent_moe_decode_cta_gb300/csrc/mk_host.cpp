@@ -53,9 +53,12 @@ struct Shape {
   int r_router, n_router_tasks, e_pad;
   int r_o, t_o, k_o;
   int moe_fs, t_moe;
+  uint64_t dense_mask;  // mixed stacks: dense layers
+  int f_dense, t_dense;
   int r_lm, v_pad, n_lm_tasks;
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
-  size_t off_qkv, off_o, off_router, off_moe, off_lm, off_embed, total;
+  size_t off_qkv, off_o, off_router, off_moe, off_dense, off_lm, off_embed, total;
+  bool dense(int l) const { return (dense_mask >> l) & 1ull; }
 };
 
 int fail(std::string* dst, int code, const char* fmt, ...) {
@@ -106,6 +109,11 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
     if ((v == 16 || v == 32) && s.f % v == 0) s.moe_fs = v;
   }
   s.t_moe = s.f / s.moe_fs;
+  s.dense_mask = s.L < 64 ? c->dense_layer_mask & ((1ull << s.L) - 1) : c->dense_layer_mask;
+  s.f_dense = s.dense_mask ? c->dense_ff : 0;
+  if (s.dense_mask && (s.f_dense < 128 || s.f_dense % 128 || s.f_dense > 4096))
+    return fail(err, MK_ERR_UNSUPPORTED, "dense_ff %d must be a multiple of 128 <= 4096", s.f_dense);
+  s.t_dense = s.f_dense / s.moe_fs;
   s.r_lm = 64; s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
@@ -120,6 +128,7 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.off_o = take(s.o_layer_bytes * s.L);
   s.off_router = take(s.router_layer_bytes * s.L);
   s.off_moe = take(s.moe_bytes_e * s.E * s.L);
+  s.off_dense = take(s.dense_mask ? (size_t)s.t_dense * s.moe_item_bytes * s.L : 0);
   s.off_lm = take(s.lm_bytes);
   s.off_embed = take(s.embed_bytes);
   s.total = o;
@@ -197,6 +206,9 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     return id;
   };
 
+  // items a layer's MoE-done counter counts: every slot of the routed experts (the
+  // route step pads the inactive ones), or the dense FFN's items
+  auto md_target = [&](int l) { return s.dense(l) ? s.t_dense : P.maxa * s.t_moe; };
   // ---- descriptors
   const int t_embed = add(OP_EMBED, 0, 0, 0, 0, 0, 0, -1, 0, P.c_lr + 0, s.nrb_d, 0, 0, -1);
   std::vector<std::vector<int>> waves((size_t)L * W_COUNT);
@@ -207,7 +219,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     // layers' wait for the previous layer's experts and O-proj tiles and build their
     // operand from its parts
     const int w1 = l == 0 ? P.c_lr : P.c_md + l - 1;
-    const int t1 = l == 0 ? s.nrb_d : P.maxa * s.t_moe;
+    const int t1 = l == 0 ? s.nrb_d : md_target(l - 1);
     auto wait2 = [&](int t) {
       if (l == 0) return t;
       P.tasks[(size_t)t * kDescInts + D_WAIT2_CTR] = P.c_od + l - 1;
@@ -223,16 +235,19 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
                                    (size_t)t * s.r_qkv * s.d * 2,
                                s.r_qkv * s.d * 2, W_QKV)));
     auto& wr = waves[(size_t)l * W_COUNT + W_ROUTER];
-    // the last tile (dealt last on its SM) collects all tiles' logits and routes
-    for (int t = 0; t < s.n_router_tasks; ++t)
+    // the last tile (dealt last on its SM) collects all tiles' logits and routes (a
+    // dense layer has no router)
+    for (int t = 0; t < (s.dense(l) ? 0 : s.n_router_tasks); ++t)
       wr.push_back(wait2(add(OP_ROUTER, l, t == s.n_router_tasks - 1 ? 1 : 0, t * s.r_router, s.r_router, 0, s.d,
                              w1, t1, P.c_rt + l, s.n_router_tasks,
                              s.off_router + l * s.router_layer_bytes + (size_t)t * s.r_router * s.d * 2,
                              s.r_router * s.d * 2, W_ROUTER)));
     drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
+    // D_AUX = 1: the dense FFN's items (every token, weight 1) instead of routed experts
+    const int dz = s.dense(l) ? 1 : 0;
     drains[(size_t)l * W_COUNT + W_MOE] =
-        add(OP_MOE_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
-    moe_oq[l] = add(OP_MOE_DRAIN, l, 0, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
+        add(OP_MOE_DRAIN, l, dz, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
+    moe_oq[l] = add(OP_MOE_DRAIN, l, dz, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
     auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
     for (int g = 0; g < s.Hkv; ++g)
       for (int t = 0; t < s.t_o; ++t)
@@ -247,7 +262,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
       const int t = add(OP_RESID, l, r, r * kRowBlock, kRowBlock, 0, 0, P.c_od + l, P.od_target,
                         P.c_lr + l + 1, s.nrb_d, 0, 0, W_RESID);
       P.tasks[(size_t)t * kDescInts + D_WAIT2_CTR] = P.c_md + l;
-      P.tasks[(size_t)t * kDescInts + D_WAIT2_TARGET] = P.maxa * s.t_moe;
+      P.tasks[(size_t)t * kDescInts + D_WAIT2_TARGET] = md_target(l);
       wx.push_back(t);
     }
   }
@@ -557,12 +572,20 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
   if (!w || !w->embed || !w->lm_head || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv ||
       !w->wo || !w->router || !w->w_gate || !w->w_up || !w->w_down)
     return fail(nullptr, MK_ERR_INVALID, "weights struct has a NULL member");
-  for (int l = 0; l < s.L; ++l)
-    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->router[l])
+  for (int l = 0; l < s.L; ++l) {
+    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || (!s.dense(l) && !w->router[l]))
       return fail(nullptr, MK_ERR_INVALID, "NULL weight pointer at layer %d", l);
-  for (int i = 0; i < s.L * s.E; ++i)
-    if (!w->w_gate[i] || !w->w_up[i] || !w->w_down[i])
-      return fail(nullptr, MK_ERR_INVALID, "NULL expert pointer at index %d", i);
+    if (s.dense(l)) {
+      if (!w->ffn_gate || !w->ffn_up || !w->ffn_down || !w->ffn_gate[l] || !w->ffn_up[l] || !w->ffn_down[l])
+        return fail(nullptr, MK_ERR_INVALID, "NULL dense FFN pointer at layer %d", l);
+      continue;
+    }
+    for (int e = 0; e < s.E; ++e) {
+      const int i = l * s.E + e;
+      if (!w->w_gate[i] || !w->w_up[i] || !w->w_down[i])
+        return fail(nullptr, MK_ERR_INVALID, "NULL expert pointer at index %d", i);
+    }
+  }
 
   mk_handle* h = new mk_handle();
   h->cfg = *cfg;
@@ -616,6 +639,14 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
     for (int g = 0; g < s.Hkv; ++g)
       PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o,
          PACK_IDENT, hd, gs, 0, s.r_o);
+    if (s.dense(l)) {  // mixed stack: the layer's FFN in the dense region, no router or experts
+      e = launch_pack_moe(h->wblob + s.off_dense + (size_t)l * s.t_dense * s.moe_item_bytes, w->ffn_gate[l],
+                          w->ffn_up[l], w->ffn_down[l], d, s.f_dense, s.moe_fs, st);
+      if (e != cudaSuccess) { cuda_fail(h, e, "pack dense FFN"); return bail(MK_ERR_CUDA); }
+      e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
+      if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
+      continue;
+    }
     PK(h->wblob + s.off_router + l * s.router_layer_bytes, w->router[l], nullptr, nullptr, s.e_pad, E, d, d, 0,
        PACK_IDENT, hd, gs, 0, s.r_router);
     for (int e2 = 0; e2 < E; ++e2) {
@@ -657,6 +688,8 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
     I[11] = s.n_router_tasks; I[12] = P.od_target; I[13] = P.c_done; I[14] = P.n_segs; I[15] = s.n_lm_tasks;
     I[16] = P.c_lr; I[17] = P.c_qkvg; I[18] = P.c_rt; I[19] = P.c_rr; I[20] = P.c_att; I[21] = P.c_og;
     I[22] = P.c_md; I[23] = P.c_od; I[24] = s.nrb_d; I[25] = s.gs; I[26] = P.c_oa;
+    I[27] = s.t_dense; I[28] = (int32_t)(uint32_t)(s.dense_mask & 0xffffffffull);
+    I[29] = (int32_t)(uint32_t)(s.dense_mask >> 32);
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
     return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
@@ -717,6 +750,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.inflight_moe = p.inflight;
   if (const char* fl = getenv("MK_INFLIGHT_MOE")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight_moe = v; }
   p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
+  p.dense_mask = s.dense_mask; p.t_dense = s.t_dense; p.off_dense = (long long)s.off_dense;
   p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
   p.rope_turns = h->rope_turns;
   p.embed = reinterpret_cast<const uint16_t*>(h->wblob + s.off_embed);

@@ -116,6 +116,11 @@ struct Params {
   int fixed, do_reset;
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   int inflight_moe;         // the same for the chunks of expert items
+  // mixed dense/MoE stacks: bit l set = layer l is dense, its FFN is t_dense items (one
+  // per moe_fs rows of dense_ff) at off_dense + (l * t_dense + t) * moe_item_bytes
+  unsigned long long dense_mask;
+  int t_dense;
+  long long off_dense;
   // multi-step decode: n_steps steps per launch, each step's greedy token (argmax of its
   // logits, lowest index on ties) written to tok_out[step][B] and fed to the next step
   int n_steps;

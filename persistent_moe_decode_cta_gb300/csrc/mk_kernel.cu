@@ -517,9 +517,32 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         bool lr_done = false;
         const unsigned* lr_ctr = ctr_ptr(p, C_LR(p, l));
         const unsigned lr_target = (unsigned)p.nrb_d;
+        // a dense layer of a mixed stack: one FFN for every token with weight 1 (no route
+        // words; only the items' operand is waited for)
+        const bool dense = T[D_AUX] == 1;
         auto fetch = [&](int a) -> bool {  // slot a's words (and n_active while unknown)
           const uint64_t t0 = gtime();
           unsigned ns = 32;
+          if (dense) {
+            for (int it = 0; ld_acquire(lr_ctr) < lr_target; ++it) {  // acquire: the ADD_RMSNORM outputs
+              __nanosleep(64);
+              if ((it & 15) == 15 && (aborted(p) || (long long)(gtime() - t0) > p.timeout_ns)) {
+                if (!aborted(p)) raise_err(p, MK_ERR_TIMEOUT, ti, C_LR(p, l), -1, (int)lr_target);
+                return false;
+              }
+            }
+            lr_done = true;
+            nact = 1;
+            tl_slot = 0;
+            tl_e = 0;
+            tl_cnt = p.B;
+#pragma unroll
+            for (int n = 0; n < kMaxBatch; ++n) {
+              tl_tok[n] = n < p.B ? n * 16 : 0;
+              tl_w[n] = n < p.B ? __float_as_int(1.f) : 0;
+            }
+            return true;
+          }
           for (int it = 0;; ++it) {
             const bool sl = a >= 0 && a < maxa;
             const int as = sl ? a : 0;
@@ -566,8 +589,8 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
             }
           }
         };
-        if (!fetch(item / p.t_moe)) { ok = false; break; }
-        const int count = nact * p.t_moe;
+        if (!fetch(dense ? 0 : item / p.t_moe)) { ok = false; break; }
+        const int count = dense ? p.t_dense : nact * p.t_moe;
         // part 1 (gate/up tile) in whole k16-groups, part 2 (down slice) in warp regions
         const int nrb1 = p.moe_fs / 8;
         const int cs1 = gemv_jpc(nrb1) * nrb1 * 8 * kFragBytes;
@@ -596,7 +619,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
             item = atomicAdd(p.qhead + q, 1);
           }
           if (item >= count) break;
-          const int a = item / p.t_moe, t = item % p.t_moe;
+          const int a = dense ? 0 : item / p.t_moe, t = dense ? item : item % p.t_moe;
           if (a != tl_slot && !fetch(a)) { ok = false; break; }
           const int e = tl_e;
           int4 extra = make_int4(tl_cnt, 0, 0, 0);
@@ -606,7 +629,9 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
             if (n < 4) extra.y |= byte << (8 * n);
             else extra.z |= byte << (8 * (n - 4));
           }
-          const uint8_t* src = p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
+          const uint8_t* src =
+              dense ? p.wblob + p.off_dense + ((long long)l * p.t_dense + t) * p.moe_item_bytes
+                    : p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
           const int fl = p.inflight_moe;
           ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
                          make_int4(tl_w[4], tl_w[5], tl_w[6], tl_w[7])) &&
@@ -1364,7 +1389,7 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
   const int l = T[D_LAYER];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g8 = lane >> 2, c = lane & 3;
-  const int a_slot = item / p.t_moe;
+  const int a_slot = T[D_AUX] == 1 ? 0 : item / p.t_moe;  // a dense layer: one token set
   const OperandKey key = {3, l, a_slot};
   // The producer claimed this item from the layer's route words and passed the
   // expert's token list and weights in the mailbox entry: no dependency wait here.

@@ -47,7 +47,10 @@ def check_routing_teacher_forced(cfg, HW, hid, gidx, gw, B):
     is >= MARGIN; weights within 1e-3 of the oracle's softmax over the GPU's
     selection.  Returns the number of (layer, token) near-ties seen."""
     ties = 0
+    dense = tuple(cfg.get("dense_layers", ()))
     for l in range(cfg["n_layers"]):
+        if l in dense:  # a dense layer of a mixed stack routes nothing
+            continue
         h = oracle.rms_norm(hid[l].astype(np.float64), oracle.bf16_to_f64(HW.attn_norm(l)),
                             cfg["rms_eps"])
         r = h @ oracle.bf16_to_f64(HW.router(l)).T
@@ -77,7 +80,8 @@ def check_step(cfg, mk, W, seq, pt, kv_before, tokens_np, logits_gpu, k_after=No
     gidx, gw = mk.routes()
     out = dict(near_ties=check_routing_teacher_forced(cfg, HW, hid, gidx, gw, B))
     forced = {(l, b): [int(e) for e in gidx[l, b]]
-              for l in range(cfg["n_layers"]) for b in range(B)}
+              for l in range(cfg["n_layers"]) for b in range(B)
+              if l not in tuple(cfg.get("dense_layers", ()))}
     ref = oracle.decode_step(cfg, HW, HK, tokens_np, seq, pt, forced=forced)
     # active-expert bookkeeping: slot order = ascending expert id, token lists by (b, j)
     act = mk.active()

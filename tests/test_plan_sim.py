@@ -46,6 +46,9 @@ class Sim:
          self.c_od) = I[16:24]
         self.nrb_d, self.L, self.Hkv = I[24], cfg["n_layers"], cfg["n_kv_heads"]
         self.c_oa = I[26]
+        self.t_dense = I[27]
+        mask = (int(I[28]) & 0xffffffff) | ((int(I[29]) & 0xffffffff) << 32)
+        self.dense = {l for l in range(self.L) if (mask >> l) & 1}
         self.pending = [None] * n_sm   # a claimed O-proj tile waiting for its group
         self.held = [None] * n_sm      # layer of an O-proj tile claimed before C_OA was full
         # queues
@@ -152,8 +155,13 @@ class Sim:
                 self.heads[("oproj", l)] += 1
                 self.pending[sm] = o_base + ho
                 return True
-            # the route words of the layer, and the ADD_RMSNORM outputs (the items' operand)
-            if not self.ready(self.c_rr + l, 1) or not self.ready(self.c_lr + l, self.nrb_d):
+            # the route words of the layer (a dense layer has none: its FFN's items take
+            # every token), and the ADD_RMSNORM outputs (the items' operand)
+            if l in self.dense:
+                self.moe_count[l] = self.t_dense
+            elif not self.ready(self.c_rr + l, 1):
+                return False
+            if not self.ready(self.c_lr + l, self.nrb_d):
                 return False
             h = self.heads[("moe", l)]
             if h < self.moe_count[l]:
@@ -191,7 +199,7 @@ class Sim:
         for l in range(self.L):
             assert self.heads[("moe", l)] == self.moe_count[l]
             assert self.heads[("att", l)] == len(self.att_queue(l))
-            assert self.ctr[self.c_md + l] == self.maxa * self.t_moe
+            assert self.ctr[self.c_md + l] == (self.t_dense if l in self.dense else self.maxa * self.t_moe)
         assert self.ctr[self.c_lr + self.L] == self.nrb_d
 
 
@@ -201,6 +209,8 @@ class Sim:
     ("tiny_b1_64", 8, 5, [64, 1, 0, 17, 33, 200, 15, 16]),
     ("small_b1_2k", 3, 16, [2048, 5, 700]),
     ("pages_b8_ragged_swa", 8, 152, [1024, 5000, 9000, 4097, 4096, 32768, 17, 0]),
+    ("tiny_dense_b1_64", 3, 7, [64, 1, 30]),
+    ("small_dense_b1_2k", 2, 152, [2048, 100]),
 ])
 def test_schedule_completes_with_exact_counter_targets(workload, batch, n_sm, lens):
     cfg = synth.model_config(workload)
