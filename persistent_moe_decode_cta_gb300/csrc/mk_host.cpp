@@ -128,7 +128,7 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.off_o = take(s.o_layer_bytes * s.L);
   s.off_router = take(s.router_layer_bytes * s.L);
   s.off_moe = take(s.moe_bytes_e * s.E * s.L);
-  s.off_dense = take(s.dense_mask ? (size_t)s.t_dense * s.moe_item_bytes * s.L : 0);
+  s.off_dense = take((size_t)__builtin_popcountll(s.dense_mask) * s.t_dense * s.moe_item_bytes);
   s.off_lm = take(s.lm_bytes);
   s.off_embed = take(s.embed_bytes);
   s.total = o;
@@ -640,7 +640,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
       PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o,
          PACK_IDENT, hd, gs, 0, s.r_o);
     if (s.dense(l)) {  // mixed stack: the layer's FFN in the dense region, no router or experts
-      e = launch_pack_moe(h->wblob + s.off_dense + (size_t)l * s.t_dense * s.moe_item_bytes, w->ffn_gate[l],
+      const int rank = __builtin_popcountll(s.dense_mask & ((1ull << l) - 1ull));  // dense layers before l
+      e = launch_pack_moe(h->wblob + s.off_dense + (size_t)rank * s.t_dense * s.moe_item_bytes, w->ffn_gate[l],
                           w->ffn_up[l], w->ffn_down[l], d, s.f_dense, s.moe_fs, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "pack dense FFN"); return bail(MK_ERR_CUDA); }
       e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);

@@ -117,7 +117,8 @@ struct Params {
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   int inflight_moe;         // the same for the chunks of expert items
   // mixed dense/MoE stacks: bit l set = layer l is dense, its FFN is t_dense items (one
-  // per moe_fs rows of dense_ff) at off_dense + (l * t_dense + t) * moe_item_bytes
+  // per moe_fs rows of dense_ff) at off_dense + (r * t_dense + t) * moe_item_bytes, r =
+  // the number of dense layers below l
   unsigned long long dense_mask;
   int t_dense;
   long long off_dense;

@@ -630,7 +630,8 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
             else extra.z |= byte << (8 * (n - 4));
           }
           const uint8_t* src =
-              dense ? p.wblob + p.off_dense + ((long long)l * p.t_dense + t) * p.moe_item_bytes
+              dense ? p.wblob + p.off_dense +
+                          ((long long)__popcll(p.dense_mask & ((1ull << l) - 1ull)) * p.t_dense + t) * p.moe_item_bytes
                     : p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
           const int fl = p.inflight_moe;
           ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),

@@ -43,8 +43,13 @@ def step_bytes(cfg: dict, seq_lens, union_sizes) -> dict:
     V, f = cfg["vocab"], cfg["d_ff"]
     B = len(seq_lens)
     pc = param_counts(cfg)
-    weights = BF16 * (L * pc["dense_layer"] + sum(union_sizes) * pc["expert"]
-                      + V * d + d + B * d)
+    # a dense layer of a mixed stack reads its FFN instead of a router and experts
+    dense = set(cfg.get("dense_layers", ()))
+    n_dense = sum(1 for l in range(L) if l in dense)
+    routed_union = sum(u for l, u in enumerate(union_sizes) if l not in dense)
+    dense_ffn = 3 * d * cfg.get("dense_ff", 0)
+    weights = BF16 * (L * pc["dense_layer"] - n_dense * d * cfg["n_experts"] + routed_union * pc["expert"]
+                      + n_dense * dense_ffn + V * d + d + B * d)
     swa = set(cfg.get("swa_layers", ()))
     kv_read = 0
     for p in seq_lens:

@@ -41,6 +41,9 @@ MODELS["small_dense"] = dict(MODELS["small"], dense_layers=(0, 5), dense_ff=1024
 # and for the oracle to run in seconds, with every tile size of the full model.
 MODELS["pages_l2"] = dict(MODELS["pages"], n_layers=2)
 MODELS["pages_l1"] = dict(MODELS["pages"], n_layers=1)
+# The pages-scale shape with its first three layers dense (FFN width 4096), for the
+# mixed-stack measurement.
+MODELS["pages_dense3"] = dict(MODELS["pages"], dense_layers=(0, 1, 2), dense_ff=4096)
 
 # Workloads: a model plus a batch of cached sequence lengths.
 WORKLOADS = {
@@ -55,6 +58,7 @@ WORKLOADS = {
     "pages_l2_b8_ragged_swa": dict(model="pages_l2", batch=8, lens=("uniform", 1024, 32768),
                                    sliding_window=4096, swa="odd"),
     "tiny_dense_b1_64": dict(model="tiny_dense", batch=1, lens=("fixed", 64)),
+    "pages_dense3_b1_8k": dict(model="pages_dense3", batch=1, lens=("fixed", 8192)),
     "small_dense_b1_2k": dict(model="small_dense", batch=1, lens=("fixed", 2048)),
 }
 
