@@ -96,11 +96,17 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.nrb_d = s.d / kRowBlock;
   s.qkv_rows_group = (s.gs + 2) * s.hd;
   s.r_qkv = (s.qkv_rows_group % 32 == 0) ? 32 : 16;  // 128 KB tiles at d 2048: one fits the ring
+  if (const char* e = getenv("MK_QKV_ROWS")) { const int v = atoi(e); if ((v == 16 || v == 32 || v == 64) && s.qkv_rows_group % v == 0) s.r_qkv = v; }
   s.qkv_tpg = s.qkv_rows_group / s.r_qkv;
   s.r_router = 16;
   s.e_pad = (s.E + 15) / 16 * 16;
   s.n_router_tasks = s.e_pad / s.r_router;
-  s.r_o = 64; s.t_o = s.d / s.r_o; s.k_o = s.gs * s.hd;
+  // O-proj tiles of 128 rows x one KV group (256 KB at the pages scale): 64 tiles a
+  // layer, each started by a free SM in the tail of the MoE phase (64-row tiles: -2.8%
+  // at batch 1, the tail ran two deep on a third of the SMs)
+  s.r_o = 128;
+  if (const char* e = getenv("MK_OPROJ_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_o = v; }
+  s.t_o = s.d / s.r_o; s.k_o = s.gs * s.hd;
   // MoE f-slice width: 32 rows of d_ff (measured best at the pages-scale shape against
   // 16/48/64: wider items start late on SMs still busy with attention items)
   s.moe_fs = (s.f % 32 == 0) ? 32 : 16;

@@ -62,8 +62,11 @@ def test_mixed_stack_multi_step_equals_single_steps():
         lg2 = torch.empty_like(lg1)
         out = mk.steps(tokens, n, k, v, lg2)
         assert mk.status()["code"] == 0
+        # the same greedy tokens; cache and logits agree within the parity tolerance (the
+        # order of the fp32 atomic adds into the layer accumulator is not fixed)
         assert np.array_equal(out.cpu().numpy(), np.stack(host))
-        assert torch.equal(k1.view(torch.int16), k.view(torch.int16))
-        assert torch.equal(lg1, lg2)
+        assert PU.rel_l2(k.float().cpu().numpy(), k1.float().cpu().numpy()) < PU.REL_L2
+        assert PU.rel_l2(v.float().cpu().numpy(), v1.float().cpu().numpy()) < PU.REL_L2
+        assert float((lg1 - lg2).abs().max()) <= PU.LOGIT_ABS
     finally:
         mk.close()

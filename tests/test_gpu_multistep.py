@@ -1,10 +1,11 @@
 """Multi-step decode (mk_decode_steps): N greedy steps in one launch, each step's
-token fed to the next on the device.  On the tiny model (deterministic run to run)
-it must equal N single steps with the greedy token fed back on the host -- tokens,
-K/V cache bytes, seq_lens and the last step's logits, bit for bit -- and the last
-step of a multi-step launch must match the oracle (routing teacher-forced, as in the
-single-step parity tests); the single steps themselves are pinned to the oracle
-there."""
+token fed to the next on the device.  On the tiny model it must equal N single steps
+with the greedy token fed back on the host -- the same tokens and seq_lens, the K/V
+cache and the last step's logits within the parity tolerance (the order of the fp32
+atomic adds into the layer accumulator is not fixed, so the last bits may differ
+between any two runs) -- and the last step of a multi-step launch must match the
+oracle (routing teacher-forced, as in the single-step parity tests); the single steps
+themselves are pinned to the oracle there."""
 import numpy as np
 import pytest
 import torch
@@ -41,9 +42,9 @@ def test_steps_in_one_launch_equal_single_steps_with_host_feedback():
         assert mk.status()["code"] == 0
         assert np.array_equal(out.cpu().numpy(), np.stack(host_tokens))
         assert list(mk.seq_lens()) == [s + n for s in seq]
-        assert torch.equal(k1.view(torch.int16), k2.view(torch.int16))
-        assert torch.equal(v1.view(torch.int16), v2.view(torch.int16))
-        assert torch.equal(lg1, lg2)
+        assert PU.rel_l2(k2.float().cpu().numpy(), k1.float().cpu().numpy()) < PU.REL_L2
+        assert PU.rel_l2(v2.float().cpu().numpy(), v1.float().cpu().numpy()) < PU.REL_L2
+        assert float((lg1 - lg2).abs().max()) <= PU.LOGIT_ABS
         # the launch can be repeated: counters, queues and the argmax keys are reset
         out2 = mk.steps(out[-1].clone(), 2, k2, v2, lg2)
         assert mk.status()["code"] == 0
