@@ -99,7 +99,8 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   if (const char* e = getenv("MK_QKV_ROWS")) { const int v = atoi(e); if ((v == 16 || v == 32 || v == 64) && s.qkv_rows_group % v == 0) s.r_qkv = v; }
   s.qkv_tpg = s.qkv_rows_group / s.r_qkv;
   s.r_router = 16;
-  s.e_pad = (s.E + 15) / 16 * 16;
+  if (const char* e = getenv("MK_ROUTER_ROWS")) { const int v = atoi(e); if (v == 16 || v == 32) s.r_router = v; }
+  s.e_pad = (s.E + s.r_router - 1) / s.r_router * s.r_router;
   s.n_router_tasks = s.e_pad / s.r_router;
   // O-proj tiles of 128 rows x one KV group (256 KB at the pages scale): 64 tiles a
   // layer, each started by a free SM in the tail of the MoE phase (64-row tiles: -2.8%
@@ -120,7 +121,9 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   if (s.dense_mask && (s.f_dense < 128 || s.f_dense % 128 || s.f_dense > 4096))
     return fail(err, MK_ERR_UNSUPPORTED, "dense_ff %d must be a multiple of 128 <= 4096", s.f_dense);
   s.t_dense = s.f_dense / s.moe_fs;
-  s.r_lm = 64; s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
+  s.r_lm = 64;
+  if (const char* e = getenv("MK_LM_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_lm = v; }
+  s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
   s.router_layer_bytes = (size_t)s.e_pad * s.d * 2;
@@ -754,7 +757,10 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.n_steps = 1; p.tok_out = nullptr;  // one step, no greedy tokens (mk_decode_steps sets both)
   p.inflight = 2;
   if (const char* fl = getenv("MK_INFLIGHT")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight = v; }
-  p.inflight_moe = p.inflight;
+  // expert items: 3 chunks in flight per SM from batch 4 up (the MoE phase streams
+  // ~1200 items a layer at batch 8 and is bandwidth-bound: +3%), 2 below (at batch 1
+  // it is latency-bound and a deeper window measured 2.6% slower)
+  p.inflight_moe = B >= 4 ? std::min(3, kStages - 1) : p.inflight;
   if (const char* fl = getenv("MK_INFLIGHT_MOE")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight_moe = v; }
   p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
   p.dense_mask = s.dense_mask; p.t_dense = s.t_dense; p.off_dense = (long long)s.off_dense;
