@@ -83,6 +83,81 @@ def f64_to_bf16(x) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # building blocks
 
+# ---------------------------------------------------------------- FP8 (E4M3) weights
+# The FP8 weight path stores expert matrices as E4M3 codes with float32 scales: gate
+# and up rows one scale per row, the down matrix one scale per row and 32-column block
+# (the f-slice the kernel streams); a code decodes as sign * value(code) * scale.
+# E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0 is
+# subnormal (m/8 * 2^-6); the largest finite value is 448; 0x7F/0xFF are NaN.
+# Quantisation rounds x / scale (a float32 division) to the nearest code, ties to
+# even, saturating to +-448; scale = max|row| / 448 (float32), 1 for an all-zero row.
+# [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "Current limitations":
+# FP8 weights are on the roadmap; the pages fix no format, E4M3 with float32 scales
+# is the reading taken]
+E4M3_MAX = 448.0
+FP8_BLOCK = 32
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    return sign * val
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """Nearest E4M3 code of each float32 value, ties to even, saturating to +-448."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)      # exact
+    neg = np.signbit(x)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))                      # a = m 2^ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, -6)                                     # binade (subnormals share -6)
+    step = np.exp2((e - 3).astype(np.float64))                     # spacing of 3 mantissa bits
+    v = np.minimum(np.round(a / step) * step, E4M3_MAX)           # np.round: ties to even
+    _, ev = np.frexp(np.where(v > 0, v, 1.0))
+    ev = ev - 1
+    sub = v < 2.0 ** -6
+    mant_sub = np.round(v / 2.0 ** -9).astype(np.int64)
+    mant_nrm = np.round((v / np.exp2(ev.astype(np.float64)) - 1.0) * 8.0).astype(np.int64)
+    code = np.where(sub, mant_sub, ((ev + 7) << 3) | mant_nrm)
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+
+
+def quantize_e4m3_rows(w_u16, block=None):
+    """E4M3 codes and float32 scales of a bf16 matrix [rows, cols]: one scale per row,
+    or per row and `block` columns.  Returns (codes uint8 [rows, cols], scales float32
+    [rows] or [rows, cols // block])."""
+    w = bf16_to_f64(w_u16).astype(np.float32)                       # exact
+    rows, cols = w.shape
+    if block is not None and (cols % block or cols < block):
+        raise ValueError(f"{cols} columns are not whole {block}-column blocks")
+    nb = 1 if block is None else cols // block
+    wb = w.reshape(rows, nb, cols // nb)
+    amax = np.max(np.abs(wb), axis=2)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    codes = f32_to_e4m3((wb / scale[:, :, None]).astype(np.float32)).reshape(rows, cols)
+    return codes, (scale[:, 0] if block is None else scale)
+
+
+def dequantize_e4m3(codes, scales, block=None) -> np.ndarray:
+    v = e4m3_to_f64(codes)
+    if block is None:
+        return v * np.asarray(scales, dtype=np.float64)[:, None]
+    rows, cols = v.shape
+    s = np.repeat(np.asarray(scales, dtype=np.float64), block, axis=1)
+    return v * s
+
+
+def fp8_expert(wg_u16, wu_u16, wd_u16):
+    """The expert's matrices as the FP8 path stores them, decoded to float64."""
+    wg = dequantize_e4m3(*quantize_e4m3_rows(wg_u16))
+    wu = dequantize_e4m3(*quantize_e4m3_rows(wu_u16))
+    wd = dequantize_e4m3(*quantize_e4m3_rows(wd_u16, FP8_BLOCK), FP8_BLOCK)
+    return wg, wu, wd
+
+
 def rms_norm(x, gain, eps):
     """x / sqrt(mean(x^2) + eps) * gain, over the last axis."""
     x = np.asarray(x, dtype=np.float64)
@@ -261,8 +336,9 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
         info["idx"].append(idx); info["w"].append(w); info["margin"].append(margin)
         for j, e in enumerate(idx):
             per_expert.setdefault(int(e), []).append((b, j))
+    fp8 = cfg.get("expert_dtype") == "fp8"
     for e in sorted(per_expert):
-        wg, wu, wd = (_mat(a) for a in W.expert(l, e))
+        wg, wu, wd = fp8_expert(*W.expert(l, e)) if fp8 else (_mat(a) for a in W.expert(l, e))
         for b, j in per_expert[e]:
             moe_out[b] += info["w"][b][j] * swiglu_expert(h[b], wg, wu, wd)
     info["experts"] = {e: per_expert[e] for e in sorted(per_expert)}
@@ -305,7 +381,8 @@ def decode_step(cfg, W, kv, tokens, seq_lens, page_table, forced=None):
     return dict(logits=logits, greedy=greedy, hidden=np.stack(hidden), layers=layers)
 
 
-__all__ = ["bf16_to_f64", "f64_to_bf16", "rms_norm", "rope", "softmax", "attention",
+__all__ = ["e4m3_to_f64", "f32_to_e4m3", "quantize_e4m3_rows", "dequantize_e4m3", "fp8_expert",
+           "bf16_to_f64", "f64_to_bf16", "rms_norm", "rope", "softmax", "attention",
            "attention_partial", "merge_partials", "router_topk", "silu", "swiglu_expert",
            "window_start", "argmax_lowest", "layer_step", "lm_head", "embed",
            "decode_step", "PAGE"]

@@ -364,3 +364,79 @@ def test_step_bytes_pages_b1_8k():
     sb = sol.step_bytes(cfg, [8192], [8] * 48)
     assert sb["kv"] == 48 * 8192 * 2 * 4 * 128 * 2
     assert abs(sb["weights"] - 6.0835e9) < 1e6
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) weights
+def test_e4m3_every_finite_code_decodes_and_encodes_back_to_itself():
+    c = np.arange(256, dtype=np.uint8)
+    finite = (c & 0x7F) != 0x7F
+    v = O.e4m3_to_f64(c[finite])
+    assert np.array_equal(O.f32_to_e4m3(v.astype(np.float32)), c[finite])
+    assert O.e4m3_to_f64(np.uint8(0x7E)) == 448.0 and O.e4m3_to_f64(np.uint8(0x01)) == 2.0 ** -9
+    assert O.e4m3_to_f64(np.uint8(0x08)) == 2.0 ** -6 and O.e4m3_to_f64(np.uint8(0x38)) == 1.0
+
+
+def test_e4m3_rounding_is_nearest_even_with_saturation_by_brute_force():
+    """Against the nearest of all 254 finite values by exhaustive search (ties to the
+    even code), for random values across the whole range and for exact midpoints."""
+    c = np.arange(256, dtype=np.uint8)
+    c = c[(c & 0x7F) != 0x7F]
+    vals = O.e4m3_to_f64(c)
+    rng = np.random.default_rng(7)
+    x = np.concatenate([rng.standard_normal(3000) * 10.0, rng.standard_normal(1000) * 1e-2,
+                        rng.uniform(-600, 600, 500)]).astype(np.float32)
+    srt = np.unique(vals)
+    mids = ((srt[1:] + srt[:-1]) / 2).astype(np.float32)            # exact in float32
+    x = np.concatenate([x, mids, -mids])
+    got = O.f32_to_e4m3(x)
+    for xi, gi in zip(x.astype(np.float64), got):
+        t = np.clip(xi, -448.0, 448.0)
+        d = np.abs(vals - t)
+        best = c[d == d.min()]
+        if len(best) > 1:                                           # a tie: the even code
+            best = best[(best & 1) == 0]
+            if len(best) > 1:                                       # +0 / -0
+                best = best[(best & 0x80) == (0x80 if np.signbit(xi) else 0)]
+        assert gi == best[0], (xi, gi, best)
+
+
+def test_e4m3_row_quantisation_scale_and_error_bound():
+    rng = np.random.default_rng(3)
+    w = O.f64_to_bf16(rng.standard_normal((16, 96)) * 0.02)
+    for block in (None, 32):
+        codes, scale = O.quantize_e4m3_rows(w, block)
+        wq = O.dequantize_e4m3(codes, scale, block)
+        wf = O.bf16_to_f64(w)
+        nb = 1 if block is None else 96 // block
+        amax = np.abs(wf.reshape(16, nb, -1)).max(axis=2)
+        # the largest magnitude of each row (block) maps to the code 448
+        assert np.allclose(np.abs(O.e4m3_to_f64(codes).reshape(16, nb, -1)).max(axis=2), 448.0)
+        assert np.array_equal(np.asarray(scale).reshape(16, nb), (amax / 448.0).astype(np.float32))
+        # error at most half a step of the code's binade (relative 2^-4) or of the subnormal grid
+        s = np.repeat(np.asarray(scale, dtype=np.float64).reshape(16, nb), 96 // nb, axis=1)
+        err = np.abs(wq - wf) / s
+        assert np.all(err <= np.maximum(np.abs(wf) / s * 2.0 ** -4, 2.0 ** -10) + 1e-12)
+
+
+def test_fp8_experts_change_the_layer_only_by_the_quantisation():
+    """With expert_dtype fp8 the layer equals the bf16 layer computed on the decoded
+    weights, and differs from the bf16 weights' layer by a small amount."""
+    cfg = dict(TINY, d_ff=64)  # the FP8 down scales come per 32 columns of d_ff
+    W, pt, k, v = _setup(cfg)
+    x = _x(2, 32)
+    HW = synth.HostWeights(W)
+    kv = synth.HostKV(k, v)
+    y16, info16 = O.layer_step(cfg, HW, kv, 0, x, [37, 5], pt)
+    y8, info8 = O.layer_step(dict(cfg, expert_dtype="fp8"), HW, kv, 0, x, [37, 5], pt)
+    assert [list(a) for a in info8["idx"]] == [list(a) for a in info16["idx"]]
+    rel = np.linalg.norm(y8 - y16) / np.linalg.norm(y16 - x)
+    assert 0 < rel < 0.1
+    # the same layer computed by hand from the decoded expert matrices
+    g = O.bf16_to_f64(HW.attn_norm(0))
+    for b in range(2):
+        h = x[b] / math.sqrt(np.mean(x[b] ** 2) + 1e-6) * g
+        moe = sum(w * O.swiglu_expert(h, *O.fp8_expert(*HW.expert(0, int(e))))
+                  for e, w in zip(info8["idx"][b], info8["w"][b]))
+        moe16 = sum(w * O.swiglu_expert(h, *(O.bf16_to_f64(a) for a in HW.expert(0, int(e))))
+                    for e, w in zip(info16["idx"][b], info16["w"][b]))
+        assert np.allclose((y8[b] - y16[b]), moe - moe16, atol=1e-12)
