@@ -408,7 +408,7 @@ def main():
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3" if cfg.get("expert_dtype") == "fp8" else "bf16",
             "data": "synthetic (seeded random bf16 weights ~N(0,0.02), K/V ~N(0,1))",
             "config": {"workload": args.workload, "batch": B, "seq_lens": st["seq"]
                        if B <= 8 else None, "mode": args.mode,

@@ -56,7 +56,16 @@ typedef enum mk_status {
  * FFN of width dense_ff (a multiple of 128, <= 4096) for every token, no router, in
  * place of the routed experts; 0 = every layer routed (dense_ff ignored).
  * [Cohere open-sources fused LLM decode kernel with 1.58x vLLM claim: the dense GEMM
- * task types FFN_UPGATE_ACT and FFN_DOWN] */
+ * task types FFN_UPGATE_ACT and FFN_DOWN]
+ * expert_dtype: MK_EXPERT_BF16 (0) keeps the routed experts' matrices in bf16;
+ * MK_EXPERT_FP8 (1) stores them, at mk_create, as E4M3 codes (nearest, ties to even,
+ * saturating) with one float32 scale per row (max |w| / 448; 1 for a zero row) -- per
+ * row over all of d_model for gate and up, per row and 32-column block for down -- and
+ * the kernel decodes the codes to fp16 for the MMA and applies the scales to its fp32
+ * results.  It needs d_ff a multiple of 32 and no dense layers (MK_ERR_UNSUPPORTED).
+ * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
+ * FP8 quantization is on the roadmap; the pages fix no format] */
+enum { MK_EXPERT_BF16 = 0, MK_EXPERT_FP8 = 1 };
 typedef struct mk_config {
   int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim;
   int32_t n_experts, top_k, d_ff, vocab, page_size, max_batch;
@@ -66,6 +75,7 @@ typedef struct mk_config {
   int32_t timeout_ms;
   uint64_t dense_layer_mask;
   int32_t dense_ff;
+  int32_t expert_dtype;
 } mk_config;
 
 /* Model weights, all bf16 DEVICE pointers, row-major [out][in]:
@@ -246,6 +256,19 @@ enum {
 };
 int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
 
+/* The stored FP8 form of routed expert `expert` of layer `layer` (expert_dtype
+ * MK_EXPERT_FP8), unpacked to row-major arrays in HOST memory, one after another:
+ *   gate codes u8 [d_ff][d_model], up codes u8 [d_ff][d_model],
+ *   down codes u8 [d_model][d_ff], gate scales f32 [d_ff], up scales f32 [d_ff],
+ *   down scales f32 [d_model][d_ff / 32]
+ * (a weight decodes as value(code) * its row's -- or row block's -- scale).  `bytes`
+ * must equal 3 * d_ff * d_model + 4 * (2 * d_ff + d_model * d_ff / 32).  Synchronises
+ * the device; needs no plan.  MK_ERR_STATE if the experts are stored in bf16,
+ * MK_ERR_INVALID for a NULL pointer, a layer or expert out of range or a wrong size.
+ * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
+ * FP8 quantization is on the roadmap] */
+int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size_t bytes);
+
 /* Integer facts about a handle/plan.  `what`: */
 enum {
   MK_Q_NUM_SMS = 1, MK_Q_NUM_TASKS = 2, MK_Q_NUM_COUNTERS = 3, MK_Q_PACKED_BYTES = 4,
@@ -269,7 +292,8 @@ int mk_query(mk_handle* h, int what, int64_t* out);
  *              attention (layer, seq, group), O-group, MoE-done, row-block
  *     [24] residual row blocks  [25] query heads per KV group
  *     [26] attention-complete counter base  [27] items of a dense layer's FFN
- *     [28], [29] dense-layer mask, low and high 32 bits
+ *     [28], [29] dense-layer mask, low and high 32 bits  [30] expert_dtype
+ *     [31] MoE item bytes
  * Returns MK_ERR_INVALID if a cap is too small (info_out[0..1] still hold the sizes
  * needed). */
 int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out,

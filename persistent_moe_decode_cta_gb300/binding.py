@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID", 2: "MK_ERR_UNSUPPORTED", 3: "MK
 
 MK_READ_HIDDEN, MK_READ_ROUTES, MK_READ_ROUTE_W, MK_READ_ACTIVE = 1, 2, 3, 4
 MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT = 5, 6, 7, 8
+MK_EXPERT_BF16, MK_EXPERT_FP8 = 0, 1
 (MK_Q_NUM_SMS, MK_Q_NUM_TASKS, MK_Q_NUM_COUNTERS, MK_Q_PACKED_BYTES, MK_Q_MAX_ACTIVE,
  MK_Q_SPLIT_PAGES, MK_Q_SMEM_BYTES, MK_Q_PEROP_LAUNCHES, MK_Q_THREADS, MK_Q_STAGE_BYTES,
  MK_Q_NUM_STAGES) = range(1, 12)
@@ -30,7 +31,7 @@ MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT =
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_decode_step_noalloc",
            "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace",
-           "mk_plan_drop_signal", "mk_read", "mk_query",
+           "mk_plan_drop_signal", "mk_read", "mk_read_expert_fp8", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
 
 
@@ -49,7 +50,7 @@ class mk_config(ctypes.Structure):
                 ("sliding_window", ctypes.c_int32), ("swa_layer_mask", ctypes.c_uint64),
                 ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
                 ("timeout_ms", ctypes.c_int32), ("dense_layer_mask", ctypes.c_uint64),
-                ("dense_ff", ctypes.c_int32)]
+                ("dense_ff", ctypes.c_int32), ("expert_dtype", ctypes.c_int32)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -94,6 +95,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_set_trace.argtypes = [H, vp, i32]
     lib.mk_plan_drop_signal.argtypes = [H, i32]
     lib.mk_read.argtypes = [H, i32, vp, sz]
+    lib.mk_read_expert_fp8.argtypes = [H, i32, i32, vp, sz]
     lib.mk_query.argtypes = [H, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.mk_plan_dry.argtypes = [ctypes.POINTER(mk_config), i32, i32, vp, i32, vp, vp, i32, vp]
     lib.mk_last_error.argtypes = [H]
@@ -126,7 +128,8 @@ def make_config(cfg: dict, max_batch: int = 8, timeout_ms: int = 2000) -> mk_con
                      cfg["head_dim"], cfg["n_experts"], cfg["top_k"], cfg["d_ff"], cfg["vocab"],
                      cfg.get("page_size", 16), max_batch, cfg.get("sliding_window", 0), mask,
                      cfg["rope_theta"], cfg["rms_eps"], timeout_ms, dense,
-                     cfg.get("dense_ff", 0) if dense else 0)
+                     cfg.get("dense_ff", 0) if dense else 0,
+                     MK_EXPERT_FP8 if cfg.get("expert_dtype", "bf16") == "fp8" else MK_EXPERT_BF16)
 
 
 def _ptrs(t, n):
@@ -244,6 +247,26 @@ def mk_read(h, what: int, shape, dtype) -> np.ndarray:
     return out
 
 
+def mk_read_expert_fp8(h, layer: int, expert: int, d_model: int, d_ff: int) -> dict:
+    """The stored FP8 form of one routed expert, row-major: codes (uint8) and scales
+    (float32) of gate [d_ff, d_model], up [d_ff, d_model] and down [d_model, d_ff]
+    (down scales per row and 32-column block)."""
+    d, f = int(d_model), int(d_ff)
+    n = 3 * f * d + 4 * (2 * f + d * (f // 32))
+    buf = np.empty(n, dtype=np.uint8)
+    _check(load_library().mk_read_expert_fp8(h, int(layer), int(expert), buf.ctypes.data, n), h)
+    o = 0
+    out = {}
+    for name, shape in (("gate", (f, d)), ("up", (f, d)), ("down", (d, f))):
+        out[name + "_codes"] = buf[o:o + f * d].reshape(shape)
+        o += f * d
+    for name, shape in (("gate", (f,)), ("up", (f,)), ("down", (d, f // 32))):
+        k = int(np.prod(shape))
+        out[name + "_scales"] = buf[o:o + 4 * k].view(np.float32).reshape(shape)
+        o += 4 * k
+    return out
+
+
 def mk_query(h, what: int) -> int:
     v = ctypes.c_int64()
     _check(load_library().mk_query(h, what, ctypes.byref(v)), h)
@@ -336,6 +359,10 @@ class Megakernel:
     def hidden(self):
         c = self.cfg
         return mk_read(self.h, MK_READ_HIDDEN, (c["n_layers"] + 1, self.B, c["d_model"]), np.float32)
+
+    def expert_fp8(self, layer: int, expert: int) -> dict:
+        c = self.cfg
+        return mk_read_expert_fp8(self.h, layer, expert, c["d_model"], c["d_ff"])
 
     def routes(self):
         c = self.cfg

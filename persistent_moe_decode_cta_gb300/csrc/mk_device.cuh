@@ -4,6 +4,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -260,6 +262,37 @@ __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t u) {
 
 // ---------------------------------------------------------------- tensor cores
 // D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulate.
+// FP8 expert weights: fragments of E4M3 codes (one byte per element, in the order of
+// the bf16 fragment) widen exactly to f16 and multiply f16 activations.
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+// Four E4M3 codes -> two f16x2 of value * 2^-8, on the integer pipe: each code is
+// sign-extended to 16 bits (prmt's sign-replicate selectors), shifted left by 7 so
+// that its 4 exponent and 3 mantissa bits land in the f16 exponent and top mantissa
+// bits (bias 15 against 7: a factor 2^-8, subnormals included), and masked to keep
+// the sign in bit 15.  lo holds codes 0 and 1, hi codes 2 and 3.
+__device__ __forceinline__ void e4m3x4_to_f16x2_scaled(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x9180;" : "=r"(a) : "r"(x), "r"(0u));
+  asm("prmt.b32 %0, %1, %2, 0xB3A2;" : "=r"(b) : "r"(x), "r"(0u));
+  lo = (a << 7) & 0xBF80BF80u;
+  hi = (b << 7) & 0xBF80BF80u;
+}
+// bf16x2 -> f16x2 (round to nearest; exact in f16's normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+  const __half2 h = __floats2half2_rn(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "

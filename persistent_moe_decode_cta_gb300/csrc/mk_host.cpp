@@ -33,6 +33,8 @@ cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, cons
 cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_t st);
 cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f, int fs,
                             cudaStream_t st);
+cudaError_t launch_pack_moe_fp8(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+                                int fs, long long item_bytes, cudaStream_t st);
 cudaError_t prepare_megakernel();
 int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
@@ -55,6 +57,7 @@ struct Shape {
   int moe_fs, t_moe;
   uint64_t dense_mask;  // mixed stacks: dense layers
   int f_dense, t_dense;
+  bool fp8;             // routed experts as E4M3 codes + f32 scales
   int r_lm, v_pad, n_lm_tasks;
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
   size_t off_qkv, off_o, off_router, off_moe, off_dense, off_lm, off_embed, total;
@@ -121,13 +124,20 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   if (s.dense_mask && (s.f_dense < 128 || s.f_dense % 128 || s.f_dense > 4096))
     return fail(err, MK_ERR_UNSUPPORTED, "dense_ff %d must be a multiple of 128 <= 4096", s.f_dense);
   s.t_dense = s.f_dense / s.moe_fs;
+  if (c->expert_dtype != MK_EXPERT_BF16 && c->expert_dtype != MK_EXPERT_FP8)
+    return fail(err, MK_ERR_INVALID, "expert_dtype %d unknown", c->expert_dtype);
+  s.fp8 = c->expert_dtype == MK_EXPERT_FP8;
+  if (s.fp8 && s.moe_fs != 32)
+    return fail(err, MK_ERR_UNSUPPORTED, "FP8 experts need d_ff a multiple of 32 (f-slices of 32)");
+  if (s.fp8 && s.dense_mask) return fail(err, MK_ERR_UNSUPPORTED, "FP8 experts with dense layers");
   s.r_lm = 64;
   if (const char* e = getenv("MK_LM_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_lm = v; }
   s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
   s.router_layer_bytes = (size_t)s.e_pad * s.d * 2;
-  s.moe_item_bytes = (size_t)3 * s.moe_fs * s.d * 2;
+  s.moe_item_bytes = s.fp8 ? (size_t)fp8_scale_bytes(s.moe_fs, s.d) + (size_t)3 * s.moe_fs * s.d
+                           : (size_t)3 * s.moe_fs * s.d * 2;
   s.moe_bytes_e = s.moe_item_bytes * s.t_moe;
   s.lm_bytes = (size_t)s.v_pad * s.d * 2;
   s.embed_bytes = (size_t)s.V * s.d * 2;
@@ -661,8 +671,10 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
        PACK_IDENT, hd, gs, 0, s.r_router);
     for (int e2 = 0; e2 < E; ++e2) {
       const int i = l * E + e2;
-      e = launch_pack_moe(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i], w->w_down[i], d,
-                          f, s.moe_fs, st);
+      e = s.fp8 ? launch_pack_moe_fp8(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i],
+                                      w->w_down[i], d, f, s.moe_fs, (long long)s.moe_item_bytes, st)
+                : launch_pack_moe(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i],
+                                  w->w_down[i], d, f, s.moe_fs, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "pack moe"); return bail(MK_ERR_CUDA); }
     }
     e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
@@ -700,6 +712,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
     I[22] = P.c_md; I[23] = P.c_od; I[24] = s.nrb_d; I[25] = s.gs; I[26] = P.c_oa;
     I[27] = s.t_dense; I[28] = (int32_t)(uint32_t)(s.dense_mask & 0xffffffffull);
     I[29] = (int32_t)(uint32_t)(s.dense_mask >> 32);
+    I[30] = s.fp8 ? MK_EXPERT_FP8 : MK_EXPERT_BF16; I[31] = (int32_t)s.moe_item_bytes;
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
     return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
@@ -764,6 +777,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   if (const char* fl = getenv("MK_INFLIGHT_MOE")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight_moe = v; }
   p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
   p.dense_mask = s.dense_mask; p.t_dense = s.t_dense; p.off_dense = (long long)s.off_dense;
+  p.fp8 = s.fp8 ? 1 : 0;
   p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
   p.rope_turns = h->rope_turns;
   p.embed = reinterpret_cast<const uint16_t*>(h->wblob + s.off_embed);
@@ -1073,6 +1087,62 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
     default:
       return fail(&h->err, MK_ERR_INVALID, "mk_read: unknown item %d", what);
   }
+}
+
+int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size_t bytes) {
+  if (!h || !host_out) return fail(h ? &h->err : nullptr, MK_ERR_INVALID, "NULL argument");
+  const Shape& s = h->s;
+  if (!s.fp8) return fail(&h->err, MK_ERR_STATE, "experts are stored in bf16");
+  if (layer < 0 || layer >= s.L || expert < 0 || expert >= s.E)
+    return fail(&h->err, MK_ERR_INVALID, "layer %d / expert %d out of range", layer, expert);
+  const int d = s.d, f = s.f, fs = s.moe_fs, nrb1 = fs / 8, k2 = fs / 16, nb = f / 32;
+  const size_t need = (size_t)3 * f * d + 4 * ((size_t)2 * f + (size_t)d * nb);
+  if (bytes != need) return fail(&h->err, MK_ERR_INVALID, "mk_read_expert_fp8: need %zu bytes, got %zu", need, bytes);
+  std::vector<uint8_t> raw(s.moe_bytes_e);
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaDeviceSynchronize());
+  CK(h, cudaMemcpy(raw.data(), h->wblob + s.off_moe + ((size_t)layer * s.E + expert) * s.moe_bytes_e, raw.size(),
+                   cudaMemcpyDeviceToHost));
+  uint8_t* gc = static_cast<uint8_t*>(host_out);
+  uint8_t* uc = gc + (size_t)f * d;
+  uint8_t* dc = uc + (size_t)f * d;
+  float* gsc = reinterpret_cast<float*>(dc + (size_t)d * f);
+  float* usc = gsc + f;
+  float* dsc = usc + f;
+  const int sb = fp8_scale_bytes(fs, d);
+  // the inverse of the item packing: scales, then gate/up and down fragments whose
+  // lane holds rows g and g + 8, columns 2c, 2c + 1, 2c + 8, 2c + 9 of a 16x16 block
+  for (int t = 0; t < s.t_moe; ++t) {
+    const uint8_t* item = raw.data() + (size_t)t * s.moe_item_bytes;
+    float scl[2 * 32 + 2048];
+    memcpy(scl, item, (size_t)sb);
+    for (int rb = 0; rb < nrb1; ++rb)
+      for (int i = 0; i < 16; ++i) (i < 8 ? gsc : usc)[t * fs + 8 * rb + (i & 7)] = scl[rb * 16 + i];
+    for (int r = 0; r < d; ++r) dsc[(size_t)r * nb + t] = scl[2 * fs + r];
+    const uint8_t* gu = item + sb;
+    for (int fi = 0; fi < nrb1 * (d / 16); ++fi) {
+      const int j = fi / (nrb1 * 8), rem = fi % (nrb1 * 8), rb = rem / 8, ks = rem % 8 + 8 * j;
+      for (int lane = 0; lane < 32; ++lane)
+        for (int q = 0; q < 4; ++q)
+          for (int e = 0; e < 2; ++e) {
+            const int i = (lane >> 2) + ((q & 1) ? 8 : 0);
+            const int k = 16 * ks + 2 * (lane & 3) + ((q & 2) ? 8 : 0) + e;
+            (i < 8 ? gc : uc)[(size_t)(t * fs + 8 * rb + (i & 7)) * d + k] = gu[((size_t)fi * 32 + lane) * 8 + 2 * q + e];
+          }
+    }
+    const uint8_t* dn = gu + (size_t)2 * fs * d;
+    for (int fi = 0; fi < (d / 16) * k2; ++fi) {
+      const int rb = fi / k2, ks = fi % k2;
+      for (int lane = 0; lane < 32; ++lane)
+        for (int q = 0; q < 4; ++q)
+          for (int e = 0; e < 2; ++e) {
+            const int row = rb * 16 + (lane >> 2) + ((q & 1) ? 8 : 0);
+            const int col = t * fs + 16 * ks + 2 * (lane & 3) + ((q & 2) ? 8 : 0) + e;
+            dc[(size_t)row * f + col] = dn[((size_t)fi * 32 + lane) * 8 + 2 * q + e];
+          }
+    }
+  }
+  return MK_OK;
 }
 
 int mk_query(mk_handle* h, int what, int64_t* out) {

@@ -31,6 +31,7 @@ constexpr int kSmallBytes = 1024;             // per-warp scalars, flags
 constexpr int kMbox = 8;                      // producer -> consumer task mailbox
 constexpr int kSq = 8;                        // consumer -> storer signal queue
 constexpr int kFragBytes = 512;               // one 16x16 bf16 MMA A-fragment
+constexpr int kFragBytes8 = 256;              // the same fragment in E4M3 codes (FP8 experts)
 constexpr int kFragsPerStage = kStageBytes / kFragBytes;
 constexpr int kMaxNrb = 8;                    // GEMV task rows <= 128
 constexpr int kMaxKsw = 16;                   // GEMV task K <= 2048 (16 k16-steps/warp)
@@ -61,6 +62,11 @@ constexpr int kMaxActive = kMaxBatch * 8;     // active experts per layer <= bat
 constexpr int kRowBlock = 128;                // residual row block (rows of d_model)
 // j-groups per ring chunk of a GEMV tile with `nrb` 16-row blocks (chunk = jpc*nrb*4 KB)
 constexpr __host__ __device__ int gemv_jpc(int nrb) { return 8 / nrb > 0 ? 8 / nrb : 1; }
+// FP8 fragments are half the bytes: twice the j-groups per 32 KB ring chunk
+constexpr __host__ __device__ int gemv_jpc8(int nrb) { return 16 / nrb > 0 ? 16 / nrb : 1; }
+// FP8 expert item: [scales: 2*fs gate/up row scales, then d down-row scales, f32]
+// [gate/up E4M3 fragments: 2*fs*d bytes][down E4M3 fragments: d*fs bytes]
+constexpr __host__ __device__ int fp8_scale_bytes(int fs, int d) { return (2 * fs + d) * 4; }
 // consumer warps whose down-slice regions share one ring chunk (a power of two)
 constexpr __host__ __device__ int moe_warps_per_chunk(int region_bytes) {
   return region_bytes * 8 <= 32768 ? 8 : region_bytes * 4 <= 32768 ? 4 : region_bytes * 2 <= 32768 ? 2 : 1;
@@ -116,6 +122,7 @@ struct Params {
   int fixed, do_reset;
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   int inflight_moe;         // the same for the chunks of expert items
+  int fp8;                  // expert weights as E4M3 codes with f32 scales (items: see fp8_scale_bytes)
   // mixed dense/MoE stacks: bit l set = layer l is dense, its FFN is t_dense items (one
   // per moe_fs rows of dense_ff) at off_dense + (r * t_dense + t) * moe_item_bytes, r =
   // the number of dense layers below l

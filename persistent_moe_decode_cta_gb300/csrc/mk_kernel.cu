@@ -592,13 +592,16 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         if (!fetch(dense ? 0 : item / p.t_moe)) { ok = false; break; }
         const int count = dense ? p.t_dense : nact * p.t_moe;
         // part 1 (gate/up tile) in whole k16-groups, part 2 (down slice) in warp regions
+        // (FP8: a chunk of the item's scales first, fragments of half the bytes)
         const int nrb1 = p.moe_fs / 8;
-        const int cs1 = gemv_jpc(nrb1) * nrb1 * 8 * kFragBytes;
-        const int gu_bytes = 2 * p.moe_fs * p.d * 2;
-        const int region = (p.d / 128) * (p.moe_fs / 16) * kFragBytes;
+        const int fb = p.fp8 ? kFragBytes8 : kFragBytes;
+        const int sb = p.fp8 ? fp8_scale_bytes(p.moe_fs, p.d) : 0;
+        const int cs1 = (p.fp8 ? gemv_jpc8(nrb1) : gemv_jpc(nrb1)) * nrb1 * 8 * fb;
+        const int gu_bytes = 2 * p.moe_fs * p.d * fb / 256;
+        const int region = (p.d / 128) * (p.moe_fs / 16) * fb;
         const int cs2 = moe_warps_per_chunk(region) * region;
-        const int dn_bytes = (int)p.moe_item_bytes - gu_bytes;
-        const int nch = (gu_bytes + cs1 - 1) / cs1 + (dn_bytes + cs2 - 1) / cs2;
+        const int dn_bytes = (int)p.moe_item_bytes - sb - gu_bytes;
+        const int nch = (sb > 0) + (gu_bytes + cs1 - 1) / cs1 + (dn_bytes + cs2 - 1) / cs2;
         // O-proj tiles of the layer as a queue (D_KLEN tiles from task D_K0; none when
         // they are dealt statically): taken before expert items once all attention
         // outputs of the layer are complete, and after the expert queue empties
@@ -636,8 +639,9 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
           const int fl = p.inflight_moe;
           ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
                          make_int4(tl_w[4], tl_w[5], tl_w[6], tl_w[7])) &&
-               issue_linear(p, S, cseq, src, gu_bytes, pol, ti, cs1, fl) &&
-               issue_linear(p, S, cseq, src + gu_bytes, dn_bytes, pol, ti, cs2, fl);
+               (sb == 0 || issue_linear(p, S, cseq, src, sb, pol, ti, sb, fl)) &&
+               issue_linear(p, S, cseq, src + sb, gu_bytes, pol, ti, cs1, fl) &&
+               issue_linear(p, S, cseq, src + sb + gu_bytes, dn_bytes, pol, ti, cs2, fl);
         }
         // after the expert queue empties: while the layer's attention outputs are
         // incomplete a producer holds at most one O-proj tile (its weights land while
@@ -752,6 +756,54 @@ __device__ __forceinline__ bool gemv_run(const Params& p, const Smem& S, uint32_
                                          const BFrag& fr, float (&v)[4], const BFrag* lo = nullptr) {
   float acc[NRB][4];
   if (!gemv_mainloop<NRB>(p, S, cseq, nch, ksw, fr, acc, lo)) return false;
+  trace_mark(p, S, 3);
+  gemv_reduce<NRB>(S, acc, v);
+  return true;
+}
+
+// The same GEMV on E4M3 weight fragments (FP8 experts): 8 bytes a lane per fragment,
+// widened exactly to f16 and multiplied with the f16 operand `fr` (f32 accumulation);
+// twice the j-groups per ring chunk.  The row scales are applied by the caller.
+// One E4M3 A-fragment (8 codes a lane) decoded on the integer pipe to f16 values
+// scaled by 2^-8 (undone with the f32 scales) and multiplied in.  (The conversion
+// instruction was measured slower here: -1.5% at batch 1 with the whole decode on it,
+// -1.3% with half.)
+__device__ __forceinline__ void fp8_mma(float (&acc)[4], uint2 a, uint32_t b0, uint32_t b1) {
+  uint32_t r0, r1, r2, r3;
+  e4m3x4_to_f16x2_scaled(a.x, r0, r1);
+  e4m3x4_to_f16x2_scaled(a.y, r2, r3);
+  mma_f16(acc, r0, r1, r2, r3, b0, b1);
+}
+
+template <int NRB>
+__device__ __forceinline__ bool gemv_run8(const Params& p, const Smem& S, uint32_t& cseq, int nch, int ksw,
+                                          const BFrag& fr, float (&v)[4]) {
+  constexpr int JPC = gemv_jpc8(NRB);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float acc[NRB][4];
+#pragma unroll
+  for (int r = 0; r < NRB; ++r) acc[r][0] = acc[r][1] = acc[r][2] = acc[r][3] = 0.f;
+  if (nch > 0) {
+#pragma unroll
+    for (int j = 0; j < kMaxKsw; ++j) {
+      if (j < ksw) {
+        const int c = j / JPC;
+        if (j % JPC == 0) {
+          if (c > 0) release_stage(S, cseq + c - 1);
+          if (!wait_full(p, S, cseq + c)) return false;
+          if (c == 0) trace_mark(p, S, 2);
+        }
+        const uint32_t base = S.stage(cseq + c) + ((j % JPC) * NRB * 8 + warp) * kFragBytes8 + lane * 8;
+#pragma unroll
+        for (int rb = 0; rb < NRB; ++rb) {
+          const uint2 a = lds64(base + rb * 8 * kFragBytes8);
+          fp8_mma(acc[rb], a, fr.b0[j], fr.b1[j]);
+        }
+      }
+    }
+    release_stage(S, cseq + (ksw - 1) / JPC);
+    cseq += nch;
+  }
   trace_mark(p, S, 3);
   gemv_reduce<NRB>(S, acc, v);
   return true;
@@ -1383,7 +1435,10 @@ __device__ bool task_resid(const Params& p, const Smem& S, uint32_t& sseq, const
 //            token's routing weight, added into the layer's MoE accumulator.
 // Completion is counted on the layer's MoE-done counter (padded to max_active * t_moe
 // by the route step).
-template <int FS>
+// F8: the expert's weights are E4M3 codes (FP8 experts): the item's first chunk holds
+// its f32 row scales (copied to shared memory), the operand and the SiLU product are
+// f16, and each GEMV output is scaled by its row's scale.
+template <int FS, bool F8 = false>
 __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, const int* T,
                                          int ti, int item, int nch, int ntok, int tok_lo, int tok_hi, int4 w_lo,
                                          int4 w_hi, BFrag& fr, OperandKey& have, float& rs_have) {
@@ -1415,13 +1470,37 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
   if (!reuse) {
     const int n = lane >> 2;
     rs_have = build_norm_bfrag(p, S, fr, ksw1, l, (n < ntok) ? (tok_byte(n) >> 3) : -1);
+    if (F8) {  // the operand in f16 (kept so for the next items of this token set)
+#pragma unroll
+      for (int j = 0; j < kMaxKsw; ++j) {
+        fr.b0[j] = bf16x2_to_f16x2(fr.b0[j]);
+        fr.b1[j] = bf16x2_to_f16x2(fr.b1[j]);
+      }
+    }
     have = key;
+  }
+  // FP8: the scales chunk -> shared memory [2*fs gate/up rows][d down rows] (f32)
+  const float* scl = reinterpret_cast<const float*>(reinterpret_cast<uint8_t*>(S.scratch) + 18432);
+  if (F8) {
+    if (!wait_full(p, S, cseq)) return false;
+    const int n16 = fp8_scale_bytes(FS, p.d) / 16;
+    const uint4* src = reinterpret_cast<const uint4*>(S.ring_g + (cseq % kStages) * kStageBytes);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(S.scratch) + 18432);
+    for (int i = threadIdx.x; i < n16; i += kConsumerThreads) dst[i] = src[i];
+    release_stage(S, cseq);
+    ++cseq;
+    bar_sync_consumers();
   }
   // ---- phase 1: 2*FS interleaved gate/up rows = FS/8 row blocks
   constexpr int fs = FS, nrb1 = FS / 8;
-  const int nch1 = (ksw1 + gemv_jpc(nrb1) - 1) / gemv_jpc(nrb1);
+  const int jpc1 = F8 ? gemv_jpc8(nrb1) : gemv_jpc(nrb1);
+  const int nch1 = (ksw1 + jpc1 - 1) / jpc1;
   float v[4];
-  if (!gemv_run<nrb1>(p, S, cseq, nch1, ksw1, fr, v)) return false;
+  if (F8) {
+    if (!gemv_run8<nrb1>(p, S, cseq, nch1, ksw1, fr, v)) return false;
+  } else {
+    if (!gemv_run<nrb1>(p, S, cseq, nch1, ksw1, fr, v)) return false;
+  }
   trace_mark(p, S, 12);
   uint16_t* a_s = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(S.scratch) + 28672);  // [8][fs]
   {
@@ -1433,9 +1512,13 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
       for (int e = 0; e < 2; ++e) {
         const int n = 2 * c + e;
         const float rs = e ? rs1 : rs0;
-        const float gt = v[e] * rs, up = v[2 + e] * rs;
+        // FP8: packed row 16w + g8 is gate row 8w + g8, row 16w + 8 + g8 its up row
+        // (x 256: the integer-pipe decode yields the codes' values x 2^-8)
+        const float sg = F8 ? scl[warp * 16 + g8] * 256.f : 1.f, su = F8 ? scl[warp * 16 + 8 + g8] * 256.f : 1.f;
+        const float gt = v[e] * rs * sg, up = v[2 + e] * rs * su;
         const float a = (n < ntok) ? gt / (1.f + __expf(-gt)) * up : 0.f;
-        a_s[n * fs + frow] = to_bf16(a);
+        // (FP8: fp16 range; a SwiGLU output beyond it saturates instead of becoming inf)
+        a_s[n * fs + frow] = F8 ? __half_as_ushort(__float2half_rn(fminf(fmaxf(a, -65504.f), 65504.f))) : to_bf16(a);
       }
     }
   }
@@ -1456,9 +1539,10 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
   // [64 rows] (stride 68 floats: conflict-free stores) and added into the accumulator
   // with 128-bit reductions, 16 lanes x 4 rows per token.
   const int rpw = p.d / 128;
-  const int rbc = moe_warps_per_chunk(rpw * k2 * kFragBytes) * rpw;
+  const int rbc = moe_warps_per_chunk(rpw * k2 * (F8 ? kFragBytes8 : kFragBytes)) * rpw;
   const int rbw = rbc / kConsumerWarps;
-  const int nch2 = nch - nch1;
+  const int nch2 = nch - nch1 - (F8 ? 1 : 0);
+  const float* sd = scl + 2 * fs;  // FP8: down-row scales of this slice
   constexpr int kStg = 68;
   float* stg = S.scratch + warp * (kMaxBatch * kStg);
   const int fq = (lane & 15) * 4;  // flush: this lane's 4 rows
@@ -1466,7 +1550,7 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
     if (!wait_full(p, S, cseq)) return false;
     if (ch == 0) trace_mark(p, S, 8);
     if (ch == nch2 - 1) trace_mark(p, S, 10);
-    const uint32_t base = S.stage(cseq) + lane * 16;
+    const uint32_t base = S.stage(cseq) + lane * (F8 ? 8 : 16);
     for (int i0 = 0; i0 < rbw; i0 += 4) {
       float acc[4][4];
 #pragma unroll
@@ -1476,18 +1560,29 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
           const int rbl = warp * rbw + i0 + u;
 #pragma unroll
           for (int ks = 0; ks < k2; ++ks) {
-            const uint4 a = lds128(base + (rbl * k2 + ks) * kFragBytes);
-            mma_bf16(acc[u], a.x, a.y, a.z, a.w, b2[ks][0], b2[ks][1]);
+            if (F8) {
+              const uint2 a = lds64(base + (rbl * k2 + ks) * kFragBytes8);
+              fp8_mma(acc[u], a, b2[ks][0], b2[ks][1]);
+            } else {
+              const uint4 a = lds128(base + (rbl * k2 + ks) * kFragBytes);
+              mma_bf16(acc[u], a.x, a.y, a.z, a.w, b2[ks][0], b2[ks][1]);
+            }
           }
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int rl = u * 16 + g8;
-        stg[(2 * c) * kStg + rl] = wt[0] * acc[u][0];
-        stg[(2 * c) * kStg + rl + 8] = wt[0] * acc[u][2];
-        stg[(2 * c + 1) * kStg + rl] = wt[1] * acc[u][1];
-        stg[(2 * c + 1) * kStg + rl + 8] = wt[1] * acc[u][3];
+        float s0 = 1.f, s1 = 1.f;
+        if (F8) {  // this slice's scales of output rows rg and rg + 8
+          const int rg = (ch * rbc + warp * rbw + i0 + u) * 16 + g8;
+          s0 = (i0 + u < rbw) ? sd[rg] * 256.f : 0.f;  // (x 256: see phase 1)
+          s1 = (i0 + u < rbw) ? sd[rg + 8] * 256.f : 0.f;
+        }
+        stg[(2 * c) * kStg + rl] = wt[0] * s0 * acc[u][0];
+        stg[(2 * c) * kStg + rl + 8] = wt[0] * s1 * acc[u][2];
+        stg[(2 * c + 1) * kStg + rl] = wt[1] * s0 * acc[u][1];
+        stg[(2 * c + 1) * kStg + rl + 8] = wt[1] * s1 * acc[u][3];
       }
       __syncwarp();
       const int nrow = min(4, rbw - i0) * 16;
@@ -1876,7 +1971,10 @@ __device__ void consumer(const Params& p, const Smem& S) {
         break;
       case OP_MOE_DRAIN:
         ok = (p.moe_fs == 32)
-                 ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have)
+                 ? (p.fp8 ? task_moe<32, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo,
+                                               ew_hi, fr, have, rs_have)
+                          : task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi,
+                                         fr, have, rs_have))
                  : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have);
         break;
       default:
@@ -2106,6 +2204,96 @@ __global__ void mk_pack_moe_kernel(uint8_t* __restrict__ dst, const uint16_t* __
   v.z = out[4] | ((uint32_t)out[5] << 16);
   v.w = out[6] | ((uint32_t)out[7] << 16);
   reinterpret_cast<uint4*>(dst)[u] = v;
+}
+
+// FP8 experts, setup (1): the f32 scales of each item of one expert -- gate/up rows
+// in packed-row order (block rb: 8 gate rows then their 8 up rows) over d, then the
+// down rows over the item's fs columns: max|w| / 448, 1 for an all-zero row.
+__global__ void mk_pack_moe_fp8_scales(uint8_t* __restrict__ dst, const uint16_t* __restrict__ gate,
+                                       const uint16_t* __restrict__ up, const uint16_t* __restrict__ down, int d,
+                                       int f, int fs, long long item_bytes) {
+  const int per = 2 * fs + d;
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= (long long)per * (f / fs)) return;
+  const int s = (int)(u / per), r = (int)(u % per);
+  float amax = 0.f;
+  if (r < 2 * fs) {
+    const int rb = r / 16, i = r % 16;
+    const uint16_t* src = (i < 8 ? gate : up) + ((size_t)s * fs + 8 * rb + (i & 7)) * d;
+    for (int k = 0; k < d; ++k) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
+  } else {
+    const uint16_t* src = down + (size_t)(r - 2 * fs) * f + (size_t)s * fs;
+    for (int k = 0; k < fs; ++k) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
+  }
+  reinterpret_cast<float*>(dst + (size_t)s * item_bytes)[r] = amax > 0.f ? amax / 448.f : 1.f;
+}
+
+// FP8 experts, setup (2): the E4M3 codes, in the bf16 fragment order (8 bytes a lane),
+// each element divided by its row's scale and rounded to the nearest code (ties to
+// even, saturating at 448).
+__global__ void mk_pack_moe_fp8_codes(uint8_t* __restrict__ dst, const uint16_t* __restrict__ gate,
+                                      const uint16_t* __restrict__ up, const uint16_t* __restrict__ down, int d,
+                                      int f, int fs, long long item_bytes) {
+  const int t_n = f / fs;
+  const int nrb1 = fs / 8, k2 = fs / 16;
+  const long long gu_units = (long long)nrb1 * (d / 16) * 32;
+  const long long dn_units = (long long)(d / 16) * k2 * 32;
+  const long long item_units = gu_units + dn_units;
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= item_units * t_n) return;
+  const int s = (int)(u / item_units);
+  const long long r = u % item_units;
+  const int lane = (int)(r & 31);
+  const int g8 = lane >> 2, c = lane & 3;
+  uint8_t* item = dst + (size_t)s * item_bytes;
+  const float* scl = reinterpret_cast<const float*>(item);
+  const int sb = fp8_scale_bytes(fs, d);
+  uint8_t out[8];
+  if (r < gu_units) {
+    const long long fi = r >> 5;
+    const int j = (int)(fi / (nrb1 * 8)), rem = (int)(fi % (nrb1 * 8));
+    const int rb = rem / 8, ks = rem % 8 + 8 * j;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = g8 + ((q & 1) ? 8 : 0);
+      const int k = 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
+      const uint16_t* src = (i < 8) ? gate : up;
+      const long long srow = (long long)s * fs + 8 * rb + (i & 7);
+      const float sc = scl[rb * 16 + i];
+      for (int e = 0; e < 2; ++e)
+        out[2 * q + e] = (uint8_t)__nv_cvt_float_to_fp8(__uint_as_float((uint32_t)src[srow * d + k + e] << 16) / sc,
+                                                        __NV_SATFINITE, __NV_E4M3);
+    }
+    *reinterpret_cast<uint2*>(item + sb + r * 8) =
+        make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 8) | ((uint32_t)out[2] << 16) | ((uint32_t)out[3] << 24),
+                   (uint32_t)out[4] | ((uint32_t)out[5] << 8) | ((uint32_t)out[6] << 16) | ((uint32_t)out[7] << 24));
+  } else {
+    const long long fi = (r - gu_units) >> 5;
+    const int rb = (int)(fi / k2), ks = (int)(fi % k2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const long long row = (long long)rb * 16 + g8 + ((q & 1) ? 8 : 0);
+      const int col = s * fs + 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
+      const float sc = scl[2 * fs + row];
+      for (int e = 0; e < 2; ++e)
+        out[2 * q + e] = (uint8_t)__nv_cvt_float_to_fp8(__uint_as_float((uint32_t)down[row * f + col + e] << 16) / sc,
+                                                        __NV_SATFINITE, __NV_E4M3);
+    }
+    *reinterpret_cast<uint2*>(item + sb + gu_units / 32 * kFragBytes8 + (r - gu_units) * 8) =
+        make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 8) | ((uint32_t)out[2] << 16) | ((uint32_t)out[3] << 24),
+                   (uint32_t)out[4] | ((uint32_t)out[5] << 8) | ((uint32_t)out[6] << 16) | ((uint32_t)out[7] << 24));
+  }
+}
+
+cudaError_t launch_pack_moe_fp8(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+                                int fs, long long item_bytes, cudaStream_t st) {
+  const long long nsc = (long long)(2 * fs + d) * (f / fs);
+  mk_pack_moe_fp8_scales<<<(unsigned)((nsc + 255) / 256), 256, 0, st>>>(
+      dst, (const uint16_t*)gate, (const uint16_t*)up, (const uint16_t*)down, d, f, fs, item_bytes);
+  const long long units = ((long long)(fs / 8) * (d / 16) * 32 + (long long)(d / 16) * (fs / 16) * 32) * (f / fs);
+  mk_pack_moe_fp8_codes<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(
+      dst, (const uint16_t*)gate, (const uint16_t*)up, (const uint16_t*)down, d, f, fs, item_bytes);
+  return cudaGetLastError();
 }
 
 __global__ void mk_convert_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, long long n) {

@@ -28,6 +28,16 @@ def param_counts(cfg: dict) -> dict:
                 active_step=active_no_embed, dense_layer=dense_layer, expert=expert)
 
 
+def expert_bytes(cfg: dict) -> int:
+    """Stored bytes of one routed expert: bf16 matrices, or (expert_dtype "fp8") E4M3
+    codes plus float32 scales -- one per gate and up row, one per down row and
+    32-column block."""
+    d, f = cfg["d_model"], cfg["d_ff"]
+    if cfg.get("expert_dtype", "bf16") == "fp8":
+        return 3 * d * f + 4 * (2 * f + d * (f // 32))
+    return BF16 * 3 * d * f
+
+
 def attended_cached_keys(p: int, window: int) -> int:
     """Cached keys (positions < p) read by a token at position p."""
     lo = 0 if window <= 0 else max(0, p - window + 1)
@@ -48,8 +58,8 @@ def step_bytes(cfg: dict, seq_lens, union_sizes) -> dict:
     n_dense = sum(1 for l in range(L) if l in dense)
     routed_union = sum(u for l, u in enumerate(union_sizes) if l not in dense)
     dense_ffn = 3 * d * cfg.get("dense_ff", 0)
-    weights = BF16 * (L * pc["dense_layer"] - n_dense * d * cfg["n_experts"] + routed_union * pc["expert"]
-                      + n_dense * dense_ffn + V * d + d + B * d)
+    weights = BF16 * (L * pc["dense_layer"] - n_dense * d * cfg["n_experts"]
+                      + n_dense * dense_ffn + V * d + d + B * d) + routed_union * expert_bytes(cfg)
     swa = set(cfg.get("swa_layers", ()))
     kv_read = 0
     for p in seq_lens:

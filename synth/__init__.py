@@ -44,6 +44,10 @@ MODELS["pages_l1"] = dict(MODELS["pages"], n_layers=1)
 # The pages-scale shape with its first three layers dense (FFN width 4096), for the
 # mixed-stack measurement.
 MODELS["pages_dense3"] = dict(MODELS["pages"], dense_layers=(0, 1, 2), dense_ff=4096)
+# The same shapes with the routed experts stored as E4M3 codes + float32 scales (the
+# weights drawn are the bf16 ones; quantisation happens when the model is loaded).
+for _m in ("tiny", "small", "pages", "pages_l2"):
+    MODELS[_m + "_fp8"] = dict(MODELS[_m], expert_dtype="fp8")
 
 # Workloads: a model plus a batch of cached sequence lengths.
 WORKLOADS = {
@@ -60,6 +64,10 @@ WORKLOADS = {
     "tiny_dense_b1_64": dict(model="tiny_dense", batch=1, lens=("fixed", 64)),
     "pages_dense3_b1_8k": dict(model="pages_dense3", batch=1, lens=("fixed", 8192)),
     "small_dense_b1_2k": dict(model="small_dense", batch=1, lens=("fixed", 2048)),
+    "tiny_fp8_b1_64": dict(model="tiny_fp8", batch=1, lens=("fixed", 64)),
+    "small_fp8_b1_2k": dict(model="small_fp8", batch=1, lens=("fixed", 2048)),
+    "pages_fp8_b1_8k": dict(model="pages_fp8", batch=1, lens=("fixed", 8192)),
+    "pages_l2_fp8_b1_8k": dict(model="pages_l2_fp8", batch=1, lens=("fixed", 8192)),
 }
 
 

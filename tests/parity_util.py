@@ -124,3 +124,39 @@ def check_step(cfg, mk, W, seq, pt, kv_before, tokens_np, logits_gpu, k_after=No
         assert torch.equal(kv_before[1].permute(0, 1, 3, 2, 4)[mask].view(torch.int16),
                            v_after.permute(0, 1, 3, 2, 4)[mask].view(torch.int16))
     return out
+
+
+def check_layer_teacher_forced(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l):
+    """Layer l checked on the GPU's own input x_l: routing (where the oracle's top-k
+    margin >= MARGIN; the oracle then takes the GPU's selection), the layer output
+    x_{l+1}, the active-expert bookkeeping and the K/V written at the layer."""
+    x = hid[l].astype(np.float64)
+    Bn = len(seq)
+    # routing on the GPU's own layer input
+    h = oracle.rms_norm(x, oracle.bf16_to_f64(HW.attn_norm(l)), cfg["rms_eps"])
+    r = h @ oracle.bf16_to_f64(HW.router(l)).T
+    forced = {}
+    for b in range(Bn):
+        idx, _, margin = oracle.router_topk(r[b], cfg["top_k"])
+        g_sel = [int(e) for e in gidx[l, b]]
+        if margin >= MARGIN:
+            assert sorted(g_sel) == sorted(int(e) for e in idx), (l, b, margin)
+        _, w_forced, _ = oracle.router_topk(r[b], cfg["top_k"], forced=g_sel)
+        assert np.abs(w_forced - gw[l, b]).max() < 1e-3, (l, b)
+        forced[b] = g_sel
+    x_next, info = oracle.layer_step(cfg, HW, HK, l, x, seq, pt, forced=forced)
+    err = rel_l2(hid[l + 1], x_next)
+    assert err <= REL_L2, (l, err)
+    want = []
+    per = {}
+    for b in range(Bn):
+        for j, e in enumerate(info["idx"][b]):
+            per.setdefault(int(e), []).append((b, j))
+    want = [(e, sorted(per[e])) for e in sorted(per)]
+    assert act[l] == want, (l, act[l], want)
+    for rec in info["kv"]:
+        gk = k[l, rec["page"], :, rec["slot"]].float().cpu().numpy()
+        gv = v[l, rec["page"], :, rec["slot"]].float().cpu().numpy()
+        assert rel_l2(gk, oracle.bf16_to_f64(rec["k"])) < REL_L2, (l, rec["b"])
+        assert rel_l2(gv, oracle.bf16_to_f64(rec["v"])) < REL_L2, (l, rec["b"])
+    return err

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "mk.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(mk_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(mk_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -49,3 +49,29 @@ def test_null_arguments_are_rejected():
     assert lib.mk_plan(None, 1, None, None, 1, 1) == B.MK_ERR_INVALID
     assert lib.mk_decode_step(None, None, None, None, None, None) == B.MK_ERR_INVALID
     lib.mk_destroy(None)
+    assert lib.mk_read_expert_fp8(None, 0, 0, None, 0) == B.MK_ERR_INVALID
+
+
+def test_fp8_expert_configs_without_device():
+    # the item size: scales (2 * 32 gate/up rows + d down rows, f32) + 3 * 32 * d codes
+    for wl in ("tiny_fp8_b1_64", "small_fp8_b1_2k", "pages_fp8_b1_8k"):
+        cfg = synth.model_config(wl)
+        _, _, _, info = B.mk_plan_dry(cfg, 1, 8)
+        d = cfg["d_model"]
+        assert info[30] == B.MK_EXPERT_FP8
+        assert info[31] == (2 * 32 + d) * 4 + 3 * 32 * d
+        assert info[5] == cfg["d_ff"] // 32
+    _, _, _, info = B.mk_plan_dry(synth.model_config("tiny_b1_64"), 1, 8)
+    assert info[30] == B.MK_EXPERT_BF16 and info[31] == 3 * 32 * 256 * 2
+    # FP8 experts need f-slices of 32 and no dense layers; an unknown dtype is invalid
+    for bad, code in ((dict(d_ff=176), B.MK_ERR_UNSUPPORTED),
+                      (dict(dense_layers=(0,), dense_ff=256), B.MK_ERR_UNSUPPORTED)):
+        cfg = dict(synth.model_config("tiny_fp8_b1_64"), **bad)
+        with pytest.raises(B.MkError) as e:
+            B.mk_plan_dry(cfg, 1, 8)
+        assert e.value.code == code, bad
+    c = B.make_config(synth.model_config("tiny_b1_64"))
+    c.expert_dtype = 7
+    info = np.zeros(32, dtype=np.int32)
+    assert B.load_library().mk_plan_dry(ctypes.byref(c), 1, 8, None, 0, None, None, 0,
+                                        info.ctypes.data) == B.MK_ERR_INVALID

@@ -1,0 +1,135 @@
+"""FP8 experts (expert_dtype "fp8"): the routed experts' matrices stored as E4M3 codes
+with float32 scales, decoded in the kernel.
+
+* The stored codes and scales, read back through mk_read_expert_fp8, are bit-equal to
+  the oracle's quantisation of the same bf16 weights (nearest code, ties to even,
+  saturating; scale = max|row| / 448 in float32) -- every expert of the tiny model,
+  sampled experts of the small and the pages-scale ones.
+* A decode step matches the oracle run on the decoded weights (routing teacher-forced,
+  the same tolerances as the bf16 path) through the megakernel, the per-op path and
+  its CUDA graph, at batch 1 to 8; and at the pages-scale sizes, on sampled layers in
+  the launch configuration the benchmark times.
+* Several steps in one launch equal the same steps with the greedy token fed back on
+  the host."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from persistent_moe_decode_cta_gb300 import binding as B
+
+import parity_util as PU
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_stored(mk, HW, l, e):
+    got = mk.expert_fp8(l, e)
+    wg, wu, wd = HW.expert(l, e)
+    for name, w, block in (("gate", wg, None), ("up", wu, None), ("down", wd, oracle.FP8_BLOCK)):
+        codes, scales = oracle.quantize_e4m3_rows(w, block)
+        assert np.array_equal(got[name + "_codes"], codes), (l, e, name)
+        assert np.array_equal(got[name + "_scales"].view(np.uint32), scales.view(np.uint32)), (l, e, name)
+
+
+@pytest.mark.parametrize("workload,pairs", [
+    ("tiny_fp8_b1_64", "all"),
+    ("small_fp8_b1_2k", [(0, 0), (3, 17), (7, 31)]),
+])
+def test_stored_codes_and_scales_equal_the_oracle_quantisation(workload, pairs):
+    cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload)
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    try:
+        HW = synth.HostWeights(W)
+        if pairs == "all":
+            pairs = [(l, e) for l in range(cfg["n_layers"]) for e in range(cfg["n_experts"])]
+        for l, e in pairs:
+            _check_stored(mk, HW, l, e)
+    finally:
+        mk.close()
+
+
+@pytest.mark.parametrize("workload,seq_lens,mode", [
+    ("tiny_fp8_b1_64", [64], "mega"),
+    ("tiny_fp8_b1_64", [61, 0, 17], "mega"),
+    ("tiny_fp8_b1_64", [61, 0, 17], "perop"),
+    ("small_fp8_b1_2k", [2048, 300], "mega"),
+    ("small_fp8_b1_2k", [2048, 300], "graph"),
+    ("small_fp8_b1_2k", [2048, 5, 900, 17, 64, 1, 333, 2000], "mega"),
+])
+def test_fp8_step_matches_oracle(workload, seq_lens, mode):
+    cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload, seq_lens=seq_lens)
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    try:
+        mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
+        kb, vb = k.clone(), v.clone()
+        logits = torch.empty(len(seq), cfg["vocab"], device="cuda")
+        if mode == "mega":
+            mk.step(tokens, k, v, logits)
+        else:
+            mk.step_perop(tokens, k, v, logits, use_graph=(mode == "graph"))
+        assert mk.status()["code"] == 0
+        PU.check_step(cfg, mk, W, seq, pt, (kb, vb), tokens.cpu().numpy(), logits, k, v)
+    finally:
+        mk.close()
+
+
+def test_fp8_multi_step_equals_single_steps():
+    n = 4
+    cfg, W, seq, pt, npages, k, v, tokens = PU.setup("tiny_fp8_b1_64", seq_lens=[62, 9, 30], steps=n)
+    pt_dev = torch.as_tensor(pt, device="cuda")
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    try:
+        k1, v1 = k.clone(), v.clone()
+        mk.plan(seq, pt_dev, npages)
+        lg1 = torch.empty(len(seq), cfg["vocab"], device="cuda")
+        t = tokens.clone()
+        host = []
+        for _ in range(n):
+            mk.step(t, k1, v1, lg1)
+            assert mk.status()["code"] == 0
+            t = lg1.argmax(-1).to(torch.int32)
+            host.append(t.cpu().numpy())
+        mk.plan(seq, pt_dev, npages)
+        lg2 = torch.empty_like(lg1)
+        out = mk.steps(tokens, n, k, v, lg2)
+        assert mk.status()["code"] == 0
+        assert np.array_equal(out.cpu().numpy(), np.stack(host))
+        assert PU.rel_l2(k.float().cpu().numpy(), k1.float().cpu().numpy()) < PU.REL_L2
+        assert PU.rel_l2(v.float().cpu().numpy(), v1.float().cpu().numpy()) < PU.REL_L2
+        assert float((lg1 - lg2).abs().max()) <= PU.LOGIT_ABS
+    finally:
+        mk.close()
+
+
+def test_fp8_pages_scale_sampled_layers_and_stored_form():
+    workload = "pages_fp8_b1_8k"
+    cfg = synth.model_config(workload)
+    W = synth.make_weights(cfg, seed=0, device="cuda")
+    seq = synth.seq_lens_for(workload, 0)
+    pt, npages = synth.make_page_table(seq, seed=0)
+    k, v = synth.make_kv(cfg, npages, seed=0, device="cuda")
+    tokens = synth.make_tokens(len(seq), cfg["vocab"], seed=0, device="cuda")
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    try:
+        HW, HK = synth.HostWeights(W), synth.HostKV(k, v)
+        for l, e in ((0, 0), (24, 63), (47, 127)):
+            _check_stored(mk, HW, l, e)
+        mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
+        logits = torch.empty(len(seq), cfg["vocab"], device="cuda")
+        mk.step(tokens, k, v, logits)
+        assert mk.status()["code"] == 0
+        hid = mk.hidden()
+        gidx, gw = mk.routes()
+        act = mk.active()
+        for l in (0, 24, 47):
+            PU.check_layer_teacher_forced(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l)
+            HW.drop_cache()
+        ref = oracle.lm_head(cfg, HW, hid[cfg["n_layers"]].astype(np.float64))
+        dmax = float(np.abs(logits.float().cpu().numpy() - ref).max())
+        assert dmax <= PU.LOGIT_ABS, dmax
+    finally:
+        mk.close()
+        del W, k, v
+        torch.cuda.empty_cache()

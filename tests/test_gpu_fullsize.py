@@ -32,39 +32,6 @@ def pages_weights():
     torch.cuda.empty_cache()
 
 
-def _check_layer(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l):
-    x = hid[l].astype(np.float64)
-    Bn = len(seq)
-    # routing on the GPU's own layer input
-    h = oracle.rms_norm(x, oracle.bf16_to_f64(HW.attn_norm(l)), cfg["rms_eps"])
-    r = h @ oracle.bf16_to_f64(HW.router(l)).T
-    forced = {}
-    for b in range(Bn):
-        idx, _, margin = oracle.router_topk(r[b], cfg["top_k"])
-        g_sel = [int(e) for e in gidx[l, b]]
-        if margin >= PU.MARGIN:
-            assert sorted(g_sel) == sorted(int(e) for e in idx), (l, b, margin)
-        _, w_forced, _ = oracle.router_topk(r[b], cfg["top_k"], forced=g_sel)
-        assert np.abs(w_forced - gw[l, b]).max() < 1e-3, (l, b)
-        forced[b] = g_sel
-    x_next, info = oracle.layer_step(cfg, HW, HK, l, x, seq, pt, forced=forced)
-    err = PU.rel_l2(hid[l + 1], x_next)
-    assert err <= PU.REL_L2, (l, err)
-    want = []
-    per = {}
-    for b in range(Bn):
-        for j, e in enumerate(info["idx"][b]):
-            per.setdefault(int(e), []).append((b, j))
-    want = [(e, sorted(per[e])) for e in sorted(per)]
-    assert act[l] == want, (l, act[l], want)
-    for rec in info["kv"]:
-        gk = k[l, rec["page"], :, rec["slot"]].float().cpu().numpy()
-        gv = v[l, rec["page"], :, rec["slot"]].float().cpu().numpy()
-        assert PU.rel_l2(gk, oracle.bf16_to_f64(rec["k"])) < PU.REL_L2, (l, rec["b"])
-        assert PU.rel_l2(gv, oracle.bf16_to_f64(rec["v"])) < PU.REL_L2, (l, rec["b"])
-    return err
-
-
 @pytest.mark.parametrize("workload,layers", [
     ("pages_b1_8k", [0, 1, 24, 47]),
     ("pages_b8_ragged_swa", [0, 1, 24, 47]),   # 1 and 47 are sliding-window layers
@@ -88,7 +55,7 @@ def test_pages_scale_step_sampled_layers_and_lm_head(pages_weights, workload, la
         act = mk.active()
         HW, HK = synth.HostWeights(W), synth.HostKV(k, v)
         for l in layers:
-            _check_layer(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l)
+            PU.check_layer_teacher_forced(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l)
             HW.drop_cache()
         # the LM head on the GPU's final hidden state
         ref = oracle.lm_head(cfg, HW, hid[cfg["n_layers"]].astype(np.float64))
