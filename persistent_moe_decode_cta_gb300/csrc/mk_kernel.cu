@@ -1649,6 +1649,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
   float oacc[NT][2];
 #pragma unroll
   for (int t = 0; t < NT; ++t) oacc[t][0] = oacc[t][1] = 0.f;
+  trace_mark(p, S, 11);  // (the Q loads are issued, not necessarily complete)
 
   for (int c0 = 0; c0 < it.np; c0 += 8) {
     const int n = min(8, it.np - c0);
@@ -1725,6 +1726,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
   float* so = S.scratch;                                   // [8][gs][HD]
   if (c == 0) sm_m[warp * 8 + g8] = m_run;
   bar_sync_consumers();
+  trace_mark(p, S, 8);
   float M = -INFINITY;
 #pragma unroll
   for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * 8 + g8]);
@@ -1738,6 +1740,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
     if (c == 0) sm_l[warp * 8 + g8] = l_run * sc;
   }
   bar_sync_consumers();
+  trace_mark(p, S, 9);
   float* dst = p.attp + ((size_t)l * p.Hkv * p.B * p.max_items_bg + it.part) * (size_t)(gs * (HD + 2));
   for (int o = threadIdx.x; o < gs * HD; o += kConsumerThreads) {
     float s = 0.f;
@@ -1753,6 +1756,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
     dst[gs * HD + h] = mm;
     dst[gs * HD + gs + h] = ll;
   }
+  trace_mark(p, S, 10);
   return true;
 }
 
