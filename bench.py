@@ -546,7 +546,7 @@ def main():
     # ---- CPU oracle baseline (rank 0, N = 1)
     if not args.no_cpu and rank == 0 and ws == 1:
         smp = OracleSampler(args.workload, args.seed)
-        step_s = smp.step_seconds(budget_s=12.0, max_layers=48)
+        step_s = smp.step_seconds(budget_s=12.0, max_layers=480)
         line["cpu_baseline"] = {"value": smp.B / step_s, "unit": UNIT, "cores": cpu_cores(),
                                 "kind": "oracle", "sample": smp.describe()}
     mk.close()
