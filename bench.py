@@ -181,7 +181,9 @@ def build_state(workload, seed, device):
     cfg = synth.model_config(workload)
     seq = synth.seq_lens_for(workload, seed)
     W = synth.make_weights(cfg, seed=seed, device=device)
-    mk = B.Megakernel(cfg, W, max_batch=8)
+    # a handle sized for the workload's batch where the packing depends on it (FP8 expert
+    # items are 32 rows of d_ff below batch 4, 64 from 4 up)
+    mk = B.Megakernel(cfg, W, max_batch=len(seq) if cfg.get("expert_dtype") == "fp8" else 8)
     st = plan_workload(mk, cfg, workload, seq, seed, device)
     return cfg, mk, st, W
 

@@ -59,10 +59,11 @@ typedef enum mk_status {
  * task types FFN_UPGATE_ACT and FFN_DOWN]
  * expert_dtype: MK_EXPERT_BF16 (0) keeps the routed experts' matrices in bf16;
  * MK_EXPERT_FP8 (1) stores them, at mk_create, as E4M3 codes (nearest, ties to even,
- * saturating) with one float32 scale per row (max |w| / 448; 1 for a zero row) -- per
- * row over all of d_model for gate and up, per row and 32-column block for down -- and
- * the kernel decodes the codes to fp16 for the MMA and applies the scales to its fp32
- * results.  It needs d_ff a multiple of 32 and no dense layers (MK_ERR_UNSUPPORTED).
+ * saturating) with one float32 scale per output channel (row) of gate, up and down
+ * (max |w| over the row / 448; 1 for a zero row), and the kernel decodes the codes to
+ * fp16 for the MMA and applies the scales to its fp32 results.  It needs no dense
+ * layers and d_ff a multiple of 64 (of 32 when max_batch < 4, where the expert items
+ * are 32 rows of d_ff instead of 64) (MK_ERR_UNSUPPORTED).
  * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
  * FP8 quantization is on the roadmap; the pages fix no format] */
 enum { MK_EXPERT_BF16 = 0, MK_EXPERT_FP8 = 1 };
@@ -260,9 +261,9 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
  * MK_EXPERT_FP8), unpacked to row-major arrays in HOST memory, one after another:
  *   gate codes u8 [d_ff][d_model], up codes u8 [d_ff][d_model],
  *   down codes u8 [d_model][d_ff], gate scales f32 [d_ff], up scales f32 [d_ff],
- *   down scales f32 [d_model][d_ff / 32]
- * (a weight decodes as value(code) * its row's -- or row block's -- scale).  `bytes`
- * must equal 3 * d_ff * d_model + 4 * (2 * d_ff + d_model * d_ff / 32).  Synchronises
+ *   down scales f32 [d_model]
+ * (a weight decodes as value(code) * its row's scale).  `bytes` must equal
+ * 3 * d_ff * d_model + 4 * (2 * d_ff + d_model).  Synchronises
  * the device; needs no plan.  MK_ERR_STATE if the experts are stored in bf16,
  * MK_ERR_INVALID for a NULL pointer, a layer or expert out of range or a wrong size.
  * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:

@@ -84,18 +84,17 @@ def f64_to_bf16(x) -> np.ndarray:
 # building blocks
 
 # ---------------------------------------------------------------- FP8 (E4M3) weights
-# The FP8 weight path stores expert matrices as E4M3 codes with float32 scales: gate
-# and up rows one scale per row, the down matrix one scale per row and 32-column block
-# (the f-slice the kernel streams); a code decodes as sign * value(code) * scale.
+# The FP8 weight path stores expert matrices as E4M3 codes with float32 scales, one
+# scale per output channel (row) of each of gate, up and down; a code decodes as
+# sign * value(code) * scale.
 # E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0 is
 # subnormal (m/8 * 2^-6); the largest finite value is 448; 0x7F/0xFF are NaN.
 # Quantisation rounds x / scale (a float32 division) to the nearest code, ties to
 # even, saturating to +-448; scale = max|row| / 448 (float32), 1 for an all-zero row.
 # [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "Current limitations":
-# FP8 weights are on the roadmap; the pages fix no format, E4M3 with float32 scales
-# is the reading taken]
+# FP8 weights are on the roadmap; the pages fix no format: E4M3 with per-channel
+# float32 scales is the reading taken]
 E4M3_MAX = 448.0
-FP8_BLOCK = 32
 
 
 def e4m3_to_f64(codes) -> np.ndarray:
@@ -151,11 +150,9 @@ def dequantize_e4m3(codes, scales, block=None) -> np.ndarray:
 
 
 def fp8_expert(wg_u16, wu_u16, wd_u16):
-    """The expert's matrices as the FP8 path stores them, decoded to float64."""
-    wg = dequantize_e4m3(*quantize_e4m3_rows(wg_u16))
-    wu = dequantize_e4m3(*quantize_e4m3_rows(wu_u16))
-    wd = dequantize_e4m3(*quantize_e4m3_rows(wd_u16, FP8_BLOCK), FP8_BLOCK)
-    return wg, wu, wd
+    """The expert's matrices as the FP8 path stores them (per-row scales), decoded to
+    float64."""
+    return tuple(dequantize_e4m3(*quantize_e4m3_rows(w)) for w in (wg_u16, wu_u16, wd_u16))
 
 
 def rms_norm(x, gain, eps):

@@ -249,10 +249,10 @@ def mk_read(h, what: int, shape, dtype) -> np.ndarray:
 
 def mk_read_expert_fp8(h, layer: int, expert: int, d_model: int, d_ff: int) -> dict:
     """The stored FP8 form of one routed expert, row-major: codes (uint8) and scales
-    (float32) of gate [d_ff, d_model], up [d_ff, d_model] and down [d_model, d_ff]
-    (down scales per row and 32-column block)."""
+    (float32, one per row) of gate [d_ff, d_model], up [d_ff, d_model] and down
+    [d_model, d_ff]."""
     d, f = int(d_model), int(d_ff)
-    n = 3 * f * d + 4 * (2 * f + d * (f // 32))
+    n = 3 * f * d + 4 * (2 * f + d)
     buf = np.empty(n, dtype=np.uint8)
     _check(load_library().mk_read_expert_fp8(h, int(layer), int(expert), buf.ctypes.data, n), h)
     o = 0
@@ -260,7 +260,7 @@ def mk_read_expert_fp8(h, layer: int, expert: int, d_model: int, d_ff: int) -> d
     for name, shape in (("gate", (f, d)), ("up", (f, d)), ("down", (d, f))):
         out[name + "_codes"] = buf[o:o + f * d].reshape(shape)
         o += f * d
-    for name, shape in (("gate", (f,)), ("up", (f,)), ("down", (d, f // 32))):
+    for name, shape in (("gate", (f,)), ("up", (f,)), ("down", (d,))):
         k = int(np.prod(shape))
         out[name + "_scales"] = buf[o:o + 4 * k].view(np.float32).reshape(shape)
         o += 4 * k

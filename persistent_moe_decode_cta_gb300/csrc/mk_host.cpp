@@ -118,17 +118,25 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
     const int v = atoi(e);
     if ((v == 16 || v == 32) && s.f % v == 0) s.moe_fs = v;
   }
+  // FP8 experts: f-slices of 64 rows for handles of max_batch >= 4 (fewer, longer items:
+  // +16% over 32-row items at batch 8 ragged), of 32 rows below (at batch 1 the 64-row
+  // items occupy only 96 SMs: -4% against 32-row ones)
+  if (c->expert_dtype != MK_EXPERT_BF16 && c->expert_dtype != MK_EXPERT_FP8)
+    return fail(err, MK_ERR_INVALID, "expert_dtype %d unknown", c->expert_dtype);
+  s.fp8 = c->expert_dtype == MK_EXPERT_FP8;
+  if (s.fp8) {
+    s.moe_fs = s.max_batch >= 4 ? 64 : 32;
+    if (const char* e = getenv("MK_FP8_FS")) { const int v = atoi(e); if (v == 32 || v == 64) s.moe_fs = v; }
+    if (s.f % s.moe_fs)
+      return fail(err, MK_ERR_UNSUPPORTED, "FP8 experts need d_ff a multiple of %d (f-slices of %d)", s.moe_fs,
+                  s.moe_fs);
+  }
   s.t_moe = s.f / s.moe_fs;
   s.dense_mask = s.L < 64 ? c->dense_layer_mask & ((1ull << s.L) - 1) : c->dense_layer_mask;
   s.f_dense = s.dense_mask ? c->dense_ff : 0;
   if (s.dense_mask && (s.f_dense < 128 || s.f_dense % 128 || s.f_dense > 4096))
     return fail(err, MK_ERR_UNSUPPORTED, "dense_ff %d must be a multiple of 128 <= 4096", s.f_dense);
   s.t_dense = s.f_dense / s.moe_fs;
-  if (c->expert_dtype != MK_EXPERT_BF16 && c->expert_dtype != MK_EXPERT_FP8)
-    return fail(err, MK_ERR_INVALID, "expert_dtype %d unknown", c->expert_dtype);
-  s.fp8 = c->expert_dtype == MK_EXPERT_FP8;
-  if (s.fp8 && s.moe_fs != 32)
-    return fail(err, MK_ERR_UNSUPPORTED, "FP8 experts need d_ff a multiple of 32 (f-slices of 32)");
   if (s.fp8 && s.dense_mask) return fail(err, MK_ERR_UNSUPPORTED, "FP8 experts with dense layers");
   s.r_lm = 64;
   if (const char* e = getenv("MK_LM_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_lm = v; }
@@ -1095,8 +1103,8 @@ int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size
   if (!s.fp8) return fail(&h->err, MK_ERR_STATE, "experts are stored in bf16");
   if (layer < 0 || layer >= s.L || expert < 0 || expert >= s.E)
     return fail(&h->err, MK_ERR_INVALID, "layer %d / expert %d out of range", layer, expert);
-  const int d = s.d, f = s.f, fs = s.moe_fs, nrb1 = fs / 8, k2 = fs / 16, nb = f / 32;
-  const size_t need = (size_t)3 * f * d + 4 * ((size_t)2 * f + (size_t)d * nb);
+  const int d = s.d, f = s.f, fs = s.moe_fs, nrb1 = fs / 8, k2 = fs / 16;
+  const size_t need = (size_t)3 * f * d + 4 * ((size_t)2 * f + (size_t)d);
   if (bytes != need) return fail(&h->err, MK_ERR_INVALID, "mk_read_expert_fp8: need %zu bytes, got %zu", need, bytes);
   std::vector<uint8_t> raw(s.moe_bytes_e);
   CK(h, cudaSetDevice(h->dev));
@@ -1114,11 +1122,12 @@ int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size
   // lane holds rows g and g + 8, columns 2c, 2c + 1, 2c + 8, 2c + 9 of a 16x16 block
   for (int t = 0; t < s.t_moe; ++t) {
     const uint8_t* item = raw.data() + (size_t)t * s.moe_item_bytes;
-    float scl[2 * 32 + 2048];
+    float scl[2 * 64 + 2048];
     memcpy(scl, item, (size_t)sb);
     for (int rb = 0; rb < nrb1; ++rb)
       for (int i = 0; i < 16; ++i) (i < 8 ? gsc : usc)[t * fs + 8 * rb + (i & 7)] = scl[rb * 16 + i];
-    for (int r = 0; r < d; ++r) dsc[(size_t)r * nb + t] = scl[2 * fs + r];
+    if (t == 0)  // (every item holds the expert's down-row scales)
+      for (int r = 0; r < d; ++r) dsc[r] = scl[2 * fs + r];
     const uint8_t* gu = item + sb;
     for (int fi = 0; fi < nrb1 * (d / 16); ++fi) {
       const int j = fi / (nrb1 * 8), rem = fi % (nrb1 * 8), rb = rem / 8, ks = rem % 8 + 8 * j;

@@ -64,7 +64,8 @@ constexpr int kRowBlock = 128;                // residual row block (rows of d_m
 constexpr __host__ __device__ int gemv_jpc(int nrb) { return 8 / nrb > 0 ? 8 / nrb : 1; }
 // FP8 fragments are half the bytes: twice the j-groups per 32 KB ring chunk
 constexpr __host__ __device__ int gemv_jpc8(int nrb) { return 16 / nrb > 0 ? 16 / nrb : 1; }
-// FP8 expert item: [scales: 2*fs gate/up row scales, then d down-row scales, f32]
+// FP8 expert item (fs = 32 or 64): [scales: 2*fs gate/up row scales, then the d
+// down-row scales of the expert, f32]
 // [gate/up E4M3 fragments: 2*fs*d bytes][down E4M3 fragments: d*fs bytes]
 constexpr __host__ __device__ int fp8_scale_bytes(int fs, int d) { return (2 * fs + d) * 4; }
 // consumer warps whose down-slice regions share one ring chunk (a power of two)

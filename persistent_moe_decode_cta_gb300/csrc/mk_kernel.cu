@@ -751,6 +751,35 @@ __device__ __forceinline__ void gemv_reduce(const Smem& S, const float (&acc)[NR
   }
 }
 
+// The same reduction through at most 16 KB of scratch (4 row blocks at a time): the
+// FP8 expert items keep their scales in the scratch above that.
+template <int NRB>
+__device__ __forceinline__ void gemv_reduce16k(const Smem& S, const float (&acc)[NRB][4], float (&out)[4]) {
+  if (NRB <= 4) {
+    gemv_reduce<NRB>(S, acc, out);
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float4* scr = reinterpret_cast<float4*>(S.scratch);
+  out[0] = out[1] = out[2] = out[3] = 0.f;
+#pragma unroll
+  for (int h = 0; h < NRB; h += 4) {
+    if (h > 0) bar_sync_consumers();  // every warp has read the previous half
+#pragma unroll
+    for (int rb = 0; rb < 4; ++rb)
+      scr[(warp * 4 + rb) * 32 + lane] =
+          make_float4(acc[h + rb][0], acc[h + rb][1], acc[h + rb][2], acc[h + rb][3]);
+    bar_sync_consumers();
+    if (warp >= h && warp < h + 4) {
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float4 v = scr[(w * 4 + warp - h) * 32 + lane];
+        out[0] += v.x; out[1] += v.y; out[2] += v.z; out[3] += v.w;
+      }
+    }
+  }
+}
+
 template <int NRB>
 __device__ __forceinline__ bool gemv_run(const Params& p, const Smem& S, uint32_t& cseq, int nch, int ksw,
                                          const BFrag& fr, float (&v)[4], const BFrag* lo = nullptr) {
@@ -805,7 +834,7 @@ __device__ __forceinline__ bool gemv_run8(const Params& p, const Smem& S, uint32
     cseq += nch;
   }
   trace_mark(p, S, 3);
-  gemv_reduce<NRB>(S, acc, v);
+  gemv_reduce16k<NRB>(S, acc, v);
   return true;
 }
 
@@ -1480,6 +1509,11 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
     have = key;
   }
   // FP8: the scales chunk -> shared memory [2*fs gate/up rows][d down rows] (f32)
+  // scratch: [0, 17408) phase-2 staging / [0, 16384) phase-1 reduction; [18432, ...) the
+  // scales; [28672, ...) the SwiGLU activations
+  static_assert(kConsumerWarps * kMaxBatch * 68 * 4 <= 18432 && 18432 + (2 * 64 + 2048) * 4 <= 28672 &&
+                    28672 + kMaxBatch * 64 * 2 <= kScratchBytes,
+                "MoE item scratch layout");
   const float* scl = reinterpret_cast<const float*>(reinterpret_cast<uint8_t*>(S.scratch) + 18432);
   if (F8) {
     if (!wait_full(p, S, cseq)) return false;
@@ -1974,11 +2008,13 @@ __device__ void consumer(const Params& p, const Smem& S) {
         for (int j = 0; j < kMaxKsw; ++j) fr.b0[j] = fr.b1[j] = 0u;
         break;
       case OP_MOE_DRAIN:
-        ok = (p.moe_fs == 32)
-                 ? (p.fp8 ? task_moe<32, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo,
-                                               ew_hi, fr, have, rs_have)
-                          : task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi,
-                                         fr, have, rs_have))
+        ok = p.fp8 ? (p.moe_fs == 64 ? task_moe<64, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
+                                                           ent2.y, ew_lo, ew_hi, fr, have, rs_have)
+                                     : task_moe<32, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
+                                                           ent2.y, ew_lo, ew_hi, fr, have, rs_have))
+             : (p.moe_fs == 32)
+                 ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have,
+                                rs_have)
                  : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have);
         break;
       default:
@@ -2210,9 +2246,10 @@ __global__ void mk_pack_moe_kernel(uint8_t* __restrict__ dst, const uint16_t* __
   reinterpret_cast<uint4*>(dst)[u] = v;
 }
 
-// FP8 experts, setup (1): the f32 scales of each item of one expert -- gate/up rows
-// in packed-row order (block rb: 8 gate rows then their 8 up rows) over d, then the
-// down rows over the item's fs columns: max|w| / 448, 1 for an all-zero row.
+// FP8 experts, setup (1): the f32 scales of each item of one expert, one per output
+// channel -- its gate/up rows in packed-row order (block rb: 8 gate rows then their 8
+// up rows), then every down row (the same in each item of the expert): max|w| over
+// the whole row / 448, 1 for an all-zero row.
 __global__ void mk_pack_moe_fp8_scales(uint8_t* __restrict__ dst, const uint16_t* __restrict__ gate,
                                        const uint16_t* __restrict__ up, const uint16_t* __restrict__ down, int d,
                                        int f, int fs, long long item_bytes) {
@@ -2226,8 +2263,8 @@ __global__ void mk_pack_moe_fp8_scales(uint8_t* __restrict__ dst, const uint16_t
     const uint16_t* src = (i < 8 ? gate : up) + ((size_t)s * fs + 8 * rb + (i & 7)) * d;
     for (int k = 0; k < d; ++k) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
   } else {
-    const uint16_t* src = down + (size_t)(r - 2 * fs) * f + (size_t)s * fs;
-    for (int k = 0; k < fs; ++k) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
+    const uint16_t* src = down + (size_t)(r - 2 * fs) * f;
+    for (int k = 0; k < f; ++k) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
   }
   reinterpret_cast<float*>(dst + (size_t)s * item_bytes)[r] = amax > 0.f ? amax / 448.f : 1.f;
 }

@@ -29,12 +29,11 @@ def param_counts(cfg: dict) -> dict:
 
 
 def expert_bytes(cfg: dict) -> int:
-    """Stored bytes of one routed expert: bf16 matrices, or (expert_dtype "fp8") E4M3
-    codes plus float32 scales -- one per gate and up row, one per down row and
-    32-column block."""
+    """Bytes of one routed expert: bf16 matrices, or (expert_dtype "fp8") E4M3 codes
+    plus one float32 scale per row of gate, up and down."""
     d, f = cfg["d_model"], cfg["d_ff"]
     if cfg.get("expert_dtype", "bf16") == "fp8":
-        return 3 * d * f + 4 * (2 * f + d * (f // 32))
+        return 3 * d * f + 4 * (2 * f + d)
     return BF16 * 3 * d * f
 
 

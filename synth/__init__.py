@@ -68,6 +68,8 @@ WORKLOADS = {
     "small_fp8_b1_2k": dict(model="small_fp8", batch=1, lens=("fixed", 2048)),
     "pages_fp8_b1_8k": dict(model="pages_fp8", batch=1, lens=("fixed", 8192)),
     "pages_l2_fp8_b1_8k": dict(model="pages_l2_fp8", batch=1, lens=("fixed", 8192)),
+    "pages_fp8_b8_ragged_swa": dict(model="pages_fp8", batch=8, lens=("uniform", 1024, 32768),
+                                    sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
 }
 
 
@@ -100,7 +102,8 @@ def seq_lens_for(workload: str, seed: int = 0) -> list[int]:
     if kind == "fixed":
         return [w["lens"][1]] * w["batch"]
     lo, hi = w["lens"][1], w["lens"][2]
-    rng = np.random.default_rng(_seed("seq_lens", workload, seed))
+    # (a variant of a workload -- e.g. its FP8 form -- draws the same lengths)
+    rng = np.random.default_rng(_seed("seq_lens", w.get("lens_of", workload), seed))
     return [int(v) for v in rng.integers(lo, hi + 1, size=w["batch"])]
 
 

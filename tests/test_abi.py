@@ -53,18 +53,26 @@ def test_null_arguments_are_rejected():
 
 
 def test_fp8_expert_configs_without_device():
-    # the item size: scales (2 * 32 gate/up rows + d down rows, f32) + 3 * 32 * d codes
+    # FP8 items are 64 rows of d_ff: scales (2 * 64 gate/up rows + d down rows, f32) +
+    # 3 * 64 * d codes
     for wl in ("tiny_fp8_b1_64", "small_fp8_b1_2k", "pages_fp8_b1_8k"):
         cfg = synth.model_config(wl)
         _, _, _, info = B.mk_plan_dry(cfg, 1, 8)
         d = cfg["d_model"]
         assert info[30] == B.MK_EXPERT_FP8
-        assert info[31] == (2 * 32 + d) * 4 + 3 * 32 * d
-        assert info[5] == cfg["d_ff"] // 32
+        assert info[31] == (2 * 64 + d) * 4 + 3 * 64 * d
+        assert info[5] == cfg["d_ff"] // 64 and info[8] == 64
+    # handles for batches below 4 take 32-row FP8 items
+    cfg = synth.model_config("pages_fp8_b1_8k")
+    _, _, _, info = B.mk_plan_dry(cfg, 1, 8, max_batch=2)
+    assert info[8] == 32 and info[31] == (2 * 32 + 2048) * 4 + 3 * 32 * 2048
     _, _, _, info = B.mk_plan_dry(synth.model_config("tiny_b1_64"), 1, 8)
     assert info[30] == B.MK_EXPERT_BF16 and info[31] == 3 * 32 * 256 * 2
-    # FP8 experts need f-slices of 32 and no dense layers; an unknown dtype is invalid
-    for bad, code in ((dict(d_ff=176), B.MK_ERR_UNSUPPORTED),
+    # FP8 experts need f-slices of 64 and no dense layers; an unknown dtype is invalid
+    with pytest.raises(B.MkError) as e:
+        B.mk_plan_dry(dict(synth.model_config("tiny_fp8_b1_64"), d_ff=176), 1, 8, max_batch=2)
+    assert e.value.code == B.MK_ERR_UNSUPPORTED
+    for bad, code in ((dict(d_ff=160), B.MK_ERR_UNSUPPORTED),
                       (dict(dense_layers=(0,), dense_ff=256), B.MK_ERR_UNSUPPORTED)):
         cfg = dict(synth.model_config("tiny_fp8_b1_64"), **bad)
         with pytest.raises(B.MkError) as e:

@@ -3,7 +3,7 @@ with float32 scales, decoded in the kernel.
 
 * The stored codes and scales, read back through mk_read_expert_fp8, are bit-equal to
   the oracle's quantisation of the same bf16 weights (nearest code, ties to even,
-  saturating; scale = max|row| / 448 in float32) -- every expert of the tiny model,
+  saturating; one scale per row = max|row| / 448 in float32) -- every expert of the tiny model,
   sampled experts of the small and the pages-scale ones.
 * A decode step matches the oracle run on the decoded weights (routing teacher-forced,
   the same tolerances as the bf16 path) through the megakernel, the per-op path and
@@ -27,19 +27,21 @@ pytestmark = pytest.mark.gpu
 def _check_stored(mk, HW, l, e):
     got = mk.expert_fp8(l, e)
     wg, wu, wd = HW.expert(l, e)
-    for name, w, block in (("gate", wg, None), ("up", wu, None), ("down", wd, oracle.FP8_BLOCK)):
-        codes, scales = oracle.quantize_e4m3_rows(w, block)
+    for name, w in (("gate", wg), ("up", wu), ("down", wd)):
+        codes, scales = oracle.quantize_e4m3_rows(w)
         assert np.array_equal(got[name + "_codes"], codes), (l, e, name)
         assert np.array_equal(got[name + "_scales"].view(np.uint32), scales.view(np.uint32)), (l, e, name)
 
 
-@pytest.mark.parametrize("workload,pairs", [
-    ("tiny_fp8_b1_64", "all"),
-    ("small_fp8_b1_2k", [(0, 0), (3, 17), (7, 31)]),
+# max_batch 8: expert items of 64 rows of d_ff; below 4: of 32 rows
+@pytest.mark.parametrize("workload,pairs,max_batch", [
+    ("tiny_fp8_b1_64", "all", 8),
+    ("tiny_fp8_b1_64", "all", 2),
+    ("small_fp8_b1_2k", [(0, 0), (3, 17), (7, 31)], 8),
 ])
-def test_stored_codes_and_scales_equal_the_oracle_quantisation(workload, pairs):
+def test_stored_codes_and_scales_equal_the_oracle_quantisation(workload, pairs, max_batch):
     cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload)
-    mk = B.Megakernel(cfg, W, max_batch=8)
+    mk = B.Megakernel(cfg, W, max_batch=max_batch)
     try:
         HW = synth.HostWeights(W)
         if pairs == "all":
@@ -50,17 +52,20 @@ def test_stored_codes_and_scales_equal_the_oracle_quantisation(workload, pairs):
         mk.close()
 
 
-@pytest.mark.parametrize("workload,seq_lens,mode", [
-    ("tiny_fp8_b1_64", [64], "mega"),
-    ("tiny_fp8_b1_64", [61, 0, 17], "mega"),
-    ("tiny_fp8_b1_64", [61, 0, 17], "perop"),
-    ("small_fp8_b1_2k", [2048, 300], "mega"),
-    ("small_fp8_b1_2k", [2048, 300], "graph"),
-    ("small_fp8_b1_2k", [2048, 5, 900, 17, 64, 1, 333, 2000], "mega"),
+@pytest.mark.parametrize("workload,seq_lens,mode,max_batch", [
+    ("tiny_fp8_b1_64", [64], "mega", 8),
+    ("tiny_fp8_b1_64", [61, 0, 17], "mega", 8),
+    ("tiny_fp8_b1_64", [61, 0, 17], "perop", 8),
+    ("tiny_fp8_b1_64", [61, 17], "mega", 2),
+    ("tiny_fp8_b1_64", [64], "perop", 1),
+    ("small_fp8_b1_2k", [2048, 300], "mega", 8),
+    ("small_fp8_b1_2k", [2048, 300], "graph", 8),
+    ("small_fp8_b1_2k", [2048, 300], "mega", 2),
+    ("small_fp8_b1_2k", [2048, 5, 900, 17, 64, 1, 333, 2000], "mega", 8),
 ])
-def test_fp8_step_matches_oracle(workload, seq_lens, mode):
+def test_fp8_step_matches_oracle(workload, seq_lens, mode, max_batch):
     cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload, seq_lens=seq_lens)
-    mk = B.Megakernel(cfg, W, max_batch=8)
+    mk = B.Megakernel(cfg, W, max_batch=max_batch)
     try:
         mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
         kb, vb = k.clone(), v.clone()
@@ -103,15 +108,18 @@ def test_fp8_multi_step_equals_single_steps():
         mk.close()
 
 
-def test_fp8_pages_scale_sampled_layers_and_stored_form():
-    workload = "pages_fp8_b1_8k"
+@pytest.mark.parametrize("workload,layers", [
+    ("pages_fp8_b1_8k", (0, 24, 47)),
+    ("pages_fp8_b8_ragged_swa", (0, 1, 47)),   # 1 and 47 are sliding-window layers
+])
+def test_fp8_pages_scale_sampled_layers_and_stored_form(workload, layers):
     cfg = synth.model_config(workload)
     W = synth.make_weights(cfg, seed=0, device="cuda")
     seq = synth.seq_lens_for(workload, 0)
     pt, npages = synth.make_page_table(seq, seed=0)
     k, v = synth.make_kv(cfg, npages, seed=0, device="cuda")
     tokens = synth.make_tokens(len(seq), cfg["vocab"], seed=0, device="cuda")
-    mk = B.Megakernel(cfg, W, max_batch=8)
+    mk = B.Megakernel(cfg, W, max_batch=len(seq))  # as the benchmark sizes it
     try:
         HW, HK = synth.HostWeights(W), synth.HostKV(k, v)
         for l, e in ((0, 0), (24, 63), (47, 127)):
@@ -123,7 +131,7 @@ def test_fp8_pages_scale_sampled_layers_and_stored_form():
         hid = mk.hidden()
         gidx, gw = mk.routes()
         act = mk.active()
-        for l in (0, 24, 47):
+        for l in layers:
             PU.check_layer_teacher_forced(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l)
             HW.drop_cache()
         ref = oracle.lm_head(cfg, HW, hid[cfg["n_layers"]].astype(np.float64))

@@ -421,7 +421,7 @@ def test_e4m3_row_quantisation_scale_and_error_bound():
 def test_fp8_experts_change_the_layer_only_by_the_quantisation():
     """With expert_dtype fp8 the layer equals the bf16 layer computed on the decoded
     weights, and differs from the bf16 weights' layer by a small amount."""
-    cfg = dict(TINY, d_ff=64)  # the FP8 down scales come per 32 columns of d_ff
+    cfg = dict(TINY, d_ff=64)
     W, pt, k, v = _setup(cfg)
     x = _x(2, 32)
     HW = synth.HostWeights(W)
@@ -440,3 +440,21 @@ def test_fp8_experts_change_the_layer_only_by_the_quantisation():
         moe16 = sum(w * O.swiglu_expert(h, *(O.bf16_to_f64(a) for a in HW.expert(0, int(e))))
                     for e, w in zip(info16["idx"][b], info16["w"][b]))
         assert np.allclose((y8[b] - y16[b]), moe - moe16, atol=1e-12)
+
+
+def test_fp8_expert_scales_are_per_output_channel():
+    """Every decoded row of gate, up and down is an E4M3 value times one scale, the
+    row's max|w| / 448 computed here from the bf16 weights, and the row's largest
+    weight decodes to 448 times it (per-block scales would fail the first check on
+    rows whose blocks have different maxima)."""
+    cfg = dict(TINY, d_ff=64)
+    W, _, _, _ = _setup(cfg)
+    HW = synth.HostWeights(W)
+    grid = np.unique(np.abs(O.e4m3_to_f64(np.arange(256, dtype=np.uint8)[(np.arange(256) & 0x7F) != 0x7F])))
+    for e in range(3):
+        for w16, wq in zip(HW.expert(0, e), O.fp8_expert(*HW.expert(0, e))):
+            wf = O.bf16_to_f64(w16)
+            scale = (np.abs(wf).max(axis=1).astype(np.float32) / np.float32(448.0)).astype(np.float64)
+            v = np.abs(wq) / scale[:, None]
+            assert np.all(np.isin(v, grid)), e
+            assert np.array_equal(v.max(axis=1), np.full(wf.shape[0], 448.0))
