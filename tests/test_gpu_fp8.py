@@ -141,3 +141,27 @@ def test_fp8_pages_scale_sampled_layers_and_stored_form(workload, layers):
         mk.close()
         del W, k, v
         torch.cuda.empty_cache()
+
+
+def test_read_expert_fp8_errors():
+    cfg, W, *_ = PU.setup("tiny_b1_64")
+    mk = B.Megakernel(cfg, W)
+    try:  # a bf16 handle has no FP8 form
+        with pytest.raises(B.MkError) as e:
+            mk.expert_fp8(0, 0)
+        assert e.value.code == B.MK_ERR_STATE
+    finally:
+        mk.close()
+    cfg, W, *_ = PU.setup("tiny_fp8_b1_64")
+    mk = B.Megakernel(cfg, W)
+    try:
+        for l, e_ in ((cfg["n_layers"], 0), (0, cfg["n_experts"]), (-1, 0)):
+            with pytest.raises(B.MkError) as e:
+                mk.expert_fp8(l, e_)
+            assert e.value.code == B.MK_ERR_INVALID
+        d, f = cfg["d_model"], cfg["d_ff"]
+        buf = np.empty(3 * f * d + 4 * (2 * f + d) - 4, dtype=np.uint8)  # one float short
+        rc = B.load_library().mk_read_expert_fp8(mk.h, 0, 0, buf.ctypes.data, buf.nbytes)
+        assert rc == B.MK_ERR_INVALID
+    finally:
+        mk.close()
