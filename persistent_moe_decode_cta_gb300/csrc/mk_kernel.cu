@@ -1262,6 +1262,21 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
     default: key = {1, l, 0}; break;  // QKV and ROUTER share the layer's normed input
   }
   const bool reuse = key == have;
+  // The QKV epilogue's inputs that do not depend on the wait -- this lane's RoPE rate
+  // and, for K/V rows, the page of each token's new slot -- are loaded first, so that
+  // their L2 round trips overlap the wait and the GEMV instead of following them.
+  unsigned long long fturn = 0ull;
+  int kv_pg[2] = {-1, -1};
+  if (op == OP_QKV && warp < nrows / 16) {
+    const int pr = T[D_ROW0] + warp * 16 + g8;
+    const int seg = pr / p.hd, j = pr % p.hd;
+    if (seg <= p.gs) fturn = __ldg(p.rope_turns + 8 * (j / 16) + g8);
+    if (seg >= p.gs)
+      for (int e = 0; e < 2; ++e) {
+        const int n = 2 * c + e;
+        if (n < p.B) kv_pg[e] = checked_page(p, n, seq_lens_s(S)[n] / 16, ti);
+      }
+  }
   if (reuse) {
     trace_mark(p, S, 1);
   } else if (!consumer_wait(p, S, T[D_WAIT_CTR], (unsigned)T[D_WAIT_TARGET], ti, T[D_WAIT2_CTR],
@@ -1334,9 +1349,8 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
         const int d1 = 8 * (j / 16) + g8, d2 = d1 + p.hd / 2;
         const bool rot = seg <= p.gs;
         // angle = pos * inv_freq[d1]; turns = frac(pos * inv_freq / 2pi) computed exactly
-        // in 64-bit fixed point (rope_turns[i] = inv_freq_i / 2pi * 2^64), then sin/cos
-        // of 2*pi*turns in fp32.
-        const unsigned long long fturn = rot ? p.rope_turns[d1] : 0ull;
+        // in 64-bit fixed point (fturn = rope_turns[d1] = inv_freq / 2pi * 2^64, loaded
+        // before the wait), then sin/cos of 2*pi*turns in fp32.
         for (int e = 0; e < 2; ++e) {
           const int n = 2 * c + e;
           if (n >= p.B) continue;
@@ -1356,7 +1370,7 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
             q[d1] = to_bf16(y1);
             q[d2] = to_bf16(y2);
           } else {
-            const int pg = checked_page(p, n, pos / 16, ti);
+            const int pg = kv_pg[e];  // (checked before the wait)
             if (pg >= 0) {
               uint16_t* dst = (seg == p.gs ? p.kc : p.vc) +
                               ((((size_t)l * p.n_pages + pg) * p.Hkv + g) * 16 + (pos % 16)) * p.hd;
