@@ -790,9 +790,6 @@ __device__ __forceinline__ bool gemv_run(const Params& p, const Smem& S, uint32_
   return true;
 }
 
-// The same GEMV on E4M3 weight fragments (FP8 experts): 8 bytes a lane per fragment,
-// widened exactly to f16 and multiplied with the f16 operand `fr` (f32 accumulation);
-// twice the j-groups per ring chunk.  The row scales are applied by the caller.
 // One E4M3 A-fragment (8 codes a lane) decoded on the integer pipe to f16 values
 // scaled by 2^-8 (undone with the f32 scales) and multiplied in.  (The conversion
 // instruction was measured slower here: -1.5% at batch 1 with the whole decode on it,
@@ -804,6 +801,10 @@ __device__ __forceinline__ void fp8_mma(float (&acc)[4], uint2 a, uint32_t b0, u
   mma_f16(acc, r0, r1, r2, r3, b0, b1);
 }
 
+// The GEMV on E4M3 weight fragments (FP8 experts): 8 bytes a lane per fragment,
+// widened exactly to f16 (x 2^-8) and multiplied with the f16 operand `fr` (f32
+// accumulation); twice the j-groups per ring chunk.  The row scales are applied by
+// the caller.
 template <int NRB>
 __device__ __forceinline__ bool gemv_run8(const Params& p, const Smem& S, uint32_t& cseq, int nch, int ksw,
                                           const BFrag& fr, float (&v)[4]) {
