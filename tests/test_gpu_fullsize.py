@@ -1,7 +1,7 @@
 """Parity at the pages-scale sizes, in the launch configuration the benchmark times (one
 cooperative megakernel launch per step, 48 layers, d 2048, 128 experts top-8, vocab
-151936): the batch-1 8K-context workload and the batch-8 ragged workload with a 4096-
-token window on odd layers.
+151936): the batch-1 8K-context workload, the batch-8 ragged workload with a 4096-
+token window on odd layers, and batch 1 at the 128K context.
 
 A full float64 oracle step at this size is chained through 48 layers; instead, sampled
 layers are checked teacher-forced -- the oracle runs layer l on the GPU's own input x_l
@@ -35,6 +35,7 @@ def pages_weights():
 @pytest.mark.parametrize("workload,layers", [
     ("pages_b1_8k", [0, 1, 24, 47]),
     ("pages_b8_ragged_swa", [0, 1, 24, 47]),   # 1 and 47 are sliding-window layers
+    ("pages_b1_128k", [0, 47]),                 # the longest context (8192 pages a sequence)
 ])
 def test_pages_scale_step_sampled_layers_and_lm_head(pages_weights, workload, layers):
     W = pages_weights
