@@ -127,14 +127,14 @@ __device__ bool consumer_wait(const Params& p, const Smem& S, int ci, unsigned t
     trace_mark(p, S, 1);
     return true;
   }
+  // thread 0 polls; one OR-reduction barrier hands its result (and, as a barrier, the
+  // order of its acquire) to the other consumer threads
+  bool ok = false;
   if (threadIdx.x == 0) {
-    S.small[0] = wait_ge2(p, ci, target, ci2, target2, task) ? 1 : 0;
+    ok = wait_ge2(p, ci, target, ci2, target2, task);
     if (p.trace) trace_slots(S)[1] = gtime();
   }
-  bar_sync_consumers();
-  const int ok = S.small[0];
-  bar_sync_consumers();
-  return ok != 0;
+  return bar_or_consumers(ok);
 }
 
 // Hand a counter release to the storer warp and carry on: each consumer warp orders
