@@ -24,7 +24,7 @@ describe, in float64 over the same bf16 weight bits (widened exactly):
 * final RMSNorm and LM head, fp logits, greedy argmax [Cohere's Open-Source
   Megakernel ..., "Current limitations": greedy sampling].
 
-Readings taken where the pages are silent (each listed in the design doc as well):
+Readings taken where the pages are silent:
 rotate-half RoPE with inv_freq_i = theta^(-2i/hd) over the full head; cached K is
 already rotated; the new token sits at position L_b and attends to itself; the
 attention window of a sliding-window layer is {j : p - W < j <= p}; q head i uses
