@@ -70,6 +70,8 @@ WORKLOADS = {
     "pages_l2_fp8_b1_8k": dict(model="pages_l2_fp8", batch=1, lens=("fixed", 8192)),
     "pages_fp8_b8_ragged_swa": dict(model="pages_fp8", batch=8, lens=("uniform", 1024, 32768),
                                     sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
+    "pages_l2_fp8_b8_ragged_swa": dict(model="pages_l2_fp8", batch=8, lens=("uniform", 1024, 32768),
+                                       sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
 }
 
 
