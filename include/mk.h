@@ -61,9 +61,9 @@ typedef enum mk_status {
  * MK_EXPERT_FP8 (1) stores them, at mk_create, as E4M3 codes (nearest, ties to even,
  * saturating) with one float32 scale per output channel (row) of gate, up and down
  * (max |w| over the row / 448; 1 for a zero row), and the kernel decodes the codes to
- * fp16 for the MMA and applies the scales to its fp32 results.  It needs no dense
- * layers and d_ff a multiple of 64 (of 32 when max_batch < 4, where the expert items
- * are 32 rows of d_ff instead of 64) (MK_ERR_UNSUPPORTED).
+ * fp16 for the MMA and applies the scales to its fp32 results.  It needs d_ff a
+ * multiple of 64 (of 32 when max_batch < 4, where the expert items are 32 rows of d_ff
+ * instead of 64) (MK_ERR_UNSUPPORTED).  The dense FFNs of a mixed stack stay bf16.
  * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
  * FP8 quantization is on the roadmap; the pages fix no format] */
 enum { MK_EXPERT_BF16 = 0, MK_EXPERT_FP8 = 1 };
@@ -265,7 +265,8 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
  * (a weight decodes as value(code) * its row's scale).  `bytes` must equal
  * 3 * d_ff * d_model + 4 * (2 * d_ff + d_model).  Synchronises
  * the device; needs no plan.  MK_ERR_STATE if the experts are stored in bf16,
- * MK_ERR_INVALID for a NULL pointer, a layer or expert out of range or a wrong size.
+ * MK_ERR_INVALID for a NULL pointer, a layer or expert out of range, a dense layer or
+ * a wrong size.
  * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
  * FP8 quantization is on the roadmap] */
 int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size_t bytes);

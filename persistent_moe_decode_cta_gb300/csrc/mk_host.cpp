@@ -56,10 +56,11 @@ struct Shape {
   int r_o, t_o, k_o;
   int moe_fs, t_moe;
   uint64_t dense_mask;  // mixed stacks: dense layers
-  int f_dense, t_dense;
+  int f_dense, t_dense, dense_fs;  // dense FFN items: bf16, f-slices of dense_fs rows
   bool fp8;             // routed experts as E4M3 codes + f32 scales
   int r_lm, v_pad, n_lm_tasks;
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
+  size_t dense_item_bytes;
   size_t off_qkv, off_o, off_router, off_moe, off_dense, off_lm, off_embed, total;
   bool dense(int l) const { return (dense_mask >> l) & 1ull; }
 };
@@ -136,8 +137,9 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.f_dense = s.dense_mask ? c->dense_ff : 0;
   if (s.dense_mask && (s.f_dense < 128 || s.f_dense % 128 || s.f_dense > 4096))
     return fail(err, MK_ERR_UNSUPPORTED, "dense_ff %d must be a multiple of 128 <= 4096", s.f_dense);
-  s.t_dense = s.f_dense / s.moe_fs;
-  if (s.fp8 && s.dense_mask) return fail(err, MK_ERR_UNSUPPORTED, "FP8 experts with dense layers");
+  // the dense FFN items keep the bf16 slice width (FP8 applies to the routed experts)
+  s.dense_fs = s.fp8 ? 32 : s.moe_fs;
+  s.t_dense = s.f_dense / s.dense_fs;
   s.r_lm = 64;
   if (const char* e = getenv("MK_LM_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_lm = v; }
   s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
@@ -147,6 +149,7 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.moe_item_bytes = s.fp8 ? (size_t)fp8_scale_bytes(s.moe_fs, s.d) + (size_t)3 * s.moe_fs * s.d
                            : (size_t)3 * s.moe_fs * s.d * 2;
   s.moe_bytes_e = s.moe_item_bytes * s.t_moe;
+  s.dense_item_bytes = (size_t)3 * s.dense_fs * s.d * 2;
   s.lm_bytes = (size_t)s.v_pad * s.d * 2;
   s.embed_bytes = (size_t)s.V * s.d * 2;
   size_t o = 0;
@@ -155,7 +158,7 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.off_o = take(s.o_layer_bytes * s.L);
   s.off_router = take(s.router_layer_bytes * s.L);
   s.off_moe = take(s.moe_bytes_e * s.E * s.L);
-  s.off_dense = take((size_t)__builtin_popcountll(s.dense_mask) * s.t_dense * s.moe_item_bytes);
+  s.off_dense = take((size_t)__builtin_popcountll(s.dense_mask) * s.t_dense * s.dense_item_bytes);
   s.off_lm = take(s.lm_bytes);
   s.off_embed = take(s.embed_bytes);
   s.total = o;
@@ -668,8 +671,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
          PACK_IDENT, hd, gs, 0, s.r_o);
     if (s.dense(l)) {  // mixed stack: the layer's FFN in the dense region, no router or experts
       const int rank = __builtin_popcountll(s.dense_mask & ((1ull << l) - 1ull));  // dense layers before l
-      e = launch_pack_moe(h->wblob + s.off_dense + (size_t)rank * s.t_dense * s.moe_item_bytes, w->ffn_gate[l],
-                          w->ffn_up[l], w->ffn_down[l], d, s.f_dense, s.moe_fs, st);
+      e = launch_pack_moe(h->wblob + s.off_dense + (size_t)rank * s.t_dense * s.dense_item_bytes, w->ffn_gate[l],
+                          w->ffn_up[l], w->ffn_down[l], d, s.f_dense, s.dense_fs, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "pack dense FFN"); return bail(MK_ERR_CUDA); }
       e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
@@ -785,6 +788,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   if (const char* fl = getenv("MK_INFLIGHT_MOE")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight_moe = v; }
   p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
   p.dense_mask = s.dense_mask; p.t_dense = s.t_dense; p.off_dense = (long long)s.off_dense;
+  p.dense_fs = s.dense_fs; p.dense_item_bytes = (long long)s.dense_item_bytes;
   p.fp8 = s.fp8 ? 1 : 0;
   p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
   p.rope_turns = h->rope_turns;
@@ -1103,6 +1107,7 @@ int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size
   if (!s.fp8) return fail(&h->err, MK_ERR_STATE, "experts are stored in bf16");
   if (layer < 0 || layer >= s.L || expert < 0 || expert >= s.E)
     return fail(&h->err, MK_ERR_INVALID, "layer %d / expert %d out of range", layer, expert);
+  if (s.dense(layer)) return fail(&h->err, MK_ERR_INVALID, "layer %d is dense (no routed experts)", layer);
   const int d = s.d, f = s.f, fs = s.moe_fs, nrb1 = fs / 8, k2 = fs / 16;
   const size_t need = (size_t)3 * f * d + 4 * ((size_t)2 * f + (size_t)d);
   if (bytes != need) return fail(&h->err, MK_ERR_INVALID, "mk_read_expert_fp8: need %zu bytes, got %zu", need, bytes);

@@ -124,6 +124,8 @@ struct Params {
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   int inflight_moe;         // the same for the chunks of expert items
   int fp8;                  // expert weights as E4M3 codes with f32 scales (items: see fp8_scale_bytes)
+  int dense_fs;             // f-slice rows of a dense layer's FFN items (bf16; = moe_fs without FP8)
+  long long dense_item_bytes;
   // mixed dense/MoE stacks: bit l set = layer l is dense, its FFN is t_dense items (one
   // per moe_fs rows of dense_ff) at off_dense + (r * t_dense + t) * moe_item_bytes, r =
   // the number of dense layers below l

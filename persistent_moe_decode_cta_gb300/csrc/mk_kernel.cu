@@ -592,15 +592,19 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         if (!fetch(dense ? 0 : item / p.t_moe)) { ok = false; break; }
         const int count = dense ? p.t_dense : nact * p.t_moe;
         // part 1 (gate/up tile) in whole k16-groups, part 2 (down slice) in warp regions
-        // (FP8: a chunk of the item's scales first, fragments of half the bytes)
-        const int nrb1 = p.moe_fs / 8;
-        const int fb = p.fp8 ? kFragBytes8 : kFragBytes;
-        const int sb = p.fp8 ? fp8_scale_bytes(p.moe_fs, p.d) : 0;
-        const int cs1 = (p.fp8 ? gemv_jpc8(nrb1) : gemv_jpc(nrb1)) * nrb1 * 8 * fb;
-        const int gu_bytes = 2 * p.moe_fs * p.d * fb / 256;
-        const int region = (p.d / 128) * (p.moe_fs / 16) * fb;
+        // (FP8 experts: a chunk of the item's scales first, fragments of half the bytes;
+        // a dense layer's FFN items stay bf16)
+        const bool f8 = p.fp8 && !dense;
+        const int fs = dense ? p.dense_fs : p.moe_fs;
+        const long long ib = dense ? p.dense_item_bytes : p.moe_item_bytes;
+        const int nrb1 = fs / 8;
+        const int fb = f8 ? kFragBytes8 : kFragBytes;
+        const int sb = f8 ? fp8_scale_bytes(fs, p.d) : 0;
+        const int cs1 = (f8 ? gemv_jpc8(nrb1) : gemv_jpc(nrb1)) * nrb1 * 8 * fb;
+        const int gu_bytes = 2 * fs * p.d * fb / 256;
+        const int region = (p.d / 128) * (fs / 16) * fb;
         const int cs2 = moe_warps_per_chunk(region) * region;
-        const int dn_bytes = (int)p.moe_item_bytes - sb - gu_bytes;
+        const int dn_bytes = (int)ib - sb - gu_bytes;
         const int nch = (sb > 0) + (gu_bytes + cs1 - 1) / cs1 + (dn_bytes + cs2 - 1) / cs2;
         // O-proj tiles of the layer as a queue (D_KLEN tiles from task D_K0; none when
         // they are dealt statically): taken before expert items once all attention
@@ -634,7 +638,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
           }
           const uint8_t* src =
               dense ? p.wblob + p.off_dense +
-                          ((long long)__popcll(p.dense_mask & ((1ull << l) - 1ull)) * p.t_dense + t) * p.moe_item_bytes
+                          ((long long)__popcll(p.dense_mask & ((1ull << l) - 1ull)) * p.t_dense + t) * ib
                     : p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
           const int fl = p.inflight_moe;
           ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
@@ -2022,16 +2026,20 @@ __device__ void consumer(const Params& p, const Smem& S) {
 #pragma unroll
         for (int j = 0; j < kMaxKsw; ++j) fr.b0[j] = fr.b1[j] = 0u;
         break;
-      case OP_MOE_DRAIN:
-        ok = p.fp8 ? (p.moe_fs == 64 ? task_moe<64, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
+      case OP_MOE_DRAIN: {
+        // (a dense layer's FFN items: bf16 f-slices of dense_fs rows)
+        const int fsi = T[D_AUX] == 1 ? p.dense_fs : p.moe_fs;
+        ok = (p.fp8 && T[D_AUX] != 1)
+                 ? (p.moe_fs == 64 ? task_moe<64, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
                                                            ent2.y, ew_lo, ew_hi, fr, have, rs_have)
                                      : task_moe<32, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
                                                            ent2.y, ew_lo, ew_hi, fr, have, rs_have))
-             : (p.moe_fs == 32)
+             : (fsi == 32)
                  ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have,
                                 rs_have)
                  : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have);
         break;
+      }
       default:
         ok = task_gemv(p, S, cseq, sseq, T, ent.x, nch, fr, have, rs_have);
         break;

@@ -46,7 +46,7 @@ MODELS["pages_l1"] = dict(MODELS["pages"], n_layers=1)
 MODELS["pages_dense3"] = dict(MODELS["pages"], dense_layers=(0, 1, 2), dense_ff=4096)
 # The same shapes with the routed experts stored as E4M3 codes + float32 scales (the
 # weights drawn are the bf16 ones; quantisation happens when the model is loaded).
-for _m in ("tiny", "small", "pages", "pages_l2"):
+for _m in ("tiny", "small", "pages", "pages_l2", "tiny_dense", "small_dense"):
     MODELS[_m + "_fp8"] = dict(MODELS[_m], expert_dtype="fp8")
 
 # Workloads: a model plus a batch of cached sequence lengths.
@@ -68,6 +68,8 @@ WORKLOADS = {
     "small_fp8_b1_2k": dict(model="small_fp8", batch=1, lens=("fixed", 2048)),
     "pages_fp8_b1_8k": dict(model="pages_fp8", batch=1, lens=("fixed", 8192)),
     "pages_l2_fp8_b1_8k": dict(model="pages_l2_fp8", batch=1, lens=("fixed", 8192)),
+    "tiny_dense_fp8_b1_64": dict(model="tiny_dense_fp8", batch=1, lens=("fixed", 64)),
+    "small_dense_fp8_b1_2k": dict(model="small_dense_fp8", batch=1, lens=("fixed", 2048)),
     "pages_fp8_b8_ragged_swa": dict(model="pages_fp8", batch=8, lens=("uniform", 1024, 32768),
                                     sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
     "pages_l2_fp8_b8_ragged_swa": dict(model="pages_l2_fp8", batch=8, lens=("uniform", 1024, 32768),

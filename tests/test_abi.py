@@ -72,12 +72,15 @@ def test_fp8_expert_configs_without_device():
     with pytest.raises(B.MkError) as e:
         B.mk_plan_dry(dict(synth.model_config("tiny_fp8_b1_64"), d_ff=176), 1, 8, max_batch=2)
     assert e.value.code == B.MK_ERR_UNSUPPORTED
-    for bad, code in ((dict(d_ff=160), B.MK_ERR_UNSUPPORTED),
-                      (dict(dense_layers=(0,), dense_ff=256), B.MK_ERR_UNSUPPORTED)):
+    for bad, code in ((dict(d_ff=160), B.MK_ERR_UNSUPPORTED),):
         cfg = dict(synth.model_config("tiny_fp8_b1_64"), **bad)
         with pytest.raises(B.MkError) as e:
             B.mk_plan_dry(cfg, 1, 8)
         assert e.value.code == code, bad
+    # FP8 experts beside dense layers: the dense FFN items stay bf16 slices of 32 rows
+    cfg = synth.model_config("small_dense_fp8_b1_2k")
+    _, _, _, info = B.mk_plan_dry(cfg, 1, 8)
+    assert info[30] == B.MK_EXPERT_FP8 and info[27] == cfg["dense_ff"] // 32 and info[8] == 64
     c = B.make_config(synth.model_config("tiny_b1_64"))
     c.expert_dtype = 7
     info = np.zeros(32, dtype=np.int32)

@@ -62,6 +62,11 @@ def test_stored_codes_and_scales_equal_the_oracle_quantisation(workload, pairs, 
     ("small_fp8_b1_2k", [2048, 300], "graph", 8),
     ("small_fp8_b1_2k", [2048, 300], "mega", 2),
     ("small_fp8_b1_2k", [2048, 5, 900, 17, 64, 1, 333, 2000], "mega", 8),
+    # FP8 experts beside bf16 dense layers (a mixed stack)
+    ("tiny_dense_fp8_b1_64", [61, 0, 17], "mega", 8),
+    ("tiny_dense_fp8_b1_64", [61, 17], "perop", 2),
+    ("small_dense_fp8_b1_2k", [2048, 300], "mega", 8),
+    ("small_dense_fp8_b1_2k", [2048], "graph", 1),
 ])
 def test_fp8_step_matches_oracle(workload, seq_lens, mode, max_batch):
     cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload, seq_lens=seq_lens)
@@ -163,5 +168,14 @@ def test_read_expert_fp8_errors():
         buf = np.empty(3 * f * d + 4 * (2 * f + d) - 4, dtype=np.uint8)  # one float short
         rc = B.load_library().mk_read_expert_fp8(mk.h, 0, 0, buf.ctypes.data, buf.nbytes)
         assert rc == B.MK_ERR_INVALID
+    finally:
+        mk.close()
+    cfg, W, *_ = PU.setup("tiny_dense_fp8_b1_64")
+    mk = B.Megakernel(cfg, W)
+    try:  # layer 0 of this mixed stack is dense: no routed experts to read back
+        with pytest.raises(B.MkError) as e:
+            mk.expert_fp8(0, 0)
+        assert e.value.code == B.MK_ERR_INVALID
+        _check_stored(mk, synth.HostWeights(W), 1, 3)
     finally:
         mk.close()
