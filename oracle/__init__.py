@@ -35,7 +35,11 @@ width cfg["dense_ff"] applied to every token with weight 1, sharing the layer's 
 
 Parity status: every building block below is pinned by tests/test_oracle_pins.py
 (closed forms, invariants, special cases, library routines for bf16 rounding and
-sorting).  Whole-model values on the larger models have no published example and
+sorting), and so are the two steps of layer_step that combine them: the query's
+rotation at the token's own position (a whole layer's invariance to shifting every
+position, and the attention peak when query and keys share one raw vector) and the
+pairing of each routing weight with its expert (a layer reduced to a closed form with
+distinct experts on disjoint outputs).  Whole-model values on the larger models have no published example and
 are pinned only through those blocks ("parity unpinned" beyond them).
 """
 from __future__ import annotations

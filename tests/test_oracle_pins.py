@@ -258,6 +258,187 @@ def test_first_token_attends_only_to_itself():
     assert np.allclose(y[0] - x[0], O.bf16_to_f64(HW.wo(0)) @ o, atol=1e-13)
 
 
+# ----------------------------------------------------------------- the query's rotation
+# The rope() pins above test the rotation alone.  These two pin that layer_step
+# rotates the QUERY at the token's own position: the first by the relative-position
+# property of a whole layer, the second by where the attention peaks when query and
+# keys share one raw vector.
+
+Q1 = dict(n_layers=1, d_model=32, n_q_heads=4, n_kv_heads=2, head_dim=8, n_experts=4,
+          top_k=2, d_ff=16, vocab=50, rope_theta=1e4, rms_eps=1e-6, sliding_window=0,
+          swa_layers=(), page_size=16)
+
+
+def _bf16_tensor(a):
+    return torch.from_numpy(O.f64_to_bf16(a).view(np.int16)).view(torch.bfloat16)
+
+
+def _with_query_rope(mutation, fn):
+    """Run fn() with the query's rotation inside layer_step replaced by mutation(v, pos,
+    theta, rope) (the query is the rope() argument with n_q_heads rows; keys have
+    n_kv_heads); mutation None runs the oracle as it is."""
+    if mutation is None:
+        return fn()
+    orig = O.rope
+
+    def patched(v, pos, theta):
+        v = np.asarray(v)
+        if v.ndim == 2 and v.shape[0] == 4:
+            return mutation(v, pos, theta, orig)
+        return orig(v, pos, theta)
+    O.rope = patched
+    try:
+        return fn()
+    finally:
+        O.rope = orig
+
+
+_Q_MUTATIONS = {
+    "unrotated": lambda v, pos, th, r: np.asarray(v, dtype=np.float64),
+    "at position 0": lambda v, pos, th, r: r(v, 0, th),
+    "one position late": lambda v, pos, th, r: r(v, pos + 1, th),
+    "one position early": lambda v, pos, th, r: r(v, pos - 1, th),
+    "negative angle": lambda v, pos, th, r: r(v, -pos, th),
+}
+
+
+def _shift_case(cfg, p, delta, x, raw_k, raw_v):
+    """Attention branch of layer 1 (a sliding-window layer) at position p + delta, the
+    cache holding at position j >= delta raw key raw_k[j - delta] rotated at j."""
+    W = synth.make_weights(cfg, seed=0, std=0.2)
+    W["w_down"] = torch.zeros_like(W["w_down"])
+    n = p + delta
+    pt, npages = synth.make_page_table([n], seed=0)
+    k = torch.zeros((2, npages, 2, 16, 8), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    for j in range(delta, n):
+        k[1, pt[0][j // 16], :, j % 16] = _bf16_tensor(O.rope(raw_k[j - delta], j, cfg["rope_theta"]))
+        v[1, pt[0][j // 16], :, j % 16] = _bf16_tensor(raw_v[j - delta])
+    y, _ = O.layer_step(cfg, synth.HostWeights(W), synth.HostKV(k, v), 1, x, [n], pt)
+    return y - x
+
+
+@pytest.mark.parametrize("mutation", [None] + list(_Q_MUTATIONS))
+def test_layer_attention_depends_only_on_relative_positions(mutation):
+    """RoPE makes a layer's attention invariant to shifting every position by delta
+    (the window moves along; cached keys are re-rotated at their new positions).  Only
+    bf16 rounding of the re-rotated keys differs, a relative error of ~1e-3 here; an
+    unrotated query, one rotated at a fixed position or with the wrong sign breaks the
+    invariance by O(1).  (A constant offset of the query's position keeps it: the next
+    test pins that.)"""
+    cfg = dict(Q1, n_layers=2, sliding_window=12, swa_layers=(1,))
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((1, 32))
+    p = 20
+    raw_k = rng.standard_normal((p, 2, 8)) * 3.0
+    raw_v = rng.standard_normal((p, 2, 8))
+    errs = []
+    for delta in (1, 13, 1000, 70000):
+        a, b = _with_query_rope(_Q_MUTATIONS.get(mutation), lambda: (
+            _shift_case(cfg, p, 0, x, raw_k, raw_v), _shift_case(cfg, p, delta, x, raw_k, raw_v)))
+        errs.append(np.linalg.norm(a - b) / np.linalg.norm(a))
+    if mutation is None:
+        assert max(errs) < 1e-2, errs
+    elif mutation in ("one position late", "one position early"):
+        assert max(errs) < 1e-2, errs        # a constant offset is shift-invariant
+    else:
+        assert max(errs) > 0.2, errs
+
+
+@pytest.mark.parametrize("p", [37, 300])
+@pytest.mark.parametrize("mutation", [None] + list(_Q_MUTATIONS))
+def test_query_rotated_at_its_own_position(p, mutation):
+    """Query and key share one raw vector u per KV group (the query rows of each head are
+    the key rows of its KV group), and the cache holds at every position j the key u
+    rotated at j + 2.  A rotation preserves length, so by Cauchy-Schwarz the score
+    rot(u, p) . rot(u, j + 2) is largest exactly where the two rotations agree: at the
+    cached position j = p - 2 and at the new token's own key (rotated at p), with equal
+    bf16 bits.  With |u| large every other key's weight vanishes, so each head's output
+    is the mean of those two values.  A query rotated at any other position moves the
+    peak."""
+    W = synth.make_weights(Q1, seed=0, std=0.2)
+    W["w_down"] = torch.zeros_like(W["w_down"])
+    W["wk"][0] = (W["wk"][0].float() * 15).to(torch.bfloat16)
+    for i in range(4):
+        g = (i * 2) // 4
+        W["wq"][0, i * 8:(i + 1) * 8] = W["wk"][0, g * 8:(g + 1) * 8]
+    W["wo"][0] = torch.eye(32, dtype=torch.bfloat16)
+    W["attn_norm"][0] = 1.0
+    HW = synth.HostWeights(W)
+    x = np.random.default_rng(2).standard_normal((1, 32))
+    u = (O.bf16_to_f64(HW.wk(0)) @ O.rms_norm(x, 1.0, 1e-6)[0]).reshape(2, 8)
+    pt, npages = synth.make_page_table([p], seed=0)
+    k = torch.zeros((1, npages, 2, 16, 8), dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    vals = O.bf16_to_f64(O.f64_to_bf16(np.random.default_rng(9).standard_normal((p, 2, 8))))
+    for j in range(p):
+        k[0, pt[0][j // 16], :, j % 16] = _bf16_tensor(O.rope(u, j + 2, 1e4))
+        v[0, pt[0][j // 16], :, j % 16] = _bf16_tensor(vals[j])
+    y, info = _with_query_rope(_Q_MUTATIONS.get(mutation), lambda: O.layer_step(
+        Q1, HW, synth.HostKV(k, v), 0, x, [p], pt))
+    o = (y - x)[0].reshape(4, 8)                      # Wo = I: the heads' outputs
+    v_new = O.bf16_to_f64(info["kv"][0]["v"])
+    want = np.stack([(vals[p - 2, (i * 2) // 4] + v_new[(i * 2) // 4]) / 2 for i in range(4)])
+    err = float(np.abs(o - want).max())
+    if mutation is None:
+        assert err < 5e-3, err
+    else:
+        assert err > 0.5, (mutation, err)
+
+
+# ----------------------------------------------------------------- routing weights x experts
+
+def _pairing_layer(swap_weights=False):
+    """One MoE layer reduced to a closed form: constant inputs x_b = +-1 (so h_b = s_b 1,
+    s_b = +-1/sqrt(1 + eps)), router row e = a_e / 32 (logit a_e s_b), gate and up rows
+    g_e / 32 and u_e / 32 (every f-row gets g_e s_b and u_e s_b), and a down matrix that
+    writes 1/16 of each f-row into output rows 8e..8e+7 only.  Expert e then adds
+    w_{b,e} silu(g_e s_b) u_e s_b to its own eight outputs."""
+    W = synth.make_weights(Q1, seed=0, std=0.2)
+    W["wo"] = torch.zeros_like(W["wo"])
+    W["attn_norm"][0] = 1.0
+    a, g, u = [1.0, 0.5, -0.25, -2.0], [1.5, -0.75, 1.25, 0.5], [0.5, 1.0, -1.5, 0.75]
+    for e in range(4):
+        W["router"][0, e] = a[e] / 32
+        W["w_gate"][0, e] = g[e] / 32
+        W["w_up"][0, e] = u[e] / 32
+        W["w_down"][0, e] = 0.0
+        W["w_down"][0, e, 8 * e:8 * e + 8] = 1.0 / 16
+    x = np.stack([np.full(32, 1.0), np.full(32, -1.0)])
+    pt, npages = synth.make_page_table([3, 9], seed=0)
+    k, v = synth.make_kv(Q1, npages, seed=0)
+    orig = O.router_topk
+    if swap_weights:                                   # a planted pairing slip
+        def swapped(r, kk, forced=None):
+            idx, w, m = orig(r, kk, forced)
+            return idx, w[::-1].copy(), m
+        O.router_topk = swapped
+    try:
+        y, info = O.layer_step(Q1, synth.HostWeights(W), synth.HostKV(k, v), 0, x, [3, 9], pt)
+    finally:
+        O.router_topk = orig
+    want = np.zeros((2, 32))
+    sel_want = []
+    for b, sb in enumerate((1 / math.sqrt(1 + 1e-6), -1 / math.sqrt(1 + 1e-6))):
+        logit = [a[e] * sb for e in range(4)]
+        first, second = sorted(range(4), key=lambda e: -logit[e])[:2]
+        sel_want.append([first, second])
+        w_first = 1 / (1 + math.exp(logit[second] - logit[first]))   # 2-way softmax
+        for e, w in ((first, w_first), (second, 1 - w_first)):
+            z = g[e] * sb
+            want[b, 8 * e:8 * e + 8] = w * (z / (1 + math.exp(-z))) * (u[e] * sb)
+    return y - x, want, info, sel_want
+
+
+def test_moe_combine_pairs_each_weight_with_its_expert():
+    got, want, info, sel = _pairing_layer()
+    assert info["idx"].tolist() == sel == [[0, 1], [3, 2]]
+    assert np.abs(got - want).max() < 1e-13
+    # the planted slip (weights handed to the wrong experts) is seen
+    got_bad, _, _, _ = _pairing_layer(swap_weights=True)
+    assert np.abs(got_bad - want).max() > 0.1
+
+
 def test_kv_write_goes_to_page_table_slot_with_rotated_bf16_k():
     W, pt, k, v = _setup()
     x = _x(2, 32)
