@@ -19,8 +19,9 @@
  *     "host pointer" arguments are ordinary host memory.  `stream` is a
  *     cudaStream_t passed as void* (NULL = legacy default stream).
  *   - Errors raised inside the kernel (timeouts of a dependency wait, a page id or
- *     token outside its range) are recorded in a device error word and surface at
- *     the next mk_get_status().  Such a step's outputs are not valid.
+ *     token outside its range, a NaN router logit) are recorded in a device error
+ *     word and surface at the next mk_get_status().  Such a step's outputs are not
+ *     valid.
  */
 #ifndef MK_H
 #define MK_H
@@ -41,7 +42,9 @@ typedef enum mk_status {
   MK_ERR_TIMEOUT = 5,      /* a dependency wait inside the kernel gave up          */
   MK_ERR_BAD_PAGE = 6,     /* a page-table entry was outside [0, n_pages)          */
   MK_ERR_BAD_TOKEN = 7,    /* a token id was outside [0, vocab)                    */
-  MK_ERR_STATE = 8         /* call out of order (e.g. decode before mk_plan)       */
+  MK_ERR_STATE = 8,        /* call out of order (e.g. decode before mk_plan)       */
+  MK_ERR_NAN = 9           /* a router logit was NaN: the step's activations are
+                              not finite (the route ranks it below every number)  */
 } mk_status;
 
 /* Model shape.  The kernels need: head_dim in {32, 64, 128}; d_model, d_ff and
@@ -116,8 +119,10 @@ typedef struct mk_error_info {
   int32_t code;      /* mk_status of the first device-side error, MK_OK if none  */
   int32_t task;      /* descriptor index that raised it (-1 if not a task)       */
   int32_t counter;   /* counter index waited on (timeouts)                       */
-  int32_t observed;  /* counter value seen at the timeout, or the bad id         */
-  int32_t target;    /* value waited for                                         */
+  int32_t observed;  /* counter value seen at the timeout, or the bad id, or the
+                        layer of a NaN router logit                              */
+  int32_t target;    /* value waited for; for a NaN router logit its index
+                        token * n_experts + expert                               */
   int32_t sm;        /* CTA index                                                */
 } mk_error_info;
 
@@ -125,11 +130,22 @@ typedef struct mk_error_info {
  * weight blob and repack every matrix into contiguous per-task tiles whose 16-byte
  * units are the mma.sync A-fragments in the order the consumer warps read them.
  * `stream` orders the packing kernels; the call synchronises it before returning.
- * On error *out is NULL. */
+ * On error *out is NULL.
+ * [Cohere Megakernel, "Getting started": the engine is a shared library
+ *  (libmk_release.so) that the serving process loads together with the model's
+ *  checkpoint; Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "One
+ *  kernel for the full decode step": weights are immutable, so their tiles can be
+ *  laid out once, ahead of time, and streamed before a task's inputs are ready.] */
 int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle** out);
 
 /* Build the task plan for a batch: per-SM descriptor lists, counter targets and
  * the buffers of a step.  Called when the batch composition changes, not per step.
+ * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "Scheduling: mostly
+ *  static, selectively dynamic": the host builds named waves per layer, deals task k
+ *  to SM k mod #SM, and leaves attention and MoE tiles to claimer tasks on shared
+ *  queues; Cohere open-sources fused LLM decode kernel with 1.58x vLLM claim: each
+ *  task is a 32-int32 descriptor naming its opcode, layer, output tile, split-K
+ *  coordinates, the counter it waits on and the counter it signals.]
  *   batch              1..max_batch
  *   seq_lens_host      HOST int32[batch], cached tokens per sequence (the next
  *                      step writes the new token at this position)
@@ -143,6 +159,9 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host,
             const int32_t* page_table_dev, int max_pages_per_seq, int n_pages);
 
 /* One decode step as ONE kernel launch on `stream` (asynchronous).
+ * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "One kernel for the
+ *  full decode step": one persistent launch runs every layer's RMSNorm, QKV with RoPE,
+ *  paged attention, router, experts, O-proj and the LM head, one CTA per SM.]
  *   tokens_dev  DEVICE int32[batch]        input token per sequence
  *   k_cache, v_cache  DEVICE bf16 [n_layers][n_pages][n_kv_heads][16][head_dim],
  *               caller-owned; the step writes the new token's K/V into slot
@@ -209,7 +228,10 @@ int mk_decode_step_perop(mk_handle* h, const int32_t* tokens_dev, void* k_cache,
                          void* v_cache, float* logits_dev, void* stream, int use_graph);
 
 /* Synchronise the handle's last stream and report the device error word; clears
- * it.  Returns info->code. */
+ * it.  Returns info->code.  (The pages describe no error path; every dependency wait
+ * of the kernel is bounded and reports here instead of hanging -- the counter waits
+ * are the ones of [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "The
+ * calling convention that makes it hand-writable"].) */
 int mk_get_status(mk_handle* h, mk_error_info* info);
 
 /* Task timeline for profiling.  records_dev: DEVICE uint64 [capacity][16], owned by
@@ -233,6 +255,18 @@ int mk_set_trace(mk_handle* h, void* records_dev, int capacity);
  * calling mk_plan again.  Synchronising. */
 int mk_plan_drop_signal(mk_handle* h, int task);
 
+/* Inspection of the schedule's bookkeeping.  on = 1: every later step's last CTA
+ * copies the final value of every counter and every queue head and count aside,
+ * before it clears them for the next step (read back with MK_READ_FINAL_COUNTERS /
+ * MK_READ_FINAL_QUEUES); on = 0 turns it off (the default; the copy costs the last
+ * CTA of a step about a microsecond).  Synchronising.  The steps of
+ * mk_decode_step_noalloc are not copied.
+ * [Cohere open-sources fused LLM decode kernel with 1.58x vLLM claim: the counters a
+ *  descriptor waits on and signals; Cohere's Open-Source Megakernel Beats vLLM by
+ *  1.58x on H100, "Scheduling: mostly static, selectively dynamic": the claimer
+ *  queues] */
+int mk_set_inspect(mk_handle* h, int on);
+
 /* fixed = 1: steps do not advance seq_lens (repeated steps move identical bytes). */
 int mk_set_fixed(mk_handle* h, int fixed);
 
@@ -249,11 +283,23 @@ int mk_set_fixed(mk_handle* h, int fixed);
  *   MK_READ_ROUTER_LOGITS float [n_layers][batch][n_experts]
  *   MK_READ_TRACE_COUNT uint32 [1] records appended since mk_set_trace (may exceed
  *                    the capacity; records past it were dropped)
+ *   MK_READ_FINAL_COUNTERS uint32[n_counters] every counter's value at the end of the
+ *                    last inspected step, before the reset (mk_set_inspect; else
+ *                    MK_ERR_STATE).  Counter indices are those of the descriptors'
+ *                    wait/signal fields; the bases are listed by mk_plan_dry.
+ *   MK_READ_FINAL_QUEUES int32 [2][3 * n_layers] the queue heads, then the queue
+ *                    counts, at the end of the last inspected step: queue l is layer
+ *                    l's attention items, n_layers + l its expert items (count = items
+ *                    routed), 2 n_layers + l its O-proj tiles.  Every claimer takes one
+ *                    failing claim when its queue is empty, so a drained queue's head
+ *                    is its items + the SMs (MK_Q_NUM_SMS) that ran its drain.
+ *   MK_READ_TASKS    int32 [n_tasks][32] the plan's descriptor table
  * `bytes` must equal the size of the requested array. */
 enum {
   MK_READ_HIDDEN = 1, MK_READ_ROUTES = 2, MK_READ_ROUTE_W = 3, MK_READ_ACTIVE = 4,
   MK_READ_SEQ_LENS = 5, MK_READ_COUNTERS = 6, MK_READ_ROUTER_LOGITS = 7,
-  MK_READ_TRACE_COUNT = 8
+  MK_READ_TRACE_COUNT = 8, MK_READ_FINAL_COUNTERS = 9, MK_READ_FINAL_QUEUES = 10,
+  MK_READ_TASKS = 11
 };
 int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
 
@@ -281,7 +327,10 @@ int mk_query(mk_handle* h, int what, int64_t* out);
 
 /* Host-only planner run (no device needed): the descriptor table and the per-SM
  * lists that mk_plan would build for `n_sms` SMs (the megakernel segment), for tests
- * of the schedule.
+ * of the schedule.  Like mk_plan it takes the per-layer wave order from the
+ * environment variable MK_WAVE_ORDER when set (letters r router, q QKV, a attention
+ * drain, m MoE drain, o O-proj, x ADD_RMSNORM; default "rqamox"; an order that breaks
+ * a dependency is MK_ERR_INVALID).
  *   tasks_out   int32[cap_tasks][32]      sm_off_out int32[n_sms + 1]
  *   sm_list_out int32[cap_list]           info_out int32[32]:
  *     [0] tasks  [1] list length  [2] counters  [3] max active experts  [4] 0

@@ -16,13 +16,14 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmk.so")
 
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_CUDA, MK_ERR_OOM = 0, 1, 2, 3, 4
-MK_ERR_TIMEOUT, MK_ERR_BAD_PAGE, MK_ERR_BAD_TOKEN, MK_ERR_STATE = 5, 6, 7, 8
+MK_ERR_TIMEOUT, MK_ERR_BAD_PAGE, MK_ERR_BAD_TOKEN, MK_ERR_STATE, MK_ERR_NAN = 5, 6, 7, 8, 9
 STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID", 2: "MK_ERR_UNSUPPORTED", 3: "MK_ERR_CUDA",
                 4: "MK_ERR_OOM", 5: "MK_ERR_TIMEOUT", 6: "MK_ERR_BAD_PAGE",
-                7: "MK_ERR_BAD_TOKEN", 8: "MK_ERR_STATE"}
+                7: "MK_ERR_BAD_TOKEN", 8: "MK_ERR_STATE", 9: "MK_ERR_NAN"}
 
 MK_READ_HIDDEN, MK_READ_ROUTES, MK_READ_ROUTE_W, MK_READ_ACTIVE = 1, 2, 3, 4
 MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT = 5, 6, 7, 8
+MK_READ_FINAL_COUNTERS, MK_READ_FINAL_QUEUES, MK_READ_TASKS = 9, 10, 11
 MK_EXPERT_BF16, MK_EXPERT_FP8 = 0, 1
 (MK_Q_NUM_SMS, MK_Q_NUM_TASKS, MK_Q_NUM_COUNTERS, MK_Q_PACKED_BYTES, MK_Q_MAX_ACTIVE,
  MK_Q_SPLIT_PAGES, MK_Q_SMEM_BYTES, MK_Q_PEROP_LAUNCHES, MK_Q_THREADS, MK_Q_STAGE_BYTES,
@@ -30,7 +31,7 @@ MK_EXPERT_BF16, MK_EXPERT_FP8 = 0, 1
 
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_decode_step_noalloc",
-           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_trace",
+           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_inspect", "mk_set_trace",
            "mk_plan_drop_signal", "mk_read", "mk_read_expert_fp8", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
 
@@ -92,6 +93,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_decode_step_perop.argtypes = [H, vp, vp, vp, vp, vp, i32]
     lib.mk_get_status.argtypes = [H, ctypes.POINTER(mk_error_info)]
     lib.mk_set_fixed.argtypes = [H, i32]
+    lib.mk_set_inspect.argtypes = [H, i32]
     lib.mk_set_trace.argtypes = [H, vp, i32]
     lib.mk_plan_drop_signal.argtypes = [H, i32]
     lib.mk_read.argtypes = [H, i32, vp, sz]
@@ -231,6 +233,10 @@ def mk_set_fixed(h, fixed: bool):
     _check(load_library().mk_set_fixed(h, int(bool(fixed))), h)
 
 
+def mk_set_inspect(h, on: bool):
+    _check(load_library().mk_set_inspect(h, int(bool(on))), h)
+
+
 def mk_plan_drop_signal(h, task: int):
     _check(load_library().mk_plan_drop_signal(h, int(task)), h)
 
@@ -304,6 +310,7 @@ class Megakernel:
 
     def __init__(self, cfg: dict, W: dict, max_batch: int = 8, timeout_ms: int = 2000):
         self.cfg = dict(cfg)
+        self.max_batch = max_batch
         self.h = mk_create(cfg, W, max_batch, timeout_ms)
         self.B = 0
 
@@ -396,6 +403,22 @@ class Megakernel:
 
     def counters(self):
         return mk_read(self.h, MK_READ_COUNTERS, (self.query(MK_Q_NUM_COUNTERS),), np.uint32)
+
+    def inspect(self, on=True):
+        mk_set_inspect(self.h, on)
+
+    def final_counters(self):
+        """Every counter's value at the end of the last inspected step (before reset)."""
+        return mk_read(self.h, MK_READ_FINAL_COUNTERS, (self.query(MK_Q_NUM_COUNTERS),), np.uint32)
+
+    def final_queues(self):
+        """(heads, counts), each int32 [3 * n_layers], at the end of the last inspected step."""
+        q = mk_read(self.h, MK_READ_FINAL_QUEUES, (2, 3 * self.cfg["n_layers"]), np.int32)
+        return q[0], q[1]
+
+    def tasks(self):
+        """The plan's descriptor table, int32 [n_tasks, 32]."""
+        return mk_read(self.h, MK_READ_TASKS, (self.query(MK_Q_NUM_TASKS), 32), np.int32)
 
     def close(self):
         if self.h:

@@ -275,9 +275,12 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     drains[(size_t)l * W_COUNT + W_ATT] = add(OP_ATT_DRAIN, l, 0, 0, 0, 0, 0, -1, 0, -1, 0, 0, 0, W_ATT);
     // D_AUX = 1: the dense FFN's items (every token, weight 1) instead of routed experts
     const int dz = s.dense(l) ? 1 : 0;
+    // (a routed layer's items wait for its route, published once by the route step; a
+    // dense layer's need no route; both count on the MoE-done counter)
+    const int rr = s.dense(l) ? -1 : P.c_rr + l;
     drains[(size_t)l * W_COUNT + W_MOE] =
-        add(OP_MOE_DRAIN, l, dz, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
-    moe_oq[l] = add(OP_MOE_DRAIN, l, dz, 0, 0, 0, 0, P.c_rr + l, 1, P.c_md + l, 1, 0, 0, W_MOE);
+        add(OP_MOE_DRAIN, l, dz, 0, 0, 0, 0, rr, 1, P.c_md + l, md_target(l), 0, 0, W_MOE);
+    moe_oq[l] = add(OP_MOE_DRAIN, l, dz, 0, 0, 0, 0, rr, 1, P.c_md + l, md_target(l), 0, 0, W_MOE);
     auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
     for (int g = 0; g < s.Hkv; ++g)
       for (int t = 0; t < s.t_o; ++t)
@@ -324,7 +327,11 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     // claims them from a queue, ahead of expert items once the layer's attention is
     // complete and all remaining ones after the expert queue is empty, so that they
     // run on whichever SMs are free instead of behind each SM's own expert items.
-    const bool oq = pos(W_OPROJ) > pos(W_MOE);
+    // Not when the attention drain follows the MoE drain: a drain that holds an O-proj
+    // tile waits for the layer's attention, which its own SM would only run later (with
+    // as many O-proj tiles as SMs every SM could be holding one); those orders deal the
+    // O-proj tiles statically, after the attention drain.
+    const bool oq = pos(W_OPROJ) > pos(W_MOE) && pos(W_ATT) < pos(W_MOE);
     for (int l = 0; l < L && oq; ++l) {
       const auto& wo = waves[(size_t)l * W_COUNT + W_OPROJ];
       int32_t* D = &P.tasks[(size_t)moe_oq[l] * kDescInts];
@@ -470,6 +477,8 @@ struct mk_handle {
   int32_t* d_tokens = nullptr;
   float* d_logits = nullptr;
   unsigned* d_trace_n = nullptr;
+  unsigned* d_snap = nullptr;  // inspection copy: counters, queue heads, queue counts
+  int inspect = 0;
   int fixed = 0;
   cudaStream_t last_stream = nullptr;
   // tensor maps
@@ -709,7 +718,9 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
   int r = derive_shape(cfg, s, nullptr);
   if (r) return r;
   std::vector<int> order;
-  parse_wave_order(default_order(), order);
+  const char* env = getenv("MK_WAVE_ORDER");
+  if (!parse_wave_order(env && *env ? env : default_order(), order))
+    return fail(nullptr, MK_ERR_INVALID, "bad wave order '%s'", env ? env : "");
   PlanOut P;
   r = build_plan(s, batch, n_sms, order, P, nullptr, prefetch_mask());
   if (r) return r;
@@ -827,6 +838,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(h->d_tokens, B);
   AL(h->d_logits, (size_t)B * s.V);
   AL(h->d_trace_n, 1);
+  AL(h->d_snap, (size_t)P.n_ctr + 6 * L);
 #undef AL
   p.c_lr = P.c_lr; p.c_qkvg = P.c_qkvg; p.c_rt = P.c_rt; p.c_rr = P.c_rr; p.c_att = P.c_att; p.c_og = P.c_og;
   p.c_md = P.c_md; p.c_od = P.c_od; p.c_oa = P.c_oa; p.c_done = P.c_done; p.n_ctr = P.n_ctr;
@@ -834,6 +846,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.od_target = P.od_target;
   p.tasks = h->d_tasks; p.sm_off = h->d_sm_off; p.sm_list = h->d_sm_list;
   p.trace = nullptr; p.trace_n = h->d_trace_n; p.trace_cap = 0;
+  p.snap = h->inspect ? h->d_snap : nullptr;
   CK(h, cudaMemcpy(h->d_tasks, P.tasks.data(), P.tasks.size() * 4, cudaMemcpyHostToDevice));
   CK(h, cudaMemcpy(h->d_sm_off, P.sm_off.data(), P.sm_off.size() * 4, cudaMemcpyHostToDevice));
   CK(h, cudaMemcpy(h->d_sm_list, P.sm_list.data(), P.sm_list.size() * 4, cudaMemcpyHostToDevice));
@@ -923,6 +936,7 @@ int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cach
   void* base = nullptr;
   CK(h, static_scratch_address(&base));
   Params p = h->prm;
+  p.snap = nullptr;  // the inspection reads describe the handle's own step buffers
   size_t z_off = 0, z_bytes = 0;
   step_scratch_layout(h, static_cast<uint8_t*>(base), &p, &z_off, &z_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1034,6 +1048,18 @@ int mk_plan_drop_signal(mk_handle* h, int task) {
   return MK_OK;
 }
 
+int mk_set_inspect(mk_handle* h, int on) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  h->inspect = on ? 1 : 0;
+  if (h->planned) {
+    CK(h, cudaSetDevice(h->dev));
+    CK(h, cudaDeviceSynchronize());
+    h->prm.snap = h->inspect ? h->d_snap : nullptr;
+    if (h->graph) { cudaGraphExecDestroy(h->graph); h->graph = nullptr; }
+  }
+  return MK_OK;
+}
+
 int mk_set_fixed(mk_handle* h, int fixed) {
   if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
   h->fixed = fixed ? 1 : 0;
@@ -1075,6 +1101,18 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
       return MK_OK;
     }
     case MK_READ_TRACE_COUNT: return copy(h->d_trace_n, 4);
+    case MK_READ_FINAL_COUNTERS:
+      if (!h->inspect) return fail(&h->err, MK_ERR_STATE, "mk_read(FINAL_COUNTERS): inspection is off");
+      return copy(h->d_snap, (size_t)p.n_ctr * 4);
+    case MK_READ_FINAL_QUEUES:
+      if (!h->inspect) return fail(&h->err, MK_ERR_STATE, "mk_read(FINAL_QUEUES): inspection is off");
+      return copy(h->d_snap + p.n_ctr, (size_t)2 * p.n_queues * 4);
+    case MK_READ_TASKS: {
+      const size_t n = h->P.tasks.size() * 4;
+      if (bytes != n) return fail(&h->err, MK_ERR_INVALID, "mk_read(TASKS): need %zu bytes, got %zu", n, bytes);
+      std::memcpy(host_out, h->P.tasks.data(), n);
+      return MK_OK;
+    }
     case MK_READ_ACTIVE: {
       const size_t maxa = p.maxa, per = 1 + maxa * (2 + B);
       if (bytes != L * per * 4) return fail(&h->err, MK_ERR_INVALID, "mk_read(ACTIVE): need %zu bytes", L * per * 4);

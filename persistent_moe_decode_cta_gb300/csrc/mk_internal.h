@@ -181,6 +181,9 @@ struct Params {
   int* err;                 // [16]
   int c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_od, c_oa, c_done, n_ctr, n_queues;
   int od_target;
+  // inspection (null = off): the step's last CTA copies the final counter values
+  // [n_ctr], then the queue heads [n_queues] and counts [n_queues], before the reset
+  unsigned* snap;
   // optional task timeline (see trace_emit)
   unsigned long long* trace;
   unsigned* trace_n;

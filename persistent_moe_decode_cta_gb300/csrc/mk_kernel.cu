@@ -17,6 +17,8 @@
 //    megakernel for 1.58x higher H100 throughput (the kitchen ticket rail, the
 //    three stalls); Cohere open-sources fused LLM decode kernel with 1.58x vLLM
 //    claim (16 task types, 32-int32 descriptor, warp roles).]
+#include <atomic>
+
 #include "mk_device.cuh"
 
 namespace mk {
@@ -1009,8 +1011,15 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     bool stale = false;
     for (int i = tid; i < BE; i += kConsumerThreads) {
       const uint64_t w = ld_relaxed_u64(src + i);
-      if ((unsigned)(w >> 32) != ep) stale = true;
-      else lg[i] = __uint_as_float((unsigned)w);
+      if ((unsigned)(w >> 32) != ep) {
+        stale = true;
+      } else {
+        // a NaN logit (non-finite activations) ranks below every number, so that all
+        // top_k slots are filled; the step reports MK_ERR_NAN
+        const float v = __uint_as_float((unsigned)w);
+        if (v != v) raise_err(p, MK_ERR_NAN, ti, -1, l, i);
+        lg[i] = (v != v) ? -INFINITY : v;
+      }
     }
     if (!bar_or_consumers(stale)) break;
     if (tid == 0) __nanosleep(ns);
@@ -1455,8 +1464,14 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
       break;
     case OP_ROUTER:
       // no fan-in: the layer's last router tile (D_AUX = 1) collects every tile's
-      // tagged logits itself and runs the route step
-      if (T[D_AUX] == 1 && !route_step(p, S, l, ti)) return false;
+      // tagged logits itself and runs the route step.  The router-tiles and route-ready
+      // counters are counted for the bookkeeping only (no task waits on them: the
+      // tagged logits and route words carry the readiness themselves).
+      if (T[D_AUX] == 1) {
+        if (!route_step(p, S, l, ti)) return false;
+        signal_async(p, S, sseq, C_RR(p, l), 1u);
+      }
+      signal_async(p, S, sseq, T[D_SIG_CTR], 1u);
       break;
     default:
       break;
@@ -2112,6 +2127,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         p.tok_out[(size_t)step * p.B + b] = best ? (int)~(unsigned)best : 0;
       }
+      if (p.do_reset && p.snap) {
+        // inspection: the step's final counters and queues, before they are cleared
+        for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x) p.snap[i] = *ctr_ptr(p, i);
+        for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) {
+          p.snap[p.n_ctr + i] = (unsigned)p.qhead[i];
+          p.snap[p.n_ctr + p.n_queues + i] = (unsigned)p.qcount[i];
+        }
+        __syncthreads();
+      }
       if (p.do_reset) {
         for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x)
           if (i != p.c_done) *ctr_ptr(p, i) = 0u;
@@ -2380,18 +2404,20 @@ namespace mk {
 // is only a stand-in and must never be passed to a kernel.
 cudaError_t static_scratch_address(void** ptr) {
   constexpr int kMaxDevices = 64;
-  static void* addr[kMaxDevices] = {};
+  // atomic entries: host threads may make their first call on a device concurrently
+  // (each looks the address up itself; they store the same value)
+  static std::atomic<void*> addr[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_mk_static_scratch);
+  void* a = addr[dev].load(std::memory_order_acquire);
+  if (!a) {
+    e = cudaGetSymbolAddress(&a, g_mk_static_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = p;
+    addr[dev].store(a, std::memory_order_release);
   }
-  *ptr = addr[dev];
+  *ptr = a;
   return cudaSuccess;
 }
 

@@ -29,8 +29,10 @@ def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
-def setup(workload, seed=0, steps=1, gain_jitter=0.1, device="cuda", seq_lens=None, batch=None):
+def setup(workload, seed=0, steps=1, gain_jitter=0.1, device="cuda", seq_lens=None, batch=None,
+          cfg_update=None):
     cfg = synth.model_config(workload)
+    cfg.update(cfg_update or {})
     W = synth.make_weights(cfg, seed=seed, device=device, gain_jitter=gain_jitter)
     seq = list(seq_lens) if seq_lens is not None else synth.seq_lens_for(workload, seed)
     if batch is not None:
@@ -160,3 +162,71 @@ def check_layer_teacher_forced(cfg, HW, HK, hid, gidx, gw, act, k, v, seq, pt, l
         assert rel_l2(gk, oracle.bf16_to_f64(rec["k"])) < REL_L2, (l, rec["b"])
         assert rel_l2(gv, oracle.bf16_to_f64(rec["v"])) < REL_L2, (l, rec["b"])
     return err
+
+
+def expected_split_count(cfg, l, pos, split_pages):
+    """Attention splits of a sequence at layer l: the oracle's attended cached keys
+    [window_start, pos) cut into pages of 16 and groups of split_pages pages."""
+    window = cfg["sliding_window"] if l in tuple(cfg.get("swa_layers", ())) else 0
+    lo = oracle.window_start(pos, window)
+    if pos <= lo:
+        return 0
+    npg = (pos - 1) // oracle.PAGE - lo // oracle.PAGE + 1
+    return -(-npg // split_pages)
+
+
+def check_bookkeeping(mk, cfg, seq):
+    """The schedule's bookkeeping after an inspected step, bit-exact:
+      * every counter's final value equals what the step must leave there -- each
+        descriptor's wait and signal targets (as planned), the per-(layer, sequence, KV
+        group) attention split counts + 1 from the oracle's attended ranges and the
+        GPU's split size, one route step per routed layer, the grid;
+      * every queue drained: head = items + one failing claim per SM, and the expert
+        queue's count = the routed experts' items (from the active lists)."""
+    from persistent_moe_decode_cta_gb300 import binding as Bd
+    T = mk.tasks()
+    fin = mk.final_counters().astype(np.int64)
+    heads, counts = mk.final_queues()
+    n_sm = mk.query(Bd.MK_Q_NUM_SMS)
+    Bn, L, Hkv = len(seq), cfg["n_layers"], cfg["n_kv_heads"]
+    _, _, _, I = Bd.mk_plan_dry(cfg, Bn, 4, max_batch=mk.max_batch)
+    maxa, t_moe, qkv_tpg, n_router = int(I[3]), int(I[5]), int(I[10]), int(I[11])
+    c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_od = (int(x) for x in I[16:24])
+    od_target, c_done, c_oa, t_dense, nrb_d = int(I[12]), int(I[13]), int(I[26]), int(I[27]), int(I[24])
+    dense = set(cfg.get("dense_layers", ()))
+    sp = mk.query(Bd.MK_Q_SPLIT_PAGES)
+    # 1. every descriptor's waits and signals end exactly at their planned targets
+    for t in T:
+        for c, tg in ((t[7], t[8]), (t[17], t[18]), (t[9], t[10])):
+            if c >= 0:
+                assert fin[c] == tg, (list(t[:3]), int(c), int(fin[c]), int(tg))
+    # 2. every counter, including those no descriptor names
+    want = np.zeros_like(fin)
+    want[c_lr:c_lr + L + 1] = nrb_d
+    want[c_qkvg:c_qkvg + L * Hkv] = qkv_tpg
+    want[c_og:c_og + L * Hkv] = Bn
+    want[c_od:c_od + L] = od_target
+    want[c_oa:c_oa + L] = Hkv * Bn
+    want[c_done] = n_sm
+    splits = np.zeros((L, Bn), dtype=np.int64)
+    for l in range(L):
+        routed = l not in dense
+        want[c_rt + l] = n_router if routed else 0
+        want[c_rr + l] = 1 if routed else 0
+        want[c_md + l] = maxa * t_moe if routed else t_dense
+        for b in range(Bn):
+            splits[l, b] = expected_split_count(cfg, l, seq[b], sp)
+            for g in range(Hkv):
+                want[c_att + (l * Bn + b) * Hkv + g] = splits[l, b] + 1
+    bad = np.flatnonzero(fin != want)
+    assert bad.size == 0, [(int(i), int(fin[i]), int(want[i])) for i in bad[:10]]
+    # 3. queues drained, each item claimed once
+    act = mk.active()
+    oq = {int(t[1]) for t in T if t[0] == 5 and t[6] > 0}      # layers whose drains serve O-proj
+    for l in range(L):
+        assert heads[l] == Hkv * int((splits[l] + 1).sum()) + n_sm, (l, heads[l])
+        items = t_dense if l in dense else len(act[l]) * t_moe
+        assert heads[L + l] == items + n_sm, (l, heads[L + l], items)
+        assert counts[L + l] == (0 if l in dense else items), (l, counts[L + l])
+        assert heads[2 * L + l] == (od_target + n_sm if l in oq else 0), (l, heads[2 * L + l])
+    return dict(splits=splits)

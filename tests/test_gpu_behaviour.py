@@ -123,6 +123,29 @@ def test_bad_token_reports_error():
     mk.close()
 
 
+def test_nan_router_logit_reports_error_and_routes_to_valid_experts():
+    """A router row of NaNs (non-finite weights: invalid input the route step checks)
+    makes that expert's logit NaN: the step completes with a full, valid top-k that
+    skips it, and reports MK_ERR_NAN with the layer and the logit's index."""
+    cfg, W, seq, pt, npages, k, v, tokens = PU.setup("tiny_b1_64", seq_lens=[40, 7])
+    W["router"][1, 3] = float("nan")
+    mk = B.Megakernel(cfg, W)
+    mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
+    logits = torch.empty(len(seq), cfg["vocab"], device="cuda")
+    mk.step(tokens, k, v, logits)
+    st = mk.status()
+    assert st["code"] == B.MK_ERR_NAN and st["observed"] == 1 and st["target"] % cfg["n_experts"] == 3
+    idx, w = mk.routes()
+    for b in range(len(seq)):
+        sel = [int(e) for e in idx[1, b]]
+        assert len(set(sel)) == cfg["top_k"] and 3 not in sel and all(0 <= e < cfg["n_experts"] for e in sel)
+        assert abs(float(w[1, b].sum()) - 1.0) < 1e-5
+    assert not mk.counters().any()
+    mk.step(tokens, k, v, logits)               # the context and the handle still work
+    assert mk.status()["code"] == B.MK_ERR_NAN
+    mk.close()
+
+
 def test_dropped_signal_times_out_and_the_context_survives():
     """A QKV tile whose completion signal is dropped (host-side injection): the
     attention splits waiting for its KV group give up after timeout_ms, the step

@@ -47,10 +47,12 @@ def test_pages_scale_step_sampled_layers_and_lm_head(pages_weights, workload, la
     mk = B.Megakernel(cfg, W, max_batch=8)
     try:
         mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
+        mk.inspect(True)
         logits = torch.empty(len(seq), cfg["vocab"], device="cuda")
         mk.step(tokens, k, v, logits)
         assert mk.status()["code"] == 0
         assert list(mk.seq_lens()) == [s + 1 for s in seq]
+        PU.check_bookkeeping(mk, cfg, seq)   # counters, split counts and queues, bit-exact
         hid = mk.hidden()
         gidx, gw = mk.routes()
         act = mk.active()

@@ -218,6 +218,55 @@ def test_schedule_completes_with_exact_counter_targets(workload, batch, n_sm, le
         Sim(cfg, batch, n_sm, lens, seed).run()
 
 
+def valid_orders():
+    """Every per-layer wave order the planner accepts: the letters r q a m o x with QKV
+    before attention before O-proj, the router before the MoE drain, and the MoE drain
+    and O-proj before ADD_RMSNORM."""
+    import itertools
+    out = []
+    for perm in itertools.permutations("rqamox"):
+        s = "".join(perm)
+        i = s.index
+        if i("q") < i("a") < i("o") and i("r") < i("m") < i("x") and i("o") < i("x"):
+            out.append(s)
+    return out
+
+
+# the pages' three named orders, as read here: the tuned order they state (QKV,
+# router, attention, MoE projections, O-proj and RMSNorm), attention-first (the whole
+# attention branch before the router), interleaved (the MoE branch's waves ahead of the
+# attention branch's, alternating)
+PAGES_ORDERS = {"tuned": "qramox", "attention-first": "qaormx", "interleaved": "rqmaox"}
+
+
+def test_valid_orders_include_the_pages_orders_and_reject_broken_ones(monkeypatch):
+    orders = valid_orders()
+    assert len(orders) == 10 and "rqamox" in orders
+    assert set(PAGES_ORDERS.values()) <= set(orders)
+    cfg = synth.model_config("tiny_b1_64")
+    for bad in ("aqrmox", "rqaxmo", "rqamo", "rqamoxx", "rqamoz"):
+        monkeypatch.setenv("MK_WAVE_ORDER", bad)
+        with pytest.raises(B.MkError):
+            B.mk_plan_dry(cfg, 1, 4)
+
+
+@pytest.mark.parametrize("order", valid_orders())
+@pytest.mark.parametrize("workload,batch,n_sm,lens", [
+    ("tiny_b1_64", 8, 3, [64, 1, 0, 17, 33, 200, 15, 16]),
+    ("small_b1_2k", 2, 5, [2048, 37]),
+    ("tiny_dense_b1_64", 2, 2, [64, 9]),
+])
+def test_every_wave_order_completes_with_exact_counter_targets(monkeypatch, order, workload, batch, n_sm,
+                                                                lens):
+    """Any order that respects the dependencies, dealt to fewer SMs than a layer has
+    O-proj tiles (the case in which a MoE drain ahead of the attention drain could hold
+    an O-proj tile on every SM), runs to completion with exact counter targets."""
+    monkeypatch.setenv("MK_WAVE_ORDER", order)
+    cfg = synth.model_config(workload)
+    for seed in range(2):
+        Sim(cfg, batch, n_sm, lens, seed).run()
+
+
 def test_tasks_are_dealt_round_robin_within_waves():
     cfg = synth.model_config("small_b1_2k")
     T, off, lst, info = B.mk_plan_dry(cfg, 1, 7)
