@@ -207,9 +207,10 @@ int mk_decode_step_host(mk_handle* h, const int32_t* tokens_host, void* k_cache,
  * device array of 64 MiB (kept on every GPU that loads the library until the process
  * exits).  The pages have no counterpart to this entry point.
  *   Arguments, layouts and results are those of mk_decode_step; the handle's packed
- *   weights, plan and seq_lens are used as usual.  The per-step state that mk_read
- *   returns (hidden states, routes, active lists, counters) is that of the last
- *   mk_decode_step, not of this call, whose scratch is not the handle's.
+ *   weights, plan and seq_lens are used as usual.  mk_read's per-step state (hidden
+ *   states, routes, router logits, active lists, counters) follows the handle's last
+ *   step: after this call it is read from the static array, as the last
+ *   allocation-free call on the device (of any handle) left it.
  *   Plans whose step scratch exceeds 64 MiB are rejected with MK_ERR_UNSUPPORTED and a
  *   message giving the size needed (the pages-scale model needs ~21 MiB at batch 1 with
  *   8K context, ~29 MiB at 128K, ~53 MiB at batch 2 with 32K, ~168 MiB at batch 8).

@@ -478,6 +478,7 @@ struct mk_handle {
   float* d_logits = nullptr;
   unsigned* d_trace_n = nullptr;
   unsigned* d_snap = nullptr;  // inspection copy: counters, queue heads, queue counts
+  bool last_noalloc = false;   // the last step ran in the static scratch (mk_read follows it)
   int inspect = 0;
   int fixed = 0;
   cudaStream_t last_stream = nullptr;
@@ -853,6 +854,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   CK(h, cudaMemcpy(p.seq_lens, seq_lens_host, (size_t)B * 4, cudaMemcpyHostToDevice));
   const unsigned first_epoch = 1;  // the cleared tagged words carry epoch 0
   CK(h, cudaMemcpy(p.epoch, &first_epoch, 4, cudaMemcpyHostToDevice));
+  h->last_noalloc = false;
   h->planned = true;
   return MK_OK;
 }
@@ -861,6 +863,7 @@ int mk_decode_step(mk_handle* h, const int32_t* tokens_dev, void* k_cache, void*
                    void* stream) {
   int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
   if (r) return r;
+  h->last_noalloc = false;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   return launch_segment(h, 0, true, true, st);
@@ -873,6 +876,7 @@ int mk_decode_steps(mk_handle* h, const int32_t* tokens_dev, int n_steps, void* 
   if (!tokens_out_dev) return fail(&h->err, MK_ERR_INVALID, "tokens_out is NULL");
   int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
   if (r) return r;
+  h->last_noalloc = false;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   Params p = h->prm;
@@ -903,16 +907,17 @@ static size_t step_scratch_layout(const mk_handle* h, uint8_t* base, Params* p, 
   q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->Q = (uint16_t*)q;
   q = take(L * s.Hkv * B * (size_t)h->max_items_bg * s.gs * (s.hd + 2) * 4); if (p) p->attp = (float*)q;
   q = take(L * B * s.Hq * s.hd * 2);                            if (p) p->atto = (uint16_t*)q;
+  // cleared each call: the routing arrays read back by mk_read (a dense layer of a
+  // mixed stack never writes its own: they must read as "no experts"), the layer
+  // accumulators, the counters and queues, and the epoch-tagged words (other handles'
+  // calls share this array and may have used the same epochs)
+  const size_t z0 = o;
   q = take(L * B * s.topk * 4);                                 if (p) p->ridx = (int*)q;
   q = take(L * B * s.topk * 4);                                 if (p) p->rw = (float*)q;
   q = take(L * maxa * 4);                                       if (p) p->active = (int*)q;
   q = take(L * 4);                                              if (p) p->nact = (int*)q;
   q = take(L * maxa * 4);                                       if (p) p->act_cnt = (int*)q;
   q = take(L * maxa * B * 4);                                   if (p) p->act_tok = (int*)q;
-  // cleared each call: the layer accumulators, the counters and queues, and the
-  // epoch-tagged words (other handles' calls share this array and may have used the
-  // same epochs)
-  const size_t z0 = o;
   q = take(L * B * s.d * 4);                                    if (p) p->moe = (float*)q;
   q = take(L * B * s.E * 8);                                    if (p) p->rlog = (uint64_t*)q;
   q = take(L * (1 + 2 * maxa + 2 * maxa * B) * 8);              if (p) { p->rword = (uint64_t*)q; p->rw_stride = (int)(1 + 2 * maxa + 2 * maxa * B); }
@@ -942,6 +947,7 @@ int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cach
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // counters, queues and tagged words must start at zero; the rest is written before it is read
   CK(h, cudaMemsetAsync(static_cast<uint8_t*>(base) + z_off, 0, z_bytes, st));
+  h->last_noalloc = true;
   h->last_stream = st;
   p.sm_off = h->d_sm_off;
   p.do_reset = 1;
@@ -968,6 +974,7 @@ int mk_decode_step_perop(mk_handle* h, const int32_t* tokens_dev, void* k_cache,
                          float* logits_dev, void* stream, int use_graph) {
   int r = prepare_step(h, tokens_dev, k_cache, v_cache, logits_dev);
   if (r) return r;
+  h->last_noalloc = false;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   const int first = 1, last = h->P.n_segs - 1;
@@ -1070,10 +1077,15 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes) {
   if (!h || !host_out) return fail(h ? &h->err : nullptr, MK_ERR_INVALID, "NULL argument");
   if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");
   const Shape& s = h->s;
-  const Params& p = h->prm;
+  Params p = h->prm;
   const size_t L = s.L, B = h->B;
   CK(h, cudaSetDevice(h->dev));
   CK(h, cudaDeviceSynchronize());
+  if (h->last_noalloc) {  // the step buffers of the last step are in the static scratch
+    void* base = nullptr;
+    CK(h, static_scratch_address(&base));
+    step_scratch_layout(h, static_cast<uint8_t*>(base), &p, nullptr, nullptr);
+  }
   auto copy = [&](const void* src, size_t n) -> int {
     if (n != bytes) return fail(&h->err, MK_ERR_INVALID, "mk_read(%d): need %zu bytes, got %zu", what, n, bytes);
     CK(h, cudaMemcpy(host_out, src, n, cudaMemcpyDeviceToHost));

@@ -175,14 +175,16 @@ def expected_split_count(cfg, l, pos, split_pages):
     return -(-npg // split_pages)
 
 
-def check_bookkeeping(mk, cfg, seq):
+def check_bookkeeping(mk, cfg, seq, megakernel=True):
     """The schedule's bookkeeping after an inspected step, bit-exact:
       * every counter's final value equals what the step must leave there -- each
         descriptor's wait and signal targets (as planned), the per-(layer, sequence, KV
         group) attention split counts + 1 from the oracle's attended ranges and the
         GPU's split size, one route step per routed layer, the grid;
       * every queue drained: head = items + one failing claim per SM, and the expert
-        queue's count = the routed experts' items (from the active lists)."""
+        queue's count = the routed experts' items (from the active lists).  The O-proj
+        queue serves the megakernel's MoE drains only (megakernel=False: the per-op
+        launches deal the O-proj tiles as a wave of their own)."""
     from persistent_moe_decode_cta_gb300 import binding as Bd
     T = mk.tasks()
     fin = mk.final_counters().astype(np.int64)
@@ -222,7 +224,7 @@ def check_bookkeeping(mk, cfg, seq):
     assert bad.size == 0, [(int(i), int(fin[i]), int(want[i])) for i in bad[:10]]
     # 3. queues drained, each item claimed once
     act = mk.active()
-    oq = {int(t[1]) for t in T if t[0] == 5 and t[6] > 0}      # layers whose drains serve O-proj
+    oq = {int(t[1]) for t in T if t[0] == 5 and t[6] > 0} if megakernel else set()
     for l in range(L):
         assert heads[l] == Hkv * int((splits[l] + 1).sum()) + n_sm, (l, heads[l])
         items = t_dense if l in dense else len(act[l]) * t_moe

@@ -50,7 +50,7 @@ def _run(workload, seq_lens=None, mode="mega", order=None, monkeypatch=None, che
         else:
             mk.step_perop(tokens, k, v, logits, use_graph=(mode == "graph"))
         assert mk.status()["code"] == 0
-        bk = PU.check_bookkeeping(mk, cfg, seq)
+        bk = PU.check_bookkeeping(mk, cfg, seq, megakernel=(mode == "mega"))
         if check_oracle:
             PU.check_step(cfg, mk, W, seq, pt, (kb, vb), tokens.cpu().numpy(), logits, k, v)
         assert not mk.counters().any()          # and cleared for the next step
