@@ -98,6 +98,8 @@ def f64_to_bf16(x) -> np.ndarray:
 # [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "Current limitations":
 # FP8 weights are on the roadmap; the pages fix no format: E4M3 with per-channel
 # float32 scales is the reading taken]
+# cfg["expert_dtype"] == "fp8": the routed experts are stored so; cfg["dense_dtype"] ==
+# "fp8" as well: QKV, O-proj and LM-head matrices too (router and embedding stay bf16).
 E4M3_MAX = 448.0
 
 
@@ -157,6 +159,17 @@ def fp8_expert(wg_u16, wu_u16, wd_u16):
     """The expert's matrices as the FP8 path stores them (per-row scales), decoded to
     float64."""
     return tuple(dequantize_e4m3(*quantize_e4m3_rows(w)) for w in (wg_u16, wu_u16, wd_u16))
+
+
+def fp8_matrix(w_u16):
+    """A dense projection (QKV, O-proj, LM head) as the FP8 weight path stores it: E4M3
+    codes with one float32 scale per output channel (row), the reading taken for the
+    experts, decoded to float64.  The router and the embedding stay bf16."""
+    return dequantize_e4m3(*quantize_e4m3_rows(w_u16))
+
+
+def _dense(cfg, w_u16):
+    return fp8_matrix(w_u16) if cfg.get("dense_dtype") == "fp8" else bf16_to_f64(w_u16)
 
 
 def rms_norm(x, gain, eps):
@@ -283,7 +296,8 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
 
     dense = l in tuple(cfg.get("dense_layers", ()))
     g = bf16_to_f64(W.attn_norm(l))
-    Wq, Wk, Wv, Wo = (_mat(W.wq(l)), _mat(W.wk(l)), _mat(W.wv(l)), _mat(W.wo(l)))
+    Wq, Wk, Wv, Wo = (_dense(cfg, W.wq(l)), _dense(cfg, W.wk(l)), _dense(cfg, W.wv(l)),
+                      _dense(cfg, W.wo(l)))
     h = rms_norm(x, g, eps)                                   # [B, d]
 
     info = dict(router_logits=np.empty((B, cfg["n_experts"])), idx=[], w=[], margin=[],
@@ -354,8 +368,8 @@ def lm_head(cfg, W, x, rows_per_chunk=16384):
     Wlm = W.lm_head()
     V = Wlm.shape[0]
     out = np.empty((x.shape[0], V))
-    for r0 in range(0, V, rows_per_chunk):
-        out[:, r0:r0 + rows_per_chunk] = h @ bf16_to_f64(Wlm[r0:r0 + rows_per_chunk]).T
+    for r0 in range(0, V, rows_per_chunk):    # (per-row scales: chunks of rows decode alone)
+        out[:, r0:r0 + rows_per_chunk] = h @ _dense(cfg, Wlm[r0:r0 + rows_per_chunk]).T
     return out
 
 
@@ -382,7 +396,7 @@ def decode_step(cfg, W, kv, tokens, seq_lens, page_table, forced=None):
     return dict(logits=logits, greedy=greedy, hidden=np.stack(hidden), layers=layers)
 
 
-__all__ = ["e4m3_to_f64", "f32_to_e4m3", "quantize_e4m3_rows", "dequantize_e4m3", "fp8_expert",
+__all__ = ["e4m3_to_f64", "f32_to_e4m3", "quantize_e4m3_rows", "dequantize_e4m3", "fp8_expert", "fp8_matrix",
            "bf16_to_f64", "f64_to_bf16", "rms_norm", "rope", "softmax", "attention",
            "attention_partial", "merge_partials", "router_topk", "silu", "swiglu_expert",
            "window_start", "argmax_lowest", "layer_step", "lm_head", "embed",

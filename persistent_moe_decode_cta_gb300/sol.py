@@ -59,6 +59,13 @@ def step_bytes(cfg: dict, seq_lens, union_sizes) -> dict:
     dense_ffn = 3 * d * cfg.get("dense_ff", 0)
     weights = BF16 * (L * pc["dense_layer"] - n_dense * d * cfg["n_experts"]
                       + n_dense * dense_ffn + V * d + d + B * d) + routed_union * expert_bytes(cfg)
+    if cfg.get("dense_dtype", "bf16") == "fp8":
+        # QKV, O-proj and LM head as E4M3 codes plus a float32 scale per row (router,
+        # norms and embedding stay bf16)
+        Hq = cfg["n_q_heads"]
+        qkv_rows, o_rows = (Hq + 2 * Hkv) * hd, d
+        fp8_elems = L * (qkv_rows * d + o_rows * Hq * hd) + V * d
+        weights += (1 - BF16) * fp8_elems + 4 * (L * (qkv_rows + o_rows) + V)
     swa = set(cfg.get("swa_layers", ()))
     kv_read = 0
     for p in seq_lens:

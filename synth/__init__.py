@@ -48,6 +48,9 @@ MODELS["pages_dense3"] = dict(MODELS["pages"], dense_layers=(0, 1, 2), dense_ff=
 # weights drawn are the bf16 ones; quantisation happens when the model is loaded).
 for _m in ("tiny", "small", "pages", "pages_l2", "tiny_dense", "small_dense"):
     MODELS[_m + "_fp8"] = dict(MODELS[_m], expert_dtype="fp8")
+# ... and with the dense projections (QKV, O-proj, LM head) in FP8 as well
+for _m in ("tiny", "small", "pages", "pages_l2", "pages_l1", "tiny_dense", "small_dense"):
+    MODELS[_m + "_fp8w"] = dict(MODELS[_m], expert_dtype="fp8", dense_dtype="fp8")
 
 # Workloads: a model plus a batch of cached sequence lengths.
 WORKLOADS = {
@@ -74,6 +77,15 @@ WORKLOADS = {
                                     sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
     "pages_l2_fp8_b8_ragged_swa": dict(model="pages_l2_fp8", batch=8, lens=("uniform", 1024, 32768),
                                        sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
+    # FP8 experts and dense projections
+    "tiny_fp8w_b1_64": dict(model="tiny_fp8w", batch=1, lens=("fixed", 64)),
+    "small_fp8w_b1_2k": dict(model="small_fp8w", batch=1, lens=("fixed", 2048)),
+    "tiny_dense_fp8w_b1_64": dict(model="tiny_dense_fp8w", batch=1, lens=("fixed", 64)),
+    "pages_fp8w_b1_8k": dict(model="pages_fp8w", batch=1, lens=("fixed", 8192)),
+    "pages_l1_fp8w_b1_8k": dict(model="pages_l1_fp8w", batch=1, lens=("fixed", 8192)),
+    "pages_l2_fp8w_b1_8k": dict(model="pages_l2_fp8w", batch=1, lens=("fixed", 8192)),
+    "pages_fp8w_b8_ragged_swa": dict(model="pages_fp8w", batch=8, lens=("uniform", 1024, 32768),
+                                     sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
 }
 
 
@@ -218,11 +230,13 @@ def _u16(t: torch.Tensor) -> np.ndarray:
 
 class HostWeights:
     """Adapter from the tensor dict of make_weights() to the oracle's weight
-    accessors."""
+    accessors.  cache_experts=True also keeps the host copy of every expert asked for
+    (for repeated oracle steps; the dense matrices are always kept)."""
 
-    def __init__(self, W: dict):
+    def __init__(self, W: dict, cache_experts: bool = False):
         self.W = W
         self._cache = {}
+        self.cache_experts = cache_experts
 
     def _get(self, key, fn):
         if key not in self._cache:
@@ -242,8 +256,9 @@ class HostWeights:
     def router(self, l): return self._get(("wr", l), lambda: _u16(self.W["router"][l]))
 
     def expert(self, l, e):
-        return (_u16(self.W["w_gate"][l, e]), _u16(self.W["w_up"][l, e]),
-                _u16(self.W["w_down"][l, e]))
+        fn = lambda: (_u16(self.W["w_gate"][l, e]), _u16(self.W["w_up"][l, e]),
+                      _u16(self.W["w_down"][l, e]))
+        return self._get(("ex", l, e), fn) if self.cache_experts else fn()
 
     def dense_ffn(self, l):
         return (_u16(self.W["ffn_gate"][l]), _u16(self.W["ffn_up"][l]), _u16(self.W["ffn_down"][l]))
@@ -257,14 +272,22 @@ class HostWeights:
 
 class HostKV:
     """Adapter from K/V pool tensors [L, n_pages, Hkv, 16, hd] to the oracle's page
-    gather accessor."""
+    gather accessor.  cache=True keeps each layer's gathered pages (repeated oracle
+    steps over the same pages)."""
 
-    def __init__(self, k: torch.Tensor, v: torch.Tensor):
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, cache: bool = False):
         self.k, self.v = k, v
+        self._cache = {} if cache else None
 
     def pages(self, l, page_ids):
+        key = (l, tuple(int(p) for p in page_ids)) if self._cache is not None else None
+        if key is not None and key in self._cache:
+            return self._cache[key]
         idx = torch.as_tensor(np.asarray(page_ids, dtype=np.int64), device=self.k.device)
-        return _u16(self.k[l].index_select(0, idx)), _u16(self.v[l].index_select(0, idx))
+        out = _u16(self.k[l].index_select(0, idx)), _u16(self.v[l].index_select(0, idx))
+        if key is not None:
+            self._cache[key] = out
+        return out
 
 
 class LazyHostWeights:

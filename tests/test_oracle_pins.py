@@ -639,3 +639,80 @@ def test_fp8_expert_scales_are_per_output_channel():
             v = np.abs(wq) / scale[:, None]
             assert np.all(np.isin(v, grid)), e
             assert np.array_equal(v.max(axis=1), np.full(wf.shape[0], 448.0))
+
+
+# ----------------------------------------------------------------- FP8 dense projections
+
+def _e4m3_grid_bf16(shape, k, seed):
+    """bf16 matrices whose rows lie exactly on the E4M3 grid of scale 2^-k: random finite
+    codes times 2^-k, each row's first element +-448 * 2^-k (so the row's max|w| / 448 is
+    2^-k and quantisation is lossless)."""
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 256, size=shape).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x10                     # no NaN codes
+    v = O.e4m3_to_f64(codes) * 2.0 ** -k
+    v[..., 0] = np.where(rng.random(shape[:-1]) < 0.5, -448.0, 448.0) * 2.0 ** -k
+    return torch.from_numpy(v).to(torch.bfloat16)            # exact: 4 significant bits
+
+
+def _fp8w(cfg):
+    return dict(cfg, expert_dtype="fp8", dense_dtype="fp8")
+
+
+def test_fp8_dense_projections_are_lossless_on_the_e4m3_grid():
+    """Projections whose weights lie on the E4M3 grid of their row scales quantise
+    without loss, so the layer and the LM head with FP8 dense projections (and FP8
+    experts on the grid too) equal the bf16 ones exactly: the FP8 reading applies the
+    same matrices in the same places."""
+    cfg = dict(TINY, d_ff=64)
+    W, pt, k, v = _setup(cfg)
+    for i, name in enumerate(("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down")):
+        W[name] = _e4m3_grid_bf16(tuple(W[name].shape), 9, seed=i)
+    W["lm_head"] = _e4m3_grid_bf16(tuple(W["lm_head"].shape), 8, seed=9)
+    HW, kv = synth.HostWeights(W), synth.HostKV(k, v)
+    x = _x(2, 32)
+    for l in (0, 1):
+        y16, i16 = O.layer_step(cfg, HW, kv, l, x, [37, 5], pt)
+        y8, i8 = O.layer_step(_fp8w(cfg), HW, kv, l, x, [37, 5], pt)
+        assert np.array_equal(y8, y16) and np.array_equal(i8["idx"], i16["idx"])
+        for r16, r8 in zip(i16["kv"], i8["kv"]):
+            assert np.array_equal(r8["k"], r16["k"]) and np.array_equal(r8["v"], r16["v"])
+    assert np.array_equal(O.lm_head(_fp8w(cfg), HW, x), O.lm_head(cfg, HW, x))
+
+
+def test_fp8_dense_projections_change_the_layer_only_by_the_quantisation():
+    """On random weights the FP8 projections move the layer's output and the logits by
+    a small relative amount (E4M3 keeps 3 mantissa bits: per-weight error <= 1/16 of
+    the value), the routing weights' source -- the bf16 router -- is untouched, and the
+    query, key and value heads differ from the bf16 ones only through Wq, Wk, Wv."""
+    cfg = dict(TINY, d_ff=64)
+    W, pt, k, v = _setup(cfg)
+    HW, kv = synth.HostWeights(W), synth.HostKV(k, v)
+    x = _x(2, 32)
+    y16, i16 = O.layer_step(dict(cfg, expert_dtype="fp8"), HW, kv, 0, x, [37, 5], pt)
+    y8, i8 = O.layer_step(_fp8w(cfg), HW, kv, 0, x, [37, 5], pt)
+    assert np.array_equal(i8["router_logits"], i16["router_logits"])   # router stays bf16
+    rel = np.linalg.norm(y8 - y16) / np.linalg.norm(y16 - x)
+    assert 0 < rel < 0.1, rel
+    # the K the layer writes is bf16(RoPE(decoded Wk h))
+    g = O.bf16_to_f64(HW.attn_norm(0))
+    for b, p in ((0, 37), (1, 5)):
+        h = x[b] / math.sqrt(np.mean(x[b] ** 2) + 1e-6) * g
+        kn = O.rope((O.fp8_matrix(HW.wk(0)) @ h).reshape(2, 8), p, 1e4)
+        assert np.array_equal(i8["kv"][b]["k"], O.f64_to_bf16(kn))
+    l8, l16 = O.lm_head(_fp8w(cfg), HW, x), O.lm_head(cfg, HW, x)
+    assert 0 < np.abs(l8 - l16).max() < 0.1 * np.abs(l16).max()
+
+
+def test_fp8_dense_scales_are_per_output_channel():
+    """Each decoded row of Wq, Wk, Wv, Wo and the LM head is an E4M3 value times one
+    scale, the row's max|w| / 448, and the row's largest weight decodes to 448 times it."""
+    W, _, _, _ = _setup(dict(TINY, d_ff=64))
+    HW = synth.HostWeights(W)
+    grid = np.unique(np.abs(O.e4m3_to_f64(np.arange(256, dtype=np.uint8)[(np.arange(256) & 0x7F) != 0x7F])))
+    for w16 in (HW.wq(0), HW.wk(1), HW.wv(0), HW.wo(1), HW.lm_head()):
+        wf = O.bf16_to_f64(w16)
+        scale = (np.abs(wf).max(axis=1).astype(np.float32) / np.float32(448.0)).astype(np.float64)
+        vq = np.abs(O.fp8_matrix(w16)) / scale[:, None]
+        assert np.all(np.isin(vq, grid))
+        assert np.array_equal(vq.max(axis=1), np.full(wf.shape[0], 448.0))
