@@ -12,8 +12,8 @@ steps.
 
 N > 1 runs under torchrun as independent replicas (the step has no data-parallel
 split; each rank decodes its own batch): value = all ranks' tokens / max-over-ranks
-time.  `--impl reference` times the CPU oracle (a bounded slice of the same step,
-scaled to a full step) on the host cores.
+time.  `--impl reference` times the CPU oracle on the host cores: whole decode steps
+of the same workload, over the benchmark's own inputs.
 """
 from __future__ import annotations
 
@@ -54,6 +54,9 @@ def parse_args():
     ap.add_argument("--multistep", type=int, default=16,
                     help="also time greedy decode with this many steps per launch (tokens fed "
                          "back on the device); 0 skips it")
+    ap.add_argument("--no-long", action="store_true", help="skip the batch-1 128K-context measurement")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8-expert batch-8 measurement")
+    ap.add_argument("--oracle-probe", default="", help=argparse.SUPPRESS)
     ap.add_argument("--trace", default="",
                     help="after timing, record one step's task timeline and write a per-opcode "
                          "summary (JSON) to this path")
@@ -270,58 +273,43 @@ def union_sizes(mk, L):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
-class OracleSampler:
-    """The CPU oracle timed on a slice of one decode step of a workload: layer steps
-    (layer-0 weights drawn on the host, the workload's batch and context length) and
-    1/lm_frac of the LM head, scaled to a full step.  Weights are drawn once, before
-    any timing."""
+class OracleSteps:
+    """Whole CPU-oracle decode steps of a workload (every layer, the full LM head) on
+    the host cores, over the same inputs as the GPU arm: the benchmark's seeded weights
+    and K/V (device tensors, copied to the host once, during an untimed first step) and
+    its page table and tokens.  Without a GPU the weights and pages are drawn on the
+    host from the same per-tensor seeds (other values, same shapes and distribution)."""
 
-    def __init__(self, workload, seed, lm_frac=16):
-        import numpy as np
+    def __init__(self, workload, seed, W=None, kv=None):
+        import numpy as np  # noqa: F401
 
         import oracle
         import synth
         self.O = oracle
+        self.workload = workload
         self.cfg = synth.model_config(workload)
         self.seq = synth.seq_lens_for(workload, seed)
         self.B = len(self.seq)
-        self.W = synth.LazyHostWeights(self.cfg, seed)
-        self.kv = synth.LazyHostKV(self.cfg, seed)
         self.pt, _ = synth.make_page_table(self.seq, steps=1, seed=seed)
-        self.x0 = np.random.default_rng(seed).standard_normal((self.B, self.cfg["d_model"])) * 0.02
-        self.lm_frac = lm_frac
-        self.n_lm = self.cfg["vocab"] // lm_frac
-        self.workload = workload
-        self.O.layer_step(self.cfg, self.W, self.kv, 0, self.x0, self.seq, self.pt)
-        self.W.lm_head(self.n_lm)
-        W = self.W
-        n_lm = self.n_lm
+        self.tokens = synth.make_tokens(self.B, self.cfg["vocab"], seed=seed).numpy()
+        if W is not None:
+            self.W = synth.HostWeights(W, cache_experts=True)
+            self.kv = synth.HostKV(*kv, cache=True)
+            self.source = "the benchmark's device weights and K/V, copied to the host once"
+        else:
+            self.W = synth.LazyHostWeights(self.cfg, seed)
+            self.kv = synth.LazyHostKV(self.cfg, seed)
+            self.source = "weights and K/V drawn on the host"
+        self.step()            # untimed: brings every tensor the step reads to the host
 
-        class LM:
-            def final_norm(self): return W.final_norm()
-            def lm_head(self): return W.lm_head(n_lm)
-        self.lm = LM()
-
-    def step_seconds(self, budget_s=0.0, max_layers=1):
-        """Seconds of a full step, estimated from >= 1 timed layer steps."""
-        x = self.x0
+    def step(self):
         t0 = time.perf_counter()
-        n = 0
-        while n < 1 or (n < max_layers and (time.perf_counter() - t0) < budget_s):
-            x, _ = self.O.layer_step(self.cfg, self.W, self.kv, 0, x, self.seq, self.pt)
-            n += 1
-        t_layers = time.perf_counter() - t0
-        t1 = time.perf_counter()
-        self.O.lm_head(self.cfg, self.lm, x)
-        t_lm = time.perf_counter() - t1
-        self.last = (n, t_layers + t_lm)
-        return t_layers / n * self.cfg["n_layers"] + t_lm * self.lm_frac
+        self.O.decode_step(self.cfg, self.W, self.kv, self.tokens, self.seq, self.pt)
+        return time.perf_counter() - t0
 
-    def describe(self):
-        n, t = self.last
-        return (f"{self.workload}: {n} layer step(s) at B={self.B} + 1/{self.lm_frac} of the LM "
-                f"head, float64 numpy oracle, scaled to {self.cfg['n_layers']} layers + the full "
-                f"LM head; {t:.1f} s timed")
+    def describe(self, n):
+        return (f"{self.workload}: {n} whole float64 numpy oracle step(s) ({self.cfg['n_layers']} layers "
+                f"+ the full LM head, batch {self.B}) over {self.source}")
 
 
 def cpu_cores():
@@ -329,24 +317,59 @@ def cpu_cores():
     return int(threads) if threads else os.cpu_count()
 
 
+def oracle_probe(workload, steps):
+    """Median seconds of `steps` whole oracle steps of a small workload (host-drawn
+    inputs); run in a child process for the single-core measurement."""
+    o = OracleSteps(workload, 0)
+    return statistics.median(o.step() for _ in range(steps))
+
+
+def small_configs_cpu(steps=3):
+    """The tiny and small parity models, whole oracle steps, median of `steps`, with all
+    cores and with one core (a child interpreter with one BLAS thread)."""
+    out = {}
+    for wl in ("tiny_b1_64", "small_b1_2k"):
+        allc = oracle_probe(wl, steps)
+        env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-probe", wl,
+                            "--steps", str(steps)], env=env, capture_output=True, text=True, timeout=600)
+        one = float(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+        out[wl] = {"tok_s_all_cores": 1.0 / allc, "tok_s_one_core": (1.0 / one) if one else None,
+                   "cores": cpu_cores(), "steps": steps}
+    return out
+
+
 def run_reference(args, rank, ws):
+    """The reference arm: the CPU oracle, as it stands, timed on the host cores with
+    whole decode steps -- args.warmup untimed, then args.steps timed -- of the
+    workload's batch, over the benchmark's own inputs."""
     if rank != 0:
         return 0
-    smp = OracleSampler(args.workload, args.seed, lm_frac=64)
-    per = []
-    for i in range(args.warmup + args.steps):
-        s = smp.step_seconds()
-        if i >= args.warmup:
-            per.append(s)
+    W = kv = None
+    try:
+        import torch
+        if torch.cuda.is_available():
+            import synth
+            cfg = synth.model_config(args.workload)
+            seq = synth.seq_lens_for(args.workload, args.seed)
+            W = synth.make_weights(cfg, seed=args.seed, device="cuda")
+            _, npages = synth.make_page_table(seq, steps=1, seed=args.seed)
+            kv = synth.make_kv(cfg, npages, seed=args.seed, device="cuda")
+    except Exception:
+        W = kv = None
+    o = OracleSteps(args.workload, args.seed, W, kv)
+    for _ in range(args.warmup):
+        o.step()
+    per = [o.step() for _ in range(args.steps)]
     step_s = statistics.mean(per)
-    value = smp.B / step_s
+    value = o.B / step_s
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": args.workload, "batch": smp.B},
+            "config": {"workload": args.workload, "batch": o.B, "seq_lens": o.seq, "mode": "oracle"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": "each step: " + smp.describe()},
+                             "sample": o.describe(args.steps)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -355,6 +378,9 @@ def run_reference(args, rank, ws):
 # ----------------------------------------------------------------------------- main
 def main():
     args = parse_args()
+    if args.oracle_probe:
+        print(oracle_probe(args.oracle_probe, args.steps))
+        return 0
     rank, ws, local = dist_init()
     if args.impl == "reference":
         return run_reference(args, rank, ws)
@@ -368,8 +394,10 @@ def main():
     stream = torch.cuda.current_stream()
     cfg, mk, st, W = build_state(args.workload, args.seed, device)
     B = len(st["seq"])
-    if args.no_bs8 or args.workload != "pages_b1_8k":
-        # the unpacked weights are only needed again to build the batch-8 handle
+    full = args.workload == "pages_b1_8k"
+    if not full:
+        # the unpacked weights are only needed again to build the batch-8 handles and
+        # for the CPU oracle's copy of the workload
         W = None
         torch.cuda.empty_cache()
 
@@ -520,43 +548,77 @@ def main():
             raise RuntimeError("device error in per-op arms")
         line["baselines"] = bl
 
-    # ---- batch 8, ragged lengths, sliding window on odd layers (same weights)
-    if not args.no_bs8 and args.workload == "pages_b1_8k":
+    # ---- CPU oracle baseline (rank 0, N = 1): whole oracle steps over this workload's
+    # inputs, and the two small parity models with all cores and with one
+    if not args.no_cpu and rank == 0 and ws == 1:
+        o = OracleSteps(args.workload, args.seed, W, (st["k"], st["v"]))
+        per = [o.step() for _ in range(2)]
+        line["cpu_baseline"] = {"value": o.B / statistics.mean(per), "unit": UNIT, "cores": cpu_cores(),
+                                "kind": "oracle", "sample": o.describe(len(per)),
+                                "small_configs": small_configs_cpu()}
+        del o
+
+    # ---- batch 1 at the 128K context (BASELINE config 5): the same handle, re-planned
+    if not args.no_long and full and args.mode == "mega":
+        import synth
+        wl5 = "pages_b1_128k"
+        cfg5 = synth.model_config(wl5)
+        seq5 = synth.seq_lens_for(wl5, args.seed)
+        del st
+        torch.cuda.empty_cache()
+        st5 = plan_workload(mk, cfg5, wl5, seq5, args.seed, device)
+
+        def step5():
+            mk.step(st5["tokens"], st5["k"], st5["v"], st5["logits"])
+        step5()
+        k5 = max(10, args.steps // 2)
+        t5, per5 = time_device(step5, k5, args.warmup, ws, stream)
+        if mk.status()["code"] != 0:
+            raise RuntimeError("device error in the 128K arm")
+        t5 = max_over_ranks(t5, ws, device)
+        sb5 = sol.step_bytes(cfg5, seq5, union_sizes(mk, cfg5["n_layers"]))
+        ach5 = sb5["total"] / statistics.mean(per5) / 1e9
+        line["long128k"] = {"workload": wl5, "value": ws * k5 / t5, "unit": UNIT, "ms_per_step": t5 / k5 * 1e3,
+                            "bytes_per_step": sb5["total"], "achieved_gbs": ach5, "frac": ach5 / hbm,
+                            "sol_tok_s": sol.sol_tok_s(sb5["total"], hbm * 1e9, 1)}
+        del st5
+        torch.cuda.empty_cache()
+
+    # ---- batch 8, ragged lengths, sliding window on odd layers (same weights), in bf16
+    # and with the routed experts stored as FP8
+    if not args.no_bs8 and full:
         import synth
         wl8 = "pages_b8_ragged_swa"
         cfg8 = synth.model_config(wl8)
         seq8 = synth.seq_lens_for(wl8, args.seed)
-        # the sliding window is a plan-time property of the layers: re-create with it
-        del st
-        mk.close()
-        torch.cuda.empty_cache()
-        mk = Bd.Megakernel(cfg8, W, max_batch=8)
-        st8 = plan_workload(mk, cfg8, wl8, seq8, args.seed, device)
+        arms = [("bs8", cfg8)]
+        if not args.no_fp8:
+            arms.append(("fp8_b8", dict(cfg8, expert_dtype="fp8")))
+        for key, c8 in arms:
+            # the sliding window is a plan-time property of the layers: a handle of its own
+            mk.close()
+            torch.cuda.empty_cache()
+            mk = Bd.Megakernel(c8, W, max_batch=8)
+            st8 = plan_workload(mk, c8, wl8, seq8, args.seed, device)
 
-        def step8():
-            mk.step(st8["tokens"], st8["k"], st8["v"], st8["logits"])
-        step8()
-        t8, per8 = time_device(step8, max(10, args.steps // 2), args.warmup, ws, stream)
-        if mk.status()["code"] != 0:
-            raise RuntimeError("device error in bs8 arm")
-        k8 = max(10, args.steps // 2)
-        t8 = max_over_ranks(t8, ws, device)
-        us8 = union_sizes(mk, cfg8["n_layers"])
-        sb8 = sol.step_bytes(cfg8, seq8, us8)
-        v8 = ws * 8 * k8 / t8
-        ach8 = sb8["total"] / statistics.mean(per8) / 1e9
-        line["bs8"] = {"workload": wl8, "value": v8, "unit": UNIT, "ms_per_step": t8 / k8 * 1e3,
-                       "bytes_per_step": sb8["total"], "achieved_gbs": ach8, "frac": ach8 / hbm,
-                       "sol_tok_s": sol.sol_tok_s(sb8["total"], hbm * 1e9, 8),
-                       "union_experts_mean": statistics.mean(us8), "seq_lens": seq8}
-        st = st8
+            def step8():
+                mk.step(st8["tokens"], st8["k"], st8["v"], st8["logits"])
+            step8()
+            k8 = max(10, args.steps // 2)
+            t8, per8 = time_device(step8, k8, args.warmup, ws, stream)
+            if mk.status()["code"] != 0:
+                raise RuntimeError(f"device error in the {key} arm")
+            t8 = max_over_ranks(t8, ws, device)
+            us8 = union_sizes(mk, c8["n_layers"])
+            sb8 = sol.step_bytes(c8, seq8, us8)
+            ach8 = sb8["total"] / statistics.mean(per8) / 1e9
+            line[key] = {"workload": wl8 + ("" if key == "bs8" else " (FP8 experts)"), "value": ws * 8 * k8 / t8,
+                         "unit": UNIT, "ms_per_step": t8 / k8 * 1e3, "bytes_per_step": sb8["total"],
+                         "achieved_gbs": ach8, "frac": ach8 / hbm,
+                         "sol_tok_s": sol.sol_tok_s(sb8["total"], hbm * 1e9, 8),
+                         "union_experts_mean": statistics.mean(us8), "seq_lens": seq8}
+            del st8
 
-    # ---- CPU oracle baseline (rank 0, N = 1)
-    if not args.no_cpu and rank == 0 and ws == 1:
-        smp = OracleSampler(args.workload, args.seed)
-        step_s = smp.step_seconds(budget_s=12.0, max_layers=480)
-        line["cpu_baseline"] = {"value": smp.B / step_s, "unit": UNIT, "cores": cpu_cores(),
-                                "kind": "oracle", "sample": smp.describe()}
     mk.close()
     del W
     if rank == 0:

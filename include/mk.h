@@ -67,9 +67,13 @@ typedef enum mk_status {
  * fp16 for the MMA and applies the scales to its fp32 results.  It needs d_ff a
  * multiple of 64 (of 32 when max_batch < 4, where the expert items are 32 rows of d_ff
  * instead of 64) (MK_ERR_UNSUPPORTED).  The dense FFNs of a mixed stack stay bf16.
+ * MK_WEIGHTS_FP8 (2) stores the QKV, O-proj and LM-head matrices the same way as well
+ * (E4M3, one float32 scale per output row, over the whole row); the router, the norms
+ * and the embedding stay bf16 (the router's logits decide the top-k; its bytes are
+ * under 1% of a step's).
  * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
  * FP8 quantization is on the roadmap; the pages fix no format] */
-enum { MK_EXPERT_BF16 = 0, MK_EXPERT_FP8 = 1 };
+enum { MK_EXPERT_BF16 = 0, MK_EXPERT_FP8 = 1, MK_WEIGHTS_FP8 = 2 };
 typedef struct mk_config {
   int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim;
   int32_t n_experts, top_k, d_ff, vocab, page_size, max_batch;
@@ -317,6 +321,19 @@ int mk_read(mk_handle* h, int what, void* host_out, size_t bytes);
  * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
  * FP8 quantization is on the roadmap] */
 int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size_t bytes);
+
+/* The stored FP8 form of a projection (expert_dtype MK_WEIGHTS_FP8), unpacked to
+ * row-major arrays in HOST memory: codes u8 [rows][cols], then the float32 scale of
+ * every row [rows] (a weight decodes as value(code) * its row's scale).  `matrix`:
+ *   MK_W_Q [Hq*hd][d_model], MK_W_K / MK_W_V [Hkv*hd][d_model], MK_W_O [d_model][Hq*hd]
+ *   of layer `layer`, MK_W_LM [vocab][d_model] (layer ignored).
+ * `bytes` must equal rows * cols + 4 * rows.  Synchronises the device; needs no plan.
+ * MK_ERR_STATE if the projections are stored in bf16; MK_ERR_INVALID for a NULL
+ * pointer, an unknown matrix, a layer out of range or a wrong size.
+ * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, Current limitations:
+ * FP8 quantization is on the roadmap] */
+enum { MK_W_Q = 0, MK_W_K = 1, MK_W_V = 2, MK_W_O = 3, MK_W_LM = 4 };
+int mk_read_weight_fp8(mk_handle* h, int matrix, int layer, void* host_out, size_t bytes);
 
 /* Integer facts about a handle/plan.  `what`: */
 enum {

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MK_OK", 1: "MK_ERR_INVALID", 2: "MK_ERR_UNSUPPORTED", 3: "MK
 MK_READ_HIDDEN, MK_READ_ROUTES, MK_READ_ROUTE_W, MK_READ_ACTIVE = 1, 2, 3, 4
 MK_READ_SEQ_LENS, MK_READ_COUNTERS, MK_READ_ROUTER_LOGITS, MK_READ_TRACE_COUNT = 5, 6, 7, 8
 MK_READ_FINAL_COUNTERS, MK_READ_FINAL_QUEUES, MK_READ_TASKS = 9, 10, 11
-MK_EXPERT_BF16, MK_EXPERT_FP8 = 0, 1
+MK_EXPERT_BF16, MK_EXPERT_FP8, MK_WEIGHTS_FP8 = 0, 1, 2
 (MK_Q_NUM_SMS, MK_Q_NUM_TASKS, MK_Q_NUM_COUNTERS, MK_Q_PACKED_BYTES, MK_Q_MAX_ACTIVE,
  MK_Q_SPLIT_PAGES, MK_Q_SMEM_BYTES, MK_Q_PEROP_LAUNCHES, MK_Q_THREADS, MK_Q_STAGE_BYTES,
  MK_Q_NUM_STAGES) = range(1, 12)
@@ -32,7 +32,7 @@ MK_EXPERT_BF16, MK_EXPERT_FP8 = 0, 1
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_decode_step_noalloc",
            "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_inspect", "mk_set_trace",
-           "mk_plan_drop_signal", "mk_read", "mk_read_expert_fp8", "mk_query",
+           "mk_plan_drop_signal", "mk_read", "mk_read_expert_fp8", "mk_read_weight_fp8", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
 
 
@@ -98,6 +98,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_plan_drop_signal.argtypes = [H, i32]
     lib.mk_read.argtypes = [H, i32, vp, sz]
     lib.mk_read_expert_fp8.argtypes = [H, i32, i32, vp, sz]
+    lib.mk_read_weight_fp8.argtypes = [H, i32, i32, vp, sz]
     lib.mk_query.argtypes = [H, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.mk_plan_dry.argtypes = [ctypes.POINTER(mk_config), i32, i32, vp, i32, vp, vp, i32, vp]
     lib.mk_last_error.argtypes = [H]
@@ -131,7 +132,8 @@ def make_config(cfg: dict, max_batch: int = 8, timeout_ms: int = 2000) -> mk_con
                      cfg.get("page_size", 16), max_batch, cfg.get("sliding_window", 0), mask,
                      cfg["rope_theta"], cfg["rms_eps"], timeout_ms, dense,
                      cfg.get("dense_ff", 0) if dense else 0,
-                     MK_EXPERT_FP8 if cfg.get("expert_dtype", "bf16") == "fp8" else MK_EXPERT_BF16)
+                     MK_WEIGHTS_FP8 if cfg.get("dense_dtype", "bf16") == "fp8"
+                     else MK_EXPERT_FP8 if cfg.get("expert_dtype", "bf16") == "fp8" else MK_EXPERT_BF16)
 
 
 def _ptrs(t, n):
@@ -273,6 +275,17 @@ def mk_read_expert_fp8(h, layer: int, expert: int, d_model: int, d_ff: int) -> d
     return out
 
 
+MK_W_Q, MK_W_K, MK_W_V, MK_W_O, MK_W_LM = 0, 1, 2, 3, 4
+
+
+def mk_read_weight_fp8(h, matrix: int, layer: int, rows: int, cols: int):
+    """The stored FP8 form of a projection: (codes uint8 [rows, cols], scales float32 [rows])."""
+    n = rows * cols + 4 * rows
+    buf = np.empty(n, dtype=np.uint8)
+    _check(load_library().mk_read_weight_fp8(h, int(matrix), int(layer), buf.ctypes.data, n), h)
+    return buf[:rows * cols].reshape(rows, cols), buf[rows * cols:].view(np.float32)
+
+
 def mk_query(h, what: int) -> int:
     v = ctypes.c_int64()
     _check(load_library().mk_query(h, what, ctypes.byref(v)), h)
@@ -370,6 +383,13 @@ class Megakernel:
     def expert_fp8(self, layer: int, expert: int) -> dict:
         c = self.cfg
         return mk_read_expert_fp8(self.h, layer, expert, c["d_model"], c["d_ff"])
+
+    def weight_fp8(self, matrix: int, layer: int = 0):
+        c = self.cfg
+        d, hq, hkv, hd = c["d_model"], c["n_q_heads"], c["n_kv_heads"], c["head_dim"]
+        rows, cols = {MK_W_Q: (hq * hd, d), MK_W_K: (hkv * hd, d), MK_W_V: (hkv * hd, d),
+                      MK_W_O: (d, hq * hd), MK_W_LM: (c["vocab"], d)}[matrix]
+        return mk_read_weight_fp8(self.h, matrix, layer, rows, cols)
 
     def routes(self):
         c = self.cfg

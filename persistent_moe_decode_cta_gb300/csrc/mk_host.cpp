@@ -35,6 +35,12 @@ cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, cons
                             cudaStream_t st);
 cudaError_t launch_pack_moe_fp8(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
                                 int fs, long long item_bytes, cudaStream_t st);
+cudaError_t launch_pack_rowscale(float* dst, const void* src_a, const void* src_b, const void* src_c,
+                                 int n_rows_packed, int n_src_rows, int k_full, long long ld, int mode, int hd,
+                                 int gs, int grp, cudaStream_t st);
+cudaError_t launch_pack_fp8(uint8_t* dst, const float* scales, const void* src_a, const void* src_b,
+                            const void* src_c, int n_rows_packed, int n_src_rows, int K, long long ld, int col0,
+                            int mode, int hd, int gs, int grp, int tile_rows, cudaStream_t st);
 cudaError_t prepare_megakernel();
 int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
@@ -58,10 +64,13 @@ struct Shape {
   uint64_t dense_mask;  // mixed stacks: dense layers
   int f_dense, t_dense, dense_fs;  // dense FFN items: bf16, f-slices of dense_fs rows
   bool fp8;             // routed experts as E4M3 codes + f32 scales
+  bool fp8d;            // QKV, O-proj and LM head as E4M3 codes + per-row f32 scales
+  int esz;              // bytes of a QKV / O-proj / LM-head weight (2 bf16, 1 E4M3)
   int r_lm, v_pad, n_lm_tasks;
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
   size_t dense_item_bytes;
   size_t off_qkv, off_o, off_router, off_moe, off_dense, off_lm, off_embed, total;
+  size_t off_qkv_scale, off_o_scale, off_lm_scale;  // FP8 projections' row scales (f32)
   bool dense(int l) const { return (dense_mask >> l) & 1ull; }
 };
 
@@ -122,9 +131,11 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   // FP8 experts: f-slices of 64 rows for handles of max_batch >= 4 (fewer, longer items:
   // +16% over 32-row items at batch 8 ragged), of 32 rows below (at batch 1 the 64-row
   // items occupy only 96 SMs: -4% against 32-row ones)
-  if (c->expert_dtype != MK_EXPERT_BF16 && c->expert_dtype != MK_EXPERT_FP8)
+  if (c->expert_dtype != MK_EXPERT_BF16 && c->expert_dtype != MK_EXPERT_FP8 && c->expert_dtype != MK_WEIGHTS_FP8)
     return fail(err, MK_ERR_INVALID, "expert_dtype %d unknown", c->expert_dtype);
-  s.fp8 = c->expert_dtype == MK_EXPERT_FP8;
+  s.fp8d = c->expert_dtype == MK_WEIGHTS_FP8;
+  s.fp8 = c->expert_dtype == MK_EXPERT_FP8 || s.fp8d;
+  s.esz = s.fp8d ? 1 : 2;
   if (s.fp8) {
     s.moe_fs = s.max_batch >= 4 ? 64 : 32;
     if (const char* e = getenv("MK_FP8_FS")) { const int v = atoi(e); if (v == 32 || v == 64) s.moe_fs = v; }
@@ -143,14 +154,14 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.r_lm = 64;
   if (const char* e = getenv("MK_LM_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_lm = v; }
   s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
-  s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * 2;
-  s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * 2;
+  s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * s.esz;
+  s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * s.esz;
   s.router_layer_bytes = (size_t)s.e_pad * s.d * 2;
   s.moe_item_bytes = s.fp8 ? (size_t)fp8_scale_bytes(s.moe_fs, s.d) + (size_t)3 * s.moe_fs * s.d
                            : (size_t)3 * s.moe_fs * s.d * 2;
   s.moe_bytes_e = s.moe_item_bytes * s.t_moe;
   s.dense_item_bytes = (size_t)3 * s.dense_fs * s.d * 2;
-  s.lm_bytes = (size_t)s.v_pad * s.d * 2;
+  s.lm_bytes = (size_t)s.v_pad * s.d * s.esz;
   s.embed_bytes = (size_t)s.V * s.d * 2;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 255) / 256 * 256; return r; };
@@ -161,6 +172,9 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.off_dense = take((size_t)__builtin_popcountll(s.dense_mask) * s.t_dense * s.dense_item_bytes);
   s.off_lm = take(s.lm_bytes);
   s.off_embed = take(s.embed_bytes);
+  s.off_qkv_scale = take(s.fp8d ? (size_t)s.L * s.Hkv * s.qkv_rows_group * 4 : 0);
+  s.off_o_scale = take(s.fp8d ? (size_t)s.L * s.d * 4 : 0);
+  s.off_lm_scale = take(s.fp8d ? (size_t)s.v_pad * 4 : 0);
   s.total = o;
   return MK_OK;
 }
@@ -202,7 +216,7 @@ bool parse_wave_order(const char* s, std::vector<int>& order) {
 }
 
 int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, PlanOut& P, std::string* err,
-               int prefetch = 0) {
+               int prefetch = 0, int router_sms = 0) {
   if (B < 1 || B > s.max_batch) return fail(err, MK_ERR_INVALID, "batch %d not in [1, %d]", B, s.max_batch);
   if (n_sm < 1) return fail(err, MK_ERR_INVALID, "n_sms %d", n_sm);
   P = PlanOut();
@@ -261,9 +275,9 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
       for (int t = 0; t < s.qkv_tpg; ++t)
         wq.push_back(wait2(add(OP_QKV, l, g, t * s.r_qkv, s.r_qkv, 0, s.d, w1, t1, P.c_qkvg + l * s.Hkv + g,
                                s.qkv_tpg,
-                               s.off_qkv + l * s.qkv_layer_bytes + (size_t)g * s.qkv_rows_group * s.d * 2 +
-                                   (size_t)t * s.r_qkv * s.d * 2,
-                               s.r_qkv * s.d * 2, W_QKV)));
+                               s.off_qkv + l * s.qkv_layer_bytes + (size_t)g * s.qkv_rows_group * s.d * s.esz +
+                                   (size_t)t * s.r_qkv * s.d * s.esz,
+                               s.r_qkv * s.d * s.esz, W_QKV)));
     auto& wr = waves[(size_t)l * W_COUNT + W_ROUTER];
     // the last tile (dealt last on its SM) collects all tiles' logits and routes (a
     // dense layer has no router)
@@ -286,8 +300,9 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
       for (int t = 0; t < s.t_o; ++t)
         wo.push_back(add(OP_OPROJ, l, g, t * s.r_o, s.r_o, g * s.k_o, s.k_o, P.c_og + l * s.Hkv + g, B,
                          P.c_od + l, P.od_target,
-                         s.off_o + l * s.o_layer_bytes + (size_t)g * s.d * s.k_o * 2 + (size_t)t * s.r_o * s.k_o * 2,
-                         s.r_o * s.k_o * 2, W_OPROJ));
+                         s.off_o + l * s.o_layer_bytes + (size_t)g * s.d * s.k_o * s.esz +
+                             (size_t)t * s.r_o * s.k_o * s.esz,
+                         s.r_o * s.k_o * s.esz, W_OPROJ));
   }
   for (int l = 0; l < L; ++l) {
     auto& wx = waves[(size_t)l * W_COUNT + W_RESID];
@@ -302,7 +317,7 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   std::vector<int> lm;
   for (int t = 0; t < s.n_lm_tasks; ++t)
     lm.push_back(add(OP_LMHEAD, L, 0, t * s.r_lm, s.r_lm, 0, s.d, P.c_lr + L, s.nrb_d, -1, 0,
-                     s.off_lm + (size_t)t * s.r_lm * s.d * 2, s.r_lm * s.d * 2, -1));
+                     s.off_lm + (size_t)t * s.r_lm * s.d * s.esz, s.r_lm * s.d * s.esz, -1));
 
   // ---- segments
   auto emit_segment = [&](const std::vector<std::vector<int>>& lists) {
@@ -322,6 +337,10 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
     lists[0].push_back(t_embed);
     long long cursor = 0;
     std::vector<char> has_router(n_sm);
+    // router_sms > 0: every layer's router tiles on the last router_sms SMs, which take
+    // no other work until the LM head; the other waves and the drains on the rest
+    const int nrs = (router_sms > 0 && router_sms < n_sm && s.n_router_tasks > 0) ? router_sms : 0;
+    const int nw = n_sm - nrs;
     auto pos = [&](int w) { return (int)(std::find(order.begin(), order.end(), w) - order.begin()); };
     // With O-proj after the MoE drain, the O-proj tiles are not dealt: the MoE drain
     // claims them from a queue, ahead of expert items once the layer's attention is
@@ -345,9 +364,15 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
       for (int w : order) {
         if (oq && w == W_OPROJ) continue;
         if (oq && w == W_MOE) {
-          for (int sm = 0; sm < n_sm; ++sm) lists[sm].push_back(moe_oq[l]);
+          for (int sm = 0; sm < nw; ++sm) lists[sm].push_back(moe_oq[l]);
         } else if (is_drain(w)) {
-          for (int sm = 0; sm < n_sm; ++sm) lists[sm].push_back(drains[(size_t)l * W_COUNT + w]);
+          for (int sm = 0; sm < nw; ++sm) lists[sm].push_back(drains[(size_t)l * W_COUNT + w]);
+        } else if (nrs > 0) {
+          int k = 0;
+          for (int t : waves[(size_t)l * W_COUNT + w]) {
+            if (w == W_ROUTER) lists[nw + (k++ % nrs)].push_back(t);
+            else lists[cursor++ % nw].push_back(t);
+          }
         } else if (w == W_QKV && pos(W_ROUTER) < pos(W_QKV) && n_sm > s.n_router_tasks) {
           // the router tiles head the MoE's critical path and the QKV tiles the
           // attention's: keep the QKV tiles off the SMs that run this layer's router
@@ -449,6 +474,12 @@ constexpr int kDefaultPrefetch = 0;
 int prefetch_mask() {
   const char* e = getenv("MK_PREFETCH");
   return e ? atoi(e) : kDefaultPrefetch;
+}
+
+// SMs reserved for the router tiles (MK_ROUTER_SMS; 0 = none): see build_plan.
+int router_sms() {
+  const char* e = getenv("MK_ROUTER_SMS");
+  return e ? atoi(e) : 0;
 }
 
 // Router first: its weights are then prefetched behind the previous layer's tasks
@@ -670,15 +701,44 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
     cudaError_t _e = launch_pack(__VA_ARGS__, st);                       \
     if (_e != cudaSuccess) { cuda_fail(h, _e, "pack"); return bail(MK_ERR_CUDA); } \
   } while (0)
+  // FP8 projections: each packed row's scale (over the whole source row), then the codes
+#define PK8(dst, scales, a, b, c, rows, srows, K, ld, col0, mode, grp, tile)                                    \
+  do {                                                                                                    \
+    cudaError_t _e = launch_pack_fp8(dst, scales, a, b, c, rows, srows, K, ld, col0, mode, hd, gs, grp, tile, st); \
+    if (_e != cudaSuccess) { cuda_fail(h, _e, "pack fp8"); return bail(MK_ERR_CUDA); }                    \
+  } while (0)
+#define PKS(scales, a, b, c, rows, srows, kfull, ld, mode, grp)                                               \
+  do {                                                                                                    \
+    cudaError_t _e = launch_pack_rowscale(scales, a, b, c, rows, srows, kfull, ld, mode, hd, gs, grp, st);      \
+    if (_e != cudaSuccess) { cuda_fail(h, _e, "pack fp8 scales"); return bail(MK_ERR_CUDA); }             \
+  } while (0)
+  float* qkv_sc = reinterpret_cast<float*>(h->wblob + s.off_qkv_scale);
+  float* o_sc = reinterpret_cast<float*>(h->wblob + s.off_o_scale);
+  float* lm_sc = reinterpret_cast<float*>(h->wblob + s.off_lm_scale);
   for (int l = 0; l < L; ++l) {
     uint8_t* q = h->wblob + s.off_qkv + l * s.qkv_layer_bytes;
-    for (int g = 0; g < s.Hkv; ++g)
-      PK(q + (size_t)g * s.qkv_rows_group * d * 2, w->wq[l], w->wk[l], w->wv[l], s.qkv_rows_group, 0, d, d, 0,
-         PACK_QKV, hd, gs, g, s.r_qkv);
+    for (int g = 0; g < s.Hkv; ++g) {
+      if (s.fp8d) {
+        float* sc = qkv_sc + ((size_t)l * s.Hkv + g) * s.qkv_rows_group;
+        PKS(sc, w->wq[l], w->wk[l], w->wv[l], s.qkv_rows_group, 0, d, d, PACK_QKV, g);
+        PK8(q + (size_t)g * s.qkv_rows_group * d, sc, w->wq[l], w->wk[l], w->wv[l], s.qkv_rows_group, 0, d, d, 0,
+            PACK_QKV, g, s.r_qkv);
+      } else {
+        PK(q + (size_t)g * s.qkv_rows_group * d * 2, w->wq[l], w->wk[l], w->wv[l], s.qkv_rows_group, 0, d, d, 0,
+           PACK_QKV, hd, gs, g, s.r_qkv);
+      }
+    }
     uint8_t* o = h->wblob + s.off_o + l * s.o_layer_bytes;
-    for (int g = 0; g < s.Hkv; ++g)
-      PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o,
-         PACK_IDENT, hd, gs, 0, s.r_o);
+    if (s.fp8d)  // one scale per row of Wo, over all its Hq * hd columns (every KV group's slice)
+      PKS(o_sc + (size_t)l * d, w->wo[l], nullptr, nullptr, d, d, s.Hq * hd, (long long)s.Hq * hd, PACK_IDENT, 0);
+    for (int g = 0; g < s.Hkv; ++g) {
+      if (s.fp8d)
+        PK8(o + (size_t)g * d * s.k_o, o_sc + (size_t)l * d, w->wo[l], nullptr, nullptr, d, d, s.k_o,
+            (long long)s.Hq * hd, g * s.k_o, PACK_IDENT, 0, s.r_o);
+      else
+        PK(o + (size_t)g * d * s.k_o * 2, w->wo[l], nullptr, nullptr, d, d, s.k_o, (long long)s.Hq * hd, g * s.k_o,
+           PACK_IDENT, hd, gs, 0, s.r_o);
+    }
     if (s.dense(l)) {  // mixed stack: the layer's FFN in the dense region, no router or experts
       const int rank = __builtin_popcountll(s.dense_mask & ((1ull << l) - 1ull));  // dense layers before l
       e = launch_pack_moe(h->wblob + s.off_dense + (size_t)rank * s.t_dense * s.dense_item_bytes, w->ffn_gate[l],
@@ -701,8 +761,15 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
     e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
     if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
   }
-  PK(h->wblob + s.off_lm, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, hd, gs, 0, s.r_lm);
+  if (s.fp8d) {
+    PKS(lm_sc, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, PACK_IDENT, 0);
+    PK8(h->wblob + s.off_lm, lm_sc, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, 0, s.r_lm);
+  } else {
+    PK(h->wblob + s.off_lm, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, hd, gs, 0, s.r_lm);
+  }
 #undef PK
+#undef PK8
+#undef PKS
   e = launch_convert(h->norms + (size_t)L * d, w->final_norm, d, st);
   if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
   e = cudaMemcpyAsync(h->wblob + s.off_embed, w->embed, s.embed_bytes, cudaMemcpyDeviceToDevice, st);
@@ -723,7 +790,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
   if (!parse_wave_order(env && *env ? env : default_order(), order))
     return fail(nullptr, MK_ERR_INVALID, "bad wave order '%s'", env ? env : "");
   PlanOut P;
-  r = build_plan(s, batch, n_sms, order, P, nullptr, prefetch_mask());
+  r = build_plan(s, batch, n_sms, order, P, nullptr, prefetch_mask(), router_sms());
   if (r) return r;
   const int list_len = P.sm_off[n_sms];  // segment 0 only
   if (info_out) {
@@ -735,7 +802,7 @@ int mk_plan_dry(const mk_config* cfg, int batch, int n_sms, int32_t* tasks_out, 
     I[22] = P.c_md; I[23] = P.c_od; I[24] = s.nrb_d; I[25] = s.gs; I[26] = P.c_oa;
     I[27] = s.t_dense; I[28] = (int32_t)(uint32_t)(s.dense_mask & 0xffffffffull);
     I[29] = (int32_t)(uint32_t)(s.dense_mask >> 32);
-    I[30] = s.fp8 ? MK_EXPERT_FP8 : MK_EXPERT_BF16; I[31] = (int32_t)s.moe_item_bytes;
+    I[30] = s.fp8d ? MK_WEIGHTS_FP8 : s.fp8 ? MK_EXPERT_FP8 : MK_EXPERT_BF16; I[31] = (int32_t)s.moe_item_bytes;
   }
   if (!tasks_out || !sm_off_out || !sm_list_out || cap_tasks < P.n_tasks() || cap_list < list_len)
     return fail(nullptr, MK_ERR_INVALID, "output capacity too small (tasks %d, list %d)", P.n_tasks(), list_len);
@@ -764,7 +831,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   const char* env = getenv("MK_WAVE_ORDER");
   if (!parse_wave_order(env && *env ? env : default_order(), order))
     return fail(&h->err, MK_ERR_INVALID, "bad wave order '%s'", env ? env : "");
-  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err, prefetch_mask());
+  int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err, prefetch_mask(), router_sms());
   if (r) return r;
   int occ = 0;
   megakernel_occupancy(&occ);
@@ -798,10 +865,26 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   // it is latency-bound and a deeper window measured 2.6% slower)
   p.inflight_moe = B >= 4 ? std::min(3, kStages - 1) : p.inflight;
   if (const char* fl = getenv("MK_INFLIGHT_MOE")) { int v = atoi(fl); if (v >= 1 && v < kStages) p.inflight_moe = v; }
+  p.tail_items = 0;
+  p.inflight_tail = 4;
+  if (const char* e = getenv("MK_TAIL_ITEMS")) { int v = atoi(e); if (v >= 0) p.tail_items = v; }
+  if (const char* e = getenv("MK_INFLIGHT_TAIL")) { int v = atoi(e); if (v >= 1 && v < kStages) p.inflight_tail = v; }
+  p.route_warp = 0;
+  if (const char* e = getenv("MK_ROUTE_WARP")) p.route_warp = atoi(e) ? 1 : 0;
+  p.route_pf_bytes = 0;
+  if (const char* e = getenv("MK_ROUTE_PF")) {
+    int v = atoi(e);
+    if (v >= 0 && v % 16 == 0 && v <= (int)s.moe_item_bytes) p.route_pf_bytes = v;
+  }
   p.wblob = h->wblob; p.off_moe = (long long)s.off_moe; p.moe_item_bytes = (long long)s.moe_item_bytes;
   p.dense_mask = s.dense_mask; p.t_dense = s.t_dense; p.off_dense = (long long)s.off_dense;
   p.dense_fs = s.dense_fs; p.dense_item_bytes = (long long)s.dense_item_bytes;
   p.fp8 = s.fp8 ? 1 : 0;
+  p.fp8d = s.fp8d ? 1 : 0;
+  p.qkv_rows_group = s.qkv_rows_group;
+  p.qkv_scale = reinterpret_cast<const float*>(h->wblob + s.off_qkv_scale);
+  p.o_scale = reinterpret_cast<const float*>(h->wblob + s.off_o_scale);
+  p.lm_scale = reinterpret_cast<const float*>(h->wblob + s.off_lm_scale);
   p.attn_norm = h->norms; p.final_norm = h->norms + (size_t)L * s.d;
   p.rope_turns = h->rope_turns;
   p.embed = reinterpret_cast<const uint16_t*>(h->wblob + s.off_embed);
@@ -1205,6 +1288,93 @@ int mk_read_expert_fp8(mk_handle* h, int layer, int expert, void* host_out, size
             dc[(size_t)row * f + col] = dn[((size_t)fi * 32 + lane) * 8 + 2 * q + e];
           }
     }
+  }
+  return MK_OK;
+}
+
+// Source row of packed row r (host twin of the packer's mapping): matrix 0/1/2 and row.
+static void host_pack_source_row(int mode, int r, int n_src_rows, int hd, int gs, int grp, int& which,
+                                 long long& srow) {
+  which = 0;
+  srow = r;
+  if (mode == PACK_QKV) {
+    const int head = r / hd, jj = r % hd, m = jj / 16, i = jj % 16;
+    const int dim = (i < 8) ? 8 * m + i : hd / 2 + 8 * m + (i - 8);
+    if (head < gs) { which = 0; srow = (long long)(grp * gs + head) * hd + dim; }
+    else { which = head == gs ? 1 : 2; srow = (long long)grp * hd + dim; }
+  } else if (srow >= n_src_rows) {
+    srow = -1;
+  }
+}
+
+// The E4M3 codes of packed row r of a region of FP8 GEMV tiles (tile_rows rows each, K
+// columns, fragment order of the packer, 8 bytes a lane).
+static void unpack_fp8_row(const uint8_t* region, int r, int K, int tile_rows, uint8_t* out) {
+  const int nrb_t = tile_rows / 16, t = r / tile_rows, rb = (r % tile_rows) / 16, i = r % 16;
+  const size_t per_tile = (size_t)nrb_t * (K / 16);
+  for (int ks = 0; ks < K / 16; ++ks) {
+    const int j = ks / 8, w = ks % 8;
+    const uint8_t* frag = region + (t * per_tile + (size_t)(j * nrb_t + rb) * 8 + w) * kFragBytes8;
+    for (int c = 0; c < 4; ++c)
+      for (int half = 0; half < 2; ++half)
+        for (int e = 0; e < 2; ++e) {
+          const int q = (i >= 8 ? 1 : 0) + 2 * half;
+          out[16 * ks + 2 * c + 8 * half + e] = frag[((i & 7) * 4 + c) * 8 + 2 * q + e];
+        }
+  }
+}
+
+int mk_read_weight_fp8(mk_handle* h, int matrix, int layer, void* host_out, size_t bytes) {
+  if (!h || !host_out) return fail(h ? &h->err : nullptr, MK_ERR_INVALID, "NULL argument");
+  const Shape& s = h->s;
+  if (!s.fp8d) return fail(&h->err, MK_ERR_STATE, "the projections are stored in bf16");
+  if (matrix < MK_W_Q || matrix > MK_W_LM) return fail(&h->err, MK_ERR_INVALID, "matrix %d unknown", matrix);
+  if (matrix != MK_W_LM && (layer < 0 || layer >= s.L))
+    return fail(&h->err, MK_ERR_INVALID, "layer %d out of range", layer);
+  const int d = s.d, hd = s.hd, gs = s.gs;
+  const int rows = matrix == MK_W_Q ? s.Hq * hd : matrix == MK_W_K || matrix == MK_W_V ? s.Hkv * hd
+                 : matrix == MK_W_O ? d : s.V;
+  const int cols = matrix == MK_W_O ? s.Hq * hd : d;
+  const size_t need = (size_t)rows * cols + 4 * (size_t)rows;
+  if (bytes != need) return fail(&h->err, MK_ERR_INVALID, "mk_read_weight_fp8: need %zu bytes, got %zu", need, bytes);
+  uint8_t* codes = static_cast<uint8_t*>(host_out);
+  float* scales = reinterpret_cast<float*>(codes + (size_t)rows * cols);
+  CK(h, cudaSetDevice(h->dev));
+  CK(h, cudaDeviceSynchronize());
+  std::vector<uint8_t> row((size_t)std::max(d, s.Hq * hd));
+  if (matrix <= MK_W_V) {  // QKV: per KV group, packed rows [q heads | k | v], RoPE-paired
+    std::vector<uint8_t> reg((size_t)s.qkv_rows_group * d);
+    std::vector<float> sc(s.qkv_rows_group);
+    for (int g = 0; g < s.Hkv; ++g) {
+      CK(h, cudaMemcpy(reg.data(), h->wblob + s.off_qkv + layer * s.qkv_layer_bytes + (size_t)g * reg.size(),
+                       reg.size(), cudaMemcpyDeviceToHost));
+      CK(h, cudaMemcpy(sc.data(), h->wblob + s.off_qkv_scale + (((size_t)layer * s.Hkv + g) * s.qkv_rows_group) * 4,
+                       sc.size() * 4, cudaMemcpyDeviceToHost));
+      for (int r = 0; r < s.qkv_rows_group; ++r) {
+        int which;
+        long long srow;
+        host_pack_source_row(PACK_QKV, r, 0, hd, gs, g, which, srow);
+        if (which != matrix) continue;
+        unpack_fp8_row(reg.data(), r, d, s.r_qkv, codes + (size_t)srow * cols);
+        scales[srow] = sc[r];
+      }
+    }
+  } else if (matrix == MK_W_O) {  // per KV group: the group's k_o columns of every row
+    std::vector<uint8_t> reg((size_t)d * s.k_o);
+    for (int g = 0; g < s.Hkv; ++g) {
+      CK(h, cudaMemcpy(reg.data(), h->wblob + s.off_o + layer * s.o_layer_bytes + (size_t)g * reg.size(),
+                       reg.size(), cudaMemcpyDeviceToHost));
+      for (int r = 0; r < d; ++r) {
+        unpack_fp8_row(reg.data(), r, s.k_o, s.r_o, row.data());
+        std::memcpy(codes + (size_t)r * cols + (size_t)g * s.k_o, row.data(), s.k_o);
+      }
+    }
+    CK(h, cudaMemcpy(scales, h->wblob + s.off_o_scale + (size_t)layer * d * 4, (size_t)d * 4, cudaMemcpyDeviceToHost));
+  } else {
+    std::vector<uint8_t> reg((size_t)s.v_pad * d);
+    CK(h, cudaMemcpy(reg.data(), h->wblob + s.off_lm, reg.size(), cudaMemcpyDeviceToHost));
+    for (int r = 0; r < s.V; ++r) unpack_fp8_row(reg.data(), r, d, s.r_lm, codes + (size_t)r * cols);
+    CK(h, cudaMemcpy(scales, h->wblob + s.off_lm_scale, (size_t)s.V * 4, cudaMemcpyDeviceToHost));
   }
   return MK_OK;
 }

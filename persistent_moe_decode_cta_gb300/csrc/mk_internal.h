@@ -123,8 +123,24 @@ struct Params {
   int fixed, do_reset;
   int inflight;             // max issued-but-not-landed ring chunks per CTA (1..kStages-1)
   int inflight_moe;         // the same for the chunks of expert items
+  // the tail of a layer's expert phase: the last tail_items expert items of the queue
+  // and the O-proj tiles claimed by the MoE drains keep inflight_tail chunks in flight
+  // (fewer SMs stream then; each needs more bytes in flight); tail_items 0 = off
+  int tail_items, inflight_tail;
+  // at the route step (batch 1), L2 prefetch of the first route_pf_bytes of every item
+  // of the selected experts (0 = off)
+  int route_pf_bytes;
+  // batch 1: the route step on one warp (route_step_b1) instead of the block-wide one
+  int route_warp;
   int fp8;                  // expert weights as E4M3 codes with f32 scales (items: see fp8_scale_bytes)
   int dense_fs;             // f-slice rows of a dense layer's FFN items (bf16; = moe_fs without FP8)
+  // FP8 projections: the QKV, O-proj and LM-head tiles hold E4M3 codes (8 bytes a lane
+  // per fragment) and their rows' float32 scales sit in these arrays (packed-row order)
+  int fp8d;
+  int qkv_rows_group;       // packed QKV rows of a KV group
+  const float* qkv_scale;   // [L][Hkv][qkv_rows_group]
+  const float* o_scale;     // [L][d]
+  const float* lm_scale;    // [v_pad]
   long long dense_item_bytes;
   // mixed dense/MoE stacks: bit l set = layer l is dense, its FFN is t_dense items (one
   // per moe_fs rows of dense_ff) at off_dense + (r * t_dense + t) * moe_item_bytes, r =

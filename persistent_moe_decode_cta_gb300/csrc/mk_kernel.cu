@@ -296,14 +296,14 @@ __device__ __forceinline__ int checked_page(const Params& p, int b, int logical,
 // ============================================================== producer
 __device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int task, int item, int nch,
                           int4 extra = make_int4(0, 0, 0, 0), int4 w_lo = make_int4(0, 0, 0, 0),
-                          int4 w_hi = make_int4(0, 0, 0, 0)) {
+                          int4 w_hi = make_int4(0, 0, 0, 0), uint64_t stamp = 0) {
   const uint32_t slot = mseq % kMbox, use = mseq / kMbox;
   if (use > 0 && !mbar_wait(S.mempty(slot), (use - 1) & 1u, 8 * p.timeout_ns)) {
     raise_err(p, MK_ERR_TIMEOUT, task, -3, (int)mseq, 0);
     return false;
   }
   S.mbox[4 * slot] = make_int4(task, item, nch, extra.x);
-  S.mbox[4 * slot + 1] = make_int4(extra.y, extra.z, 0, 0);
+  S.mbox[4 * slot + 1] = make_int4(extra.y, extra.z, (int)(unsigned)stamp, (int)(unsigned)(stamp >> 32));
   S.mbox[4 * slot + 2] = w_lo;
   S.mbox[4 * slot + 3] = w_hi;
   mbar_arrive(S.mfull(slot));
@@ -447,14 +447,15 @@ __device__ bool issue_kv(const Params& p, const Smem& S, uint32_t& cseq, const C
 
 // A GEMV tile task: mailbox entry, then its weight chunks.
 __device__ __forceinline__ bool push_gemv(const Params& p, const Smem& S, uint32_t& mseq, uint32_t& cseq, int ti,
-                                          uint64_t pol) {
+                                          uint64_t pol, int inflight) {
   const int* T = p.tasks + ti * kDescInts;
   const long long off = (long long)(((unsigned long long)(unsigned)T[D_WOFF_HI] << 32) | (unsigned)T[D_WOFF_LO]);
   const int bytes = T[D_WBYTES];
   const int nrb = T[D_NROWS] / 16;
-  const int cs = gemv_jpc(nrb) * nrb * 8 * kFragBytes;
+  const bool f8 = p.fp8d && T[D_OP] != OP_ROUTER;  // (FP8 projections: QKV, O-proj, LM head)
+  const int cs = f8 ? gemv_jpc8(nrb) * nrb * 8 * kFragBytes8 : gemv_jpc(nrb) * nrb * 8 * kFragBytes;
   const int nch = (bytes + cs - 1) / cs;
-  return mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs, p.inflight);
+  return mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs, inflight);
 }
 
 __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK, const CUtensorMap* tmV) {
@@ -486,7 +487,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
       case OP_ROUTER:
       case OP_OPROJ:
       case OP_LMHEAD:
-        ok = push_gemv(p, S, mseq, cseq, ti, pol);
+        ok = push_gemv(p, S, mseq, cseq, ti, pol, p.inflight);
         break;
       case OP_ATT_DRAIN: {
         const int count = att_item_count(p, S, l);
@@ -616,7 +617,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         auto claim_oproj = [&]() {
           const int o = atomicAdd(p.qhead + qo, 1);
           if (o >= n_o) { o_left = false; return false; }
-          ok = push_gemv(p, S, mseq, cseq, o_base + o, pol);
+          ok = push_gemv(p, S, mseq, cseq, o_base + o, pol, p.tail_items > 0 ? p.inflight_tail : p.inflight);
           return true;
         };
         for (bool first = true; ok; first = false) {
@@ -642,9 +643,9 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
               dense ? p.wblob + p.off_dense +
                           ((long long)__popcll(p.dense_mask & ((1ull << l) - 1ull)) * p.t_dense + t) * ib
                     : p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
-          const int fl = p.inflight_moe;
+          const int fl = (p.tail_items > 0 && item >= count - p.tail_items) ? p.inflight_tail : p.inflight_moe;
           ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
-                         make_int4(tl_w[4], tl_w[5], tl_w[6], tl_w[7])) &&
+                         make_int4(tl_w[4], tl_w[5], tl_w[6], tl_w[7]), p.trace ? gtime() : 0ull) &&
                (sb == 0 || issue_linear(p, S, cseq, src, sb, pol, ti, sb, fl)) &&
                issue_linear(p, S, cseq, src + sb, gu_bytes, pol, ti, cs1, fl) &&
                issue_linear(p, S, cseq, src + sb + gu_bytes, dn_bytes, pol, ti, cs2, fl);
@@ -811,7 +812,7 @@ __device__ __forceinline__ void fp8_mma(float (&acc)[4], uint2 a, uint32_t b0, u
 // widened exactly to f16 (x 2^-8) and multiplied with the f16 operand `fr` (f32
 // accumulation); twice the j-groups per ring chunk.  The row scales are applied by
 // the caller.
-template <int NRB>
+template <int NRB, bool CVT = false>
 __device__ __forceinline__ bool gemv_run8(const Params& p, const Smem& S, uint32_t& cseq, int nch, int ksw,
                                           const BFrag& fr, float (&v)[4]) {
   constexpr int JPC = gemv_jpc8(NRB);
@@ -830,10 +831,13 @@ __device__ __forceinline__ bool gemv_run8(const Params& p, const Smem& S, uint32
           if (c == 0) trace_mark(p, S, 2);
         }
         const uint32_t base = S.stage(cseq + c) + ((j % JPC) * NRB * 8 + warp) * kFragBytes8 + lane * 8;
+        // CVT: the operand is bf16 (shared with the bf16 tiles), widened to f16 here
+        const uint32_t b0 = CVT ? bf16x2_to_f16x2(fr.b0[j]) : fr.b0[j];
+        const uint32_t b1 = CVT ? bf16x2_to_f16x2(fr.b1[j]) : fr.b1[j];
 #pragma unroll
         for (int rb = 0; rb < NRB; ++rb) {
           const uint2 a = lds64(base + rb * 8 * kFragBytes8);
-          fp8_mma(acc[rb], a, fr.b0[j], fr.b1[j]);
+          fp8_mma(acc[rb], a, b0, b1);
         }
       }
     }
@@ -957,6 +961,7 @@ __device__ float build_operand_parts(const Params& p, const Smem& S, BFrag& fr, 
         if (lane == 0 && n < t1) ssw[warp * 8 + n] = s2;
       }
     }
+    if (t0 == 0) trace_mark(p, S, 15);
     bar_sync_consumers();
     if (tid >= t0 && tid < t1) {
       float s2 = 0.f;
@@ -986,6 +991,111 @@ __device__ float build_operand_parts(const Params& p, const Smem& S, BFrag& fr, 
 }
 
 // ============================================================== epilogues / fan-in steps
+
+// Route step of a batch of one token, on one warp (warp 0; the other consumer warps
+// do not take part): the 128-or-fewer tagged logits are polled four to a lane until they
+// all carry this step's epoch, the top_k are taken in K rounds of a warp-wide argmax (the
+// larger logit wins, then the lower expert id; a NaN ranks below every number and reports
+// MK_ERR_NAN), the softmax over them runs in registers, and each selected expert is placed
+// in its slot (the number of selected ids below it) and published in the route words.
+// Returns nothing: a timeout raises the error word (every wait then drains).
+__device__ void route_step_b1(const Params& p, const Smem& S, int l, int ti) {
+  const int lane = threadIdx.x & 31;
+  const int E = p.E, K = p.topk;
+  constexpr int kPer = 8;  // logits a lane holds (E <= 256)
+  const unsigned ep = step_epoch(S);
+  const uint64_t* src = p.rlog + (size_t)l * E;
+  float v[kPer];
+  const uint64_t t0 = gtime();
+  for (int it = 0;; ++it) {
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      uint64_t w = tagged(ep, 0xff800000u);  // -inf for lanes past E
+      ld_relaxed_u64_pred(w, src + e, e < E);
+      if ((unsigned)(w >> 32) != ep) ok = false;
+      v[j] = __uint_as_float((unsigned)w);
+    }
+    if (__all_sync(0xffffffffu, ok)) break;
+    __nanosleep(32);
+    if ((it & 15) == 15 && (aborted(p) || (long long)(gtime() - t0) > p.timeout_ns)) {
+      if (lane == 0 && !aborted(p)) raise_err(p, MK_ERR_TIMEOUT, ti, -11, l, 0);
+      return;
+    }
+  }
+  if (p.trace && lane == 0) trace_slots(S)[6] = gtime();
+#pragma unroll
+  for (int j = 0; j < kPer; ++j)
+    if (v[j] != v[j]) {
+      raise_err(p, MK_ERR_NAN, ti, -1, l, lane + 32 * j);
+      v[j] = -INFINITY;
+    }
+  // K rounds: this lane's best (value, lowest id), then the warp's; the winner's lane
+  // takes it out of its list
+  float sv = -INFINITY;   // lane j < K: the j-th selected logit
+  int se = 0x7fffffff;    //             and its expert id
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && (v[j] > bv || (v[j] == bv && e < be))) { bv = v[j]; be = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if (lane == k) { sv = bv; se = be; }
+    // the winner is taken: NaN never compares larger or equal, so it is not chosen again
+    // (not even among ties at -inf)
+#pragma unroll
+    for (int j = 0; j < kPer; ++j)
+      if (lane + 32 * j == be) v[j] = __int_as_float(0x7fc00000u);
+  }
+  if (p.trace && lane == 0) trace_slots(S)[13] = gtime();
+  // softmax over the selected logits (lane 0 holds the largest)
+  const float mx = __shfl_sync(0xffffffffu, sv, 0);
+  const float w = (lane < K) ? __expf(sv - mx) : 0.f;
+  float sum = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const float wk = w / sum;
+  trace_mark(p, S, 8);
+  const int maxa = p.maxa;
+  int slot = 0;
+  for (int j = 0; j < K; ++j) slot += __shfl_sync(0xffffffffu, se, j) < se ? 1 : 0;
+  uint64_t* rw = p.rword + (size_t)l * p.rw_stride;
+  if (lane < K) {
+    rw[1 + 2 * maxa + slot] = tagged(ep, (unsigned)lane);  // token 0, selection rank
+    rw[1 + 2 * maxa + maxa + slot] = tagged(ep, __float_as_uint(wk));
+    rw[1 + slot] = tagged(ep, (unsigned)se);
+    rw[1 + maxa + slot] = tagged(ep, 1u);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    rw[0] = tagged(ep, (unsigned)K);
+    if (p.trace) trace_slots(S)[10] = gtime();
+  }
+  // the routing in plain arrays (host-side readers), and the MoE-done padding
+  if (lane < K) {
+    p.ridx[(size_t)l * K + lane] = se;
+    p.rw[(size_t)l * K + lane] = wk;
+    p.active[l * maxa + slot] = se;
+    p.act_cnt[l * maxa + slot] = 1;
+    p.act_tok[(size_t)l * maxa + slot] = lane;
+  }
+  if (lane == 0) {
+    p.nact[l] = K;
+    p.qcount[p.L + l] = K * p.t_moe;
+    const unsigned pad = (unsigned)((maxa - K) * p.t_moe);
+    if (pad > 0) atomicAdd(ctr_ptr(p, C_MD(p, l)), pad);
+    if (p.trace) trace_slots(S)[11] = gtime();
+  }
+}
 
 // Route step: top-k of the router logits per token (ties to the lower expert id),
 // softmax over the selected logits, the active-expert list in ascending expert id,
@@ -1030,6 +1140,7 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     }
   }
   if (p.trace && tid == 0) trace_slots(S)[6] = gtime();
+  const long long c_rank0 = clock64();
   float* wsel = reinterpret_cast<float*>(tok_s + kMaxActive * kMaxBatch);  // [B][topk] weights
   int* prk = reinterpret_cast<int*>(wsel + kMaxActive);                    // [2][B*E] partial ranks
   int* tot_s = prk + 256;                                                 // n_active
@@ -1060,6 +1171,8 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
       prk[t] = rank;
     }
   }
+  trace_mark(p, S, 13);
+  if (p.trace && tid == 0) trace_slots(S)[9] = (unsigned long long)(clock64() - c_rank0);
   if (H == 2) {
     bar_sync_consumers();
     for (int i = tid; i < BE; i += kConsumerThreads) {
@@ -1068,6 +1181,7 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     }
   }
   bar_sync_consumers();
+  trace_mark(p, S, 14);
   if (warp < B) {  // softmax over the selected logits of token `warp`
     const int b = warp;
     const float* r = lg + b * E;
@@ -1080,6 +1194,16 @@ __device__ bool route_step(const Params& p, const Smem& S, int l, int ti) {
     if (lane < K) wsel[b * K + lane] = w / sum;
   }
   trace_mark(p, S, 8);
+  if (B == 1 && p.route_pf_bytes > 0 && warp >= 1) {
+    // warps 1..7: the first route_pf_bytes of every item of the selected experts into
+    // L2, while warp 0 publishes the route (the claimers' copies then start from L2)
+    const int n = K * p.t_moe;
+    for (int i = tid - 32; i < n; i += kConsumerThreads - 32) {
+      const int e = sel[i / p.t_moe], t = i % p.t_moe;
+      prefetch_l2(p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes,
+                  (uint32_t)p.route_pf_bytes);
+    }
+  }
   if (B == 1) {
     // one token: the active experts are its selection (maxa = top_k); warp 0 places
     // each in its slot (the number of selected ids below it) and writes everything
@@ -1281,6 +1405,18 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
   // their L2 round trips overlap the wait and the GEMV instead of following them.
   unsigned long long fturn = 0ull;
   int kv_pg[2] = {-1, -1};
+  // FP8 projections: this lane's two epilogue rows' scales (x 256: the integer-pipe
+  // decode yields the codes' values x 2^-8), loaded before the wait as well
+  const bool f8 = p.fp8d && op != OP_ROUTER;
+  float rsc0 = 1.f, rsc1 = 1.f;
+  if (f8 && warp < nrows / 16) {
+    const int r0 = T[D_ROW0] + warp * 16 + g8;
+    const float* sp = op == OP_QKV ? p.qkv_scale + ((size_t)l * p.Hkv + T[D_AUX]) * p.qkv_rows_group
+                    : op == OP_OPROJ ? p.o_scale + (size_t)l * p.d
+                                     : p.lm_scale;
+    rsc0 = __ldg(sp + r0) * 256.f;
+    rsc1 = __ldg(sp + r0 + 8) * 256.f;
+  }
   if (op == OP_QKV && warp < nrows / 16) {
     const int pr = T[D_ROW0] + warp * 16 + g8;
     const int seg = pr / p.hd, j = pr % p.hd;
@@ -1335,11 +1471,22 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
       }
     }
     have = key;
-    switch (nrb) {
-      case 1: ran = gemv_run<1>(p, S, cseq, nch, ksw, fr, v); break;
-      case 2: ran = gemv_run<2>(p, S, cseq, nch, ksw, fr, v); break;
-      case 4: ran = gemv_run<4>(p, S, cseq, nch, ksw, fr, v); break;
-      default: ran = gemv_run<8>(p, S, cseq, nch, ksw, fr, v); break;
+    if (f8) {
+      switch (nrb) {
+        case 1: ran = gemv_run8<1, true>(p, S, cseq, nch, ksw, fr, v); break;
+        case 2: ran = gemv_run8<2, true>(p, S, cseq, nch, ksw, fr, v); break;
+        case 4: ran = gemv_run8<4, true>(p, S, cseq, nch, ksw, fr, v); break;
+        default: ran = gemv_run8<8, true>(p, S, cseq, nch, ksw, fr, v); break;
+      }
+      v[0] *= rsc0; v[1] *= rsc0;   // row 16w + g8, tokens 2c, 2c + 1
+      v[2] *= rsc1; v[3] *= rsc1;   // row 16w + g8 + 8
+    } else {
+      switch (nrb) {
+        case 1: ran = gemv_run<1>(p, S, cseq, nch, ksw, fr, v); break;
+        case 2: ran = gemv_run<2>(p, S, cseq, nch, ksw, fr, v); break;
+        case 4: ran = gemv_run<4>(p, S, cseq, nch, ksw, fr, v); break;
+        default: ran = gemv_run<8>(p, S, cseq, nch, ksw, fr, v); break;
+      }
     }
   }
   if (!ran) return false;
@@ -1468,7 +1615,11 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
       // counters are counted for the bookkeeping only (no task waits on them: the
       // tagged logits and route words carry the readiness themselves).
       if (T[D_AUX] == 1) {
-        if (!route_step(p, S, l, ti)) return false;
+        if (p.B == 1 && p.route_warp) {
+          if (warp == 0) route_step_b1(p, S, l, ti);
+        } else if (!route_step(p, S, l, ti)) {
+          return false;
+        }
         signal_async(p, S, sseq, C_RR(p, l), 1u);
       }
       signal_async(p, S, sseq, T[D_SIG_CTR], 1u);
@@ -2015,8 +2166,10 @@ __device__ void consumer(const Params& p, const Smem& S) {
     const int nch = ent.z;
     if (p.trace && threadIdx.x == 0) {
       unsigned long long* t = trace_slots(S);
-      t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = t[8] = t[9] = t[10] = t[11] = 0ull;
+      t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = t[8] = t[9] = t[10] = 0ull;
       t[12] = t[13] = t[14] = t[15] = 0ull;
+      // (expert items: when the producer pushed the entry, route words in hand)
+      t[11] = ((unsigned long long)(unsigned)ent2.w << 32) | (unsigned)ent2.z;
     }
     if (abort_now) skip = true;
     if (skip) {
@@ -2185,6 +2338,88 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================== weight packer
+// Source of packed row r (see mk_pack_kernel): the matrix (0 = a, 1 = b, 2 = c) and its
+// row, or row -1 for a zero padding row.
+__device__ __forceinline__ void pack_source_row(int mode, int r, int n_src_rows, int hd, int gs, int grp,
+                                                int& which, long long& srow) {
+  which = 0;
+  srow = r;
+  if (mode == PACK_QKV) {
+    const int head = r / hd, jj = r % hd, m = jj / 16, i = jj % 16;
+    const int dim = (i < 8) ? 8 * m + i : hd / 2 + 8 * m + (i - 8);
+    if (head < gs) { which = 0; srow = (long long)(grp * gs + head) * hd + dim; }
+    else { which = head == gs ? 1 : 2; srow = (long long)grp * hd + dim; }
+  } else if (mode == PACK_GATE_UP) {
+    const int blk = r / 16, i = r % 16;
+    which = i < 8 ? 0 : 1;
+    srow = 8LL * blk + (i & 7);
+    if (srow >= n_src_rows) srow = -1;
+  } else if (srow >= n_src_rows) {
+    srow = -1;
+  }
+}
+
+// FP8 projections, setup (1): the float32 scale of every packed row -- max|w| over the
+// source row's first k_full columns / 448, 1 for an all-zero or padding row.
+__global__ void mk_pack_rowscale_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src_a,
+                                        const uint16_t* __restrict__ src_b, const uint16_t* __restrict__ src_c,
+                                        int n_rows_packed, int n_src_rows, int k_full, long long ld, int mode,
+                                        int hd, int gs, int grp) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= n_rows_packed) return;
+  int which;
+  long long srow;
+  pack_source_row(mode, r, n_src_rows, hd, gs, grp, which, srow);
+  float amax = 0.f;
+  if (srow >= 0) {
+    const uint16_t* src = (which == 0 ? src_a : which == 1 ? src_b : src_c) + srow * ld;
+    for (int k = 0; k < k_full; ++k) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)src[k] << 16)));
+  }
+  dst[r] = amax > 0.f ? amax / 448.f : 1.f;
+}
+
+// FP8 projections, setup (2): the E4M3 codes of the packed tiles, in the bf16 fragment
+// order of mk_pack_kernel with 8 bytes a lane: each element divided by its packed row's
+// scale and rounded to the nearest code (ties to even, saturating at 448).
+__global__ void mk_pack_fp8_kernel(uint8_t* __restrict__ dst, const float* __restrict__ scales,
+                                   const uint16_t* __restrict__ src_a, const uint16_t* __restrict__ src_b,
+                                   const uint16_t* __restrict__ src_c, int n_rows_packed, int n_src_rows, int K,
+                                   long long ld, int col0, int mode, int hd, int gs, int grp, int tile_rows) {
+  const long long total = (long long)(n_rows_packed / 16) * (K / 16) * 32;
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= total) return;
+  const int lane = (int)(u & 31);
+  const long long fr = u >> 5;
+  const int nrb_t = tile_rows / 16;
+  const int ks_n = K / 16;
+  const long long per_tile = (long long)nrb_t * ks_n;
+  const int t = (int)(fr / per_tile);
+  const int fi = (int)(fr % per_tile);
+  const int j = fi / (nrb_t * 8), rem = fi % (nrb_t * 8);
+  const int rb = t * nrb_t + rem / 8;
+  const int ks = rem % 8 + 8 * j;
+  const int g8 = lane >> 2, c = lane & 3;
+  uint8_t out[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = rb * 16 + g8 + ((q & 1) ? 8 : 0);
+    const int k = 16 * ks + 2 * c + ((q & 2) ? 8 : 0);
+    int which;
+    long long srow;
+    pack_source_row(mode, r, n_src_rows, hd, gs, grp, which, srow);
+    const uint16_t* src = which == 0 ? src_a : which == 1 ? src_b : src_c;
+    const float sc = scales[r];
+    for (int e = 0; e < 2; ++e) {
+      const float x = srow >= 0 ? __uint_as_float((uint32_t)src[srow * ld + col0 + k + e] << 16) : 0.f;
+      out[2 * q + e] = (uint8_t)__nv_cvt_float_to_fp8(x / sc, __NV_SATFINITE, __NV_E4M3);
+    }
+  }
+  reinterpret_cast<uint2*>(dst)[u] =
+      make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 8) | ((uint32_t)out[2] << 16) | ((uint32_t)out[3] << 24),
+                 (uint32_t)out[4] | ((uint32_t)out[5] << 8) | ((uint32_t)out[6] << 16) | ((uint32_t)out[7] << 24));
+}
+
+
 // Packs a row-major bf16 matrix into 16x16 MMA A-fragments (16 bytes per lane):
 //   lane -> (g, 2c..2c+1) (g+8, 2c..2c+1) (g, 2c+8..2c+9) (g+8, 2c+8..2c+9), g = lane/4, c = lane%4.
 // Packed rows are cut into tiles of `tile_rows`; inside a tile of NRB row blocks,
@@ -2431,6 +2666,27 @@ cudaError_t launch_pack(uint8_t* dst, const void* src_a, const void* src_b, cons
   mk_pack_kernel<<<(unsigned)blocks, threads, 0, st>>>(dst, (const uint16_t*)src_a, (const uint16_t*)src_b,
                                                      (const uint16_t*)src_c, n_rows_packed, n_src_rows, K, ld,
                                                      col0, mode, hd, gs, grp, tile_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_rowscale(float* dst, const void* src_a, const void* src_b, const void* src_c,
+                                 int n_rows_packed, int n_src_rows, int k_full, long long ld, int mode, int hd,
+                                 int gs, int grp, cudaStream_t st) {
+  if (n_rows_packed == 0) return cudaSuccess;
+  mk_pack_rowscale_kernel<<<(unsigned)((n_rows_packed + 127) / 128), 128, 0, st>>>(
+      dst, (const uint16_t*)src_a, (const uint16_t*)src_b, (const uint16_t*)src_c, n_rows_packed, n_src_rows, k_full,
+      ld, mode, hd, gs, grp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_fp8(uint8_t* dst, const float* scales, const void* src_a, const void* src_b,
+                            const void* src_c, int n_rows_packed, int n_src_rows, int K, long long ld, int col0,
+                            int mode, int hd, int gs, int grp, int tile_rows, cudaStream_t st) {
+  const long long total = (long long)(n_rows_packed / 16) * (K / 16) * 32;
+  if (total == 0) return cudaSuccess;
+  mk_pack_fp8_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
+      dst, scales, (const uint16_t*)src_a, (const uint16_t*)src_b, (const uint16_t*)src_c, n_rows_packed, n_src_rows,
+      K, ld, col0, mode, hd, gs, grp, tile_rows);
   return cudaGetLastError();
 }
 

@@ -123,6 +123,36 @@ def test_bad_token_reports_error():
     mk.close()
 
 
+@pytest.mark.parametrize("batch", [1, 3])
+def test_exact_router_ties_go_to_the_lower_expert_id(batch):
+    """Three experts with identical router rows, scaled to be every token's largest
+    logits, give bit-equal logits: top-2 must take the two lowest ids of the three, in
+    that order, with equal weights (the oracle's tie rule)."""
+    lens = [40, 7, 100][:batch]
+    cfg, W, seq, pt, npages, k, v, tokens = PU.setup("tiny_b1_64", seq_lens=lens, gain_jitter=0.0)
+    W["attn_norm"][:] = 1.0
+    for l in range(cfg["n_layers"]):
+        W["router"][l] *= 0.1
+        row = W["router"][l, 0].clone() * 0.0 + 0.05      # every logit of these rows: 0.05 * sum(h)
+        for e in (6, 1, 4):
+            W["router"][l, e] = row
+    # sum(h) > 0 for every token makes the tied logits the largest
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
+    logits = torch.empty(len(seq), cfg["vocab"], device="cuda")
+    mk.step(tokens, k, v, logits)
+    assert mk.status()["code"] == 0
+    lg = mk.router_logits()
+    idx, w = mk.routes()
+    for l in range(cfg["n_layers"]):
+        for b in range(len(seq)):
+            if lg[l, b, 1] > np.sort(lg[l, b])[-4]:     # the tied three lead this token
+                assert lg[l, b, 1] == lg[l, b, 4] == lg[l, b, 6]
+                assert [int(e) for e in idx[l, b]] == [1, 4], (l, b, idx[l, b])
+                assert w[l, b, 0] == w[l, b, 1]
+    mk.close()
+
+
 def test_nan_router_logit_reports_error_and_routes_to_valid_experts():
     """A router row of NaNs (non-finite weights: invalid input the route step checks)
     makes that expert's logit NaN: the step completes with a full, valid top-k that

@@ -10,7 +10,11 @@ with float32 scales, decoded in the kernel.
   its CUDA graph, at batch 1 to 8; and at the pages-scale sizes, on sampled layers in
   the launch configuration the benchmark times.
 * Several steps in one launch equal the same steps with the greedy token fed back on
-  the host."""
+  the host.
+* With the projections in FP8 as well (expert_dtype MK_WEIGHTS_FP8: QKV, O-proj and
+  LM head as E4M3 codes with one float32 scale per output row, read back through
+  mk_read_weight_fp8), the same: stored form bit-equal to the oracle's quantisation,
+  steps against the oracle on the decoded weights."""
 import numpy as np
 import pytest
 import torch
@@ -62,6 +66,15 @@ def test_stored_codes_and_scales_equal_the_oracle_quantisation(workload, pairs, 
     ("small_fp8_b1_2k", [2048, 300], "graph", 8),
     ("small_fp8_b1_2k", [2048, 300], "mega", 2),
     ("small_fp8_b1_2k", [2048, 5, 900, 17, 64, 1, 333, 2000], "mega", 8),
+    # FP8 experts and projections
+    ("tiny_fp8w_b1_64", [64], "mega", 8),
+    ("tiny_fp8w_b1_64", [61, 0, 17], "mega", 8),
+    ("tiny_fp8w_b1_64", [61, 0, 17], "perop", 8),
+    ("tiny_fp8w_b1_64", [64], "graph", 1),
+    ("small_fp8w_b1_2k", [2048], "mega", 1),
+    ("small_fp8w_b1_2k", [2048, 300], "graph", 8),
+    ("small_fp8w_b1_2k", [2048, 5, 900, 17, 64, 1, 333, 2000], "mega", 8),
+    ("tiny_dense_fp8w_b1_64", [61, 0, 17], "mega", 8),
     # FP8 experts beside bf16 dense layers (a mixed stack)
     ("tiny_dense_fp8_b1_64", [61, 0, 17], "mega", 8),
     ("tiny_dense_fp8_b1_64", [61, 17], "perop", 2),
@@ -85,9 +98,10 @@ def test_fp8_step_matches_oracle(workload, seq_lens, mode, max_batch):
         mk.close()
 
 
-def test_fp8_multi_step_equals_single_steps():
+@pytest.mark.parametrize("workload", ["tiny_fp8_b1_64", "tiny_fp8w_b1_64"])
+def test_fp8_multi_step_equals_single_steps(workload):
     n = 4
-    cfg, W, seq, pt, npages, k, v, tokens = PU.setup("tiny_fp8_b1_64", seq_lens=[62, 9, 30], steps=n)
+    cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload, seq_lens=[62, 9, 30], steps=n)
     pt_dev = torch.as_tensor(pt, device="cuda")
     mk = B.Megakernel(cfg, W, max_batch=8)
     try:
@@ -113,9 +127,51 @@ def test_fp8_multi_step_equals_single_steps():
         mk.close()
 
 
+def _check_stored_projections(mk, HW, cfg, layers, lm=True):
+    pairs = [(B.MK_W_Q, HW.wq), (B.MK_W_K, HW.wk), (B.MK_W_V, HW.wv), (B.MK_W_O, HW.wo)]
+    for l in layers:
+        for m, get in pairs:
+            codes, scales = mk.weight_fp8(m, l)
+            want_c, want_s = oracle.quantize_e4m3_rows(get(l))
+            assert np.array_equal(codes, want_c), (m, l)
+            assert np.array_equal(scales.view(np.uint32), want_s.view(np.uint32)), (m, l)
+    if lm:
+        codes, scales = mk.weight_fp8(B.MK_W_LM)
+        want_c, want_s = oracle.quantize_e4m3_rows(HW.lm_head())
+        assert np.array_equal(codes, want_c) and np.array_equal(scales.view(np.uint32), want_s.view(np.uint32))
+
+
+@pytest.mark.parametrize("workload,layers,lm", [
+    ("tiny_fp8w_b1_64", (0, 1), True),
+    ("small_fp8w_b1_2k", (0, 7), True),
+])
+def test_stored_projection_codes_and_scales_equal_the_oracle_quantisation(workload, layers, lm):
+    cfg, W, *_ = PU.setup(workload)
+    mk = B.Megakernel(cfg, W, max_batch=8)
+    try:
+        HW = synth.HostWeights(W)
+        _check_stored_projections(mk, HW, cfg, layers, lm)
+        _check_stored(mk, HW, layers[-1], 3)          # the experts as with FP8 experts alone
+        with pytest.raises(B.MkError) as e:             # out of range
+            mk.weight_fp8(B.MK_W_Q, cfg["n_layers"])
+        assert e.value.code == B.MK_ERR_INVALID
+    finally:
+        mk.close()
+    cfg, W, *_ = PU.setup("tiny_fp8_b1_64")            # FP8 experts only: bf16 projections
+    mk = B.Megakernel(cfg, W)
+    try:
+        with pytest.raises(B.MkError) as e:
+            mk.weight_fp8(B.MK_W_Q, 0)
+        assert e.value.code == B.MK_ERR_STATE
+    finally:
+        mk.close()
+
+
 @pytest.mark.parametrize("workload,layers", [
     ("pages_fp8_b1_8k", (0, 24, 47)),
     ("pages_fp8_b8_ragged_swa", (0, 1, 47)),   # 1 and 47 are sliding-window layers
+    ("pages_fp8w_b1_8k", (0, 24, 47)),
+    ("pages_fp8w_b8_ragged_swa", (0, 1, 47)),
 ])
 def test_fp8_pages_scale_sampled_layers_and_stored_form(workload, layers):
     cfg = synth.model_config(workload)
@@ -129,6 +185,8 @@ def test_fp8_pages_scale_sampled_layers_and_stored_form(workload, layers):
         HW, HK = synth.HostWeights(W), synth.HostKV(k, v)
         for l, e in ((0, 0), (24, 63), (47, 127)):
             _check_stored(mk, HW, l, e)
+        if cfg.get("dense_dtype") == "fp8":
+            _check_stored_projections(mk, HW, cfg, (0, 47), lm=False)
         mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
         logits = torch.empty(len(seq), cfg["vocab"], device="cuda")
         mk.step(tokens, k, v, logits)
