@@ -172,37 +172,6 @@ def _dense(cfg, w_u16):
     return fp8_matrix(w_u16) if cfg.get("dense_dtype") == "fp8" else bf16_to_f64(w_u16)
 
 
-# FP8 activations (cfg["act_dtype"] == "fp8", with FP8 experts and projections): the
-# input of every GEMV whose weights are FP8 is quantised to E4M3 too, in blocks, each
-# with its own float32 scale (max|x| over the block / 448, 1 for an all-zero block) --
-# the weights-and-activations FP8 reading: per token over the normed layer input (QKV and
-# the experts' gate/up) and the final normed input (LM head), per token and KV group for
-# the O-proj input, per token and ACT_BLOCK consecutive SwiGLU outputs for the experts'
-# down projection.  The router keeps the unquantised input.
-ACT_BLOCK = 32
-
-
-def quantize_e4m3_act(x, block=None):
-    """E4M3 quantisation of an activation vector x [n] in blocks of `block` (None = the
-    whole vector): the values as float32, scale = max|x| over the block / 448 (float32),
-    codes = nearest E4M3 of x / scale (ties to even, saturating).  Returns the decoded
-    values (codes times scales) in float64."""
-    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
-    n = x32.shape[0]
-    b = n if block is None else block
-    if n % b:
-        raise ValueError(f"{n} values are not whole {b}-value blocks")
-    xb = x32.reshape(n // b, b)
-    amax = np.max(np.abs(xb), axis=1)
-    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    codes = f32_to_e4m3((xb / scale[:, None]).astype(np.float32))
-    return (e4m3_to_f64(codes) * scale[:, None].astype(np.float64)).reshape(n)
-
-
-def _act(cfg, x, block=None):
-    return quantize_e4m3_act(x, block) if cfg.get("act_dtype") == "fp8" else x
-
-
 def rms_norm(x, gain, eps):
     """x / sqrt(mean(x^2) + eps) * gain, over the last axis."""
     x = np.asarray(x, dtype=np.float64)
@@ -336,10 +305,9 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
     attn_out = np.empty((B, d))
     for b in range(B):
         p = int(positions[b])
-        hq = _act(cfg, h[b])                                  # (FP8 activations: per token)
-        q = rope((Wq @ hq).reshape(Hq, hd), p, theta)
-        k_new = rope((Wk @ hq).reshape(Hkv, hd), p, theta)
-        v_new = (Wv @ hq).reshape(Hkv, hd)
+        q = rope((Wq @ h[b]).reshape(Hq, hd), p, theta)
+        k_new = rope((Wk @ h[b]).reshape(Hkv, hd), p, theta)
+        v_new = (Wv @ h[b]).reshape(Hkv, hd)
         k16, v16 = f64_to_bf16(k_new), f64_to_bf16(v_new)    # stored in the bf16 cache
         page, slot = int(page_table[b][p // PAGE]), p % PAGE
         info["kv"].append(dict(b=b, page=page, slot=slot, k=k16, v=v16))
@@ -357,7 +325,7 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
         keys[-1] = bf16_to_f64(k16)
         vals[-1] = bf16_to_f64(v16)
         o = attention(q, keys, vals)
-        attn_out[b] = Wo @ _act(cfg, o.reshape(-1), (Hq // Hkv) * hd)   # (per KV group)
+        attn_out[b] = Wo @ o.reshape(-1)
 
     if dense:
         # a dense layer of a mixed stack: one SwiGLU FFN for every token, no router
@@ -387,12 +355,7 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
     for e in sorted(per_expert):
         wg, wu, wd = fp8_expert(*W.expert(l, e)) if fp8 else (_mat(a) for a in W.expert(l, e))
         for b, j in per_expert[e]:
-            if cfg.get("act_dtype") == "fp8":   # quantised input, and down input per block
-                hq = _act(cfg, h[b])
-                y = wd @ _act(cfg, silu(wg @ hq) * (wu @ hq), ACT_BLOCK)
-            else:
-                y = swiglu_expert(h[b], wg, wu, wd)
-            moe_out[b] += info["w"][b][j] * y
+            moe_out[b] += info["w"][b][j] * swiglu_expert(h[b], wg, wu, wd)
     info["experts"] = {e: per_expert[e] for e in sorted(per_expert)}
     info["idx"] = np.array(info["idx"]); info["w"] = np.array(info["w"])
     info["margin"] = np.array(info["margin"])
@@ -402,8 +365,6 @@ def layer_step(cfg, W, kv, l, x, positions, page_table, forced=None):
 def lm_head(cfg, W, x, rows_per_chunk=16384):
     """logits [B, V] = (RMSNorm(x) * g_final) @ Wlm^T."""
     h = rms_norm(x, bf16_to_f64(W.final_norm()), cfg["rms_eps"])
-    if cfg.get("act_dtype") == "fp8":
-        h = np.stack([_act(cfg, r) for r in h])
     Wlm = W.lm_head()
     V = Wlm.shape[0]
     out = np.empty((x.shape[0], V))
@@ -436,7 +397,6 @@ def decode_step(cfg, W, kv, tokens, seq_lens, page_table, forced=None):
 
 
 __all__ = ["e4m3_to_f64", "f32_to_e4m3", "quantize_e4m3_rows", "dequantize_e4m3", "fp8_expert", "fp8_matrix",
-           "quantize_e4m3_act", "ACT_BLOCK",
            "bf16_to_f64", "f64_to_bf16", "rms_norm", "rope", "softmax", "attention",
            "attention_partial", "merge_partials", "router_topk", "silu", "swiglu_expert",
            "window_start", "argmax_lowest", "layer_step", "lm_head", "embed",

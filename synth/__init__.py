@@ -48,11 +48,6 @@ MODELS["pages_dense3"] = dict(MODELS["pages"], dense_layers=(0, 1, 2), dense_ff=
 # weights drawn are the bf16 ones; quantisation happens when the model is loaded).
 for _m in ("tiny", "small", "pages", "pages_l2", "tiny_dense", "small_dense"):
     MODELS[_m + "_fp8"] = dict(MODELS[_m], expert_dtype="fp8")
-# FP8 weights and activations: a tiny shape whose GEMV depths are multiples of 256 (the
-# depth of one FP8 k32-step for the 8 consumer warps), and the small and pages shapes
-MODELS["tiny8"] = dict(MODELS["tiny"], n_q_heads=8, n_kv_heads=2, head_dim=64)
-for _m in ("tiny8", "small", "pages", "pages_l1", "pages_l2"):
-    MODELS[_m + "_a8"] = dict(MODELS[_m], expert_dtype="fp8", dense_dtype="fp8", act_dtype="fp8")
 # ... and with the dense projections (QKV, O-proj, LM head) in FP8 as well
 for _m in ("tiny", "small", "pages", "pages_l2", "pages_l1", "tiny_dense", "small_dense"):
     MODELS[_m + "_fp8w"] = dict(MODELS[_m], expert_dtype="fp8", dense_dtype="fp8")
@@ -82,13 +77,6 @@ WORKLOADS = {
                                     sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
     "pages_l2_fp8_b8_ragged_swa": dict(model="pages_l2_fp8", batch=8, lens=("uniform", 1024, 32768),
                                        sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
-    # FP8 weights and activations
-    "tiny8_a8_b1_64": dict(model="tiny8_a8", batch=1, lens=("fixed", 64)),
-    "small_a8_b1_2k": dict(model="small_a8", batch=1, lens=("fixed", 2048)),
-    "pages_a8_b1_8k": dict(model="pages_a8", batch=1, lens=("fixed", 8192)),
-    "pages_l1_a8_b1_8k": dict(model="pages_l1_a8", batch=1, lens=("fixed", 8192)),
-    "pages_a8_b8_ragged_swa": dict(model="pages_a8", batch=8, lens=("uniform", 1024, 32768),
-                                   sliding_window=4096, swa="odd", lens_of="pages_b8_ragged_swa"),
     # FP8 experts and dense projections
     "tiny_fp8w_b1_64": dict(model="tiny_fp8w", batch=1, lens=("fixed", 64)),
     "small_fp8w_b1_2k": dict(model="small_fp8w", batch=1, lens=("fixed", 2048)),

@@ -716,97 +716,3 @@ def test_fp8_dense_scales_are_per_output_channel():
         vq = np.abs(O.fp8_matrix(w16)) / scale[:, None]
         assert np.all(np.isin(vq, grid))
         assert np.array_equal(vq.max(axis=1), np.full(wf.shape[0], 448.0))
-
-
-# ----------------------------------------------------------------- FP8 activations
-
-def test_act_quantiser_is_lossless_on_the_grid_and_blockwise():
-    """Values on the E4M3 grid of a block's scale (one of them at +-448 times it)
-    quantise without loss; each block keeps its own scale (a block of tiny values next to
-    one of large values stays within the half-step error bound of its own grid, which a
-    single scale for both would flush to zero); an all-zero block stays zero."""
-    rng = np.random.default_rng(7)
-    codes = rng.integers(0, 256, size=64).astype(np.uint8)
-    codes[(codes & 0x7F) == 0x7F] = 0x22
-    x = O.e4m3_to_f64(codes) * 2.0 ** -5
-    x[0], x[32] = 448.0 * 2.0 ** -5, -448.0 * 2.0 ** -5
-    assert np.array_equal(O.quantize_e4m3_act(x, 32), x)
-    assert np.array_equal(O.quantize_e4m3_act(x), x)
-    small = rng.standard_normal(32) * 1e-6
-    big = rng.standard_normal(32) * 1e3
-    y = O.quantize_e4m3_act(np.concatenate([small, big]), 32)
-    assert np.all(np.abs(y[:32] - small) <= np.abs(small) / 16 + 1e-20)   # 3 mantissa bits
-    assert np.all(O.quantize_e4m3_act(np.concatenate([small, big]))[:32] == 0)
-    assert np.array_equal(O.quantize_e4m3_act(np.zeros(32), 32), np.zeros(32))
-
-
-def _a8(cfg):
-    return dict(cfg, expert_dtype="fp8", dense_dtype="fp8", act_dtype="fp8")
-
-
-def test_fp8_activation_moe_layer_is_the_closed_form_on_constant_inputs():
-    """The closed-form MoE layer of the pairing pin (constant inputs, dyadic weights on
-    the E4M3 grid of their row scales): its activations -- the constant normed input and
-    the SwiGLU outputs, constant per expert -- quantise without loss (up to their float32
-    rounding), so with FP8 weights and activations the layer is still the closed form."""
-    got16, want, info, sel = _pairing_layer()
-    W = synth.make_weights(Q1, seed=0, std=0.2)
-    W["wo"] = torch.zeros_like(W["wo"])
-    W["attn_norm"][0] = 1.0
-    a, g, u = [1.0, 0.5, -0.25, -2.0], [1.5, -0.75, 1.25, 0.5], [0.5, 1.0, -1.5, 0.75]
-    for e in range(4):
-        W["router"][0, e] = a[e] / 32
-        W["w_gate"][0, e] = g[e] / 32
-        W["w_up"][0, e] = u[e] / 32
-        W["w_down"][0, e] = 0.0
-        W["w_down"][0, e, 8 * e:8 * e + 8] = 1.0 / 16
-    x = np.stack([np.full(32, 1.0), np.full(32, -1.0)])
-    pt, npages = synth.make_page_table([3, 9], seed=0)
-    k, v = synth.make_kv(Q1, npages, seed=0)
-    cfg = dict(_a8(Q1), d_ff=32)
-    W2 = dict(W)
-    for name in ("w_gate", "w_up"):
-        W2[name] = torch.cat([W[name], W[name]], dim=2)            # d_ff 32: one 32-block
-    W2["w_down"] = torch.cat([W["w_down"], torch.zeros_like(W["w_down"])], dim=3)
-    y, info8 = O.layer_step(cfg, synth.HostWeights(W2), synth.HostKV(k, v), 0, x, [3, 9], pt)
-    assert info8["idx"].tolist() == sel
-    # (the quantiser reads the activations as float32: 1e-6 covers that rounding; one
-    # E4M3 step would be 1/16 of a value)
-    assert np.abs((y - x) - want).max() < 1e-6
-
-
-def test_fp8_activation_lm_head_on_a_constant_hidden_state_equals_fp8_weights_only():
-    """A constant final hidden state (unit final-norm gain) normalises to a constant
-    vector, which quantises without loss, so the LM head with FP8 activations equals the
-    one with FP8 weights only (up to the float32 rounding of the activations); a random
-    state changes the logits by the activation quantisation alone (small, not zero)."""
-    cfg = dict(TINY, d_ff=64)
-    W, pt, k, v = _setup(cfg)
-    W["wo"] = torch.zeros_like(W["wo"])
-    W["w_down"] = torch.zeros_like(W["w_down"])
-    W["final_norm"][:] = 1.0
-    HW = synth.HostWeights(W)
-    xc = np.full((1, 32), 0.37)
-    w8 = dict(cfg, expert_dtype="fp8", dense_dtype="fp8")
-    # (equal up to the float32 rounding of the activations the quantiser reads)
-    lc8 = O.lm_head(w8, HW, xc)
-    assert np.allclose(O.lm_head(_a8(cfg), HW, xc), lc8, rtol=1e-6, atol=1e-7)
-    xr = _x(2, 32)
-    la, lw = O.lm_head(_a8(cfg), HW, xr), O.lm_head(w8, HW, xr)
-    assert 0 < np.abs(la - lw).max() < 0.1 * np.abs(lw).max()
-
-
-def test_fp8_activation_layer_differs_from_weights_only_by_the_activation_quantisation():
-    """On random weights the FP8-activation layer moves the output by a small relative
-    amount from the FP8-weights-only layer (not zero); the router logits -- computed on
-    the unquantised input -- are identical."""
-    cfg = dict(TINY, d_ff=64)
-    W, pt, k, v = _setup(cfg)
-    HW, kv = synth.HostWeights(W), synth.HostKV(k, v)
-    x = _x(2, 32)
-    w8 = dict(cfg, expert_dtype="fp8", dense_dtype="fp8")
-    yw, iw = O.layer_step(w8, HW, kv, 0, x, [37, 5], pt)
-    ya, ia = O.layer_step(_a8(cfg), HW, kv, 0, x, [37, 5], pt)
-    assert np.array_equal(ia["router_logits"], iw["router_logits"])
-    rel = np.linalg.norm(ya - yw) / np.linalg.norm(yw - x)
-    assert 0 < rel < 0.1, rel
