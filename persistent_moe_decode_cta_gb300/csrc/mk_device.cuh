@@ -82,6 +82,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
   asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// One fp32 atomic add whose old value is not needed (a reduction, no round trip).
+__device__ __forceinline__ void red_add_f32(float* dst, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst), "f"(v) : "memory");
+}
 // Four consecutive fp32 atomic adds in one 128-bit reduction (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y),

@@ -1560,8 +1560,8 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
           const int n = 2 * c + e;
           if (n >= p.B) continue;
           float* out = p.moe + ((size_t)l * p.B + n) * p.d;
-          atomicAdd(out + r0, v[e]);
-          atomicAdd(out + r0 + 8, v[2 + e]);
+          red_add_f32(out + r0, v[e]);
+          red_add_f32(out + r0 + 8, v[2 + e]);
         }
         break;
       }
@@ -2103,33 +2103,78 @@ __device__ bool task_attention(const Params& p, const Smem& S, uint32_t& cseq, u
 }
 
 // ============================================================== embed
+// x0 = Embed[token] for every token.  The rows are read as 16-byte chunks of 8 values,
+// four chunks a thread in flight together (the loads of a serial per-element loop each
+// paid a full HBM round trip); 16 consecutive chunks are one 128-row block of one
+// token, so each block's sum of squares is a reduction over 16 lanes.
 __device__ void task_embed(const Params& p, const Smem& S, uint32_t& sseq, int ti) {
-  const int tid = threadIdx.x;
-  for (int i = tid; i < p.B * p.d; i += kConsumerThreads) {
-    const int b = i / p.d, k = i % p.d;
-    // step 0 reads the caller's tokens, later steps (multi-step decode) the previous
-    // step's greedy tokens
-    const int step = S.small[249];
-    int t = step == 0 ? p.tokens[b] : ld_volatile(p.tok_out + (size_t)(step - 1) * p.B + b);
+  const int tid = threadIdx.x, lane = tid & 31;
+  int* tok = reinterpret_cast<int*>(S.scratch);
+  // step 0 reads the caller's tokens, later steps (multi-step decode) the previous
+  // step's greedy tokens
+  const int step = S.small[249];
+  if (tid < p.B) {
+    int t = step == 0 ? p.tokens[tid] : ld_volatile(p.tok_out + (size_t)(step - 1) * p.B + tid);
     if (t < 0 || t >= p.V) {
-      if (k == 0) raise_err(p, MK_ERR_BAD_TOKEN, ti, -1, t, b);
+      raise_err(p, MK_ERR_BAD_TOKEN, ti, -1, t, tid);
       t = 0;
     }
-    const float x = bf16_to_f(p.embed[(size_t)t * p.d + k]);
-    p.X[(size_t)b * p.d + k] = x;
-    const float xg = x * p.attn_norm[k];
-    const uint16_t hi = to_bf16(xg);
-    p.XG[(size_t)b * p.d + k] = hi;
-    p.XGL[(size_t)b * p.d + k] = to_bf16(xg - bf16_to_f(hi));
+    tok[tid] = t;
   }
   bar_sync_consumers();
-  for (int i = tid; i < p.B * p.nrb_d; i += kConsumerThreads) {
-    const int b = i / p.nrb_d, r = i % p.nrb_d;
-    const float* x = p.X + (size_t)b * p.d + r * kRowBlock;
-    float s = 0.f;
-    for (int k = 0; k < kRowBlock; ++k) s += x[k] * x[k];
-    p.SS[(size_t)r * kSsStride + b] = s;
+  const int cpr = p.d / 8, n = p.B * cpr;  // chunks a row, in all
+  const float4* gain = reinterpret_cast<const float4*>(p.attn_norm);
+  constexpr int kU = 4;
+  for (int c0 = 0; c0 < n; c0 += kU * kConsumerThreads) {
+    uint4 e[kU];
+    float4 g0[kU], g1[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int c = c0 + u * kConsumerThreads + tid;
+      e[u] = make_uint4(0u, 0u, 0u, 0u);
+      g0[u] = g1[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < n) {
+        const int b = c / cpr, k8 = c - b * cpr;
+        e[u] = __ldg(reinterpret_cast<const uint4*>(p.embed + (size_t)tok[b] * p.d) + k8);
+        g0[u] = __ldg(gain + 2 * k8);
+        g1[u] = __ldg(gain + 2 * k8 + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int c = c0 + u * kConsumerThreads + tid;
+      const bool on = c < n;
+      const int b = on ? c / cpr : 0, k8 = on ? c - b * cpr : 0;
+      const uint32_t ew[4] = {e[u].x, e[u].y, e[u].z, e[u].w};
+      const float gw[8] = {g0[u].x, g0[u].y, g0[u].z, g0[u].w, g1[u].x, g1[u].y, g1[u].z, g1[u].w};
+      float x[8];
+      uint32_t hw[4], lw[4];
+      float sq = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        x[j] = bf16_to_f((uint16_t)(ew[j / 2] >> (16 * (j & 1))));
+        sq += x[j] * x[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float y0 = x[2 * j] * gw[2 * j], y1 = x[2 * j + 1] * gw[2 * j + 1];
+        const uint16_t h0 = to_bf16(y0), h1 = to_bf16(y1);
+        hw[j] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lw[j] = (uint32_t)to_bf16(y0 - bf16_to_f(h0)) | ((uint32_t)to_bf16(y1 - bf16_to_f(h1)) << 16);
+      }
+      if (on) {
+        const size_t o = (size_t)b * p.d + 8 * k8;
+        reinterpret_cast<float4*>(p.X + o)[0] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4*>(p.X + o)[1] = make_float4(x[4], x[5], x[6], x[7]);
+        *reinterpret_cast<uint4*>(p.XG + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(p.XGL + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+      if (on && (lane & 15) == 0) p.SS[(size_t)(k8 >> 4) * kSsStride + b] = sq;
+    }
   }
+  bar_sync_consumers();
   signal_async(p, S, sseq, C_LR(p, 0), (unsigned)p.nrb_d);
   bar_sync_consumers();
 }
@@ -2259,6 +2304,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       consumer(p, S);
     }
     __syncthreads();
+    // every CTA clears its slice of the layer accumulators for the next step, once the
+    // last layer's input is complete (every read of them is then done: each layer's
+    // accumulator is read by its ADD_RMSNORM tasks and the next layer's router and QKV
+    // tiles, all before the last layer-ready count completes)
+    // (after an error the last CTA clears them all instead)
+    if (p.do_reset) {
+      if (threadIdx.x == 0)
+        S.small[2] = (!aborted(p) && wait_ge(p, C_LR(p, p.L), (unsigned)p.nrb_d, -1)) ? 1 : 0;
+      __syncthreads();
+      if (S.small[2]) {
+        float4* acc = reinterpret_cast<float4*>(p.moe);
+        const size_t n4 = (size_t)p.L * p.B * p.d / 4;
+        const size_t i0 = n4 * blockIdx.x / gridDim.x, i1 = n4 * (blockIdx.x + 1) / gridDim.x;
+        for (size_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncthreads();
+    }
     // last CTA out resets the counters and queues for the next step or launch
     if (threadIdx.x == 0) {
       __threadfence();
@@ -2293,10 +2355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = threadIdx.x; i < p.n_ctr; i += blockDim.x)
           if (i != p.c_done) *ctr_ptr(p, i) = 0u;
         for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
-        // the layer accumulators start the next step at zero (nothing reads them now)
-        float4* acc = reinterpret_cast<float4*>(p.moe);
-        const size_t n4 = (size_t)p.L * p.B * p.d / 4;
-        for (size_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (aborted(p)) {
+          float4* acc = reinterpret_cast<float4*>(p.moe);
+          const size_t n4 = (size_t)p.L * p.B * p.d / 4;
+          for (size_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         if (!p.fixed)
           for (int b = threadIdx.x; b < p.B; b += blockDim.x) p.seq_lens[b] += 1;
         // the next step's epoch (never 0: freshly cleared words must not look current)
