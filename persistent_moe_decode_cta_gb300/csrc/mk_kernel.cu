@@ -294,8 +294,15 @@ __device__ __forceinline__ int checked_page(const Params& p, int b, int logical,
 }
 
 // ============================================================== producer
+// The entry's op word: the task's op, layer and whether its aux field is 1 (a dense
+// FFN layer, the last router tile), so that the consumer dispatches, and starts an
+// expert item, without reading the descriptor from global memory.
+__device__ __forceinline__ int op_word(const int* T) {
+  return (T[D_OP] & 0xff) | ((T[D_LAYER] & 0xffff) << 8) | ((T[D_AUX] == 1 ? 1 : 0) << 24);
+}
+
 __device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int task, int item, int nch,
-                          int4 extra = make_int4(0, 0, 0, 0), int4 w_lo = make_int4(0, 0, 0, 0),
+                          int word, int4 extra = make_int4(0, 0, 0, 0), int4 w_lo = make_int4(0, 0, 0, 0),
                           int4 w_hi = make_int4(0, 0, 0, 0), uint64_t stamp = 0) {
   const uint32_t slot = mseq % kMbox, use = mseq / kMbox;
   if (use > 0 && !mbar_wait(S.mempty(slot), (use - 1) & 1u, 8 * p.timeout_ns)) {
@@ -303,7 +310,7 @@ __device__ bool mbox_push(const Params& p, const Smem& S, uint32_t& mseq, int ta
     return false;
   }
   S.mbox[4 * slot] = make_int4(task, item, nch, extra.x);
-  S.mbox[4 * slot + 1] = make_int4(extra.y, extra.z, (int)(unsigned)stamp, (int)(unsigned)(stamp >> 32));
+  S.mbox[4 * slot + 1] = make_int4(extra.y, extra.z, (int)(unsigned)stamp, word);
   S.mbox[4 * slot + 2] = w_lo;
   S.mbox[4 * slot + 3] = w_hi;
   mbar_arrive(S.mfull(slot));
@@ -455,7 +462,8 @@ __device__ __forceinline__ bool push_gemv(const Params& p, const Smem& S, uint32
   const bool f8 = p.fp8d && T[D_OP] != OP_ROUTER;  // (FP8 projections: QKV, O-proj, LM head)
   const int cs = f8 ? gemv_jpc8(nrb) * nrb * 8 * kFragBytes8 : gemv_jpc(nrb) * nrb * 8 * kFragBytes;
   const int nch = (bytes + cs - 1) / cs;
-  return mbox_push(p, S, mseq, ti, 0, nch) && issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs, inflight);
+  return mbox_push(p, S, mseq, ti, 0, nch, op_word(T)) &&
+         issue_linear(p, S, cseq, p.wblob + off, bytes, pol, ti, cs, inflight);
 }
 
 __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK, const CUtensorMap* tmV) {
@@ -472,7 +480,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
     switch (op) {
       case OP_EMBED:
       case OP_RESID:
-        ok = mbox_push(p, S, mseq, ti, 0, 0);
+        ok = mbox_push(p, S, mseq, ti, 0, 0, op_word(T));
         break;
       case OP_PREFETCH: {
         const long long off = (long long)(((unsigned long long)(unsigned)T[D_WOFF_HI] << 32) |
@@ -498,7 +506,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
           if (item >= count) break;
           const AttItem it = att_decode(p, S, l, item);
           const int nch = 2 * ((it.np + 7) / 8);
-          ok = mbox_push(p, S, mseq, ti, item, nch) && issue_kv(p, S, cseq, tmK, tmV, l, it, pol, ti);
+          ok = mbox_push(p, S, mseq, ti, item, nch, op_word(T)) && issue_kv(p, S, cseq, tmK, tmV, l, it, pol, ti);
         }
         break;
       }
@@ -644,7 +652,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
                           ((long long)__popcll(p.dense_mask & ((1ull << l) - 1ull)) * p.t_dense + t) * ib
                     : p.wblob + p.off_moe + ((long long)(l * p.E + e) * p.t_moe + t) * p.moe_item_bytes;
           const int fl = (p.tail_items > 0 && item >= count - p.tail_items) ? p.inflight_tail : p.inflight_moe;
-          ok = mbox_push(p, S, mseq, ti, item, nch, extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
+          ok = mbox_push(p, S, mseq, ti, item, nch, op_word(T), extra, make_int4(tl_w[0], tl_w[1], tl_w[2], tl_w[3]),
                          make_int4(tl_w[4], tl_w[5], tl_w[6], tl_w[7]), p.trace ? gtime() : 0ull) &&
                (sb == 0 || issue_linear(p, S, cseq, src, sb, pol, ti, sb, fl)) &&
                issue_linear(p, S, cseq, src + sb, gu_bytes, pol, ti, cs1, fl) &&
@@ -667,7 +675,7 @@ __device__ void producer(const Params& p, const Smem& S, const CUtensorMap* tmK,
         break;
     }
   }
-  mbox_push(p, S, mseq, -1, 0, 0);
+  mbox_push(p, S, mseq, -1, 0, 0, 0);
   // make sure no copy is still landing in shared memory when the CTA retires
   const uint32_t first = cseq > (uint32_t)kStages ? cseq - kStages : 0;
   for (uint32_t q = first; q < cseq; ++q) mbar_wait(S.full(q % kStages), (q / kStages) & 1u, 8 * p.timeout_ns);
@@ -1653,13 +1661,12 @@ __device__ bool task_resid(const Params& p, const Smem& S, uint32_t& sseq, const
 // its f32 row scales (copied to shared memory), the operand and the SiLU product are
 // f16, and each GEMV output is scaled by its row's scale.
 template <int FS, bool F8 = false>
-__device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, const int* T,
-                                         int ti, int item, int nch, int ntok, int tok_lo, int tok_hi, int4 w_lo,
-                                         int4 w_hi, BFrag& fr, OperandKey& have, float& rs_have) {
-  const int l = T[D_LAYER];
+__device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, int l,
+                                         bool dense, int ti, int item, int nch, int ntok, int tok_lo, int tok_hi,
+                                         int4 w_lo, int4 w_hi, BFrag& fr, OperandKey& have, float& rs_have) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g8 = lane >> 2, c = lane & 3;
-  const int a_slot = T[D_AUX] == 1 ? 0 : item / p.t_moe;  // a dense layer: one token set
+  const int a_slot = dense ? 0 : item / p.t_moe;  // a dense layer: one token set
   const OperandKey key = {3, l, a_slot};
   // The producer claimed this item from the layer's route words and passed the
   // expert's token list and weights in the mailbox entry: no dependency wait here.
@@ -2186,6 +2193,9 @@ __device__ void consumer(const Params& p, const Smem& S) {
   BFrag fr;
   OperandKey have = {-1, -1, -1};
   float rs_have = 0.f;
+  // thread 0: the abort flag as loaded one entry earlier (the load's round trip then
+  // overlaps the task instead of delaying the start of the next one)
+  int abort_seen = threadIdx.x == 0 ? ld_volatile(&p.err[E_ABORT]) : 0;
   while (true) {
     // Thread 0 takes the mailbox entry and the abort flag; every consumer thread
     // then follows the same path, so the named barriers stay matched.
@@ -2194,7 +2204,8 @@ __device__ void consumer(const Params& p, const Smem& S) {
       const bool got = mbar_wait(S.mfull(slot), (mseq / kMbox) & 1u, 16 * p.timeout_ns);
       if (!got) raise_err(p, MK_ERR_TIMEOUT, -5, -1, (int)mseq, 0);
       S.small[3] = got ? 1 : 0;
-      S.small[4] = aborted(p) ? 1 : 0;
+      S.small[4] = abort_seen != 0 ? 1 : 0;
+      abort_seen = ld_volatile(&p.err[E_ABORT]);
     }
     bar_sync_consumers();
     const bool got = S.small[3] != 0;
@@ -2209,12 +2220,14 @@ __device__ void consumer(const Params& p, const Smem& S) {
     if (ent.x < 0) break;
     const int* T = p.tasks + ent.x * kDescInts;
     const int nch = ent.z;
+    const int op = ent2.w & 0xff, wl = (ent2.w >> 8) & 0xffff;
+    const bool aux1 = ((ent2.w >> 24) & 1) != 0;
     if (p.trace && threadIdx.x == 0) {
       unsigned long long* t = trace_slots(S);
       t[0] = gtime(); t[1] = t[2] = t[3] = t[6] = t[8] = t[9] = t[10] = 0ull;
       t[12] = t[13] = t[14] = t[15] = 0ull;
       // (expert items: when the producer pushed the entry, route words in hand)
-      t[11] = ((unsigned long long)(unsigned)ent2.w << 32) | (unsigned)ent2.z;
+      t[11] = ent2.z ? t[0] - (unsigned)((unsigned)t[0] - (unsigned)ent2.z) : 0ull;
     }
     if (abort_now) skip = true;
     if (skip) {
@@ -2222,7 +2235,7 @@ __device__ void consumer(const Params& p, const Smem& S) {
       continue;
     }
     bool ok = true;
-    switch (T[D_OP]) {
+    switch (op) {
       case OP_EMBED:
         task_embed(p, S, sseq, ent.x);
         break;
@@ -2241,16 +2254,17 @@ __device__ void consumer(const Params& p, const Smem& S) {
         break;
       case OP_MOE_DRAIN: {
         // (a dense layer's FFN items: bf16 f-slices of dense_fs rows)
-        const int fsi = T[D_AUX] == 1 ? p.dense_fs : p.moe_fs;
-        ok = (p.fp8 && T[D_AUX] != 1)
-                 ? (p.moe_fs == 64 ? task_moe<64, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
+        const int fsi = aux1 ? p.dense_fs : p.moe_fs;
+        ok = (p.fp8 && !aux1)
+                 ? (p.moe_fs == 64 ? task_moe<64, true>(p, S, cseq, sseq, wl, aux1, ent.x, ent.y, nch, ent.w, ent2.x,
                                                            ent2.y, ew_lo, ew_hi, fr, have, rs_have)
-                                     : task_moe<32, true>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x,
+                                     : task_moe<32, true>(p, S, cseq, sseq, wl, aux1, ent.x, ent.y, nch, ent.w, ent2.x,
                                                            ent2.y, ew_lo, ew_hi, fr, have, rs_have))
              : (fsi == 32)
-                 ? task_moe<32>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have,
-                                rs_have)
-                 : task_moe<16>(p, S, cseq, sseq, T, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr, have, rs_have);
+                 ? task_moe<32>(p, S, cseq, sseq, wl, aux1, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr,
+                                have, rs_have)
+                 : task_moe<16>(p, S, cseq, sseq, wl, aux1, ent.x, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr,
+                                have, rs_have);
         break;
       }
       default:
@@ -2258,7 +2272,7 @@ __device__ void consumer(const Params& p, const Smem& S) {
         break;
     }
     if (!ok) skip = true;
-    trace_emit(p, S, T[D_OP], T[D_LAYER], ent.y);
+    trace_emit(p, S, op, wl, ent.y);
   }
   signal_async(p, S, sseq, -1, 0u);  // tells the storer to finish
 }
