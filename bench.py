@@ -223,12 +223,16 @@ def time_device(run_step, K, W, ws, stream):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # (an NVTX range around the timed steps: a profiler's launch list can be restricted
+    # to it with `ncu --nvtx --nvtx-include "timed/"`)
+    torch.cuda.nvtx.range_push("timed")
     t0.record(stream)
     for i in range(K):
         evs[i][0].record(stream)
         run_step()
         evs[i][1].record(stream)
     t1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(ws)
     total = t0.elapsed_time(t1) / 1e3
