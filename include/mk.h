@@ -275,6 +275,20 @@ int mk_set_inspect(mk_handle* h, int on);
 /* fixed = 1: steps do not advance seq_lens (repeated steps move identical bytes). */
 int mk_set_fixed(mk_handle* h, int fixed);
 
+/* on = 1: deterministic steps, from the next mk_plan on.  The experts' and O-proj
+ * tiles' outputs are added into each layer's accumulator as 64-bit fixed-point
+ * integers (32 fraction bits; |value| < 2^31) with integer reductions, whose sum does
+ * not depend on the order in which the tiles finish; every other reduction of the step
+ * has a fixed order, so two steps on the same inputs give bit-identical hidden states,
+ * routing, K/V and logits.  (With on = 0, the default, the accumulators are float32 and
+ * the order of the atomic adds changes their last bits from run to run; at a router
+ * near-tie that can change the experts chosen.)  Costs twice the accumulator memory and
+ * 64-bit scalar reductions in place of 128-bit float ones.  No counterpart in the pages,
+ * whose combine is described only as the weighted sum of the experts' outputs
+ * [Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "One kernel for the full
+ * decode step": MOE_COMBINE].  Errors: MK_ERR_INVALID for a NULL handle. */
+int mk_set_deterministic(mk_handle* h, int on);
+
 /* Debug/inspection reads into HOST memory (synchronising).  `what`:
  *   MK_READ_HIDDEN   float [n_layers+1][batch][d_model] residual entering each layer
  *                    (index n_layers = input of the final norm)

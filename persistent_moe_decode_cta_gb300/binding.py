@@ -31,7 +31,7 @@ MK_EXPERT_BF16, MK_EXPERT_FP8, MK_WEIGHTS_FP8 = 0, 1, 2
 
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_decode_step_noalloc",
-           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_inspect", "mk_set_trace",
+           "mk_decode_step_perop", "mk_get_status", "mk_set_fixed", "mk_set_deterministic", "mk_set_inspect", "mk_set_trace",
            "mk_plan_drop_signal", "mk_read", "mk_read_expert_fp8", "mk_read_weight_fp8", "mk_query",
            "mk_plan_dry", "mk_last_error", "mk_destroy", "mk_version"]
 
@@ -93,6 +93,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mk_decode_step_perop.argtypes = [H, vp, vp, vp, vp, vp, i32]
     lib.mk_get_status.argtypes = [H, ctypes.POINTER(mk_error_info)]
     lib.mk_set_fixed.argtypes = [H, i32]
+    lib.mk_set_deterministic.argtypes = [H, i32]
     lib.mk_set_inspect.argtypes = [H, i32]
     lib.mk_set_trace.argtypes = [H, vp, i32]
     lib.mk_plan_drop_signal.argtypes = [H, i32]
@@ -235,6 +236,10 @@ def mk_set_fixed(h, fixed: bool):
     _check(load_library().mk_set_fixed(h, int(bool(fixed))), h)
 
 
+def mk_set_deterministic(h, on: bool):
+    _check(load_library().mk_set_deterministic(h, int(bool(on))), h)
+
+
 def mk_set_inspect(h, on: bool):
     _check(load_library().mk_set_inspect(h, int(bool(on))), h)
 
@@ -357,6 +362,10 @@ class Megakernel:
 
     def set_fixed(self, fixed=True):
         mk_set_fixed(self.h, fixed)
+
+    def set_deterministic(self, on=True):
+        """Deterministic steps from the next plan() on (fixed-point layer accumulators)."""
+        mk_set_deterministic(self.h, on)
 
     def trace_on(self, capacity=1 << 20):
         import torch

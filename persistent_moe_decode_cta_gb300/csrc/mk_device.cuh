@@ -86,6 +86,14 @@ __device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
 __device__ __forceinline__ void red_add_f32(float* dst, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(dst), "f"(v) : "memory");
 }
+// Deterministic accumulation: x as a 64-bit fixed-point integer with 32 fraction bits
+// (|x| < 2^31; x * 2^32 is exact in float, then rounded to the nearest integer), added
+// with an integer reduction: the sum of such adds does not depend on their order.
+__device__ __forceinline__ void red_add_fx(long long* dst, float v) {
+  const long long q = __float2ll_rn(v * 4294967296.f);
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(dst), "l"(q) : "memory");
+}
+__device__ __forceinline__ float fx_to_f(long long q) { return __ll2float_rn(q) * 2.3283064365386963e-10f; }
 // Four consecutive fp32 atomic adds in one 128-bit reduction (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float* dst, float4 v) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(v.x), "f"(v.y),

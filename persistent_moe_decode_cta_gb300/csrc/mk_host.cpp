@@ -47,6 +47,13 @@ cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUte
                               bool cooperative, cudaStream_t st);
 cudaError_t static_scratch_address(void** ptr);
 }  // namespace mk
+// the same megakernel with deterministic (64-bit fixed-point) layer accumulators
+namespace mk_det {
+cudaError_t prepare_megakernel();
+int megakernel_occupancy(int* blocks);
+cudaError_t launch_megakernel(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                              bool cooperative, cudaStream_t st);
+}  // namespace mk_det
 
 using namespace mk;
 
@@ -512,6 +519,7 @@ struct mk_handle {
   bool last_noalloc = false;   // the last step ran in the static scratch (mk_read follows it)
   int inspect = 0;
   int fixed = 0;
+  int det = 0;     // deterministic accumulation, from the next mk_plan (mk_set_deterministic)
   cudaStream_t last_stream = nullptr;
   // tensor maps
   CUtensorMap tmK{}, tmV{};
@@ -620,7 +628,8 @@ int launch_segment(mk_handle* h, int seg, bool cooperative, bool reset, cudaStre
   Params p = h->prm;
   p.sm_off = h->d_sm_off + (size_t)seg * (h->n_sm + 1);
   p.do_reset = reset ? 1 : 0;
-  cudaError_t e = launch_megakernel(p, h->tmK, h->tmV, h->n_sm, cooperative, st);
+  cudaError_t e = p.det ? mk_det::launch_megakernel(p, h->tmK, h->tmV, h->n_sm, cooperative, st)
+                        : launch_megakernel(p, h->tmK, h->tmV, h->n_sm, cooperative, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch");
   return MK_OK;
 }
@@ -675,6 +684,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
     return bail(MK_ERR_UNSUPPORTED);
   }
   e = prepare_megakernel();
+  if (e == cudaSuccess) e = mk_det::prepare_megakernel();
   if (e != cudaSuccess) { cuda_fail(h, e, "cudaFuncSetAttribute"); return bail(MK_ERR_CUDA); }
   e = cudaMalloc(&h->wblob, s.total);
   if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "packed weights (%zu B): %s", s.total, cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
@@ -834,7 +844,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   int r = build_plan(s, batch, h->n_sm, order, h->P, &h->err, prefetch_mask(), router_sms());
   if (r) return r;
   int occ = 0;
-  megakernel_occupancy(&occ);
+  if (h->det) mk_det::megakernel_occupancy(&occ);
+  else megakernel_occupancy(&occ);
   if (occ < 1) return fail(&h->err, MK_ERR_UNSUPPORTED, "megakernel cannot be resident (occupancy %d)", occ);
   PlanOut& P = h->P;
   h->B = batch;
@@ -909,7 +920,8 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   AL(p.nact, (size_t)L);
   AL(p.act_cnt, (size_t)L * maxa);
   AL(p.act_tok, (size_t)L * maxa * B);
-  AL(p.moe, (size_t)L * B * s.d);
+  p.det = h->det;
+  AL(p.moe, (size_t)L * B * s.d * (h->det ? 2 : 1));  // 64-bit fixed point when deterministic
   AL(p.ctr, (size_t)P.n_ctr * kCtrStride);
   AL(p.qhead, (size_t)3 * L);
   AL(p.qcount, (size_t)3 * L);
@@ -967,7 +979,8 @@ int mk_decode_steps(mk_handle* h, const int32_t* tokens_dev, int n_steps, void* 
   p.do_reset = 1;
   p.n_steps = n_steps;
   p.tok_out = tokens_out_dev;
-  cudaError_t e = launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
+  cudaError_t e = p.det ? mk_det::launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st)
+                        : launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch (multi-step)");
   return MK_OK;
 }
@@ -1001,7 +1014,7 @@ static size_t step_scratch_layout(const mk_handle* h, uint8_t* base, Params* p, 
   q = take(L * 4);                                              if (p) p->nact = (int*)q;
   q = take(L * maxa * 4);                                       if (p) p->act_cnt = (int*)q;
   q = take(L * maxa * B * 4);                                   if (p) p->act_tok = (int*)q;
-  q = take(L * B * s.d * 4);                                    if (p) p->moe = (float*)q;
+  q = take(L * B * s.d * 4 * (h->prm.det ? 2 : 1));             if (p) p->moe = (float*)q;
   q = take(L * B * s.E * 8);                                    if (p) p->rlog = (uint64_t*)q;
   q = take(L * (1 + 2 * maxa + 2 * maxa * B) * 8);              if (p) { p->rword = (uint64_t*)q; p->rw_stride = (int)(1 + 2 * maxa + 2 * maxa * B); }
   q = take((size_t)h->P.n_ctr * kCtrStride * 4);                if (p) p->ctr = (unsigned*)q;
@@ -1034,7 +1047,8 @@ int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cach
   h->last_stream = st;
   p.sm_off = h->d_sm_off;
   p.do_reset = 1;
-  cudaError_t e = launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
+  cudaError_t e = p.det ? mk_det::launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st)
+                        : launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch (static scratch)");
   return MK_OK;
 }
@@ -1153,6 +1167,12 @@ int mk_set_inspect(mk_handle* h, int on) {
 int mk_set_fixed(mk_handle* h, int fixed) {
   if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
   h->fixed = fixed ? 1 : 0;
+  return MK_OK;
+}
+
+int mk_set_deterministic(mk_handle* h, int on) {
+  if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  h->det = on ? 1 : 0;
   return MK_OK;
 }
 

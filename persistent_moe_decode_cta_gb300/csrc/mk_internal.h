@@ -132,6 +132,10 @@ struct Params {
   int route_pf_bytes;
   // batch 1: the route step on one warp (route_step_b1) instead of the block-wide one
   int route_warp;
+  // deterministic accumulation: the layer accumulators `moe` hold 64-bit fixed-point
+  // integers (32 fraction bits) added with integer reductions, so that their sums, and
+  // everything downstream, do not depend on the order of the expert and O-proj adds
+  int det;
   int fp8;                  // expert weights as E4M3 codes with f32 scales (items: see fp8_scale_bytes)
   int dense_fs;             // f-slice rows of a dense layer's FFN items (bf16; = moe_fs without FP8)
   // FP8 projections: the QKV, O-proj and LM-head tiles hold E4M3 codes (8 bytes a lane

@@ -21,7 +21,21 @@
 
 #include "mk_device.cuh"
 
-namespace mk {
+// This file is compiled twice: as is (float32 layer accumulators), and by
+// mk_kernel_det.cu with MK_DET = 1 (deterministic steps: 64-bit fixed-point
+// accumulators), whose megakernel and launchers live in namespace mk_det.  The weight
+// packers and the static step scratch exist in the first build only.
+#ifndef MK_DET
+#define MK_DET 0
+#endif
+#if MK_DET
+#define MK_KNS mk_det
+#else
+#define MK_KNS mk
+#endif
+
+namespace MK_KNS {
+using namespace ::mk;
 
 // ============================================================== errors / waits
 __device__ void raise_err(const Params& p, int code, int task, int ctr, int obs, int target) {
@@ -90,6 +104,38 @@ __device__ bool wait_ge(const Params& p, int ci, unsigned target, int task) {
 }
 
 __device__ __forceinline__ unsigned* ctr_ptr(const Params& p, int ci) { return p.ctr + (size_t)ci * kCtrStride; }
+
+// The layer accumulators [L][B][d] (expert and O-proj outputs), float or, in the
+// deterministic build, 64-bit fixed point: element i (4 consecutive from a multiple of
+// 4 for the vector forms)
+__device__ __forceinline__ float acc_ld1(const Params& p, size_t i) {
+  if (MK_DET) return fx_to_f(__ldcg(reinterpret_cast<const long long*>(p.moe) + i));
+  return __ldcg(p.moe + i);
+}
+__device__ __forceinline__ float4 acc_ld4(const Params& p, size_t i) {
+  if (MK_DET) {
+    const longlong2* q = reinterpret_cast<const longlong2*>(reinterpret_cast<const long long*>(p.moe) + i);
+    const longlong2 a = __ldcg(q), b = __ldcg(q + 1);
+    return make_float4(fx_to_f(a.x), fx_to_f(a.y), fx_to_f(b.x), fx_to_f(b.y));
+  }
+  return __ldcg(reinterpret_cast<const float4*>(p.moe + i));
+}
+__device__ __forceinline__ void acc_add1(const Params& p, size_t i, float v) {
+  if (MK_DET) red_add_fx(reinterpret_cast<long long*>(p.moe) + i, v);
+  else red_add_f32(p.moe + i, v);
+}
+__device__ __forceinline__ void acc_add4(const Params& p, size_t i, float4 v) {
+  if (MK_DET) {
+    long long* q = reinterpret_cast<long long*>(p.moe) + i;
+    red_add_fx(q, v.x); red_add_fx(q + 1, v.y); red_add_fx(q + 2, v.z); red_add_fx(q + 3, v.w);
+  } else {
+    red_add_v4(p.moe + i, v);
+  }
+}
+// float4 words of the accumulators (twice as many with 64-bit entries)
+__device__ __forceinline__ size_t acc_words4(const Params& p) {
+  return (size_t)p.L * p.B * p.d / 4 * (MK_DET ? 2 : 1);
+}
 
 // Greedy-token key: larger for a larger logit, then for a lower row (ties go to the
 // lowest index); -0 and +0 compare equal; 0 is below every key of a real logit.
@@ -905,7 +951,7 @@ __device__ float build_operand_parts(const Params& p, const Smem& S, BFrag& fr, 
   const int c = lane & 3, nl = lane >> 2;
   const int d = p.d, B = p.B, d4 = d / 4;
   const float* xa = p.X + (size_t)(l - 1) * B * d;
-  const float* ma = p.moe + (size_t)(l - 1) * B * d;
+  const size_t ma = (size_t)(l - 1) * B * d;  // accumulator of layer l - 1
   const float4* gain4 = reinterpret_cast<const float4*>(p.attn_norm + (size_t)l * d);
   uint8_t* st = reinterpret_cast<uint8_t*>(S.scratch);
   float* ssw = reinterpret_cast<float*>(S.small + 16);  // [8 warps][8 tokens] partial sums
@@ -937,7 +983,7 @@ __device__ float build_operand_parts(const Params& p, const Smem& S, BFrag& fr, 
           av[u][q] = mv[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (n < t1 && g < d4) {
             av[u][q] = __ldcg(reinterpret_cast<const float4*>(xa + (size_t)n * d) + g);
-            mv[u][q] = __ldcg(reinterpret_cast<const float4*>(ma + (size_t)n * d) + g);
+            mv[u][q] = acc_ld4(p, ma + (size_t)n * d + 4 * (size_t)g);
           }
         }
 #pragma unroll
@@ -1339,7 +1385,7 @@ __device__ void residual_blocks(const Params& p, const Smem& S, uint32_t& sseq, 
     const int blk = q >> 2;                      // (block index, token)
     const int r = rbl[blk / p.B], b = blk % p.B;
     const int row = r * kRowBlock + (q & 3) * 32 + lane;
-    const float x = ldg_cg(p.X + ((size_t)l * p.B + b) * p.d + row) + ldg_cg(p.moe + ((size_t)l * p.B + b) * p.d + row);
+    const float x = ldg_cg(p.X + ((size_t)l * p.B + b) * p.d + row) + acc_ld1(p, ((size_t)l * p.B + b) * p.d + row);
     const size_t o = ((size_t)(l + 1) * p.B + b) * p.d + row;
     p.X[o] = x;
     const float xg = x * gain_next[row];
@@ -1567,9 +1613,9 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
         for (int e = 0; e < 2; ++e) {
           const int n = 2 * c + e;
           if (n >= p.B) continue;
-          float* out = p.moe + ((size_t)l * p.B + n) * p.d;
-          red_add_f32(out + r0, v[e]);
-          red_add_f32(out + r0 + 8, v[2 + e]);
+          const size_t out = ((size_t)l * p.B + n) * p.d;
+          acc_add1(p, out + r0, v[e]);
+          acc_add1(p, out + r0 + 8, v[2 + e]);
         }
         break;
       }
@@ -1820,8 +1866,7 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
         const int x1 = __shfl_sync(0xffffffffu, bt[1], (n >> 1) & 3);
         const int b = (n & 1) ? x1 : x0;
         if (n < ntok && fq < nrow)
-          red_add_v4(p.moe + ((size_t)l * p.B + b) * p.d + row0 + fq,
-                     *reinterpret_cast<const float4*>(stg + n * kStg + fq));
+          acc_add4(p, ((size_t)l * p.B + b) * p.d + row0 + fq, *reinterpret_cast<const float4*>(stg + n * kStg + fq));
       }
       __syncwarp();
     }
@@ -2329,7 +2374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       if (S.small[2]) {
         float4* acc = reinterpret_cast<float4*>(p.moe);
-        const size_t n4 = (size_t)p.L * p.B * p.d / 4;
+        const size_t n4 = acc_words4(p);
         const size_t i0 = n4 * blockIdx.x / gridDim.x, i1 = n4 * (blockIdx.x + 1) / gridDim.x;
         for (size_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -2371,7 +2416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = threadIdx.x; i < p.n_queues; i += blockDim.x) { p.qhead[i] = 0; p.qcount[i] = 0; }
         if (aborted(p)) {
           float4* acc = reinterpret_cast<float4*>(p.moe);
-          const size_t n4 = (size_t)p.L * p.B * p.d / 4;
+          const size_t n4 = acc_words4(p);
           for (size_t i = threadIdx.x; i < n4; i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (!p.fixed)
@@ -2414,6 +2459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+#if !MK_DET
 // ============================================================== weight packer
 // Source of packed row r (see mk_pack_kernel): the matrix (0 = a, 1 = b, 2 = c) and its
 // row, or row -1 for a zero padding row.
@@ -2709,7 +2755,7 @@ __global__ void mk_convert_kernel(float* __restrict__ dst, const uint16_t* __res
 static __device__ __align__(256) uint8_t g_mk_static_scratch[mk::kStaticScratchBytes];
 
 // ============================================================== host-side launchers
-namespace mk {
+namespace MK_KNS {
 
 // Device address of the static scratch array on the current device, looked up once
 // per device (with that device current) and cached.  The host-side name of the array
@@ -2781,6 +2827,8 @@ cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_
   mk_convert_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dst, (const uint16_t*)src, n);
   return cudaGetLastError();
 }
+
+#endif  // !MK_DET
 
 cudaError_t prepare_megakernel() {
   return cudaFuncSetAttribute(mk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
