@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["mk_kernel.cu", "mk_kernel_det.cu", "mk_host.cpp"]
+SOURCES = ["mk_kernel.cu", "mk_kernel_det.cu", "mk_kernel_umma.cu", "mk_host.cpp"]
 
 
 def nvcc_path() -> str:

@@ -46,6 +46,7 @@ int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                               bool cooperative, cudaStream_t st);
 cudaError_t static_scratch_address(void** ptr);
+cudaError_t launch_pack_umma(uint8_t* dst, const void* src, int n_rows_packed, int n_src_rows, int K, cudaStream_t st);
 }  // namespace mk
 // the same megakernel with deterministic (64-bit fixed-point) layer accumulators
 namespace mk_det {
@@ -54,6 +55,24 @@ int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                               bool cooperative, cudaStream_t st);
 }  // namespace mk_det
+// ... and with the LM head on the tcgen05 tensor cores
+namespace mk_umma {
+cudaError_t prepare_megakernel();
+int megakernel_occupancy(int* blocks);
+cudaError_t launch_megakernel(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                              bool cooperative, cudaStream_t st);
+}  // namespace mk_umma
+
+namespace {
+// the kernel build a plan runs: deterministic accumulators, the tensor-core LM head, or
+// the default
+cudaError_t launch_variant(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                           bool cooperative, cudaStream_t st) {
+  if (p.det) return mk_det::launch_megakernel(p, tk, tv, grid, cooperative, st);
+  if (p.lm_umma) return mk_umma::launch_megakernel(p, tk, tv, grid, cooperative, st);
+  return mk::launch_megakernel(p, tk, tv, grid, cooperative, st);
+}
+}  // namespace
 
 using namespace mk;
 
@@ -74,6 +93,7 @@ struct Shape {
   bool fp8d;            // QKV, O-proj and LM head as E4M3 codes + per-row f32 scales
   int esz;              // bytes of a QKV / O-proj / LM-head weight (2 bf16, 1 E4M3)
   int r_lm, v_pad, n_lm_tasks;
+  int lm_umma;  // LM head on the tensor cores (128-row tiles in the core-matrix layout)
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
   size_t dense_item_bytes;
   size_t off_qkv, off_o, off_router, off_moe, off_dense, off_lm, off_embed, total;
@@ -160,6 +180,11 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.t_dense = s.f_dense / s.dense_fs;
   s.r_lm = 64;
   if (const char* e = getenv("MK_LM_ROWS")) { const int v = atoi(e); if (v == 32 || v == 64 || v == 128) s.r_lm = v; }
+  // MK_LM_UMMA=1 (read at mk_create): the LM head's tiles on the tcgen05 tensor cores,
+  // 64 rows each (bf16 weights; d a multiple of 256, at most 2048)
+  s.lm_umma = 0;
+  if (const char* e = getenv("MK_LM_UMMA"))
+    if (atoi(e) && !s.fp8d && s.d % 256 == 0 && s.d / 128 <= kMaxKsw) { s.lm_umma = 1; s.r_lm = 64; }
   s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * s.esz;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * s.esz;
@@ -628,8 +653,7 @@ int launch_segment(mk_handle* h, int seg, bool cooperative, bool reset, cudaStre
   Params p = h->prm;
   p.sm_off = h->d_sm_off + (size_t)seg * (h->n_sm + 1);
   p.do_reset = reset ? 1 : 0;
-  cudaError_t e = p.det ? mk_det::launch_megakernel(p, h->tmK, h->tmV, h->n_sm, cooperative, st)
-                        : launch_megakernel(p, h->tmK, h->tmV, h->n_sm, cooperative, st);
+  cudaError_t e = launch_variant(p, h->tmK, h->tmV, h->n_sm, cooperative, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch");
   return MK_OK;
 }
@@ -685,6 +709,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
   }
   e = prepare_megakernel();
   if (e == cudaSuccess) e = mk_det::prepare_megakernel();
+  if (e == cudaSuccess) e = mk_umma::prepare_megakernel();
   if (e != cudaSuccess) { cuda_fail(h, e, "cudaFuncSetAttribute"); return bail(MK_ERR_CUDA); }
   e = cudaMalloc(&h->wblob, s.total);
   if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "packed weights (%zu B): %s", s.total, cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
@@ -774,6 +799,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
   if (s.fp8d) {
     PKS(lm_sc, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, PACK_IDENT, 0);
     PK8(h->wblob + s.off_lm, lm_sc, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, 0, s.r_lm);
+  } else if (s.lm_umma) {
+    e = launch_pack_umma(h->wblob + s.off_lm, w->lm_head, s.v_pad, s.V, d, st);
+    if (e != cudaSuccess) { cuda_fail(h, e, "pack"); return bail(MK_ERR_CUDA); }
   } else {
     PK(h->wblob + s.off_lm, w->lm_head, nullptr, nullptr, s.v_pad, s.V, d, d, 0, PACK_IDENT, hd, gs, 0, s.r_lm);
   }
@@ -845,6 +873,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   if (r) return r;
   int occ = 0;
   if (h->det) mk_det::megakernel_occupancy(&occ);
+  else if (h->s.lm_umma) mk_umma::megakernel_occupancy(&occ);
   else megakernel_occupancy(&occ);
   if (occ < 1) return fail(&h->err, MK_ERR_UNSUPPORTED, "megakernel cannot be resident (occupancy %d)", occ);
   PlanOut& P = h->P;
@@ -892,6 +921,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.dense_fs = s.dense_fs; p.dense_item_bytes = (long long)s.dense_item_bytes;
   p.fp8 = s.fp8 ? 1 : 0;
   p.fp8d = s.fp8d ? 1 : 0;
+  p.lm_umma = s.lm_umma;
   p.qkv_rows_group = s.qkv_rows_group;
   p.qkv_scale = reinterpret_cast<const float*>(h->wblob + s.off_qkv_scale);
   p.o_scale = reinterpret_cast<const float*>(h->wblob + s.off_o_scale);
@@ -979,8 +1009,7 @@ int mk_decode_steps(mk_handle* h, const int32_t* tokens_dev, int n_steps, void* 
   p.do_reset = 1;
   p.n_steps = n_steps;
   p.tok_out = tokens_out_dev;
-  cudaError_t e = p.det ? mk_det::launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st)
-                        : launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
+  cudaError_t e = launch_variant(p, h->tmK, h->tmV, h->n_sm, true, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch (multi-step)");
   return MK_OK;
 }
@@ -1047,8 +1076,7 @@ int mk_decode_step_noalloc(mk_handle* h, const int32_t* tokens_dev, void* k_cach
   h->last_stream = st;
   p.sm_off = h->d_sm_off;
   p.do_reset = 1;
-  cudaError_t e = p.det ? mk_det::launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st)
-                        : launch_megakernel(p, h->tmK, h->tmV, h->n_sm, true, st);
+  cudaError_t e = launch_variant(p, h->tmK, h->tmV, h->n_sm, true, st);
   if (e != cudaSuccess) return cuda_fail(h, e, "megakernel launch (static scratch)");
   return MK_OK;
 }
@@ -1172,6 +1200,8 @@ int mk_set_fixed(mk_handle* h, int fixed) {
 
 int mk_set_deterministic(mk_handle* h, int on) {
   if (!h) return fail(nullptr, MK_ERR_INVALID, "handle is NULL");
+  if (on && h->s.lm_umma)
+    return fail(&h->err, MK_ERR_UNSUPPORTED, "deterministic steps with the tensor-core LM head (MK_LM_UMMA)");
   h->det = on ? 1 : 0;
   return MK_OK;
 }

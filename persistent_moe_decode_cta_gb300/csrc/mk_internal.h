@@ -27,7 +27,11 @@ constexpr int kThreads = kConsumerThreads + 64;
 constexpr int kStageBytes = 32768;            // one ring slot
 constexpr int kStages = 6;                    // 192 KB of copies in flight per SM
 constexpr int kScratchBytes = 32768;          // cross-warp reductions / merges
-constexpr int kSmallBytes = 1024;             // per-warp scalars, flags
+constexpr int kSmallBytes = 1024;             // per-warp scalars, flags (256 ints):
+// [1, 5) flags; [5] the tensor-memory base address; [16, 144) per-task scratch (route
+// step selection, attention combine maxima and sums, residual block list, operand
+// partial sums); [192, 224) trace slots; [224, 232) sequence lengths; [240, 248) 1/rms
+// per token; [248, 252) epoch, step, grid-barrier generation
 constexpr int kMbox = 8;                      // producer -> consumer task mailbox
 constexpr int kSq = 8;                        // consumer -> storer signal queue
 constexpr int kFragBytes = 512;               // one 16x16 bf16 MMA A-fragment
@@ -35,7 +39,7 @@ constexpr int kFragBytes8 = 256;              // the same fragment in E4M3 codes
 constexpr int kFragsPerStage = kStageBytes / kFragBytes;
 constexpr int kMaxNrb = 8;                    // GEMV task rows <= 128
 constexpr int kMaxKsw = 16;                   // GEMV task K <= 2048 (16 k16-steps/warp)
-constexpr int kBarBytes = (2 * kStages + 2 * kMbox + 2 * kSq) * 8;
+constexpr int kBarBytes = (2 * kStages + 2 * kMbox + 2 * kSq + 2) * 8;  // + 2: tensor-core chunk commits
 // mailbox entry: {task, item, chunks, n_tok}, {token bytes 0..3, 4..7, -, -}, {weights
 // 0..3}, {weights 4..7} (MoE items carry their expert's token list -- byte n = b * 8 + j
 // for the n-th token b, rank j -- and the tokens' routing weights as f32 bits)
@@ -132,6 +136,10 @@ struct Params {
   int route_pf_bytes;
   // batch 1: the route step on one warp (route_step_b1) instead of the block-wide one
   int route_warp;
+  // LM head on the 5th-generation tensor cores: 128-row tiles whose weight chunks are in
+  // the K-major core-matrix layout, accumulated in tensor memory (tcgen05.mma); selects
+  // the kernel build compiled with MK_UMMA
+  int lm_umma;
   // deterministic accumulation: the layer accumulators `moe` hold 64-bit fixed-point
   // integers (32 fraction bits) added with integer reductions, so that their sums, and
   // everything downstream, do not depend on the order of the expert and O-proj adds

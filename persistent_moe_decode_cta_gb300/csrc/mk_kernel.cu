@@ -21,15 +21,24 @@
 
 #include "mk_device.cuh"
 
-// This file is compiled twice: as is (float32 layer accumulators), and by
-// mk_kernel_det.cu with MK_DET = 1 (deterministic steps: 64-bit fixed-point
-// accumulators), whose megakernel and launchers live in namespace mk_det.  The weight
-// packers and the static step scratch exist in the first build only.
+// This file is compiled three times: as is (float32 layer accumulators, the LM head on
+// mma.sync), by mk_kernel_det.cu with MK_DET = 1 (deterministic steps: 64-bit
+// fixed-point accumulators; namespace mk_det), and by mk_kernel_umma.cu with MK_UMMA = 1
+// (the LM head on tcgen05 tensor cores with a tensor-memory accumulator; namespace
+// mk_umma).  The weight packers and the static step scratch exist in the first build only.
 #ifndef MK_DET
 #define MK_DET 0
 #endif
+#ifndef MK_UMMA
+#define MK_UMMA 0
+#endif
+#if MK_DET && MK_UMMA
+#error "one kernel variant per build"
+#endif
 #if MK_DET
 #define MK_KNS mk_det
+#elif MK_UMMA
+#define MK_KNS mk_umma
 #else
 #define MK_KNS mk
 #endif
@@ -1437,9 +1446,108 @@ struct OperandKey {
   }
 };
 
+
+// ---------------------------------------------------------------- LM head on tcgen05
+// Completion of the tensor-core MMAs committed as chunk number u of this step (two
+// mbarriers, alternating; every consumer thread waits).
+__device__ __forceinline__ bool wait_mma(const Params& p, const Smem& S, uint32_t u) {
+  if (mbar_wait(S.mmadone(u & 1u), (u >> 1) & 1u, 4 * p.timeout_ns)) return true;
+  if ((threadIdx.x & 31) == 0) raise_err(p, MK_ERR_TIMEOUT, -15, -1, (int)u, 0);
+  return false;
+}
+
+// LM_HEAD tile of 64 rows on the 5th-generation tensor cores (the MK_UMMA build).  Every
+// 32 KB weight chunk holds the tile's 64 rows x 256 columns in the K-major core-matrix
+// layout (core matrix (kc, mg) -- rows 8 mg .. 8 mg + 7, columns 8 kc .. 8 kc + 7, 16
+// bytes a row -- at (kc * 8 + mg) * 128 bytes).  The tokens' operand (N = 8, rows beyond
+// the batch zero) is staged once per tile from the warps' fragments into shared memory
+// in the same layout, all K columns (core matrix kc at kc * 128 bytes: 32 KB at K = 2048).
+// One thread issues each chunk's 16 MMAs (K = 16) into a 64 x 8 f32 accumulator in tensor
+// memory as soon as the chunk lands, and commits them to an mbarrier; a weight stage is
+// released once the MMAs that read it completed.  The accumulator's row m sits in lane
+// 32 (m / 16) + m % 16: warps 0-3 read 16 rows each.  useq counts the chunks committed in
+// this step (the mbarriers' phases).
+__device__ bool lm_umma_tile(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& useq, int nch, int ksw,
+                             const BFrag& fr, float rs_have, const int* T) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = lane >> 2, c = lane & 3;
+  uint8_t* bsm = reinterpret_cast<uint8_t*>(S.scratch);  // [K / 8][8 rows][16 bytes]
+  const uint32_t taddr = (uint32_t)S.small[5];
+  constexpr uint32_t kIdesc = umma_idesc_bf16(64, 8);
+  // the operand: warp w holds k16-steps ks = w + 8 j, columns 16 ks + 2 c (+1) and + 8 of
+  // token n, i.e. core matrices 2 ks and 2 ks + 1, row n, bytes 4 c
+#pragma unroll
+  for (int j = 0; j < kMaxKsw; ++j) {
+    if (j < ksw) {
+      const int ks = warp + 8 * j;
+      *reinterpret_cast<uint32_t*>(bsm + (2 * ks) * 128 + n * 16 + 4 * c) = fr.b0[j];
+      *reinterpret_cast<uint32_t*>(bsm + (2 * ks + 1) * 128 + n * 16 + 4 * c) = fr.b1[j];
+    }
+  }
+  fence_proxy_async_smem();
+  bar_sync_consumers();
+  bool ok = true;
+  for (int j = 0; j < nch; ++j) {
+    const uint32_t u = useq + (uint32_t)j;
+    if (tid == 0) {
+      // (after a failed wait the MMAs are skipped; the commit keeps the phases in step)
+      if (wait_full(p, S, cseq + j)) {
+        if (j == 0) trace_mark(p, S, 2);
+        tc_fence_after();
+        const uint32_t a0 = S.stage(cseq + j), b0 = S.scratch_s + (uint32_t)j * 4096;
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+          umma_bf16(taddr, umma_sdesc(a0 + s * 2048, 1024, 128), umma_sdesc(b0 + s * 256, 128, 128), kIdesc,
+                    j > 0 || s > 0);
+      }
+      umma_commit(S.mmadone(u & 1u));
+    }
+    if (j >= 1) {  // chunk j - 1's MMAs are done with its stage
+      ok = wait_mma(p, S, u - 1) && ok;
+      release_stage(S, cseq + j - 1);
+    }
+  }
+  if (nch >= 1) {
+    ok = wait_mma(p, S, useq + (uint32_t)nch - 1) && ok;
+    release_stage(S, cseq + nch - 1);
+  }
+  useq += (uint32_t)nch;
+  cseq += (uint32_t)nch;
+  trace_mark(p, S, 3);
+  tc_fence_after();
+  // epilogue: warps 0-3, lanes 0-15: row 16 w + lane of the tile, every token
+  float rs[8];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) rs[b] = __shfl_sync(0xffffffffu, rs_have, 4 * b);  // 1/rms of token b
+  if (warp < 4) {
+    float v[8];
+    tmem_ld8(taddr + ((uint32_t)(32 * warp) << 16), v);
+    const int r0 = T[D_ROW0] + 16 * warp + (lane & 15);
+    const bool mine = lane < 16 && r0 < p.V;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (b < p.B) {
+        const float x = v[b] * rs[b];
+        if (mine) p.logits[(size_t)b * p.V + r0] = x;
+        if (p.tok_out) {
+          unsigned long long best = mine ? argmax_key(x, r0) : 0ull;
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) {
+            const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+            best = y > best ? y : best;
+          }
+          if (lane == 0) atomicMax(p.amax + (size_t)(blockIdx.x % kAmaxReplicas) * p.B + b, best);
+        }
+      }
+    }
+  }
+  tc_fence_before();  // (the next tile's MMAs overwrite the accumulator after the caller's barrier)
+  return ok;
+}
+
 __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq,
-                                          const int* T, int ti, int nch, BFrag& fr, OperandKey& have,
-                                          float& rs_have) {
+                                          uint32_t& useq, const int* T, int ti, int nch, BFrag& fr,
+                                          OperandKey& have, float& rs_have) {
   const int op = T[D_OP];
   const int l = T[D_LAYER];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -1525,6 +1633,12 @@ __device__ __forceinline__ bool task_gemv(const Params& p, const Smem& S, uint32
       }
     }
     have = key;
+    if (MK_UMMA && op == OP_LMHEAD) {
+      const bool done = lm_umma_tile(p, S, cseq, useq, nch, ksw, fr, rs_have, T);
+      trace_mark(p, S, 12);
+      bar_sync_consumers();
+      return done;
+    }
     if (f8) {
       switch (nrb) {
         case 1: ran = gemv_run8<1, true>(p, S, cseq, nch, ksw, fr, v); break;
@@ -2234,6 +2348,7 @@ __device__ void task_embed(const Params& p, const Smem& S, uint32_t& sseq, int t
 // ============================================================== consumer loop
 __device__ void consumer(const Params& p, const Smem& S) {
   uint32_t cseq = 0, mseq = 0, sseq = 0;
+  uint32_t useq = 0;  // tensor-core chunk commits of this step (LM head on tcgen05)
   bool skip = false;
   BFrag fr;
   OperandKey have = {-1, -1, -1};
@@ -2313,7 +2428,7 @@ __device__ void consumer(const Params& p, const Smem& S) {
         break;
       }
       default:
-        ok = task_gemv(p, S, cseq, sseq, T, ent.x, nch, fr, have, rs_have);
+        ok = task_gemv(p, S, cseq, sseq, useq, T, ent.x, nch, fr, have, rs_have);
         break;
     }
     if (!ok) skip = true;
@@ -2331,6 +2446,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // multi-step decode: the generation word of the grid barrier between steps, read
   // before any CTA can advance it (the first advance waits for every CTA's arrival)
   if (threadIdx.x == 0 && p.n_steps > 1) S.small[250] = (int)ld_volatile(reinterpret_cast<const int*>(p.gen));
+  // tensor memory for the LM head's accumulator (32 columns; one CTA per SM)
+  if (MK_UMMA) {
+    if ((threadIdx.x >> 5) == 0) tmem_alloc(smem_u32(S.small + 5), 32);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   for (int step = 0; step < p.n_steps; ++step) {
     if (threadIdx.x == 0) {  // (re)initialised per step: no copy or arrival is pending here
       for (int s = 0; s < kStages; ++s) {
@@ -2344,6 +2466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < kSq; ++q) {
         mbar_init(S.sfull(q), kConsumerWarps);
         mbar_init(S.sempty(q), 1);
+      }
+      if (MK_UMMA) {
+        mbar_init(S.mmadone(0), 1);
+        mbar_init(S.mmadone(1), 1);
       }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -2457,9 +2583,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (S.small[251]) break;
   }
+  // every MMA and tensor-memory read of the launch has completed (waited in its task)
+  if (MK_UMMA) {
+    tc_fence_before();
+    __syncthreads();
+    if ((threadIdx.x >> 5) == 0) {
+      tc_fence_after();
+      tmem_dealloc((uint32_t)S.small[5], 32);
+    }
+  }
 }
 
-#if !MK_DET
+#if !MK_DET && !MK_UMMA
 // ============================================================== weight packer
 // Source of packed row r (see mk_pack_kernel): the matrix (0 = a, 1 = b, 2 = c) and its
 // row, or row -1 for a zero padding row.
@@ -2742,6 +2877,27 @@ cudaError_t launch_pack_moe_fp8(uint8_t* dst, const void* gate, const void* up, 
   return cudaGetLastError();
 }
 
+// LM-head tiles for the tensor-core path: 64-row tiles, each cut into chunks of 256
+// columns (32 KB, one ring stage), each chunk in the K-major core-matrix layout: core
+// matrix (kc, mg) -- rows 8 mg .. 8 mg + 7, columns 8 kc .. 8 kc + 7, 16 bytes a row --
+// at (kc * 8 + mg) * 128 bytes.  One thread per 16-byte core-matrix row; rows past
+// n_src_rows are zero.  K is a multiple of 256.
+__global__ void mk_pack_umma_kernel(uint8_t* __restrict__ dst, const uint16_t* __restrict__ src, int n_rows_packed,
+                                    int n_src_rows, int K) {
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int g8 = K / 8;
+  if (u >= (long long)n_rows_packed * g8) return;
+  const int r = (int)(u / g8), kk = (int)(u % g8);
+  const int tile = r / 64, m = r % 64, chunk = kk / 32, kc = kk % 32;
+  uint16_t e[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e[i] = r < n_src_rows ? src[(size_t)r * K + 8 * kk + i] : (uint16_t)0;
+  const size_t off = ((size_t)tile * (K / 256) + chunk) * 32768 + ((size_t)kc * 8 + m / 8) * 128 + (m % 8) * 16;
+  *reinterpret_cast<uint4*>(dst + off) =
+      make_uint4((uint32_t)e[0] | ((uint32_t)e[1] << 16), (uint32_t)e[2] | ((uint32_t)e[3] << 16),
+                 (uint32_t)e[4] | ((uint32_t)e[5] << 16), (uint32_t)e[6] | ((uint32_t)e[7] << 16));
+}
+
 __global__ void mk_convert_kernel(float* __restrict__ dst, const uint16_t* __restrict__ src, long long n) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) dst[i] = __uint_as_float((uint32_t)src[i] << 16);
@@ -2822,13 +2978,21 @@ cudaError_t launch_pack_moe(uint8_t* dst, const void* gate, const void* up, cons
   return cudaGetLastError();
 }
 
+cudaError_t launch_pack_umma(uint8_t* dst, const void* src, int n_rows_packed, int n_src_rows, int K, cudaStream_t st) {
+  const long long units = (long long)n_rows_packed * (K / 8);
+  if (units == 0) return cudaSuccess;
+  mk_pack_umma_kernel<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(dst, (const uint16_t*)src, n_rows_packed,
+                                                                      n_src_rows, K);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_convert(float* dst, const void* src, long long n, cudaStream_t st) {
   if (n == 0) return cudaSuccess;
   mk_convert_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(dst, (const uint16_t*)src, n);
   return cudaGetLastError();
 }
 
-#endif  // !MK_DET
+#endif  // !MK_DET && !MK_UMMA
 
 cudaError_t prepare_megakernel() {
   return cudaFuncSetAttribute(mk_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
