@@ -42,6 +42,10 @@ def parse_args():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--workload", default="pages_b1_8k")
     ap.add_argument("--mode", default="mega", choices=["mega", "perop", "graph"])
+    ap.add_argument("--deterministic", action="store_true",
+                    help="deterministic steps (fixed-point layer accumulators) for the main measurement")
+    ap.add_argument("--lm-umma", action="store_true",
+                    help="the LM head on the tcgen05 tensor cores (every handle of the run)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-baselines", action="store_true", help="skip per-op / graph arms")
     ap.add_argument("--no-bs8", action="store_true", help="skip the batch-8 ragged measurement")
@@ -179,7 +183,7 @@ def profiled_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
-def build_state(workload, seed, device):
+def build_state(workload, seed, device, deterministic=False):
     import torch
 
     import synth
@@ -190,6 +194,8 @@ def build_state(workload, seed, device):
     # a handle sized for the workload's batch where the packing depends on it (FP8 expert
     # items are 32 rows of d_ff below batch 4, 64 from 4 up)
     mk = B.Megakernel(cfg, W, max_batch=len(seq) if cfg.get("expert_dtype") == "fp8" else 8)
+    if deterministic:
+        mk.set_deterministic(True)
     st = plan_workload(mk, cfg, workload, seq, seed, device)
     return cfg, mk, st, W
 
@@ -396,7 +402,9 @@ def main():
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
     stream = torch.cuda.current_stream()
-    cfg, mk, st, W = build_state(args.workload, args.seed, device)
+    if args.lm_umma:
+        os.environ["MK_LM_UMMA"] = "1"  # read by mk_create
+    cfg, mk, st, W = build_state(args.workload, args.seed, device, deterministic=args.deterministic)
     B = len(st["seq"])
     full = args.workload == "pages_b1_8k"
     if not full:
@@ -440,7 +448,8 @@ def main():
     hbm = float(peaks["hbm_gbs"])
     launch_s = statistics.mean(per) / launches_per_step if args.mode != "mega" else statistics.mean(per)
     achieved = sb["total"] / statistics.mean(per) / 1e9
-    traffic = profiled_traffic(args.workload) if args.mode == "mega" else None
+    # (the committed DRAM counters were taken on the default kernel build)
+    traffic = profiled_traffic(args.workload) if args.mode == "mega" and not (args.deterministic or args.lm_umma) else None
     sol_tok = sol.sol_tok_s(sb["total"], hbm * 1e9, B)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -450,7 +459,9 @@ def main():
             "config": {"workload": args.workload, "batch": B, "seq_lens": st["seq"]
                        if B <= 8 else None, "mode": args.mode,
                        "l2": "per-step working set %.2f GB >> 129 MB L2; no flush" % (sb["total"] / 1e9),
-                       "parallelism": f"replicas x{ws}"},
+                       "parallelism": f"replicas x{ws}",
+                       **({"accumulators": "64-bit fixed point (deterministic)"} if args.deterministic else {}),
+                       **({"lm_head": "tcgen05"} if args.lm_umma else {})},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic,
