@@ -46,6 +46,8 @@ def parse_args():
                     help="deterministic steps (fixed-point layer accumulators) for the main measurement")
     ap.add_argument("--lm-umma", action="store_true",
                     help="the LM head on the tcgen05 tensor cores (every handle of the run)")
+    ap.add_argument("--ffn-umma", action="store_true",
+                    help="with --lm-umma: the bf16 expert and dense-FFN items on the tensor cores too")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-baselines", action="store_true", help="skip per-op / graph arms")
     ap.add_argument("--no-bs8", action="store_true", help="skip the batch-8 ragged measurement")
@@ -402,8 +404,11 @@ def main():
     device = f"cuda:{local}"
     torch.cuda.set_device(local)
     stream = torch.cuda.current_stream()
+    args.lm_umma = args.lm_umma or args.ffn_umma
     if args.lm_umma:
         os.environ["MK_LM_UMMA"] = "1"  # read by mk_create
+    if args.ffn_umma:
+        os.environ["MK_MOE_UMMA"] = "1"
     cfg, mk, st, W = build_state(args.workload, args.seed, device, deterministic=args.deterministic)
     B = len(st["seq"])
     full = args.workload == "pages_b1_8k"
@@ -461,7 +466,8 @@ def main():
                        "l2": "per-step working set %.2f GB >> 129 MB L2; no flush" % (sb["total"] / 1e9),
                        "parallelism": f"replicas x{ws}",
                        **({"accumulators": "64-bit fixed point (deterministic)"} if args.deterministic else {}),
-                       **({"lm_head": "tcgen05"} if args.lm_umma else {})},
+                       **({"lm_head": "tcgen05"} if args.lm_umma else {}),
+                       **({"ffn": "tcgen05"} if args.ffn_umma else {})},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "traffic": traffic,

@@ -134,7 +134,11 @@ typedef struct mk_error_info {
  * weight blob and repack every matrix into contiguous per-task tiles whose 16-byte
  * units are the mma.sync A-fragments in the order the consumer warps read them.
  * `stream` orders the packing kernels; the call synchronises it before returning.
- * On error *out is NULL.
+ * On error *out is NULL.  Two environment variables, read here, select the tensor-core
+ * build of the kernel: MK_LM_UMMA=1 packs the LM head in 64-row tiles in the tcgen05
+ * K-major core-matrix layout (bf16 projections, d_model a multiple of 256), and
+ * MK_MOE_UMMA=1 beside it does the same for the bf16 expert and dense-FFN items (32-row
+ * f-slices); MK_Q_TENSOR_CORES reports what took effect.
  * [Cohere Megakernel, "Getting started": the engine is a shared library
  *  (libmk_release.so) that the serving process loads together with the model's
  *  checkpoint; Cohere's Open-Source Megakernel Beats vLLM by 1.58x on H100, "One
@@ -353,7 +357,11 @@ int mk_read_weight_fp8(mk_handle* h, int matrix, int layer, void* host_out, size
 enum {
   MK_Q_NUM_SMS = 1, MK_Q_NUM_TASKS = 2, MK_Q_NUM_COUNTERS = 3, MK_Q_PACKED_BYTES = 4,
   MK_Q_MAX_ACTIVE = 5, MK_Q_SPLIT_PAGES = 6, MK_Q_SMEM_BYTES = 7, MK_Q_PEROP_LAUNCHES = 8,
-  MK_Q_THREADS = 9, MK_Q_STAGE_BYTES = 10, MK_Q_NUM_STAGES = 11
+  MK_Q_THREADS = 9, MK_Q_STAGE_BYTES = 10, MK_Q_NUM_STAGES = 11,
+  /* which GEMVs of the handle run on the tcgen05 tensor cores (fixed at mk_create by the
+   * environment): bit 0 the LM head (MK_LM_UMMA=1), bit 1 the bf16 expert and dense-FFN
+   * items (MK_MOE_UMMA=1 beside it); needs no plan */
+  MK_Q_TENSOR_CORES = 12
 };
 int mk_query(mk_handle* h, int what, int64_t* out);
 

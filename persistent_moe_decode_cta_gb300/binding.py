@@ -27,7 +27,7 @@ MK_READ_FINAL_COUNTERS, MK_READ_FINAL_QUEUES, MK_READ_TASKS = 9, 10, 11
 MK_EXPERT_BF16, MK_EXPERT_FP8, MK_WEIGHTS_FP8 = 0, 1, 2
 (MK_Q_NUM_SMS, MK_Q_NUM_TASKS, MK_Q_NUM_COUNTERS, MK_Q_PACKED_BYTES, MK_Q_MAX_ACTIVE,
  MK_Q_SPLIT_PAGES, MK_Q_SMEM_BYTES, MK_Q_PEROP_LAUNCHES, MK_Q_THREADS, MK_Q_STAGE_BYTES,
- MK_Q_NUM_STAGES) = range(1, 12)
+ MK_Q_NUM_STAGES, MK_Q_TENSOR_CORES) = range(1, 13)
 
 # exported symbols (kept equal to the declarations of include/mk.h)
 EXPORTS = ["mk_create", "mk_plan", "mk_decode_step", "mk_decode_steps", "mk_decode_step_host", "mk_decode_step_noalloc",

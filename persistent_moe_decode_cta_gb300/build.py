@@ -1,8 +1,8 @@
 """Build libmk.so (the C-ABI megakernel library) in-tree with nvcc for sm_103a.
 
-Two translation units (device code, host planner/ABI) compile in parallel, then
-link into persistent_moe_decode_cta_gb300/libmk.so with the CUDA runtime linked
-statically.  Usable as `python -m persistent_moe_decode_cta_gb300.build`.
+Four builds of the device code (default, deterministic, two tensor-core variants)
+and the host planner/ABI compile in parallel, then link into
+persistent_moe_decode_cta_gb300/libmk.so with the CUDA runtime linked statically.  Usable as `python -m persistent_moe_decode_cta_gb300.build`.
 """
 from __future__ import annotations
 
@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["mk_kernel.cu", "mk_kernel_det.cu", "mk_kernel_umma.cu", "mk_host.cpp"]
+SOURCES = ["mk_kernel.cu", "mk_kernel_det.cu", "mk_kernel_umma.cu", "mk_kernel_umma_ffn.cu", "mk_host.cpp"]
 
 
 def nvcc_path() -> str:

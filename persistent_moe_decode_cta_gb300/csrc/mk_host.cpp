@@ -47,6 +47,8 @@ cudaError_t launch_megakernel(const Params& p, const CUtensorMap& tk, const CUte
                               bool cooperative, cudaStream_t st);
 cudaError_t static_scratch_address(void** ptr);
 cudaError_t launch_pack_umma(uint8_t* dst, const void* src, int n_rows_packed, int n_src_rows, int K, cudaStream_t st);
+cudaError_t launch_pack_moe_umma(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+                                 cudaStream_t st);
 }  // namespace mk
 // the same megakernel with deterministic (64-bit fixed-point) layer accumulators
 namespace mk_det {
@@ -62,13 +64,21 @@ int megakernel_occupancy(int* blocks);
 cudaError_t launch_megakernel(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                               bool cooperative, cudaStream_t st);
 }  // namespace mk_umma
+// ... and with the bf16 expert and dense-FFN items on them too
+namespace mk_umma_ffn {
+cudaError_t prepare_megakernel();
+int megakernel_occupancy(int* blocks);
+cudaError_t launch_megakernel(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                              bool cooperative, cudaStream_t st);
+}  // namespace mk_umma_ffn
 
 namespace {
-// the kernel build a plan runs: deterministic accumulators, the tensor-core LM head, or
-// the default
+// the kernel build a plan runs: deterministic accumulators, the tensor-core LM head (and
+// FFN items), or the default
 cudaError_t launch_variant(const mk::Params& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid,
                            bool cooperative, cudaStream_t st) {
   if (p.det) return mk_det::launch_megakernel(p, tk, tv, grid, cooperative, st);
+  if (p.moe_umma) return mk_umma_ffn::launch_megakernel(p, tk, tv, grid, cooperative, st);
   if (p.lm_umma) return mk_umma::launch_megakernel(p, tk, tv, grid, cooperative, st);
   return mk::launch_megakernel(p, tk, tv, grid, cooperative, st);
 }
@@ -93,7 +103,8 @@ struct Shape {
   bool fp8d;            // QKV, O-proj and LM head as E4M3 codes + per-row f32 scales
   int esz;              // bytes of a QKV / O-proj / LM-head weight (2 bf16, 1 E4M3)
   int r_lm, v_pad, n_lm_tasks;
-  int lm_umma;  // LM head on the tensor cores (128-row tiles in the core-matrix layout)
+  int lm_umma;   // LM head on the tensor cores (64-row tiles in the core-matrix layout)
+  int moe_umma;  // ... and the bf16 expert / dense-FFN items (32-row f-slices)
   size_t qkv_layer_bytes, o_layer_bytes, router_layer_bytes, moe_item_bytes, moe_bytes_e, lm_bytes, embed_bytes;
   size_t dense_item_bytes;
   size_t off_qkv, off_o, off_router, off_moe, off_dense, off_lm, off_embed, total;
@@ -185,6 +196,10 @@ int derive_shape(const mk_config* c, Shape& s, std::string* err) {
   s.lm_umma = 0;
   if (const char* e = getenv("MK_LM_UMMA"))
     if (atoi(e) && !s.fp8d && s.d % 256 == 0 && s.d / 128 <= kMaxKsw) { s.lm_umma = 1; s.r_lm = 64; }
+  // MK_MOE_UMMA=1 beside it: the bf16 expert and dense-FFN items (32-row f-slices) too
+  s.moe_umma = 0;
+  if (const char* e = getenv("MK_MOE_UMMA"))
+    if (atoi(e) && s.lm_umma && !s.fp8 && s.moe_fs == 32 && s.dense_fs == 32) s.moe_umma = 1;
   s.v_pad = (s.V + s.r_lm - 1) / s.r_lm * s.r_lm; s.n_lm_tasks = s.v_pad / s.r_lm;
   s.qkv_layer_bytes = (size_t)s.Hkv * s.qkv_rows_group * s.d * s.esz;
   s.o_layer_bytes = (size_t)s.Hkv * s.d * s.k_o * s.esz;
@@ -710,6 +725,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
   e = prepare_megakernel();
   if (e == cudaSuccess) e = mk_det::prepare_megakernel();
   if (e == cudaSuccess) e = mk_umma::prepare_megakernel();
+  if (e == cudaSuccess) e = mk_umma_ffn::prepare_megakernel();
   if (e != cudaSuccess) { cuda_fail(h, e, "cudaFuncSetAttribute"); return bail(MK_ERR_CUDA); }
   e = cudaMalloc(&h->wblob, s.total);
   if (e != cudaSuccess) { fail(&h->err, MK_ERR_OOM, "packed weights (%zu B): %s", s.total, cudaGetErrorString(e)); return bail(MK_ERR_OOM); }
@@ -776,8 +792,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
     }
     if (s.dense(l)) {  // mixed stack: the layer's FFN in the dense region, no router or experts
       const int rank = __builtin_popcountll(s.dense_mask & ((1ull << l) - 1ull));  // dense layers before l
-      e = launch_pack_moe(h->wblob + s.off_dense + (size_t)rank * s.t_dense * s.dense_item_bytes, w->ffn_gate[l],
-                          w->ffn_up[l], w->ffn_down[l], d, s.f_dense, s.dense_fs, st);
+      uint8_t* dd = h->wblob + s.off_dense + (size_t)rank * s.t_dense * s.dense_item_bytes;
+      e = s.moe_umma ? launch_pack_moe_umma(dd, w->ffn_gate[l], w->ffn_up[l], w->ffn_down[l], d, s.f_dense, st)
+                     : launch_pack_moe(dd, w->ffn_gate[l], w->ffn_up[l], w->ffn_down[l], d, s.f_dense, s.dense_fs, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "pack dense FFN"); return bail(MK_ERR_CUDA); }
       e = launch_convert(h->norms + (size_t)l * d, w->attn_norm[l], d, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "convert"); return bail(MK_ERR_CUDA); }
@@ -789,6 +806,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
       const int i = l * E + e2;
       e = s.fp8 ? launch_pack_moe_fp8(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i],
                                       w->w_down[i], d, f, s.moe_fs, (long long)s.moe_item_bytes, st)
+                : s.moe_umma ? launch_pack_moe_umma(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i],
+                                                    w->w_up[i], w->w_down[i], d, f, st)
                 : launch_pack_moe(h->wblob + s.off_moe + (size_t)i * s.moe_bytes_e, w->w_gate[i], w->w_up[i],
                                   w->w_down[i], d, f, s.moe_fs, st);
       if (e != cudaSuccess) { cuda_fail(h, e, "pack moe"); return bail(MK_ERR_CUDA); }
@@ -873,6 +892,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   if (r) return r;
   int occ = 0;
   if (h->det) mk_det::megakernel_occupancy(&occ);
+  else if (h->s.moe_umma) mk_umma_ffn::megakernel_occupancy(&occ);
   else if (h->s.lm_umma) mk_umma::megakernel_occupancy(&occ);
   else megakernel_occupancy(&occ);
   if (occ < 1) return fail(&h->err, MK_ERR_UNSUPPORTED, "megakernel cannot be resident (occupancy %d)", occ);
@@ -922,6 +942,7 @@ int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host, const int32_t
   p.fp8 = s.fp8 ? 1 : 0;
   p.fp8d = s.fp8d ? 1 : 0;
   p.lm_umma = s.lm_umma;
+  p.moe_umma = s.moe_umma;
   p.qkv_rows_group = s.qkv_rows_group;
   p.qkv_scale = reinterpret_cast<const float*>(h->wblob + s.off_qkv_scale);
   p.o_scale = reinterpret_cast<const float*>(h->wblob + s.off_o_scale);
@@ -1442,6 +1463,7 @@ int mk_query(mk_handle* h, int what, int64_t* out) {
   switch (what) {
     case MK_Q_NUM_SMS: *out = h->n_sm; return MK_OK;
     case MK_Q_PACKED_BYTES: *out = (int64_t)h->s.total; return MK_OK;
+    case MK_Q_TENSOR_CORES: *out = (h->s.lm_umma ? 1 : 0) | (h->s.moe_umma ? 2 : 0); return MK_OK;
     default: break;
   }
   if (!h->planned) return fail(&h->err, MK_ERR_STATE, "mk_plan has not been called");

@@ -140,6 +140,7 @@ struct Params {
   // the K-major core-matrix layout, accumulated in tensor memory (tcgen05.mma); selects
   // the kernel build compiled with MK_UMMA
   int lm_umma;
+  int moe_umma;  // (in that build) the bf16 expert and dense-FFN items on tcgen05 too
   // deterministic accumulation: the layer accumulators `moe` hold 64-bit fixed-point
   // integers (32 fraction bits) added with integer reductions, so that their sums, and
   // everything downstream, do not depend on the order of the expert and O-proj adds

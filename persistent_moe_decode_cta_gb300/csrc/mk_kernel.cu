@@ -21,11 +21,13 @@
 
 #include "mk_device.cuh"
 
-// This file is compiled three times: as is (float32 layer accumulators, the LM head on
+// This file is compiled four times: as is (float32 layer accumulators, every GEMV on
 // mma.sync), by mk_kernel_det.cu with MK_DET = 1 (deterministic steps: 64-bit
-// fixed-point accumulators; namespace mk_det), and by mk_kernel_umma.cu with MK_UMMA = 1
+// fixed-point accumulators; namespace mk_det), by mk_kernel_umma.cu with MK_UMMA = 1
 // (the LM head on tcgen05 tensor cores with a tensor-memory accumulator; namespace
-// mk_umma).  The weight packers and the static step scratch exist in the first build only.
+// mk_umma) and by mk_kernel_umma_ffn.cu with MK_UMMA = 2 (the bf16 expert and dense-FFN
+// items on them too; namespace mk_umma_ffn).  The weight packers and the static step
+// scratch exist in the first build only.
 #ifndef MK_DET
 #define MK_DET 0
 #endif
@@ -37,6 +39,8 @@
 #endif
 #if MK_DET
 #define MK_KNS mk_det
+#elif MK_UMMA == 2
+#define MK_KNS mk_umma_ffn
 #elif MK_UMMA
 #define MK_KNS mk_umma
 #else
@@ -1456,24 +1460,58 @@ __device__ __forceinline__ bool wait_mma(const Params& p, const Smem& S, uint32_
   return false;
 }
 
+// A ring chunk consumed by tcgen05 MMAs: every consumer thread waits for it to land;
+// thread 0 issues the MMAs (issue(stage address)) and commits them to the stage's empty
+// barrier, which then completes once they have read it; warps 1-7 arrive there at once
+// (their share of the release).  Nothing waits for the MMAs here.
+template <class Issue>
+__device__ __forceinline__ bool umma_chunk(const Params& p, const Smem& S, uint32_t seq, Issue issue) {
+  const bool ok = wait_full(p, S, seq);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    if (ok) {
+      tc_fence_after();
+      issue(S.stage(seq));
+    }
+    umma_commit(S.empty(seq % kStages));
+  } else if (warp > 0) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_relaxed(S.empty(seq % kStages));
+  }
+  return ok;
+}
+
+// Thread 0 commits every MMA issued so far to the phase-end mbarrier number u (two,
+// alternating); every consumer thread waits for it.
+__device__ __forceinline__ bool umma_phase_end(const Params& p, const Smem& S, uint32_t& u) {
+  if (threadIdx.x == 0) umma_commit(S.mmadone(u & 1u));
+  const bool ok = wait_mma(p, S, u);
+  ++u;
+  tc_fence_after();
+  return ok;
+}
+
 // LM_HEAD tile of 64 rows on the 5th-generation tensor cores (the MK_UMMA build).  Every
 // 32 KB weight chunk holds the tile's 64 rows x 256 columns in the K-major core-matrix
-// layout (core matrix (kc, mg) -- rows 8 mg .. 8 mg + 7, columns 8 kc .. 8 kc + 7, 16
-// bytes a row -- at (kc * 8 + mg) * 128 bytes).  The tokens' operand (N = 8, rows beyond
-// the batch zero) is staged once per tile from the warps' fragments into shared memory
-// in the same layout, all K columns (core matrix kc at kc * 128 bytes: 32 KB at K = 2048).
-// One thread issues each chunk's 16 MMAs (K = 16) into a 64 x 8 f32 accumulator in tensor
-// memory as soon as the chunk lands, and commits them to an mbarrier; a weight stage is
-// released once the MMAs that read it completed.  The accumulator's row m sits in lane
-// 32 (m / 16) + m % 16: warps 0-3 read 16 rows each.  useq counts the chunks committed in
-// this step (the mbarriers' phases).
+// layout with the second 128 columns stacked under the first as rows 64..127 (core
+// matrix (kc, mg): rows 8 mg .. 8 mg + 7 of that stacking, columns 8 kc .. 8 kc + 7 of
+// its half, 16 bytes a row, at (kc * 16 + mg) * 128 bytes), so that every MMA has
+// M = 128: an MMA costs about the same time for any N up to 64.  The tokens' operand is
+// staged once per tile from the warps' fragments into shared memory (core matrix kc of
+// the K columns at kc * 128 bytes, rows beyond the batch zero) and read as N = 16 rows:
+// rows 0-7 the chunk's first-half columns, rows 8-15 its second-half ones (2048 bytes
+// on).  One thread issues each chunk's 8 MMAs (K = 16) into a 128 x 16 f32 accumulator
+// in tensor memory as soon as the chunk lands, committing them to the stage's release;
+// row m of the tile is D[m][n] + D[64 + m][8 + n].  Warps 2-3 hand the second-half sums
+// to warps 0-1 through shared memory, whose lanes then hold one row each.  useq counts
+// the phase-end commits of this step (the mbarriers' phases).
 __device__ bool lm_umma_tile(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& useq, int nch, int ksw,
                              const BFrag& fr, float rs_have, const int* T) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = lane >> 2, c = lane & 3;
   uint8_t* bsm = reinterpret_cast<uint8_t*>(S.scratch);  // [K / 8][8 rows][16 bytes]
   const uint32_t taddr = (uint32_t)S.small[5];
-  constexpr uint32_t kIdesc = umma_idesc_bf16(64, 8);
+  constexpr uint32_t kIdesc = umma_idesc_bf16(128, 16);
   // the operand: warp w holds k16-steps ks = w + 8 j, columns 16 ks + 2 c (+1) and + 8 of
   // token n, i.e. core matrices 2 ks and 2 ks + 1, row n, bytes 4 c
 #pragma unroll
@@ -1488,51 +1526,44 @@ __device__ bool lm_umma_tile(const Params& p, const Smem& S, uint32_t& cseq, uin
   bar_sync_consumers();
   bool ok = true;
   for (int j = 0; j < nch; ++j) {
-    const uint32_t u = useq + (uint32_t)j;
-    if (tid == 0) {
-      // (after a failed wait the MMAs are skipped; the commit keeps the phases in step)
-      if (wait_full(p, S, cseq + j)) {
-        if (j == 0) trace_mark(p, S, 2);
-        tc_fence_after();
-        const uint32_t a0 = S.stage(cseq + j), b0 = S.scratch_s + (uint32_t)j * 4096;
+    const uint32_t b0 = S.scratch_s + (uint32_t)j * 4096;
+    ok = umma_chunk(p, S, cseq + j, [&](uint32_t a0) {
+      if (j == 0) trace_mark(p, S, 2);
 #pragma unroll
-        for (int s = 0; s < 16; ++s)
-          umma_bf16(taddr, umma_sdesc(a0 + s * 2048, 1024, 128), umma_sdesc(b0 + s * 256, 128, 128), kIdesc,
-                    j > 0 || s > 0);
-      }
-      umma_commit(S.mmadone(u & 1u));
-    }
-    if (j >= 1) {  // chunk j - 1's MMAs are done with its stage
-      ok = wait_mma(p, S, u - 1) && ok;
-      release_stage(S, cseq + j - 1);
-    }
+      for (int s = 0; s < 8; ++s)
+        umma_bf16(taddr, umma_sdesc(a0 + s * 4096, 2048, 128), umma_sdesc(b0 + s * 256, 128, 2048), kIdesc,
+                  j > 0 || s > 0);
+    }) && ok;
   }
-  if (nch >= 1) {
-    ok = wait_mma(p, S, useq + (uint32_t)nch - 1) && ok;
-    release_stage(S, cseq + nch - 1);
-  }
-  useq += (uint32_t)nch;
   cseq += (uint32_t)nch;
+  ok = umma_phase_end(p, S, useq) && ok;
   trace_mark(p, S, 3);
-  tc_fence_after();
-  // epilogue: warps 0-3, lanes 0-15: row 16 w + lane of the tile, every token
+  // epilogue (the operand is no longer read: its first 2 KB take the second-half sums)
   float rs[8];
 #pragma unroll
   for (int b = 0; b < 8; ++b) rs[b] = __shfl_sync(0xffffffffu, rs_have, 4 * b);  // 1/rms of token b
-  if (warp < 4) {
+  float* xch = S.scratch;  // [8 tokens][64 rows]
+  if (warp == 2 || warp == 3) {
+    float v[8];
+    tmem_ld8(taddr + 8 + ((uint32_t)(32 * warp) << 16), v);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) xch[b * 64 + 32 * (warp - 2) + lane] = v[b];
+  }
+  bar_sync_consumers();
+  if (warp < 2) {
     float v[8];
     tmem_ld8(taddr + ((uint32_t)(32 * warp) << 16), v);
-    const int r0 = T[D_ROW0] + 16 * warp + (lane & 15);
-    const bool mine = lane < 16 && r0 < p.V;
+    const int r0 = T[D_ROW0] + 32 * warp + lane;
+    const bool mine = r0 < p.V;
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       if (b < p.B) {
-        const float x = v[b] * rs[b];
+        const float x = (v[b] + xch[b * 64 + 32 * warp + lane]) * rs[b];
         if (mine) p.logits[(size_t)b * p.V + r0] = x;
         if (p.tok_out) {
           unsigned long long best = mine ? argmax_key(x, r0) : 0ull;
 #pragma unroll
-          for (int o = 8; o > 0; o >>= 1) {
+          for (int o = 16; o > 0; o >>= 1) {
             const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
             best = y > best ? y : best;
           }
@@ -1997,6 +2028,179 @@ __device__ __forceinline__ bool task_moe(const Params& p, const Smem& S, uint32_
   return true;
 }
 
+// One MoE item (bf16, 32-row f-slice) on the 5th-generation tensor cores (the MK_UMMA = 2
+// build, with items packed by mk_pack_moe_umma_kernel).  An MMA costs about the same
+// time for any N up to 64, so every MMA here has M = 128 (twice the weight bytes of
+// M = 64 per instruction).  Phase 1: each 32 KB gate/up chunk holds 64 packed rows x 256
+// columns with the second 128 columns stacked under the first as rows 64..127; the
+// operand (N = 16) pairs them block-diagonally -- rows 0-7 the tokens' first-half
+// columns, rows 8-15 their second-half columns -- so that 8 MMAs a chunk accumulate
+// D[m][n] (first half, m < 64, n < 8) and D[64 + m][8 + n] (second half) into tensor
+// memory columns 256..271 as soon as the chunk lands.  SwiGLU: warps 2-3 hand the
+// second-half sums to warps 0-1 through shared memory; lane l of warp w holds packed row
+// 32 w + l (gate rows at l % 16 < 8, their up rows 8 lanes above) and writes
+// silu(gate) * up (bf16) as the phase-2 operand (K = 32; rows 8-15 zero).  Phase 2:
+// every 128-row block of the down slice (8 KB; a chunk holds several) gets 2 MMAs into
+// its own 128 x 16 accumulator (block j: columns 16 j; columns 8-15 unused).  Epilogue:
+// warp w reads quadrant w % 4 of the blocks j = w / 4 mod 2, scales by the tokens'
+// routing weights and adds them into the layer accumulator with 128-bit reductions.
+// Stages go back to the producer once the MMAs that read them completed.
+__device__ bool task_moe_umma(const Params& p, const Smem& S, uint32_t& cseq, uint32_t& sseq, uint32_t& useq, int l,
+                              bool dense, int item, int nch, int ntok, int tok_lo, int tok_hi, int4 w_lo, int4 w_hi,
+                              BFrag& fr, OperandKey& have, float& rs_have) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n8 = lane >> 2, c = lane & 3;
+  const int a_slot = dense ? 0 : item / p.t_moe;
+  const OperandKey key = {3, l, a_slot};
+  trace_mark(p, S, 1);
+  auto tok_byte = [&](int n) { return ((n < 4 ? tok_lo : tok_hi) >> (8 * (n & 3))) & 0xff; };
+  const int ksw1 = p.d / 128;
+  if (!(key == have)) {
+    rs_have = build_norm_bfrag(p, S, fr, ksw1, l, (n8 < ntok) ? (tok_byte(n8) >> 3) : -1);
+    have = key;
+  }
+  uint8_t* sm = reinterpret_cast<uint8_t*>(S.scratch);
+  const uint32_t taddr = (uint32_t)S.small[5];
+  constexpr uint32_t kIdesc = umma_idesc_bf16(128, 16);
+  // ---- phase 1 operand: warp w's k16-steps ks = w + 8 j -> core matrices 2 ks, 2 ks + 1
+  //      (core kc of the K columns at kc * 128 bytes, 8 token rows of 16 bytes)
+#pragma unroll
+  for (int j = 0; j < kMaxKsw; ++j) {
+    if (j < ksw1) {
+      const int ks = warp + 8 * j;
+      *reinterpret_cast<uint32_t*>(sm + (2 * ks) * 128 + n8 * 16 + 4 * c) = fr.b0[j];
+      *reinterpret_cast<uint32_t*>(sm + (2 * ks + 1) * 128 + n8 * 16 + 4 * c) = fr.b1[j];
+    }
+  }
+  fence_proxy_async_smem();
+  bar_sync_consumers();
+  bool ok = true;
+  const int nch1 = p.d / 256;
+  for (int j = 0; j < nch1; ++j) {
+    // k-step s: weight cores (kc, mg) at s * 4096 (K-adjacent 2048 apart, row groups 128);
+    // operand: first-half cores 32 j + 2 s (+1), second-half ones 16 cores (2048 B) on
+    const uint32_t b0 = S.scratch_s + (uint32_t)j * 4096;
+    ok = umma_chunk(p, S, cseq + j, [&](uint32_t a0) {
+      if (j == 0) trace_mark(p, S, 2);
+      if (j == nch1 - 1) trace_mark(p, S, 11);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        umma_bf16(taddr + 256, umma_sdesc(a0 + k * 4096, 2048, 128), umma_sdesc(b0 + k * 256, 128, 2048), kIdesc,
+                  j > 0 || k > 0);
+    }) && ok;
+  }
+  cseq += (uint32_t)nch1;
+  ok = umma_phase_end(p, S, useq) && ok;
+  trace_mark(p, S, 12);
+  // ---- SwiGLU into the phase-2 operand: element (token n, f) at (f / 8) * 128 + n * 16 +
+  //      (f % 8) * 2; rows 8-15 (512 bytes on) zero
+  float rs[8];
+#pragma unroll
+  for (int b = 0; b < 8; ++b) rs[b] = __shfl_sync(0xffffffffu, rs_have, 4 * b);  // 1/rms of token slot b
+  float* xch = reinterpret_cast<float*>(sm + 4096);  // [8 tokens][64 rows]: second-half sums
+  if (warp == 2 || warp == 3) {
+    float v[8];
+    tmem_ld8(taddr + 256 + 8 + ((uint32_t)(32 * warp) << 16), v);
+#pragma unroll
+    for (int n = 0; n < 8; ++n) xch[n * 64 + 32 * (warp - 2) + lane] = v[n];
+  } else if (warp == 4) {
+    for (int i = lane; i < 128; i += 32) reinterpret_cast<uint32_t*>(sm + 512)[i] = 0u;
+  }
+  bar_sync_consumers();
+  if (warp < 2) {
+    float v[8];
+    tmem_ld8(taddr + 256 + ((uint32_t)(32 * warp) << 16), v);
+    const int f = 16 * warp + 8 * (lane >> 4) + (lane & 7);  // gate row of this lane's pair
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const float x = v[n] + xch[n * 64 + 32 * warp + lane];
+      const float upv = __shfl_down_sync(0xffffffffu, x, 8);
+      if ((lane & 8) == 0) {
+        const float gt = x * rs[n], upr = upv * rs[n];
+        const float a = (n < ntok) ? gt / (1.f + __expf(-gt)) * upr : 0.f;
+        *reinterpret_cast<uint16_t*>(sm + (f >> 3) * 128 + n * 16 + (f & 7) * 2) = to_bf16(a);
+      }
+    }
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  bar_sync_consumers();
+  trace_mark(p, S, 13);
+  // ---- phase 2: 128-row blocks of the down slice, each into its own accumulator
+  const int region = (p.d / 128) * 2 * kFragBytes;
+  const int bpc = moe_warps_per_chunk(region) * region / 8192;  // blocks a chunk
+  const int nblk = p.d / 128;
+  const int nch2 = nch - nch1;
+  for (int j = 0; j < nch2; ++j) {
+    ok = umma_chunk(p, S, cseq + j, [&](uint32_t a0) {
+      if (j == 0) trace_mark(p, S, 8);
+      if (j == nch2 - 1) trace_mark(p, S, 10);
+      for (int bb = 0; bb < bpc; ++bb) {
+        const int blk = j * bpc + bb;
+        if (blk < nblk) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            umma_bf16(taddr + 16 * blk, umma_sdesc(a0 + bb * 8192 + k * 4096, 2048, 128),
+                      umma_sdesc(S.scratch_s + k * 256, 128, 512), kIdesc, k > 0);
+        }
+      }
+    }) && ok;
+  }
+  cseq += (uint32_t)nch2;
+  ok = umma_phase_end(p, S, useq) && ok;
+  trace_mark(p, S, 9);
+  // ---- epilogue: weighted block outputs into the layer accumulator
+  const int wbits[8] = {w_lo.x, w_lo.y, w_lo.z, w_lo.w, w_hi.x, w_hi.y, w_hi.z, w_hi.w};
+  constexpr int kStg = 36;                                              // row stride of a token
+  float* stg = reinterpret_cast<float*>(sm + 4096) + warp * 8 * kStg;  // [8 tokens][32 rows]
+  const int q = warp & 3;
+  const int r4 = (lane & 7) * 4;  // flush: 4 rows of tokens lane / 8 and lane / 8 + 4
+  float wn[2];
+  int bn[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int nt = (lane >> 3) + 4 * h;
+    int wb = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) wb = (k == nt) ? wbits[k] : wb;
+    wn[h] = nt < ntok ? __int_as_float(wb) : 0.f;
+    bn[h] = nt < ntok ? (tok_byte(nt) >> 3) : 0;
+  }
+  for (int b4 = warp >> 2; b4 < nblk; b4 += 8) {
+    uint32_t v[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (b4 + 2 * i < nblk) tmem_ld8_async(taddr + 16 * (b4 + 2 * i) + ((uint32_t)(32 * q) << 16), v[i]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int blk = b4 + 2 * i;
+      if (blk < nblk) {
+#pragma unroll
+        for (int n = 0; n < 8; ++n) stg[n * kStg + lane] = __uint_as_float(v[i][n]);
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int nt = (lane >> 3) + 4 * h;
+          if (nt < ntok) {
+            const float4 x = *reinterpret_cast<const float4*>(stg + nt * kStg + r4);
+            acc_add4(p, ((size_t)l * p.B + bn[h]) * p.d + 128 * blk + 32 * q + r4,
+                     make_float4(wn[h] * x.x, wn[h] * x.y, wn[h] * x.z, wn[h] * x.w));
+          }
+        }
+        __syncwarp();
+      }
+    }
+  }
+  tc_fence_before();
+  trace_mark(p, S, 3);
+  signal_async(p, S, sseq, C_MD(p, l), 1u);
+  trace_mark(p, S, 14);
+  bar_sync_consumers();
+  trace_mark(p, S, 15);
+  return ok;
+}
+
 // ============================================================== attention
 // Address of the 16-byte chunk `ch` (8 dims) of key row `key` inside a page of the
 // stage, as the tensor-map copy lays it out: 16 keys x hd dims, row-major, cut into
@@ -2415,6 +2619,11 @@ __device__ void consumer(const Params& p, const Smem& S) {
       case OP_MOE_DRAIN: {
         // (a dense layer's FFN items: bf16 f-slices of dense_fs rows)
         const int fsi = aux1 ? p.dense_fs : p.moe_fs;
+        if (MK_UMMA == 2 && p.moe_umma) {
+          ok = task_moe_umma(p, S, cseq, sseq, useq, wl, aux1, ent.y, nch, ent.w, ent2.x, ent2.y, ew_lo, ew_hi, fr,
+                             have, rs_have);
+          break;
+        }
         ok = (p.fp8 && !aux1)
                  ? (p.moe_fs == 64 ? task_moe<64, true>(p, S, cseq, sseq, wl, aux1, ent.x, ent.y, nch, ent.w, ent2.x,
                                                            ent2.y, ew_lo, ew_hi, fr, have, rs_have)
@@ -2446,9 +2655,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // multi-step decode: the generation word of the grid barrier between steps, read
   // before any CTA can advance it (the first advance waits for every CTA's arrival)
   if (threadIdx.x == 0 && p.n_steps > 1) S.small[250] = (int)ld_volatile(reinterpret_cast<const int*>(p.gen));
-  // tensor memory for the LM head's accumulator (32 columns; one CTA per SM)
+  // tensor memory for the LM head's and the expert items' accumulators (all 512
+  // columns; one CTA per SM)
   if (MK_UMMA) {
-    if ((threadIdx.x >> 5) == 0) tmem_alloc(smem_u32(S.small + 5), 32);
+    if ((threadIdx.x >> 5) == 0) tmem_alloc(smem_u32(S.small + 5), 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -2589,7 +2799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if ((threadIdx.x >> 5) == 0) {
       tc_fence_after();
-      tmem_dealloc((uint32_t)S.small[5], 32);
+      tmem_dealloc((uint32_t)S.small[5], 512);
     }
   }
 }
@@ -2878,21 +3088,61 @@ cudaError_t launch_pack_moe_fp8(uint8_t* dst, const void* gate, const void* up, 
 }
 
 // LM-head tiles for the tensor-core path: 64-row tiles, each cut into chunks of 256
-// columns (32 KB, one ring stage), each chunk in the K-major core-matrix layout: core
-// matrix (kc, mg) -- rows 8 mg .. 8 mg + 7, columns 8 kc .. 8 kc + 7, 16 bytes a row --
-// at (kc * 8 + mg) * 128 bytes.  One thread per 16-byte core-matrix row; rows past
-// n_src_rows are zero.  K is a multiple of 256.
+// columns (32 KB, one ring stage), each chunk in the K-major core-matrix layout with its
+// second 128 columns stacked under the first as rows 64..127: core matrix (kc, mg) --
+// rows 8 mg .. 8 mg + 7 of the stacking, columns 8 kc .. 8 kc + 7 of its half, 16 bytes
+// a row -- at (kc * 16 + mg) * 128 bytes.  One thread per 16-byte core-matrix row; rows
+// past n_src_rows are zero.  K is a multiple of 256.
 __global__ void mk_pack_umma_kernel(uint8_t* __restrict__ dst, const uint16_t* __restrict__ src, int n_rows_packed,
                                     int n_src_rows, int K) {
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int g8 = K / 8;
   if (u >= (long long)n_rows_packed * g8) return;
   const int r = (int)(u / g8), kk = (int)(u % g8);
-  const int tile = r / 64, m = r % 64, chunk = kk / 32, kc = kk % 32;
+  const int tile = r / 64, m = r % 64, chunk = kk / 32, kc = kk % 16, mg = m / 8 + 8 * ((kk % 32) / 16);
   uint16_t e[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) e[i] = r < n_src_rows ? src[(size_t)r * K + 8 * kk + i] : (uint16_t)0;
-  const size_t off = ((size_t)tile * (K / 256) + chunk) * 32768 + ((size_t)kc * 8 + m / 8) * 128 + (m % 8) * 16;
+  const size_t off = ((size_t)tile * (K / 256) + chunk) * 32768 + ((size_t)kc * 16 + mg) * 128 + (m % 8) * 16;
+  *reinterpret_cast<uint4*>(dst + off) =
+      make_uint4((uint32_t)e[0] | ((uint32_t)e[1] << 16), (uint32_t)e[2] | ((uint32_t)e[3] << 16),
+                 (uint32_t)e[4] | ((uint32_t)e[5] << 16), (uint32_t)e[6] | ((uint32_t)e[7] << 16));
+}
+
+// Expert items (bf16, 32-row f-slices) for the tensor-core path, item s of an expert:
+// [gate/up: 64 packed rows x d] then [down: d rows x 32].  Packed row 16 rb + i is gate
+// row 32 s + 8 rb + i (i < 8) or its up row (i >= 8), so that the pair sits 8 lanes apart
+// in one warp's lane quadrant of the accumulator.  The gate/up rows come in chunks of
+// 256 columns (32 KB) laid out like the LM-head chunks (the second 128 columns stacked
+// under the first as rows 64..127; core (kc, mg) at (kc * 16 + mg) * 128 bytes), the down
+// rows in blocks of 128 rows (8 KB, core (kc, mg) at (kc * 16 + mg) * 128 bytes).  One
+// thread per 16-byte core row.
+__global__ void mk_pack_moe_umma_kernel(uint8_t* __restrict__ dst, const uint16_t* __restrict__ gate,
+                                        const uint16_t* __restrict__ up, const uint16_t* __restrict__ down, int d,
+                                        int f) {
+  constexpr int FS = 32;
+  const long long per_item = 12LL * d;  // 64 rows x d/8 + d rows x 4 core rows
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= per_item * (f / FS)) return;
+  const int s = (int)(u / per_item);
+  const long long r = u % per_item;
+  const uint16_t* src;
+  size_t off = (size_t)s * 192 * d;  // item bytes
+  if (r < 8LL * d) {
+    const int m = (int)(r / (d / 8)), kk = (int)(r % (d / 8));
+    const int rb = m / 16, i = m % 16;
+    const int frow = FS * s + 8 * rb + (i & 7);
+    src = (i < 8 ? gate : up) + (size_t)frow * d + 8 * kk;
+    off += (size_t)(kk / 32) * 32768 + ((size_t)(kk % 16) * 16 + m / 8 + 8 * ((kk % 32) / 16)) * 128 + (m % 8) * 16;
+  } else {
+    const long long q = r - 8LL * d;
+    const int row = (int)(q / 4), kk = (int)(q % 4);
+    src = down + (size_t)row * f + FS * s + 8 * kk;
+    off += (size_t)128 * d + (size_t)(row / 128) * 8192 + ((size_t)kk * 16 + (row % 128) / 8) * 128 + (row % 8) * 16;
+  }
+  uint16_t e[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e[i] = src[i];
   *reinterpret_cast<uint4*>(dst + off) =
       make_uint4((uint32_t)e[0] | ((uint32_t)e[1] << 16), (uint32_t)e[2] | ((uint32_t)e[3] << 16),
                  (uint32_t)e[4] | ((uint32_t)e[5] << 16), (uint32_t)e[6] | ((uint32_t)e[7] << 16));
@@ -2983,6 +3233,14 @@ cudaError_t launch_pack_umma(uint8_t* dst, const void* src, int n_rows_packed, i
   if (units == 0) return cudaSuccess;
   mk_pack_umma_kernel<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(dst, (const uint16_t*)src, n_rows_packed,
                                                                       n_src_rows, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_moe_umma(uint8_t* dst, const void* gate, const void* up, const void* down, int d, int f,
+                                 cudaStream_t st) {
+  const long long units = 12LL * d * (f / 32);
+  mk_pack_moe_umma_kernel<<<(unsigned)((units + 255) / 256), 256, 0, st>>>(
+      dst, (const uint16_t*)gate, (const uint16_t*)up, (const uint16_t*)down, d, f);
   return cudaGetLastError();
 }
 

@@ -1,9 +1,11 @@
-"""The LM head on the 5th-generation tensor cores (MK_LM_UMMA=1 at mk_create): 64-row
-tiles whose weight chunks sit in shared memory in the K-major core-matrix layout, the
-tokens' operand staged beside them, tcgen05.mma into a 64 x 8 f32 accumulator in tensor
-memory, read back with tcgen05.ld.  Through the C ABI against the oracle: whole
-steps (batch 1 and ragged batch 8, megakernel / per-op / graph), greedy multi-step
-launches, and the pages-scale LM head on the GPU's own final hidden state."""
+"""The tensor-core build (MK_LM_UMMA=1 at mk_create, and MK_MOE_UMMA=1 beside it): the
+LM head's 64-row tiles and, with the second, the bf16 expert / dense-FFN items (32-row
+f-slices), their weight chunks in shared memory in the K-major core-matrix layout, the
+tokens' operands staged beside them, tcgen05.mma (M = 128) into f32 accumulators in
+tensor memory, read back with tcgen05.ld (FP8 expert items stay on mma.sync).  Through
+the C ABI against the oracle: whole steps (batch 1 and ragged batch 8, megakernel /
+per-op / graph, MoE and dense FFN layers), greedy multi-step launches, and the
+pages-scale LM head on the GPU's own final hidden state."""
 import numpy as np
 import pytest
 import torch
@@ -19,9 +21,11 @@ pytestmark = pytest.mark.gpu
 OP_LMHEAD = 8
 
 
-@pytest.fixture(autouse=True)
-def _umma(monkeypatch):
+@pytest.fixture(autouse=True, params=["lm", "lm+ffn"])
+def umma(request, monkeypatch):
     monkeypatch.setenv("MK_LM_UMMA", "1")
+    monkeypatch.setenv("MK_MOE_UMMA", "1" if request.param == "lm+ffn" else "0")
+    return request.param
 
 
 @pytest.mark.parametrize("workload,lens,mode", [
@@ -32,11 +36,16 @@ def _umma(monkeypatch):
     ("small_b1_2k", [2048, 37], "perop"),
     ("small_b1_2k", [2048, 37], "graph"),
     ("small_fp8_b1_2k", [2048, 9, 300], "mega"),
+    ("small_dense_b1_2k", [2048, 9, 300, 1024], "mega"),
+    ("tiny_dense_b1_64", [64, 3], "graph"),
 ])
-def test_tensor_core_lm_head_matches_oracle(workload, lens, mode):
+def test_tensor_core_lm_head_matches_oracle(workload, lens, mode, umma):
     cfg, W, seq, pt, npages, k, v, tokens = PU.setup(workload, seq_lens=lens)
     mk = B.Megakernel(cfg, W, max_batch=8)
     try:
+        # the FFN items move to the tensor cores only where they are bf16
+        ffn = umma == "lm+ffn" and cfg.get("expert_dtype", "bf16") == "bf16"
+        assert mk.query(B.MK_Q_TENSOR_CORES) == (3 if ffn else 1)
         mk.plan(seq, torch.as_tensor(pt, device="cuda"), npages)
         T = mk.tasks()
         lm = T[T[:, 0] == OP_LMHEAD]
