@@ -191,7 +191,8 @@ def check_bookkeeping(mk, cfg, seq, megakernel=True):
     heads, counts = mk.final_queues()
     n_sm = mk.query(Bd.MK_Q_NUM_SMS)
     Bn, L, Hkv = len(seq), cfg["n_layers"], cfg["n_kv_heads"]
-    _, _, _, I = Bd.mk_plan_dry(cfg, Bn, 4, max_batch=mk.max_batch)
+    # (on the handle's SM count: the QKV tiling follows the SMs free of router tiles)
+    _, _, _, I = Bd.mk_plan_dry(cfg, Bn, n_sm, max_batch=mk.max_batch)
     maxa, t_moe, qkv_tpg, n_router = int(I[3]), int(I[5]), int(I[10]), int(I[11])
     c_lr, c_qkvg, c_rt, c_rr, c_att, c_og, c_md, c_od = (int(x) for x in I[16:24])
     od_target, c_done, c_oa, t_dense, nrb_d = int(I[12]), int(I[13]), int(I[26]), int(I[27]), int(I[24])
