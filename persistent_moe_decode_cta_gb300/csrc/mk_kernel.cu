@@ -2257,6 +2257,7 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
         mma_bf16(sc[1], qa[ks][0], 0u, qa[ks][1], 0u, r2, r3);
       }
     }
+    release_stage(S, cseq);  // the K page is in registers: its stage goes back now
     if (!wait_full(p, S, cseq + 1)) return false;
     if (have) {
       const int kbase = (it.pg0 + c0 + warp) * 16;
@@ -2301,7 +2302,6 @@ __device__ bool attention_split(const Params& p, const Smem& S, uint32_t& cseq, 
         oacc[2 * t2 + 1][0] = d1[0]; oacc[2 * t2 + 1][1] = d1[1];
       }
     }
-    release_stage(S, cseq);
     release_stage(S, cseq + 1);
     cseq += 2;
   }
