@@ -579,7 +579,7 @@ def main():
                                 "small_configs": small_configs_cpu()}
         del o
 
-    # ---- batch 1 at the 128K context (BASELINE config 5): the same handle, re-planned
+    # ---- batch 1 at the 128K context (131072 cached tokens): the same handle, re-planned
     if not args.no_long and full and args.mode == "mega":
         import synth
         wl5 = "pages_b1_128k"
