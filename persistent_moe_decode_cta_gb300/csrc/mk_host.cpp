@@ -504,30 +504,36 @@ int build_plan(const Shape& s, int B, int n_sm, const std::vector<int>& order, P
   return MK_OK;
 }
 
-// Pages per attention split, in whole 8-page ring stages.  Every SM claims splits, and
-// a split is one long serial stream of pages, so a layer's attention ends with its
-// longest run of splits on one SM: the size chosen is the smallest for which the
-// splits of a full-attention layer, with one more per (sequence, group) for the
-// sequences to grow into before the next plan, number at most the SMs (one wave).
-// (At 128K, 37 splits of 224 pages per group on 152 SMs ran 7% faster than 32 of 256,
-// which left 24 SMs without a split; 43 of 192 ran two waves on 20 SMs: -22%.)  Where
-// no size fits, about 32 splits per (sequence, group) at the longest context.
+// Pages per attention split, in whole 8-page ring stages.  The base size gives about 32
+// splits per (sequence, group) at the longest context.  Every SM claims splits and a
+// split is one long serial stream of pages, so a layer's attention ends with its longest
+// run of splits on one SM.  Where the base size's splits of a full-attention layer do
+// not fit the SMs in one wave, or fit with long splits (128 pages or more) and SMs to
+// spare, the size becomes the smallest for which they fit, with one more split per
+// (sequence, group) for the sequences to grow into before the next plan.  (Same-box
+// A/Bs: 128K, 37 splits of 224 pages per group on 152 SMs against 32 of 256: +5.7%;
+// batch 8 ragged up to 32K, 120 splits of 296 pages against 508 of 64: +1.5%; at 8K,
+// 32 splits of 16 pages per group against the base 22 of 24: -9%, so short splits keep
+// the base size.)
 int choose_split_pages(const int32_t* lens, int B, int Hkv, int n_sm, int max_pages) {
+  int base = (max_pages + 31) / 32;
+  base = std::max(8, (base + 7) / 8 * 8);
   std::vector<int> npg(B);
   int longest = 0;
   for (int b = 0; b < B; ++b) {
     npg[b] = lens[b] > 0 ? (lens[b] - 1) / 16 + 1 : 0;  // pages of the cached keys
     longest = std::max(longest, npg[b]);
   }
+  auto splits = [&](int sp) {
+    long long n = 0;
+    for (int b = 0; b < B; ++b) n += (npg[b] + sp - 1) / sp;
+    return n * Hkv;
+  };
   const long long budget = (long long)n_sm - (long long)B * Hkv;
-  for (int sp = 8; budget > 0 && sp < longest + 8; sp += 8) {
-    long long splits = 0;
-    for (int b = 0; b < B; ++b) splits += (npg[b] + sp - 1) / sp;
-    if (splits * Hkv <= budget) return sp;
-  }
-  int sp = (max_pages + 31) / 32;
-  sp = (sp + 7) / 8 * 8;
-  return std::max(8, sp);
+  if (budget <= 0 || (splits(base) <= budget && base < 128)) return base;
+  for (int sp = 8; sp < longest + 8; sp += 8)
+    if (splits(sp) <= budget) return sp;
+  return base;
 }
 
 constexpr int kDefaultPrefetch = 0;
