@@ -314,14 +314,34 @@ class OracleSteps:
             self.source = "weights and K/V drawn on the host"
         self.step()            # untimed: brings every tensor the step reads to the host
 
-    def step(self):
+    def step(self, n_layers=None):
+        """Seconds of one decode step.  With n_layers, a bounded sample of it: the
+        embedding, the first n_layers layers and the full LM head, each timed, the
+        layers' time scaled to all of them (every layer has the same shapes)."""
+        O, cfg = self.O, self.cfg
+        L = cfg["n_layers"]
+        if n_layers is None or n_layers >= L:
+            t0 = time.perf_counter()
+            O.decode_step(cfg, self.W, self.kv, self.tokens, self.seq, self.pt)
+            return time.perf_counter() - t0
         t0 = time.perf_counter()
-        self.O.decode_step(self.cfg, self.W, self.kv, self.tokens, self.seq, self.pt)
-        return time.perf_counter() - t0
+        x = O.embed(self.W, self.tokens)
+        t1 = time.perf_counter()
+        for l in range(n_layers):
+            x, _ = O.layer_step(cfg, self.W, self.kv, l, x, self.seq, self.pt)
+        t2 = time.perf_counter()
+        O.lm_head(cfg, self.W, x)
+        t3 = time.perf_counter()
+        return (t1 - t0) + (t2 - t1) * L / n_layers + (t3 - t2)
 
-    def describe(self, n):
-        return (f"{self.workload}: {n} whole float64 numpy oracle step(s) ({self.cfg['n_layers']} layers "
-                f"+ the full LM head, batch {self.B}) over {self.source}")
+    def describe(self, n, n_layers=None):
+        L = self.cfg["n_layers"]
+        if n_layers is None or n_layers >= L:
+            return (f"{self.workload}: {n} whole float64 numpy oracle step(s) ({L} layers "
+                    f"+ the full LM head, batch {self.B}) over {self.source}")
+        return (f"{self.workload}: {n} sampled float64 numpy oracle step(s), each the embedding, the "
+                f"first {n_layers} of {L} layers (time scaled by {L}/{n_layers}) and the full LM head, "
+                f"batch {self.B}, over {self.source}")
 
 
 def cpu_cores():
@@ -370,9 +390,18 @@ def run_reference(args, rank, ws):
     except Exception:
         W = kv = None
     o = OracleSteps(args.workload, args.seed, W, kv)
-    for _ in range(args.warmup):
-        o.step()
-    per = [o.step() for _ in range(args.steps)]
+    # whole steps while warm-up + timed steps fit the time budget; else each step is a
+    # bounded sample of the layers (the first warm-up step, or one extra untimed step,
+    # measures a whole step)
+    budget_s = 150.0
+    t_whole = o.step()
+    n_steps = max(1, args.warmup + args.steps)
+    n_layers = None
+    if t_whole * n_steps > budget_s:
+        n_layers = max(1, int(o.cfg["n_layers"] * budget_s / (n_steps * t_whole)))
+    for _ in range(max(0, args.warmup - 1)):
+        o.step(n_layers)
+    per = [o.step(n_layers) for _ in range(args.steps)]
     step_s = statistics.mean(per)
     value = o.B / step_s
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
@@ -381,7 +410,7 @@ def run_reference(args, rank, ws):
             "data": "synthetic",
             "config": {"workload": args.workload, "batch": o.B, "seq_lens": o.seq, "mode": "oracle"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                             "sample": o.describe(args.steps)},
+                             "sample": o.describe(args.steps, n_layers)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
