@@ -162,7 +162,12 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* stream, mk_handle
  *                      length may be -1.  Must stay valid while the plan is used.
  *   n_pages            pages in the caller's K/V pools
  * The step reads seq_lens from a device copy that mk_decode_step advances by one
- * after each step (unless mk_set_fixed(h, 1)). */
+ * after each step (unless mk_set_fixed(h, 1)).  The attention split size (pages per
+ * split, MK_Q_SPLIT_PAGES) is fixed here from seq_lens_host and the SM count: about 32
+ * splits per (sequence, KV group) at the longest context, or, for long or numerous
+ * splits, the size whose splits fill the SMs in one wave with one more per (sequence,
+ * group) left for growth; sequences that later outgrow it still run correctly, with
+ * more splits (re-plan to re-balance).  MK_SPLIT_PAGES (a multiple of 8) overrides it. */
 int mk_plan(mk_handle* h, int batch, const int32_t* seq_lens_host,
             const int32_t* page_table_dev, int max_pages_per_seq, int n_pages);
 
